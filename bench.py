@@ -1,0 +1,449 @@
+"""Benchmark: layout_copy GB/s (bytes read + written) on GB300.
+
+One step = one pass of the relayout suite, each workload one layout_copy
+through the C ABI:
+
+  C2  fp32 4096x4096 column-major -> row-major             (STAGED)
+  C3  bf16 8192x8192 -> 64x64 tiles, Swizzle<3,4,3> inside (VEC 16 B)
+  C4  fp64 2^20 padded 8x8 tiles gathered into TV order    (STAGED)
+  C5a fp16 NHWC (64,56,56,256) -> NCHW                     (STAGED)
+  C5b fp16 (2,16384,128) head-major -> stride-2 interleave (STAGED)
+
+value = algorithmic bytes (read + written, SURVEY 8(d) per workload) over
+the summed CUDA-event time of the copies, on the launching stream.  The five
+buffer pairs (1.87 GB per step) are each reused only after > 1.6 GB of other
+traffic, larger than the 126 MiB L2, so no explicit flush is done.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun (N > 1) every rank runs the whole suite on its own GPU (weak
+scaling, no collective on the data path); rank 0 prints the line with the
+max-over-ranks time.  ``--impl reference`` times the CPU oracle instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from workloads import BENCH_SUITE, WORKLOADS, seeded_bytes  # noqa: E402
+
+METRIC = ("layout_copy GB/s (read+write) and % of GB300 HBM peak; "
+          "bit-exact vs CPU oracle")
+UNIT = "GB/s"
+# algorithmic bytes per copy (read + written), SURVEY 8(d)
+ALGO_BYTES = {"C2": 134_217_728, "C3": 268_435_456, "C4": 1_140_850_688,
+              "C5a": 205_520_896, "C5b": 16_777_216}
+DOMINANT = "C4"          # largest share of the step: lm_staged_kernel<8>
+FALLBACK_HBM_GBS = 6800.0
+
+
+def peaks() -> tuple[float, str]:
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            return float(json.load(fh)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# --------------------------------------------------------------------------
+# clocks during the timed region
+# --------------------------------------------------------------------------
+
+class ClockSampler:
+    """nvidia-smi samples (every 100 ms) of the GPU under test; only samples
+    stamped inside the timed window count."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,"
+              "clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+               "sw_power_cap"]
+
+    def __init__(self, gpu_id: str):
+        self.gpu = gpu_id
+        self.proc = None
+        self.lines = []
+        self.window = (0.0, float("inf"))
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}",
+                 f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self) -> dict:
+        import datetime
+        rows = []
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                ts = datetime.datetime.strptime(
+                    parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if self.window[0] <= r[0] <= self.window[1]]
+        use = inside if inside else rows
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                    "samples": 0}
+        reasons = sorted({name for r in use for name, flag in
+                          zip(self.REASONS, r[3]) if flag.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in use),
+                "sm_max_mhz": max(r[2] for r in use), "reasons": reasons,
+                "samples": len(use), "in_timed_window": bool(inside)}
+
+
+def gpu_smi_id(local: int) -> str:
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(local).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        first = vis.split(",")[local] if vis else str(local)
+        return first.strip()
+
+
+# --------------------------------------------------------------------------
+# the suite on the GPU
+# --------------------------------------------------------------------------
+
+class Suite:
+    def __init__(self, device, names=BENCH_SUITE):
+        import torch
+        import layout_driven_movement_gb300 as lm
+        self.torch, self.lm = torch, lm
+        self.items = []
+        for name in names:
+            w = WORKLOADS[name]
+            S, D = lm.build_layout(w.src), lm.build_layout(w.dst)
+            plan = lm.Plan(S, D, w.elem_bytes)
+            host = seeded_bytes(w.values, w.dtype, S.cosize, w.seed)
+            src = torch.from_numpy(host).to(device)
+            dst = torch.empty(D.cosize * w.elem_bytes, dtype=torch.uint8,
+                              device=device)
+            self.items.append(dict(name=name, w=w, plan=plan, src=src,
+                                   dst=dst, host=host, S=S, D=D,
+                                   bytes=ALGO_BYTES[name]))
+        self.bytes_per_step = sum(it["bytes"] for it in self.items)
+        self.launches_per_step = sum(it["plan"].launches for it in self.items)
+
+    def step(self, events=None):
+        lm = self.lm
+        for k, it in enumerate(self.items):
+            if events is not None:
+                events[k][0].record()
+            lm.layout_copy(it["plan"], it["src"], it["dst"])
+            if events is not None:
+                events[k][1].record()
+
+
+def run_native(args) -> dict | None:
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if rank == 0:
+        import __graft_entry__ as g
+        g.build()
+    if world > 1:
+        dist.barrier()
+    import layout_driven_movement_gb300 as lm
+    lm.lib()
+    suite = Suite(device)
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        suite.step()
+    torch.cuda.synchronize()
+
+    n = len(suite.items)
+    events = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)]
+               for _ in range(n)] for _ in range(args.steps)]
+    with ClockSampler(gpu_smi_id(local)) as clk:
+        time.sleep(1.0)             # let the sampler start
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t_start = time.time()
+        t0 = time.perf_counter()
+        for s in range(args.steps):
+            suite.step(events[s])
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+        clk.window = (t_start, time.time())
+        if world > 1:
+            dist.barrier()
+    per = {it["name"]: [] for it in suite.items}
+    for s in range(args.steps):
+        for k, it in enumerate(suite.items):
+            per[it["name"]].append(events[s][k][0].elapsed_time(events[s][k][1]))
+    total_ms = sum(sum(v) for v in per.values())
+    if world > 1:
+        t = torch.tensor([total_ms, wall], dtype=torch.float64)
+        gathered = [torch.zeros_like(t) for _ in range(world)]
+        dist.all_gather(gathered, t)
+        total_ms = max(float(g[0]) for g in gathered)
+        wall = max(float(g[1]) for g in gathered)
+    value = suite.bytes_per_step * args.steps * world / (total_ms * 1e-3) / 1e9
+
+    peak, peak_kind = peaks()
+    per_cfg = {}
+    for it in suite.items:
+        ms = statistics.median(per[it["name"]])
+        gbs = it["bytes"] / (ms * 1e-3) / 1e9
+        per_cfg[it["name"]] = {
+            "path": "+".join(p["path"] for p in it["plan"].describe()["pieces"]),
+            "bytes": it["bytes"], "median_us": round(ms * 1e3, 2),
+            "gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4)}
+    dom = per[DOMINANT]
+    dom_ms = sum(dom) / len(dom)
+    achieved = ALGO_BYTES[DOMINANT] / (dom_ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1),
+                "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4),
+                "traffic": measured_traffic("lm_staged_kernel<8>"),
+                "kernel": "lm_staged_kernel<8> (C4 padded TV gather)",
+                "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+                if peak_kind == "measured" else "fallback 6.8 TB/s"}
+    if rank != 0:
+        return None
+
+    e2e = measure_e2e(suite, args, torch)
+    cpu = cpu_baseline(suite) if world == 1 else None
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "u8", "data": "synthetic (seeded numpy PCG64, shapes and "
+        "value distributions of the five relayouts)",
+        "config": {
+            "workload": "relayout suite C2+C3+C4+C5a+C5b, one layout_copy "
+                        "each per step",
+            "bytes_per_step": suite.bytes_per_step,
+            "element_types": "fp32, bf16, fp64, fp16, fp16 (moved as raw bytes)",
+            "l2": "no flush: 1.87 GB/step over five buffer pairs, each reused "
+                  "after >1.6 GB of other traffic (L2 126 MiB)",
+            "wall_s_timed": round(wall, 4),
+            "per_config": per_cfg,
+        },
+        "clocks": clocks,
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": suite.launches_per_step * args.steps,
+    }
+    return line
+
+
+def measured_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or
+    None if absent or taken on different kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as fh:
+            rec = json.load(fh)[kernel]
+        src = os.path.join(ROOT, "layout_driven_movement_gb300", "csrc",
+                           "lm_kernels.cu")
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        if rec.get("kernel_source_sha") != sha:
+            return None
+        return rec["dram_bytes_per_launch"]
+    except Exception:
+        return None
+
+
+def measure_e2e(suite, args, torch) -> dict:
+    """The same metric through the public API with host buffers: every step
+    copies each workload's source from pinned host memory, runs
+    layout_copy, and reads the destination back into pinned host memory."""
+    steps = max(2, min(args.steps, 5))
+    hs = [torch.from_numpy(it["host"]).pin_memory() for it in suite.items]
+    hd = [torch.empty(it["dst"].numel(), dtype=torch.uint8).pin_memory()
+          for it in suite.items]
+    h2d = sum(h.numel() for h in hs)
+    d2h = sum(h.numel() for h in hd)
+    lm = suite.lm
+
+    def one():
+        for it, a, b in zip(suite.items, hs, hd):
+            it["src"].copy_(a, non_blocking=True)
+            lm.layout_copy(it["plan"], it["src"], it["dst"])
+            b.copy_(it["dst"], non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    start, end = (torch.cuda.Event(enable_timing=True),
+                  torch.cuda.Event(enable_timing=True))
+    start.record()
+    for _ in range(steps):
+        one()
+    end.record()
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end)
+    val = suite.bytes_per_step * steps / (ms * 1e-3) / 1e9
+    return {"value": round(val, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps}
+
+
+# --------------------------------------------------------------------------
+# the CPU oracle (baseline leg and reference arm)
+# --------------------------------------------------------------------------
+
+class OracleWindows:
+    """The CPU oracle's copy over windows of each workload's logical
+    indices (the same fraction of every workload, so a sample mirrors the
+    suite's mix).  Buffers are full-size host arrays."""
+
+    def __init__(self, names, bufs):
+        from oracle import layout_oracle as lo
+        self.lo = lo
+        self.names = names
+        self.bufs = bufs
+        self.exprs = {n: (lo.build(WORKLOADS[n].src), lo.build(WORKLOADS[n].dst))
+                      for n in names}
+
+    def run(self, frac: float, shift: int = 0):
+        nbytes, elems = 0.0, 0
+        t0 = time.perf_counter()
+        for name in self.names:
+            S, D = self.exprs[name]
+            eb = WORKLOADS[name].elem_bytes
+            inp, out = self.bufs[name]
+            n = max(1, min(S.size, int(S.size * frac)))
+            start = (shift * n) % max(1, S.size - n + 1)
+            idx = np.arange(start, start + n, dtype=np.int64)
+            self.lo.copy(S, D, inp, out, eb, indices=idx)
+            nbytes += ALGO_BYTES[name] * n / S.size
+            elems += n
+        return time.perf_counter() - t0, nbytes, elems
+
+    def calibrate(self, seconds: float) -> float:
+        """Fraction of every workload that takes about `seconds`."""
+        probe = 2.0 ** -12
+        t, _, _ = self.run(probe)
+        return min(1.0, probe * seconds / max(t, 1e-4))
+
+
+def cpu_baseline(suite) -> dict:
+    bufs = {it["name"]: (it["host"],
+                         np.zeros(it["dst"].numel(), dtype=np.uint8))
+            for it in suite.items}
+    ow = OracleWindows(BENCH_SUITE, bufs)
+    frac = ow.calibrate(12.0)
+    secs, nbytes, elems = ow.run(frac)
+    return {"value": round(nbytes / secs / 1e9, 3), "unit": UNIT, "cores": 1,
+            "kind": "oracle",
+            "sample": f"numpy oracle copy of {frac:.4f} of every workload's "
+                      f"logical indices (one contiguous window each), "
+                      f"{elems} elements in {secs:.1f} s, single thread"}
+
+
+def run_reference(args) -> dict | None:
+    """The reference arm: the CPU oracle as it stands, on this host's cores,
+    each step a window of every workload sized so the whole run takes about
+    a minute."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    from oracle import layout_oracle as lo
+    bufs = {}
+    for name in BENCH_SUITE:
+        w = WORKLOADS[name]
+        S, D = lo.build(w.src), lo.build(w.dst)
+        bufs[name] = (seeded_bytes(w.values, w.dtype, lo.cosize(S), w.seed),
+                      np.zeros(lo.cosize(D) * w.elem_bytes, dtype=np.uint8))
+    ow = OracleWindows(BENCH_SUITE, bufs)
+    per_step = 60.0 / (args.steps + args.warmup)
+    frac = ow.calibrate(per_step)
+    for k in range(args.warmup):
+        ow.run(frac, shift=k)
+    secs, nbytes, elems = 0.0, 0.0, 0
+    for k in range(args.steps):
+        t, b, e = ow.run(frac, shift=args.warmup + k)
+        secs += t
+        nbytes += b
+        elems += e
+    gbs = nbytes / secs / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4),
+        "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(secs * 1e3 / max(args.steps, 1), 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "u8", "data": "synthetic",
+        "config": {"workload": "relayout suite C2+C3+C4+C5a+C5b, one "
+                               "layout_copy each per step",
+                   "sample_fraction_per_step": frac},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": UNIT, "cores": 1,
+                         "kind": "oracle",
+                         "sample": f"{frac:.2e} of every workload per step, "
+                                   f"{elems} logical indices in {secs:.1f} s"},
+        "e2e": {"value": round(gbs, 4), "unit": UNIT,
+                "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    return line
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    if args.impl == "reference":
+        line = run_reference(args)
+    else:
+        line = run_native(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,255 @@
+/*
+ * layoutmove.h -- C ABI of the GB300 layout-driven data movement library.
+ *
+ * A layout is a function from a logical coordinate to an element offset,
+ * written shape:stride with nested modes, e.g. ((4,2),(2,4)):((2,16),(1,8)):
+ * the offset is the inner product of the coordinate with the strides
+ * ("CUTLASS Layout可视化：从print_layout理解GPU内存映射与性能优化" §2.1, §3.2;
+ * "CUTE布局代数：GPU张量计算的内存优化革命" §2.1).  Optionally the affine
+ * offset then passes through an XOR Swizzle<B,M,S> ("CUTLASS Layout可视化"
+ * §4.3).  A copy moves a tensor from one layout to another over the same
+ * logical coordinates: out[dst(i)] = in[src(i)] for every logical index i
+ * ("CUTE布局代数" §5.1, make_copy(gmem_layout, smem_layout)).
+ *
+ * Conventions that hold for every function below:
+ *  - Offsets, strides, sizes and capacities count ELEMENTS, not bytes
+ *    (the PitchLinearStripminedThreadMap article, hotelren.com, §1.2).
+ *  - A 1-D logical index is split over the leaves first-leaf-fastest
+ *    ("colex"): the leaves of mode 0 before those of mode 1, the first leaf
+ *    of each mode fastest.
+ *  - Extents are >= 0, strides >= 0; an extent of 0 makes an empty layout
+ *    (size 0, cosize 0) whose copy enqueues nothing.  All arithmetic is
+ *    int64 and checked:
+ *    a result that does not fit returns LM_E_OVERFLOW.
+ *  - Every function returns an lm_status (LM_OK = 0, errors < 0) except the
+ *    destroy functions and the string lookups.  No function aborts, exits or
+ *    lets a C++ exception cross this boundary.  On error, output handles are
+ *    set to NULL and output scalars are left unchanged.
+ *  - Handles are immutable after creation; they may be shared between
+ *    threads.  The caller owns every handle it receives and frees it with the
+ *    matching destroy function (NULL is accepted and ignored).
+ *  - Device buffers are owned by the caller and must stay valid until the
+ *    stream has finished the work enqueued on them.
+ */
+#ifndef LAYOUTMOVE_H
+#define LAYOUTMOVE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct lm_layout lm_layout; /* opaque, freed by lm_layout_destroy */
+typedef struct lm_plan lm_plan;     /* opaque, freed by lm_plan_destroy   */
+
+typedef enum lm_status {
+  LM_OK = 0,
+  LM_E_INVALID = -1,           /* malformed argument (NULL, bad extent, ...)  */
+  LM_E_INCOMPATIBLE = -2,      /* src and dst sizes differ                    */
+  LM_E_NOT_REPRESENTABLE = -3, /* the algebraic result is no shape:stride
+                                  (+swizzle) layout: divisibility fails, or
+                                  the inner layout of a composition is
+                                  swizzled                                    */
+  LM_E_NOT_INJECTIVE = -4,     /* destination not shown to be one-to-one      */
+  LM_E_OVERFLOW = -5,          /* int64 overflow in sizes or offsets          */
+  LM_E_CAPACITY = -6,          /* a buffer is smaller than the layout needs   */
+  LM_E_OVERLAP = -7,           /* src and dst byte ranges overlap             */
+  LM_E_CUDA = -8,              /* a CUDA call failed; see lm_last_cuda_error  */
+  LM_E_TIMEOUT = -9,           /* reserved: a bounded device wait gave up     */
+  LM_E_NOMEM = -10,            /* host allocation failed                      */
+  LM_E_BUFFER = -11            /* a text output buffer is too small           */
+} lm_status;
+
+/* ---------------------------------------------------------------------------
+ * Layout construction and inspection (host only)
+ * ------------------------------------------------------------------------- */
+
+/* Build shape:stride from its leaves.  leaves_per_mode[m] leaves form
+ * top-level mode m (n_modes modes, the counts summing to n_leaves); a mode of
+ * one leaf is a plain integer mode, a mode of several leaves a nested tuple.
+ * n_modes == 0 means one flat mode holding all leaves as an integer
+ * (n_leaves must then be 1).  Example: ((4,2),(2,4)):((2,16),(1,8)) is
+ * n_leaves=4, shape={4,2,2,4}, stride={2,16,1,8}, n_modes=2,
+ * leaves_per_mode={2,2}.  ("CUTE布局代数" §2.1.)
+ * Errors: LM_E_INVALID (NULL, extent < 1, stride < 0, counts that do not add
+ * up), LM_E_OVERFLOW. */
+int lm_layout_make(int n_leaves, const int64_t* shape, const int64_t* stride,
+                   int n_modes, const int* leaves_per_mode, lm_layout** out);
+
+/* Parse the printed notation, any nesting depth: "8:1", "(4,2):(2,1)",
+ * "((4,2),(2,4)):((2,16),(1,8))", static marks accepted ("(4,2):(_2,_1)",
+ * "CUTLASS Layout可视化" §3.2), and a swizzle prefix
+ * "Sw<3,4,3> o ((64,64),(128,128)):((64,1),(524288,4096))".
+ * Errors: LM_E_INVALID with no partial result. */
+int lm_layout_parse(const char* text, lm_layout** out);
+
+/* Print the same notation (no static marks).  Writes a NUL-terminated string
+ * into buf; LM_E_BUFFER if cap is too small (buf then holds a truncated,
+ * NUL-terminated prefix when cap > 0). */
+int lm_layout_to_string(const lm_layout* layout, char* buf, size_t cap);
+
+/* size = product of all extents.  cosize = one past the largest offset of
+ * the affine part; with a swizzle, rounded up to a multiple of 2^(M+B), the
+ * smallest bound that holds every swizzled offset whatever the layout.  A
+ * buffer of cosize elements holds every offset. */
+int lm_layout_size(const lm_layout* layout, int64_t* size);
+int lm_layout_cosize(const lm_layout* layout, int64_t* cosize);
+
+/* Number of top-level modes and of leaves; the leaves themselves (shape and
+ * stride arrays of at least n_leaves entries, either may be NULL); the
+ * swizzle (b = 0 when there is none).  leaves_per_mode may be NULL. */
+int lm_layout_rank(const lm_layout* layout, int* n_modes, int* n_leaves);
+int lm_layout_leaves(const lm_layout* layout, int64_t* shape, int64_t* stride,
+                     int* leaves_per_mode);
+int lm_layout_get_swizzle(const lm_layout* layout, int* b, int* m, int* s);
+
+/* offset = L(i) for a colex index 0 <= i < size, swizzle included.
+ * Errors: LM_E_INVALID for i out of range. */
+int lm_layout_eval(const lm_layout* layout, int64_t index, int64_t* offset);
+
+/* offset = swizzle(sum_k coord[k] * stride[k]) for a full leaf coordinate
+ * (n == number of leaves).  No bounds check on the coordinates: this is the
+ * bare offset formula of "CUTLASS Layout可视化" §2.1, under which the
+ * blocked layout's printed sample of "CUTE布局代数" §6.1 reads
+ * (r, c) -> 2r + 16c as leaf coordinate (r, c, 0, 0).
+ * Errors: LM_E_INVALID (n mismatch, negative coordinate), LM_E_OVERFLOW. */
+int lm_layout_eval_coord(const lm_layout* layout, int n,
+                         const int64_t* leaf_coord, int64_t* offset);
+
+/* ---------------------------------------------------------------------------
+ * Layout algebra (host only)
+ * ------------------------------------------------------------------------- */
+
+/* R = A o B, R(i) = A(B(i)), shaped like B ("CUTE布局代数" §2.2, §3.1).  B's
+ * value is read by A as a colex index; past A's last extent A's last leaf
+ * keeps counting.  A may carry a swizzle (it stays outermost in R).
+ * Example: (8,8):(1,9) o ((4,8),2):((16,1),8) = ((4,8),2):((18,1),9).
+ * Errors: LM_E_NOT_REPRESENTABLE when B is swizzled or a B stride/extent does
+ * not divide A's leaf structure; LM_E_OVERFLOW. */
+int lm_layout_compose(const lm_layout* a, const lm_layout* b, lm_layout** r);
+
+/* zipped_divide(L, tiler) ("CUTE布局代数" §3.2): n must equal L's number of
+ * top-level modes; tiler[k] consecutive coordinates of mode k form a tile.
+ * Result ((tile_0,...,tile_n-1),(rest_0,...,rest_n-1)), each piece the mode
+ * composed with t:1 (tile) and (n_k/t_k):t_k (rest); L's swizzle is kept.
+ * Example: (128,128):(1,128) / (4,8) = ((4,8),(32,16)):((1,128),(4,1024)).
+ * Errors: LM_E_INVALID (n mismatch, tiler < 1), LM_E_NOT_REPRESENTABLE
+ * (a tiler entry that does not divide its mode, or a mode whose leaves it
+ * cannot split). */
+int lm_layout_zipped_divide(const lm_layout* layout, int n,
+                            const int64_t* tiler, lm_layout** r);
+
+/* R = Swizzle<B,M,S> o L: offsets o -> o ^ ((o >> S) & ((2^B - 1) << M))
+ * ("CUTLASS Layout可视化" §4.3; Swizzle<3,0,3> on (8,8):(8,1) is the page's
+ * row*8 + (col ^ row)).  Requires B >= 0, M >= 0, S >= B, B+M+S <= 40.
+ * Errors: LM_E_INVALID, LM_E_NOT_REPRESENTABLE (L already swizzled). */
+int lm_layout_swizzle(const lm_layout* layout, int b, int m, int s,
+                      lm_layout** r);
+
+/* R = (A, B): A's modes become mode 0, B's mode 1, so B is the slower
+ * (batch) mode.  Errors: LM_E_NOT_REPRESENTABLE if either is swizzled. */
+int lm_layout_concat(const lm_layout* a, const lm_layout* b, lm_layout** r);
+
+/* Flat layout with the same function: extent-1 leaves dropped, neighbours
+ * (e0:d0, e1:d1) with d1 == e0*d0 merged.  Swizzle kept. */
+int lm_layout_coalesce(const lm_layout* layout, lm_layout** r);
+
+/* Right inverse L‡ ("CUTE布局代数" §2.3): the layout R with L(R(j)) = j for
+ * 0 <= j < size(R), where size(R) is the length of the contiguous run of
+ * offsets 0, 1, 2, ... that L reaches (size(L) for a bijection onto
+ * [0, size)).  Errors: LM_E_NOT_REPRESENTABLE for a swizzled L. */
+int lm_layout_right_inverse(const lm_layout* layout, lm_layout** r);
+
+/* K = max{k : A‡(j) = B‡(j) for all j < k} ("CUTE布局代数" §2.3): the number
+ * of leading offsets at which both layouts hold the same logical element.
+ * Offsets with no or several preimages end the run.
+ * Errors: LM_E_INCOMPATIBLE (sizes differ). */
+int lm_layout_max_common_vector(const lm_layout* a, const lm_layout* b,
+                                int64_t* k);
+
+/* The stripmined thread map of the PitchLinearStripminedThreadMap article
+ * (hotelren.com, §2.2) as a layout over thread ids:
+ * (pitch, strips, ceil(threads/(pitch*strips))):(1, k_row,
+ * pitch*strips*k_row), whose colex evaluation is get_offset(thread_id).
+ * Errors: LM_E_INVALID for arguments < 1. */
+int lm_layout_stripmined(int64_t threads, int64_t pitch, int64_t strips,
+                         int64_t k_row, lm_layout** r);
+
+void lm_layout_destroy(lm_layout* layout);
+
+/* ---------------------------------------------------------------------------
+ * Copy plans and device work
+ * ------------------------------------------------------------------------- */
+
+/* Lower a src/dst layout pair into a copy plan for elements of elem_bytes in
+ * {1, 2, 4, 8, 16}.  The plan refines both leaf lists to common modes,
+ * coalesces and reorders them, checks that dst is injective, finds the
+ * common contiguous run (the common vector of "CUTE布局代数" §2.3) and
+ * chooses per piece of the domain a kernel: VEC (16-byte vectors along a run
+ * both sides share), STAGED (tiles staged through swizzled shared memory,
+ * loads contiguous along src, stores contiguous along dst) or GENERIC (one
+ * element per thread).  Pairs without a common refinement of their leaves
+ * are planned GENERIC over each side's own leaves.  The plan is host data
+ * only; it holds no device memory and may be used on any device and stream.
+ * Errors: LM_E_INVALID, LM_E_INCOMPATIBLE (sizes differ),
+ * LM_E_NOT_INJECTIVE (dst offsets could collide; proven exactly for every
+ * layout up to 2^28 elements, otherwise by a sufficient test),
+ * LM_E_OVERFLOW, LM_E_NOMEM. */
+int lm_plan_copy(const lm_layout* src, const lm_layout* dst, int elem_bytes,
+                 lm_plan** out);
+
+/* One-line JSON description: pieces, path, modes, vector width, tile. */
+int lm_plan_describe(const lm_plan* plan, char* buf, size_t cap);
+
+/* Elements of src and dst that the plan reads and writes (sizes of their
+ * layouts' domains are equal; this is that size), and the cosizes a buffer
+ * must cover. */
+int lm_plan_extent(const lm_plan* plan, int64_t* size, int64_t* src_cosize,
+                   int64_t* dst_cosize);
+
+/* Enqueue out[dst(i)] = in[src(i)] on cuda_stream (a cudaStream_t; NULL is
+ * the legacy default stream).  src_dev/dst_dev are device pointers to
+ * buffers of src_capacity_elems / dst_capacity_elems elements.  Host checks
+ * before launch: capacities >= the layouts' cosizes (LM_E_CAPACITY), the byte
+ * ranges [ptr, ptr + cosize*elem_bytes) do not overlap (LM_E_OVERLAP).  Base
+ * pointers need only elem_bytes alignment: where a vector path needs 16-byte
+ * alignment and the pointers lack it, the same plan runs with narrower
+ * accesses.  Destination slots outside dst's image are not written.  The
+ * call returns after enqueueing; it synchronises nothing.  A launch failure
+ * returns LM_E_CUDA (lm_last_cuda_error has the cudaError_t). */
+int lm_layout_copy(const lm_plan* plan, const void* src_dev,
+                   int64_t src_capacity_elems, void* dst_dev,
+                   int64_t dst_capacity_elems, void* cuda_stream);
+
+/* Number of kernel launches lm_layout_copy makes for this plan. */
+int lm_plan_launches(const lm_plan* plan, int* launches);
+
+/* Enqueue table[i] = L(i) for 0 <= i < size(L) into a device table of
+ * offset_bytes (4 or 8) entries; capacity counts entries and must be
+ * >= size(L).  With offset_bytes == 4 every offset must fit in int32
+ * (LM_E_OVERFLOW otherwise).  ("CUTLASS Layout可视化" §2.3: the offset of
+ * every logical coordinate, in logical order.)  Returns LM_E_CUDA on launch
+ * failure. */
+int lm_layout_eval_device(const lm_layout* layout, void* table_dev,
+                          int offset_bytes, int64_t capacity,
+                          void* cuda_stream);
+
+void lm_plan_destroy(lm_plan* plan);
+
+/* Static, NUL-terminated name of a status code. */
+const char* lm_status_string(int status);
+
+/* The cudaError_t of the last LM_E_CUDA returned on this thread (0 if
+ * none). */
+int lm_last_cuda_error(void);
+
+/* Library version, "major.minor.patch". */
+const char* lm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LAYOUTMOVE_H */

@@ -1,0 +1,388 @@
+"""Python binding of the layoutmove C ABI (``include/layoutmove.h``).
+
+Argument marshalling only: every computation -- the layout algebra, the
+copy planning and all device work -- happens in ``liblayoutmove.so``.  There
+is no Python or CPU fallback: if the library is missing, every call raises.
+
+Names follow the C ABI without the ``lm_`` prefix.  PyTorch is used only to
+pass device pointers and streams (``tensor.data_ptr()``,
+``torch.cuda.current_stream().cuda_stream``).
+"""
+
+from __future__ import annotations
+
+import ctypes as C
+import json
+import os
+from typing import Iterable, Sequence
+
+__all__ = [
+    "LayoutMoveError", "Layout", "Plan", "lib", "layout_copy",
+    "layout_eval_device", "build_layout", "STATUS",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "liblayoutmove.so")
+
+STATUS = {
+    0: "LM_OK", -1: "LM_E_INVALID", -2: "LM_E_INCOMPATIBLE",
+    -3: "LM_E_NOT_REPRESENTABLE", -4: "LM_E_NOT_INJECTIVE",
+    -5: "LM_E_OVERFLOW", -6: "LM_E_CAPACITY", -7: "LM_E_OVERLAP",
+    -8: "LM_E_CUDA", -9: "LM_E_TIMEOUT", -10: "LM_E_NOMEM",
+    -11: "LM_E_BUFFER",
+}
+
+# (name, restype, argtypes) of every function include/layoutmove.h declares
+_P = C.c_void_p
+_I64 = C.c_int64
+_I64P = C.POINTER(C.c_int64)
+_IP = C.POINTER(C.c_int)
+SIGNATURES = [
+    ("lm_layout_make", C.c_int,
+     [C.c_int, _I64P, _I64P, C.c_int, _IP, C.POINTER(_P)]),
+    ("lm_layout_parse", C.c_int, [C.c_char_p, C.POINTER(_P)]),
+    ("lm_layout_to_string", C.c_int, [_P, C.c_char_p, C.c_size_t]),
+    ("lm_layout_size", C.c_int, [_P, _I64P]),
+    ("lm_layout_cosize", C.c_int, [_P, _I64P]),
+    ("lm_layout_rank", C.c_int, [_P, _IP, _IP]),
+    ("lm_layout_leaves", C.c_int, [_P, _I64P, _I64P, _IP]),
+    ("lm_layout_get_swizzle", C.c_int, [_P, _IP, _IP, _IP]),
+    ("lm_layout_eval", C.c_int, [_P, _I64, _I64P]),
+    ("lm_layout_eval_coord", C.c_int, [_P, C.c_int, _I64P, _I64P]),
+    ("lm_layout_compose", C.c_int, [_P, _P, C.POINTER(_P)]),
+    ("lm_layout_zipped_divide", C.c_int, [_P, C.c_int, _I64P, C.POINTER(_P)]),
+    ("lm_layout_swizzle", C.c_int,
+     [_P, C.c_int, C.c_int, C.c_int, C.POINTER(_P)]),
+    ("lm_layout_concat", C.c_int, [_P, _P, C.POINTER(_P)]),
+    ("lm_layout_coalesce", C.c_int, [_P, C.POINTER(_P)]),
+    ("lm_layout_right_inverse", C.c_int, [_P, C.POINTER(_P)]),
+    ("lm_layout_max_common_vector", C.c_int, [_P, _P, _I64P]),
+    ("lm_layout_stripmined", C.c_int, [_I64, _I64, _I64, _I64, C.POINTER(_P)]),
+    ("lm_layout_destroy", None, [_P]),
+    ("lm_plan_copy", C.c_int, [_P, _P, C.c_int, C.POINTER(_P)]),
+    ("lm_plan_describe", C.c_int, [_P, C.c_char_p, C.c_size_t]),
+    ("lm_plan_extent", C.c_int, [_P, _I64P, _I64P, _I64P]),
+    ("lm_layout_copy", C.c_int, [_P, _P, _I64, _P, _I64, _P]),
+    ("lm_plan_launches", C.c_int, [_P, _IP]),
+    ("lm_layout_eval_device", C.c_int, [_P, _P, C.c_int, _I64, _P]),
+    ("lm_plan_destroy", None, [_P]),
+    ("lm_status_string", C.c_char_p, [C.c_int]),
+    ("lm_last_cuda_error", C.c_int, []),
+    ("lm_version", C.c_char_p, []),
+]
+
+_lib = None
+
+
+def lib() -> C.CDLL:
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'` "
+                "(no CPU fallback exists)")
+        handle = C.CDLL(LIB_PATH)
+        for name, res, args in SIGNATURES:
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+class LayoutMoveError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        name = STATUS.get(status, str(status))
+        extra = ""
+        if status == -8:
+            extra = f" (cudaError {lib().lm_last_cuda_error()})"
+        super().__init__(f"{what}: {name}{extra}")
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != 0:
+        raise LayoutMoveError(rc, what)
+
+
+def _i64s(vals: Sequence[int]):
+    return (C.c_int64 * max(len(vals), 1))(*vals)
+
+
+def _fmt(x) -> str:
+    if isinstance(x, int):
+        return str(x)
+    return "(" + ",".join(_fmt(k) for k in x) + ")"
+
+
+class Layout:
+    """A layout handle: shape:stride with nested modes, optionally swizzled."""
+
+    __slots__ = ("_h",)
+
+    def __init__(self, handle):
+        if not handle:
+            raise ValueError("null layout handle")
+        self._h = C.c_void_p(handle)
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h and _lib is not None:
+            _lib.lm_layout_destroy(h)
+            self._h = None
+
+    @property
+    def handle(self):
+        return self._h
+
+    # -- construction ---------------------------------------------------
+    @classmethod
+    def parse(cls, text: str) -> "Layout":
+        out = C.c_void_p()
+        _check(lib().lm_layout_parse(text.encode(), C.byref(out)),
+               f"lm_layout_parse({text!r})")
+        return cls(out.value)
+
+    @classmethod
+    def of(cls, shape, stride) -> "Layout":
+        """From nested Python tuples, e.g. Layout.of((4, 2), (2, 1))."""
+        return cls.parse(f"{_fmt(shape)}:{_fmt(stride)}")
+
+    @classmethod
+    def make(cls, shape: Sequence[int], stride: Sequence[int],
+             leaves_per_mode: Sequence[int] | None = None) -> "Layout":
+        out = C.c_void_p()
+        n = len(shape)
+        lpm = list(leaves_per_mode) if leaves_per_mode is not None else []
+        arr = (C.c_int * max(len(lpm), 1))(*lpm)
+        _check(lib().lm_layout_make(n, _i64s(shape), _i64s(stride), len(lpm),
+                                    arr, C.byref(out)), "lm_layout_make")
+        return cls(out.value)
+
+    @classmethod
+    def stripmined(cls, threads: int, pitch: int, strips: int,
+                   k_row: int) -> "Layout":
+        out = C.c_void_p()
+        _check(lib().lm_layout_stripmined(threads, pitch, strips, k_row,
+                                          C.byref(out)), "lm_layout_stripmined")
+        return cls(out.value)
+
+    # -- inspection -----------------------------------------------------
+    def __str__(self) -> str:
+        cap = 256
+        while True:
+            buf = C.create_string_buffer(cap)
+            rc = lib().lm_layout_to_string(self._h, buf, cap)
+            if rc == -11:
+                cap *= 4
+                continue
+            _check(rc, "lm_layout_to_string")
+            return buf.value.decode()
+
+    __repr__ = __str__
+
+    @property
+    def size(self) -> int:
+        v = C.c_int64()
+        _check(lib().lm_layout_size(self._h, C.byref(v)), "lm_layout_size")
+        return v.value
+
+    @property
+    def cosize(self) -> int:
+        v = C.c_int64()
+        _check(lib().lm_layout_cosize(self._h, C.byref(v)), "lm_layout_cosize")
+        return v.value
+
+    def leaves(self) -> tuple[list[int], list[int], list[int]]:
+        nm, nl = C.c_int(), C.c_int()
+        _check(lib().lm_layout_rank(self._h, C.byref(nm), C.byref(nl)),
+               "lm_layout_rank")
+        sh = (C.c_int64 * max(nl.value, 1))()
+        st = (C.c_int64 * max(nl.value, 1))()
+        lpm = (C.c_int * max(nm.value, 1))()
+        _check(lib().lm_layout_leaves(self._h, sh, st, lpm), "lm_layout_leaves")
+        return (list(sh)[:nl.value], list(st)[:nl.value], list(lpm)[:nm.value])
+
+    @property
+    def swizzle_params(self) -> tuple[int, int, int]:
+        b, m, s = C.c_int(), C.c_int(), C.c_int()
+        _check(lib().lm_layout_get_swizzle(self._h, C.byref(b), C.byref(m),
+                                           C.byref(s)), "lm_layout_get_swizzle")
+        return b.value, m.value, s.value
+
+    def __call__(self, index: int) -> int:
+        v = C.c_int64()
+        _check(lib().lm_layout_eval(self._h, int(index), C.byref(v)),
+               "lm_layout_eval")
+        return v.value
+
+    def eval_coord(self, coord: Sequence[int]) -> int:
+        v = C.c_int64()
+        _check(lib().lm_layout_eval_coord(self._h, len(coord), _i64s(coord),
+                                          C.byref(v)), "lm_layout_eval_coord")
+        return v.value
+
+    # -- algebra --------------------------------------------------------
+    def _binary(self, fn, other, what) -> "Layout":
+        out = C.c_void_p()
+        _check(fn(self._h, other._h, C.byref(out)), what)
+        return Layout(out.value)
+
+    def compose(self, inner: "Layout") -> "Layout":
+        """self o inner."""
+        return self._binary(lib().lm_layout_compose, inner, "lm_layout_compose")
+
+    def concat(self, other: "Layout") -> "Layout":
+        return self._binary(lib().lm_layout_concat, other, "lm_layout_concat")
+
+    def zipped_divide(self, tiler: Sequence[int]) -> "Layout":
+        out = C.c_void_p()
+        _check(lib().lm_layout_zipped_divide(self._h, len(tiler), _i64s(tiler),
+                                             C.byref(out)),
+               "lm_layout_zipped_divide")
+        return Layout(out.value)
+
+    def swizzle(self, b: int, m: int, s: int) -> "Layout":
+        out = C.c_void_p()
+        _check(lib().lm_layout_swizzle(self._h, b, m, s, C.byref(out)),
+               "lm_layout_swizzle")
+        return Layout(out.value)
+
+    def coalesce(self) -> "Layout":
+        out = C.c_void_p()
+        _check(lib().lm_layout_coalesce(self._h, C.byref(out)),
+               "lm_layout_coalesce")
+        return Layout(out.value)
+
+    def right_inverse(self) -> "Layout":
+        out = C.c_void_p()
+        _check(lib().lm_layout_right_inverse(self._h, C.byref(out)),
+               "lm_layout_right_inverse")
+        return Layout(out.value)
+
+    def max_common_vector(self, other: "Layout") -> int:
+        v = C.c_int64()
+        _check(lib().lm_layout_max_common_vector(self._h, other._h,
+                                                 C.byref(v)),
+               "lm_layout_max_common_vector")
+        return v.value
+
+
+class Plan:
+    """A lowered copy plan for out[dst(i)] = in[src(i)]."""
+
+    __slots__ = ("_h", "elem_bytes")
+
+    def __init__(self, src: Layout, dst: Layout, elem_bytes: int):
+        out = C.c_void_p()
+        _check(lib().lm_plan_copy(src.handle, dst.handle, int(elem_bytes),
+                                  C.byref(out)), "lm_plan_copy")
+        self._h = out
+        self.elem_bytes = int(elem_bytes)
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h and _lib is not None:
+            _lib.lm_plan_destroy(h)
+            self._h = None
+
+    @property
+    def handle(self):
+        return self._h
+
+    def describe(self) -> dict:
+        cap = 4096
+        while True:
+            buf = C.create_string_buffer(cap)
+            rc = lib().lm_plan_describe(self._h, buf, cap)
+            if rc == -11:
+                cap *= 4
+                continue
+            _check(rc, "lm_plan_describe")
+            return json.loads(buf.value.decode())
+
+    def extent(self) -> tuple[int, int, int]:
+        n, sc, dc = C.c_int64(), C.c_int64(), C.c_int64()
+        _check(lib().lm_plan_extent(self._h, C.byref(n), C.byref(sc),
+                                    C.byref(dc)), "lm_plan_extent")
+        return n.value, sc.value, dc.value
+
+    @property
+    def launches(self) -> int:
+        v = C.c_int()
+        _check(lib().lm_plan_launches(self._h, C.byref(v)), "lm_plan_launches")
+        return v.value
+
+
+def _stream_handle(stream) -> C.c_void_p:
+    if stream is None:
+        import torch
+        return C.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return C.c_void_p(stream)
+    return C.c_void_p(stream.cuda_stream)
+
+
+def _dev_buffer(t, elem_bytes: int) -> tuple[int, int]:
+    """(device pointer, capacity in elements) of a CUDA tensor."""
+    if not t.is_cuda:
+        raise ValueError("layout_copy takes CUDA tensors")
+    if not t.is_contiguous():
+        raise ValueError("buffers must be contiguous")
+    nbytes = t.numel() * t.element_size()
+    return t.data_ptr(), nbytes // elem_bytes
+
+
+def layout_copy(plan: Plan, src, dst, stream=None) -> None:
+    """Enqueue dst[dst_layout(i)] = src[src_layout(i)] on ``stream`` (default:
+    torch's current stream).  src/dst are contiguous CUDA tensors viewed as
+    flat arrays of plan.elem_bytes-byte elements."""
+    sp, scap = _dev_buffer(src, plan.elem_bytes)
+    dp, dcap = _dev_buffer(dst, plan.elem_bytes)
+    _check(lib().lm_layout_copy(plan.handle, C.c_void_p(sp), scap,
+                                C.c_void_p(dp), dcap, _stream_handle(stream)),
+           "lm_layout_copy")
+
+
+def layout_copy_ptr(plan: Plan, src_ptr: int, src_cap: int, dst_ptr: int,
+                    dst_cap: int, stream=None) -> None:
+    """Raw-pointer form of layout_copy (capacities in elements)."""
+    _check(lib().lm_layout_copy(plan.handle, C.c_void_p(src_ptr), src_cap,
+                                C.c_void_p(dst_ptr), dst_cap,
+                                _stream_handle(stream)), "lm_layout_copy")
+
+
+def layout_eval_device(layout: Layout, table, stream=None) -> None:
+    """Enqueue table[i] = layout(i) into an int32 or int64 CUDA tensor."""
+    import torch
+    if table.dtype not in (torch.int32, torch.int64) or not table.is_cuda:
+        raise ValueError("table must be a CUDA int32 or int64 tensor")
+    _check(lib().lm_layout_eval_device(layout.handle,
+                                       C.c_void_p(table.data_ptr()),
+                                       table.element_size(), table.numel(),
+                                       _stream_handle(stream)),
+           "lm_layout_eval_device")
+
+
+def build_layout(spec) -> Layout:
+    """A layout from a workload description (see ``workloads``), built with
+    the library's own algebra calls."""
+    kind = spec[0]
+    if kind == "layout":
+        return Layout.of(spec[1], spec[2])
+    if kind == "swizzle":
+        return build_layout(spec[4]).swizzle(spec[1], spec[2], spec[3])
+    if kind == "compose":
+        return build_layout(spec[1]).compose(build_layout(spec[2]))
+    if kind == "zipped_divide":
+        return build_layout(spec[1]).zipped_divide(list(spec[2]))
+    if kind == "concat":
+        parts: Iterable = [build_layout(s) for s in spec[1:]]
+        it = iter(parts)
+        acc = next(it)
+        for p in it:
+            acc = acc.concat(p)
+        return acc
+    raise ValueError(f"unknown layout description {kind!r}")

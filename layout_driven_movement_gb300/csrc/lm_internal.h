@@ -1,0 +1,256 @@
+// Internal data structures of the layoutmove library: the layout tree, the
+// lowered copy plan, and the plain-old-data argument blocks handed to the
+// CUDA kernels.  Included by the host C++ files and by the .cu file.
+#pragma once
+
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "layoutmove.h"
+
+#if defined(__CUDACC__)
+#define LM_HD __host__ __device__ __forceinline__
+#else
+#define LM_HD inline
+#endif
+
+namespace lm {
+
+// ---------------------------------------------------------------------------
+// Status handling: every internal failure throws Error(status); the C ABI
+// catches it and returns the code.
+// ---------------------------------------------------------------------------
+struct Error {
+  int status;
+  explicit Error(int s) : status(s) {}
+};
+
+[[noreturn]] inline void fail(int status) { throw Error(status); }
+
+inline int64_t mul_chk(int64_t a, int64_t b) {
+  int64_t r;
+  if (__builtin_mul_overflow(a, b, &r)) fail(LM_E_OVERFLOW);
+  return r;
+}
+inline int64_t add_chk(int64_t a, int64_t b) {
+  int64_t r;
+  if (__builtin_add_overflow(a, b, &r)) fail(LM_E_OVERFLOW);
+  return r;
+}
+
+// ---------------------------------------------------------------------------
+// Swizzle<B,M,S>: o ^ ((o >> S) & ((2^B - 1) << M)).
+// ---------------------------------------------------------------------------
+struct Swz {
+  int32_t b = 0, m = 0, s = 0;
+  LM_HD bool on() const { return b > 0; }
+  LM_HD int64_t apply(int64_t o) const {
+    return b > 0 ? (o ^ ((o >> s) & (((int64_t(1) << b) - 1) << m))) : o;
+  }
+};
+
+// ---------------------------------------------------------------------------
+// Layout tree.  A node is a leaf (extent:stride) or a tuple of nodes.
+// ---------------------------------------------------------------------------
+struct Node {
+  bool leaf = true;
+  int64_t shape = 1;
+  int64_t stride = 0;
+  std::vector<Node> kids;
+
+  static Node make_leaf(int64_t e, int64_t d) {
+    Node n;
+    n.leaf = true;
+    n.shape = e;
+    n.stride = d;
+    return n;
+  }
+  static Node make_tuple(std::vector<Node> k) {
+    Node n;
+    n.leaf = false;
+    n.kids = std::move(k);
+    return n;
+  }
+};
+
+struct Leaf {
+  int64_t e;  // extent
+  int64_t d;  // stride (elements)
+};
+
+}  // namespace lm
+
+// The opaque handle of the C ABI.
+struct lm_layout {
+  lm::Node root;   // a leaf (integer layout) or a tuple of top-level modes
+  lm::Swz swz;     // swizzle on the whole offset (b == 0: none)
+  // derived, filled by finalize()
+  std::vector<lm::Leaf> leaves;    // flattened, colex order
+  std::vector<int> mode_leaves;    // leaves per top-level mode
+  int64_t size = 1;
+  int64_t cosize = 1;              // see lm_layout_cosize
+};
+
+namespace lm {
+
+void finalize(lm_layout& L);                  // fills the derived fields
+std::vector<Leaf> flatten(const Node& n);
+std::vector<Node> top_modes(const lm_layout& L);
+int64_t eval_affine(const std::vector<Leaf>& leaves, int64_t idx);
+std::string to_string(const lm_layout& L);
+std::vector<Leaf> coalesce_leaves(const std::vector<Leaf>& leaves);
+bool affine_injective(std::vector<Leaf> leaves);
+
+// ---------------------------------------------------------------------------
+// Fast division by an invariant 32-bit divisor: Granlund & Montgomery,
+// "Division by invariant integers using multiplication" (PLDI 1994), the
+// round-up method of their Figure 4.1.  For 1 <= d < 2^31 and any 32-bit n:
+//   l = ceil(log2 d), m = floor(2^32 (2^l - d) / d) + 1,
+//   t = mulhi(m, n), q = (t + ((n - t) >> min(l,1))) >> max(l-1, 0).
+// ---------------------------------------------------------------------------
+struct FastDiv {
+  uint32_t d = 1, m = 1, s1 = 0, s2 = 0;
+};
+
+inline FastDiv make_fastdiv(uint32_t d) {
+  FastDiv f;
+  if (d == 0) fail(LM_E_INVALID);
+  uint32_t l = 0;
+  while ((uint64_t(1) << l) < d) ++l;
+  f.d = d;
+  f.m = uint32_t(((uint64_t(1) << 32) * ((uint64_t(1) << l) - d)) / d + 1);
+  f.s1 = l > 0 ? 1u : 0u;
+  f.s2 = l > 0 ? l - 1 : 0u;
+  return f;
+}
+
+#if defined(__CUDACC__)
+__device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv& f) {
+  uint32_t t = __umulhi(f.m, n);
+  return (t + ((n - t) >> f.s1)) >> f.s2;
+}
+#endif
+inline uint32_t fdiv_host(uint32_t n, const FastDiv& f) {
+  uint32_t t = uint32_t((uint64_t(f.m) * n) >> 32);
+  return (t + ((n - t) >> f.s1)) >> f.s2;
+}
+
+// ---------------------------------------------------------------------------
+// Kernel argument blocks (passed by value; everything in BYTES unless noted).
+// ---------------------------------------------------------------------------
+constexpr int kMaxModes = 8;    // joint modes of a piece after coalescing
+constexpr int kMaxLeaves = 16;  // leaves of one side (GENERIC over own leaves)
+constexpr int kMaxTile = 6;     // modes of a staged tile per role
+
+struct GenericArgs {
+  uint64_t n = 0;            // elements in the piece
+  int32_t ns = 0, nd = 0;    // leaves per side
+  int32_t eb = 1;            // element bytes moved per element (1..16)
+  int32_t wide = 0;          // 1 if n >= 2^32 (64-bit index arithmetic)
+  uint32_t s_ext[kMaxLeaves], d_ext[kMaxLeaves];
+  FastDiv s_div[kMaxLeaves], d_div[kMaxLeaves];
+  int64_t s_str[kMaxLeaves], d_str[kMaxLeaves];  // bytes per coordinate step
+  int64_t s_ext64[kMaxLeaves], d_ext64[kMaxLeaves];
+  int64_t s_base = 0, d_base = 0;                // bytes
+  Swz s_swz, d_swz;                              // in bytes
+};
+
+struct VecArgs {
+  uint32_t n_vec = 0;        // vectors in the piece
+  int32_t nm = 0;            // modes; mode 0 counts vectors along the run
+  uint32_t ext[kMaxModes];
+  FastDiv div[kMaxModes];
+  int64_t s[kMaxModes], d[kMaxModes];   // bytes per coordinate step
+  int64_t s_base = 0, d_base = 0;       // bytes
+  Swz s_swz, d_swz;                     // in bytes
+};
+
+struct StagedArgs {
+  // tiles: colex over the grid modes
+  uint32_t n_tiles = 0;
+  int32_t ng = 0;
+  uint32_t g_ext[kMaxModes];
+  FastDiv g_pre[kMaxModes];             // division by the product of faster
+  FastDiv g_div[kMaxModes];             //   grid extents, then by the extent
+  int64_t g_s[kMaxModes], g_d[kMaxModes];
+  int64_t s_base = 0, d_base = 0;
+  Swz s_swz, d_swz;                     // global swizzles, bytes
+  // load side: n_seg segments (colex over the src-outer tile modes), each
+  // cps 16-byte chunks long
+  uint32_t n_lchunks = 0, cps = 1;
+  FastDiv cps_div;
+  int32_t nso = 0;
+  uint32_t so_ext[kMaxTile];
+  FastDiv so_div[kMaxTile];
+  int64_t so_s[kMaxTile];               // src bytes per segment coordinate
+  uint32_t so_m[kMaxTile];              // smem bytes per segment coordinate
+  // store side: n_dout spans (colex over the dst-outer tile modes), each cpd
+  // 16-byte chunks of dst-contiguous elements
+  uint32_t n_schunks = 0, cpd = 1;
+  FastDiv cpd_div;
+  int32_t ndo = 0;
+  uint32_t do_ext[kMaxTile];
+  FastDiv do_div[kMaxTile];
+  int64_t do_d[kMaxTile];               // dst bytes per span coordinate
+  uint32_t do_m[kMaxTile];              // smem bytes per span coordinate
+  int32_t ndi = 0;                      // dst-inner modes, dst order
+  uint32_t di_ext[kMaxTile];
+  FastDiv di_div[kMaxTile];
+  uint32_t di_m[kMaxTile];              // smem bytes per coordinate
+  // shared memory
+  uint32_t stage_bytes = 0;
+  Swz m_swz;                            // smem swizzle, bytes
+};
+
+struct EvalArgs {
+  uint64_t n = 0;
+  int32_t nl = 0;
+  int32_t wide = 0;
+  uint32_t ext[kMaxLeaves];
+  FastDiv div[kMaxLeaves];
+  int64_t ext64[kMaxLeaves];
+  int64_t str[kMaxLeaves];              // elements
+  Swz swz;                              // elements
+};
+
+// ---------------------------------------------------------------------------
+// The lowered plan.
+// ---------------------------------------------------------------------------
+enum Path : int { PATH_GENERIC = 0, PATH_VEC = 1, PATH_STAGED = 2 };
+
+struct JMode {
+  int64_t e, s, d;  // extent, src stride, dst stride (elements)
+};
+
+struct Piece {
+  Path path = PATH_GENERIC;
+  std::vector<JMode> modes;  // joint modes (empty for the non-joint case)
+  int64_t s_base = 0, d_base = 0;  // elements
+  int vec_bytes = 0;               // VEC: bytes per vector
+  int64_t tile_elems = 0;          // STAGED: elements per tile
+  GenericArgs gen;                 // always filled (fallback)
+  VecArgs vec;
+  StagedArgs st;
+  int64_t bank_cost = 0, bank_ideal = 0;  // STAGED: simulated smem wavefronts
+};
+
+}  // namespace lm
+
+struct lm_plan {
+  int eb = 1;
+  int64_t size = 0, src_cosize = 0, dst_cosize = 0;
+  lm::Swz s_swz, d_swz;  // elements
+  bool joint = true;
+  std::vector<lm::Piece> pieces;
+  std::string describe;
+};
+
+namespace lm {
+// implemented in lm_kernels.cu
+int launch_piece(const lm_plan& plan, const Piece& pc, const char* src,
+                 int64_t src_cap_bytes, char* dst, void* stream);
+int launch_eval(const lm_layout& L, void* table, int offset_bytes,
+                void* stream);
+void set_cuda_error(int e);
+}  // namespace lm

@@ -1,0 +1,653 @@
+// sm_103a kernels of the layoutmove library and the ABI entry points that
+// enqueue them.
+//
+//  layout_eval  : table[i] = L(i)                        (one offset/thread)
+//  GENERIC copy : out[dst(i)] = in[src(i)], one element per thread, each
+//                 side's offset from its own leaves
+//  VEC copy     : the same over 16-byte vectors along the run both sides
+//                 share (the common vector of the inverse layouts,
+//                 "CUTE布局代数" §2.3)
+//  STAGED copy  : tiles staged through shared memory -- 16-byte cp.async
+//                 loads along the source's contiguous modes into an
+//                 XOR-swizzled shared-memory image, double-buffered across
+//                 tiles ("CUTE布局代数" §5.2), then per-element gathers into
+//                 16-byte stores along the destination's contiguous modes.
+//                 The thread -> chunk map is pitch-linear over the tile's
+//                 chunks (the PitchLinearStripminedThreadMap article §1.2:
+//                 adjacent threads take adjacent 16-byte chunks), so every
+//                 warp-wide load and store covers whole 128-byte lines.
+//
+// No tensor cores: the work is pure data movement.
+
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+
+#include "lm_internal.h"
+
+namespace lm {
+
+namespace {
+thread_local int g_last_cuda = 0;
+}
+void set_cuda_error(int e) { g_last_cuda = e; }
+
+// ---------------------------------------------------------------------------
+// device helpers
+// ---------------------------------------------------------------------------
+
+template <int B>
+struct VecT;
+template <>
+struct VecT<16> {
+  using T = uint4;
+};
+template <>
+struct VecT<8> {
+  using T = uint2;
+};
+template <>
+struct VecT<4> {
+  using T = uint32_t;
+};
+template <>
+struct VecT<2> {
+  using T = uint16_t;
+};
+template <>
+struct VecT<1> {
+  using T = uint8_t;
+};
+
+__device__ __forceinline__ int64_t swz_apply(const Swz& z, int64_t o) {
+  return z.b > 0 ? (o ^ ((o >> z.s) & (((int64_t(1) << z.b) - 1) << z.m))) : o;
+}
+
+__device__ __forceinline__ uint32_t swz_apply32(const Swz& z, uint32_t o) {
+  return z.b > 0 ? (o ^ ((o >> z.s) & (((1u << z.b) - 1u) << z.m))) : o;
+}
+
+// offset (bytes) of a 32-bit colex index over one side's leaves
+__device__ __forceinline__ int64_t side_offset32(uint32_t q, int n,
+                                                 const uint32_t* ext,
+                                                 const FastDiv* div,
+                                                 const int64_t* str) {
+  int64_t off = 0;
+#pragma unroll
+  for (int k = 0; k < kMaxLeaves; ++k) {
+    if (k >= n) break;
+    const uint32_t qn = fdiv(q, div[k]);
+    off += int64_t(q - qn * ext[k]) * str[k];
+    q = qn;
+  }
+  return off;
+}
+
+__device__ __forceinline__ int64_t side_offset64(uint64_t q, int n,
+                                                 const int64_t* ext,
+                                                 const int64_t* str) {
+  int64_t off = 0;
+  for (int k = 0; k < n; ++k) {
+    const uint64_t e = uint64_t(ext[k]);
+    off += int64_t(q % e) * str[k];
+    q /= e;
+  }
+  return off;
+}
+
+// ---------------------------------------------------------------------------
+// layout_eval
+// ---------------------------------------------------------------------------
+
+template <typename OUT>
+__global__ void __launch_bounds__(256)
+    lm_eval_kernel(const __grid_constant__ EvalArgs a, OUT* __restrict__ table) {
+  const uint64_t stride = uint64_t(gridDim.x) * blockDim.x;
+  for (uint64_t i = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < a.n;
+       i += stride) {
+    int64_t off;
+    if (a.wide) {
+      off = side_offset64(i, a.nl, a.ext64, a.str);
+    } else {
+      off = side_offset32(uint32_t(i), a.nl, a.ext, a.div, a.str);
+    }
+    table[i] = OUT(swz_apply(a.swz, off));
+  }
+}
+
+// ---------------------------------------------------------------------------
+// GENERIC copy
+// ---------------------------------------------------------------------------
+
+template <int EB>
+__global__ void __launch_bounds__(256)
+    lm_generic_kernel(const __grid_constant__ GenericArgs a,
+                      const char* __restrict__ src, char* __restrict__ dst) {
+  using T = typename VecT<EB>::T;
+  const uint64_t stride = uint64_t(gridDim.x) * blockDim.x;
+  for (uint64_t i = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < a.n;
+       i += stride) {
+    int64_t so, dof;
+    if (a.wide) {
+      so = side_offset64(i, a.ns, a.s_ext64, a.s_str);
+      dof = side_offset64(i, a.nd, a.d_ext64, a.d_str);
+    } else {
+      so = side_offset32(uint32_t(i), a.ns, a.s_ext, a.s_div, a.s_str);
+      dof = side_offset32(uint32_t(i), a.nd, a.d_ext, a.d_div, a.d_str);
+    }
+    so = swz_apply(a.s_swz, a.s_base + so);
+    dof = swz_apply(a.d_swz, a.d_base + dof);
+    *reinterpret_cast<T*>(dst + dof) =
+        *reinterpret_cast<const T*>(src + so);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// VEC copy: 16-byte (or narrower) vectors along the shared run
+// ---------------------------------------------------------------------------
+
+constexpr int kVecUnroll = 4;
+
+template <int VB>
+__global__ void __launch_bounds__(256)
+    lm_vec_kernel(const __grid_constant__ VecArgs a,
+                  const char* __restrict__ src, char* __restrict__ dst) {
+  using T = typename VecT<VB>::T;
+  const uint64_t nthreads = uint64_t(gridDim.x) * blockDim.x;
+  for (uint64_t q0 = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+       q0 < a.n_vec; q0 += kVecUnroll * nthreads) {
+    T v[kVecUnroll];
+    int64_t doff[kVecUnroll];
+#pragma unroll
+    for (int u = 0; u < kVecUnroll; ++u) {
+      const uint64_t q64 = q0 + u * nthreads;
+      doff[u] = -1;
+      if (q64 < a.n_vec) {
+        uint32_t q = uint32_t(q64);
+        int64_t s = a.s_base, d = a.d_base;
+#pragma unroll
+        for (int k = 0; k < kMaxModes; ++k) {
+          if (k >= a.nm) break;
+          const uint32_t qn = fdiv(q, a.div[k]);
+          const int64_t c = int64_t(q - qn * a.ext[k]);
+          s += c * a.s[k];
+          d += c * a.d[k];
+          q = qn;
+        }
+        s = swz_apply(a.s_swz, s);
+        doff[u] = swz_apply(a.d_swz, d);
+        v[u] = __ldcs(reinterpret_cast<const T*>(src + s));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kVecUnroll; ++u)
+      if (doff[u] >= 0) __stcs(reinterpret_cast<T*>(dst + doff[u]), v[u]);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// STAGED copy
+// ---------------------------------------------------------------------------
+
+constexpr int kStagedThreads = 256;
+constexpr int kMaxLoadSlots = 8;
+
+template <int EB>
+struct StagedTraits {
+  static constexpr int V = 16 / EB;  // elements per 16-byte chunk
+  static constexpr int MaxStore = (32 / V) < 8 ? ((32 / V) > 0 ? 32 / V : 1) : 8;
+  static constexpr int Packed = (V + 1) / 2;  // 16-bit smem addresses, 2/reg
+};
+
+__device__ __forceinline__ void cp_async16(uint32_t smem_addr, const void* g,
+                                           int src_bytes) {
+  asm volatile(
+      "cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_addr),
+      "l"(g), "r"(src_bytes)
+      : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+// Tile origin offsets (bytes).  Lane k of each group of 8 lanes computes
+// grid coordinate k in parallel (tile / product-of-faster-extents, mod the
+// extent); a 3-step butterfly of warp shuffles sums the contributions, so
+// every lane of the warp ends with both totals.
+__device__ __forceinline__ void tile_base(const StagedArgs& a, uint32_t tile,
+                                          int64_t& sb, int64_t& db) {
+  const int k = threadIdx.x & 7;
+  int64_t s = 0, d = 0;
+  if (k < a.ng) {
+    uint32_t c = fdiv(tile, a.g_pre[k]);
+    c -= fdiv(c, a.g_div[k]) * a.g_ext[k];
+    s = int64_t(c) * a.g_s[k];
+    d = int64_t(c) * a.g_d[k];
+  }
+#pragma unroll
+  for (int off = 4; off > 0; off >>= 1) {
+    s += __shfl_xor_sync(0xffffffffu, s, off);
+    d += __shfl_xor_sync(0xffffffffu, d, off);
+  }
+  sb = s;
+  db = d;
+}
+
+template <int EB>
+__device__ __forceinline__ uint4 gather16(const unsigned char* sm,
+                                          const uint32_t* packed) {
+  constexpr int V = StagedTraits<EB>::V;
+  auto addr = [&](int e) -> uint32_t {
+    return (packed[e >> 1] >> ((e & 1) * 16)) & 0xffffu;
+  };
+  uint4 r;
+  uint32_t w[4];
+  if constexpr (EB == 16) {
+    r = *reinterpret_cast<const uint4*>(sm + addr(0));
+    return r;
+  } else if constexpr (EB == 8) {
+    const uint2 x = *reinterpret_cast<const uint2*>(sm + addr(0));
+    const uint2 y = *reinterpret_cast<const uint2*>(sm + addr(1));
+    w[0] = x.x;
+    w[1] = x.y;
+    w[2] = y.x;
+    w[3] = y.y;
+  } else if constexpr (EB == 4) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      w[e] = *reinterpret_cast<const uint32_t*>(sm + addr(e));
+  } else if constexpr (EB == 2) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t lo = *reinterpret_cast<const uint16_t*>(sm + addr(2 * i));
+      const uint32_t hi =
+          *reinterpret_cast<const uint16_t*>(sm + addr(2 * i + 1));
+      w[i] = lo | (hi << 16);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t b0 = sm[addr(4 * i)];
+      const uint32_t b1 = sm[addr(4 * i + 1)];
+      const uint32_t b2 = sm[addr(4 * i + 2)];
+      const uint32_t b3 = sm[addr(4 * i + 3)];
+      w[i] = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+    }
+  }
+  (void)V;
+  r.x = w[0];
+  r.y = w[1];
+  r.z = w[2];
+  r.w = w[3];
+  return r;
+}
+
+template <int EB>
+__global__ void __launch_bounds__(kStagedThreads)
+    lm_staged_kernel(const __grid_constant__ StagedArgs a,
+                     const char* __restrict__ src, char* __restrict__ dst,
+                     int64_t src_cap) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  using Tr = StagedTraits<EB>;
+  constexpr int V = Tr::V;
+  const uint32_t tid = threadIdx.x;
+  const uint32_t nt = blockDim.x;
+
+  // ---- per-thread slots, the same for every tile -----------------------
+  int32_t l_src[kMaxLoadSlots];
+  uint32_t l_sm[kMaxLoadSlots];
+#pragma unroll
+  for (int k = 0; k < kMaxLoadSlots; ++k) {
+    const uint32_t j = tid + uint32_t(k) * nt;
+    l_src[k] = -1;
+    l_sm[k] = 0;
+    if (j < a.n_lchunks) {
+      const uint32_t seg = fdiv(j, a.cps_div);
+      const uint32_t c = j - seg * a.cps;
+      int64_t srel = int64_t(c) * 16;
+      uint32_t mrel = c * 16u;
+      uint32_t r = seg;
+#pragma unroll
+      for (int t = 0; t < kMaxTile; ++t) {
+        if (t >= a.nso) break;
+        const uint32_t rn = fdiv(r, a.so_div[t]);
+        const uint32_t x = r - rn * a.so_ext[t];
+        srel += int64_t(x) * a.so_s[t];
+        mrel += x * a.so_m[t];
+        r = rn;
+      }
+      l_src[k] = int32_t(srel);
+      l_sm[k] = swz_apply32(a.m_swz, mrel);
+    }
+  }
+  int32_t s_dst[Tr::MaxStore];
+  uint32_t s_sm[Tr::MaxStore][Tr::Packed];
+#pragma unroll
+  for (int k = 0; k < Tr::MaxStore; ++k) {
+    const uint32_t j = tid + uint32_t(k) * nt;
+    s_dst[k] = -1;
+#pragma unroll
+    for (int i = 0; i < Tr::Packed; ++i) s_sm[k][i] = 0;
+    if (j < a.n_schunks) {
+      const uint32_t o = fdiv(j, a.cpd_div);
+      const uint32_t p = j - o * a.cpd;
+      int64_t drel = int64_t(p) * 16;
+      uint32_t mb = 0, r = o;
+#pragma unroll
+      for (int t = 0; t < kMaxTile; ++t) {
+        if (t >= a.ndo) break;
+        const uint32_t rn = fdiv(r, a.do_div[t]);
+        const uint32_t x = r - rn * a.do_ext[t];
+        drel += int64_t(x) * a.do_d[t];
+        mb += x * a.do_m[t];
+        r = rn;
+      }
+      s_dst[k] = int32_t(drel);
+#pragma unroll
+      for (int e = 0; e < V; ++e) {
+        uint32_t q = p * uint32_t(V) + uint32_t(e);
+        uint32_t m = mb;
+#pragma unroll
+        for (int t = 0; t < kMaxTile; ++t) {
+          if (t >= a.ndi) break;
+          const uint32_t qn = fdiv(q, a.di_div[t]);
+          m += (q - qn * a.di_ext[t]) * a.di_m[t];
+          q = qn;
+        }
+        m = swz_apply32(a.m_swz, m);
+        s_sm[k][e >> 1] |= (m & 0xffffu) << ((e & 1) * 16);
+      }
+    }
+  }
+
+  uint32_t tile = blockIdx.x;
+  if (tile >= a.n_tiles) return;
+  const uint32_t smem0 = uint32_t(__cvta_generic_to_shared(smem));
+
+  auto issue = [&](uint32_t t, int stage) {
+    int64_t sb, db;
+    tile_base(a, t, sb, db);
+    const int64_t base = a.s_base + sb;
+    const uint32_t sm_stage = smem0 + uint32_t(stage) * a.stage_bytes;
+#pragma unroll
+    for (int k = 0; k < kMaxLoadSlots; ++k) {
+      if (l_src[k] < 0) continue;
+      const int64_t off = swz_apply(a.s_swz, base + l_src[k]);
+      const int64_t room = src_cap - off;
+      const int nbytes = room >= 16 ? 16 : (room > 0 ? int(room) : 0);
+      cp_async16(sm_stage + l_sm[k], nbytes ? src + off : src, nbytes);
+    }
+  };
+
+  int stage = 0;
+  issue(tile, 0);
+  cp_async_commit();
+  for (;;) {
+    const uint64_t next64 = uint64_t(tile) + gridDim.x;
+    const bool has_next = next64 < a.n_tiles;
+    if (has_next) {
+      issue(uint32_t(next64), stage ^ 1);
+      cp_async_commit();
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+    int64_t sb, db;
+    tile_base(a, tile, sb, db);
+    const int64_t dbase = a.d_base + db;
+    const unsigned char* sm = smem + size_t(stage) * a.stage_bytes;
+#pragma unroll
+    for (int k = 0; k < Tr::MaxStore; ++k) {
+      if (s_dst[k] < 0) continue;
+      const uint4 v = gather16<EB>(sm, s_sm[k]);
+      const int64_t off = swz_apply(a.d_swz, dbase + s_dst[k]);
+      __stcs(reinterpret_cast<uint4*>(dst + off), v);
+    }
+    __syncthreads();
+    if (!has_next) break;
+    tile = uint32_t(next64);
+    stage ^= 1;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side: launches
+// ---------------------------------------------------------------------------
+
+struct DeviceInfo {
+  int sms = 0;
+};
+
+DeviceInfo device_info() {
+  static std::mutex mu;
+  static DeviceInfo cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return {148};
+  std::lock_guard<std::mutex> g(mu);
+  if (!cache[dev].sms) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev].sms = v > 0 ? v : 148;
+  }
+  return cache[dev];
+}
+
+int check_launch() {
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_cuda_error(int(e));
+    return LM_E_CUDA;
+  }
+  return LM_OK;
+}
+
+template <int EB>
+int launch_generic_t(const GenericArgs& g, const char* src, char* dst,
+                     cudaStream_t st) {
+  const DeviceInfo di = device_info();
+  const uint64_t want = (g.n + 255) / 256;
+  const uint64_t cap = uint64_t(di.sms) * 16;
+  const unsigned grid = unsigned(std::max<uint64_t>(1, std::min(want, cap)));
+  lm_generic_kernel<EB><<<grid, 256, 0, st>>>(g, src, dst);
+  return check_launch();
+}
+
+int launch_generic(const GenericArgs& g0, const char* src, char* dst,
+                   cudaStream_t st) {
+  const uintptr_t ps = reinterpret_cast<uintptr_t>(src);
+  const uintptr_t pd = reinterpret_cast<uintptr_t>(dst);
+  GenericArgs g = g0;
+  if ((ps | pd) % uintptr_t(g.eb)) {
+    // pointers aligned to less than an element: move bytes, with one more
+    // leaf (the byte inside the element) in front of each side
+    if (g.ns + 1 > kMaxLeaves || g.nd + 1 > kMaxLeaves) {
+      set_cuda_error(0);
+      return LM_E_INVALID;
+    }
+    auto shift = [&](uint32_t* ext, FastDiv* div, int64_t* str,
+                     int64_t* ext64, int32_t& n) {
+      for (int k = n; k > 0; --k) {
+        ext[k] = ext[k - 1];
+        div[k] = div[k - 1];
+        str[k] = str[k - 1];
+        ext64[k] = ext64[k - 1];
+      }
+      ext[0] = uint32_t(g.eb);
+      div[0] = make_fastdiv(uint32_t(g.eb));
+      str[0] = 1;
+      ext64[0] = g.eb;
+      ++n;
+    };
+    shift(g.s_ext, g.s_div, g.s_str, g.s_ext64, g.ns);
+    shift(g.d_ext, g.d_div, g.d_str, g.d_ext64, g.nd);
+    g.n *= uint64_t(g.eb);
+    if (g.n >= (uint64_t(1) << 31)) g.wide = 1;
+    g.eb = 1;
+  }
+  switch (g.eb) {
+    case 1: return launch_generic_t<1>(g, src, dst, st);
+    case 2: return launch_generic_t<2>(g, src, dst, st);
+    case 4: return launch_generic_t<4>(g, src, dst, st);
+    case 8: return launch_generic_t<8>(g, src, dst, st);
+    case 16: return launch_generic_t<16>(g, src, dst, st);
+    default: return LM_E_INVALID;
+  }
+}
+
+template <int VB>
+int launch_vec_t(const VecArgs& v, const char* src, char* dst,
+                 cudaStream_t st) {
+  const DeviceInfo di = device_info();
+  const uint64_t want = (uint64_t(v.n_vec) + 256 * kVecUnroll - 1) /
+                        (256 * kVecUnroll);
+  const uint64_t cap = uint64_t(di.sms) * 8;
+  const unsigned grid = unsigned(std::max<uint64_t>(1, std::min(want, cap)));
+  lm_vec_kernel<VB><<<grid, 256, 0, st>>>(v, src, dst);
+  return check_launch();
+}
+
+template <int EB>
+int launch_staged_t(const StagedArgs& a, const char* src, int64_t src_cap,
+                    char* dst, cudaStream_t st) {
+  // two stages of at most 24 KiB each: within the default 48 KiB of
+  // dynamic shared memory, so no per-device attribute is needed
+  const int smem = int(2 * a.stage_bytes);
+  const DeviceInfo di = device_info();
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+          &per_sm, lm_staged_kernel<EB>, kStagedThreads, size_t(smem)) !=
+          cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  const uint64_t cap = uint64_t(di.sms) * uint64_t(per_sm);
+  const unsigned grid =
+      unsigned(std::max<uint64_t>(1, std::min<uint64_t>(a.n_tiles, cap)));
+  lm_staged_kernel<EB><<<grid, kStagedThreads, size_t(smem), st>>>(
+      a, src, dst, src_cap);
+  return check_launch();
+}
+
+int launch_piece(const lm_plan& P, const Piece& pc, const char* src,
+                 int64_t src_cap_bytes, char* dst, void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const uintptr_t ps = reinterpret_cast<uintptr_t>(src);
+  const uintptr_t pd = reinterpret_cast<uintptr_t>(dst);
+  if (pc.path == PATH_VEC && ((ps | pd) % uintptr_t(pc.vec_bytes)) == 0) {
+    switch (pc.vec_bytes) {
+      case 16: return launch_vec_t<16>(pc.vec, src, dst, st);
+      case 8: return launch_vec_t<8>(pc.vec, src, dst, st);
+      case 4: return launch_vec_t<4>(pc.vec, src, dst, st);
+      default: break;
+    }
+  }
+  if (pc.path == PATH_STAGED && ((ps | pd) % 16) == 0) {
+    switch (P.eb) {
+      case 1: return launch_staged_t<1>(pc.st, src, src_cap_bytes, dst, st);
+      case 2: return launch_staged_t<2>(pc.st, src, src_cap_bytes, dst, st);
+      case 4: return launch_staged_t<4>(pc.st, src, src_cap_bytes, dst, st);
+      case 8: return launch_staged_t<8>(pc.st, src, src_cap_bytes, dst, st);
+      case 16: return launch_staged_t<16>(pc.st, src, src_cap_bytes, dst, st);
+      default: break;
+    }
+  }
+  return launch_generic(pc.gen, src, dst, st);
+}
+
+int launch_eval(const lm_layout& L, void* table, int offset_bytes,
+                void* stream) {
+  EvalArgs a;
+  a.n = uint64_t(L.size);
+  std::vector<Leaf> c = coalesce_leaves(L.leaves);
+  if (c.size() > size_t(kMaxLeaves)) return LM_E_NOT_REPRESENTABLE;
+  a.nl = int32_t(c.size());
+  a.wide = L.size >= (int64_t(1) << 31) ? 1 : 0;
+  for (size_t k = 0; k < c.size(); ++k) {
+    a.ext64[k] = c[k].e;
+    if (c[k].e >= (int64_t(1) << 31)) a.wide = 1;
+    a.ext[k] = uint32_t(std::min<int64_t>(c[k].e, 0x7fffffff));
+    a.div[k] = make_fastdiv(a.ext[k] ? a.ext[k] : 1u);
+    a.str[k] = c[k].d;
+  }
+  a.swz = L.swz;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const DeviceInfo di = device_info();
+  const uint64_t want = (a.n + 255) / 256;
+  const unsigned grid = unsigned(
+      std::max<uint64_t>(1, std::min<uint64_t>(want, uint64_t(di.sms) * 16)));
+  if (offset_bytes == 4)
+    lm_eval_kernel<int32_t>
+        <<<grid, 256, 0, st>>>(a, static_cast<int32_t*>(table));
+  else
+    lm_eval_kernel<int64_t>
+        <<<grid, 256, 0, st>>>(a, static_cast<int64_t*>(table));
+  return check_launch();
+}
+
+}  // namespace lm
+
+// ===========================================================================
+// C ABI: device work
+// ===========================================================================
+
+extern "C" {
+
+int lm_layout_copy(const lm_plan* plan, const void* src_dev,
+                   int64_t src_capacity_elems, void* dst_dev,
+                   int64_t dst_capacity_elems, void* cuda_stream) {
+  try {
+    if (!plan) return LM_E_INVALID;
+    if (plan->size == 0) return LM_OK;
+    if (!src_dev || !dst_dev) return LM_E_INVALID;
+    if (src_capacity_elems < plan->src_cosize ||
+        dst_capacity_elems < plan->dst_cosize)
+      return LM_E_CAPACITY;
+    const int64_t eb = plan->eb;
+    const uintptr_t s0 = reinterpret_cast<uintptr_t>(src_dev);
+    const uintptr_t d0 = reinterpret_cast<uintptr_t>(dst_dev);
+    const uintptr_t s1 = s0 + uintptr_t(lm::mul_chk(plan->src_cosize, eb));
+    const uintptr_t d1 = d0 + uintptr_t(lm::mul_chk(plan->dst_cosize, eb));
+    if (s0 < d1 && d0 < s1) return LM_E_OVERLAP;
+    const int64_t cap_bytes = lm::mul_chk(src_capacity_elems, eb);
+    for (const lm::Piece& pc : plan->pieces) {
+      const int rc = lm::launch_piece(*plan, pc, static_cast<const char*>(src_dev),
+                                      cap_bytes, static_cast<char*>(dst_dev),
+                                      cuda_stream);
+      if (rc != LM_OK) return rc;
+    }
+    return LM_OK;
+  } catch (const lm::Error& e) {
+    return e.status;
+  } catch (...) {
+    return LM_E_INVALID;
+  }
+}
+
+int lm_layout_eval_device(const lm_layout* layout, void* table_dev,
+                          int offset_bytes, int64_t capacity,
+                          void* cuda_stream) {
+  try {
+    if (!layout || (offset_bytes != 4 && offset_bytes != 8))
+      return LM_E_INVALID;
+    if (layout->size == 0) return LM_OK;
+    if (!table_dev) return LM_E_INVALID;
+    if (capacity < layout->size) return LM_E_CAPACITY;
+    if (offset_bytes == 4 && layout->cosize - 1 > int64_t(0x7fffffff))
+      return LM_E_OVERFLOW;
+    return lm::launch_eval(*layout, table_dev, offset_bytes, cuda_stream);
+  } catch (const lm::Error& e) {
+    return e.status;
+  } catch (...) {
+    return LM_E_INVALID;
+  }
+}
+
+int lm_last_cuda_error(void) { return lm::g_last_cuda; }
+
+}  // extern "C"

@@ -1,0 +1,807 @@
+// Lowering of a src/dst layout pair into a copy plan.
+//
+// 1. Both layouts are split over the same logical domain into joint modes
+//    (extent, src stride, dst stride): the common refinement of their leaf
+//    lists.  The copy out[dst(i)] = in[src(i)] is a set of (src, dst) offset
+//    pairs, so the order of the joint modes is free; modes that continue one
+//    another on both sides are merged ("coalescing").
+// 2. The destination must be one-to-one (two logical indices writing one
+//    slot would leave the result undefined).
+// 3. A mode with unit stride on both sides is the common contiguous run --
+//    the common vector of the inverse layouts ("CUTE布局代数" §2.3); when it
+//    spans 16 bytes the VEC kernel moves 16-byte vectors directly.
+// 4. Otherwise, when the source has a unit-stride mode and the destination
+//    has one, the STAGED kernel copies tiles: loads run along the source's
+//    contiguous modes, stores along the destination's, and the tile passes
+//    through shared memory laid out with an XOR swizzle chosen here by
+//    simulating the bank conflicts of both phases ("CUTLASS Layout可视化" §5.2
+//    and §4.3: spread one warp's accesses over the 32 banks; the
+//    PitchLinearStripminedThreadMap article §4.1: 128-byte lines).
+// 5. Everything else runs GENERIC: one element per thread.
+
+#include <algorithm>
+#include <cstdlib>
+#include <cstring>
+#include <memory>
+#include <numeric>
+#include <sstream>
+
+#include "lm_internal.h"
+
+namespace lm {
+
+bool refine(const std::vector<Leaf>& a, const std::vector<Leaf>& b,
+            std::vector<JMode>& out);  // lm_layout.cpp
+
+namespace {
+
+constexpr int64_t kSmall = 4096;            // elements: GENERIC below this
+constexpr int64_t kMaxPiece = int64_t(1) << 31;
+constexpr int kThreads = 256;               // STAGED block size
+
+int ilog2(int64_t v) {
+  int l = 0;
+  while ((int64_t(1) << l) < v) ++l;
+  return l;
+}
+
+Swz to_bytes(const Swz& z, int eb) {
+  if (!z.on()) return Swz{};
+  return Swz{z.b, z.m + ilog2(eb), z.s};
+}
+
+int64_t prod_e(const std::vector<JMode>& ms) {
+  int64_t p = 1;
+  for (const JMode& m : ms) p = mul_chk(p, m.e);
+  return p;
+}
+
+std::vector<JMode> coalesce_joint(std::vector<JMode> ms) {
+  ms.erase(std::remove_if(ms.begin(), ms.end(),
+                          [](const JMode& m) { return m.e == 1; }),
+           ms.end());
+  bool merged = true;
+  while (merged) {
+    merged = false;
+    for (size_t i = 0; i < ms.size() && !merged; ++i)
+      for (size_t j = 0; j < ms.size() && !merged; ++j) {
+        if (i == j) continue;
+        if (ms[j].s == ms[i].e * ms[i].s && ms[j].d == ms[i].e * ms[i].d) {
+          ms[i].e = mul_chk(ms[i].e, ms[j].e);
+          ms.erase(ms.begin() + long(j));
+          merged = true;
+        }
+      }
+  }
+  return ms;
+}
+
+// ---------------------------------------------------------------------------
+// GENERIC
+// ---------------------------------------------------------------------------
+
+void fill_side(const std::vector<Leaf>& ls, int eb, uint32_t* ext,
+               FastDiv* div, int64_t* str, int64_t* ext64, int32_t& n) {
+  std::vector<Leaf> c;
+  for (const Leaf& l : ls)
+    if (l.e != 1) c.push_back(l);
+  if (c.size() > size_t(kMaxLeaves)) fail(LM_E_NOT_REPRESENTABLE);
+  n = int32_t(c.size());
+  for (size_t k = 0; k < c.size(); ++k) {
+    ext64[k] = c[k].e;
+    ext[k] = c[k].e < (int64_t(1) << 31) ? uint32_t(c[k].e) : 0u;
+    div[k] = make_fastdiv(ext[k] ? ext[k] : 1u);
+    str[k] = mul_chk(c[k].d, eb);
+  }
+}
+
+GenericArgs make_generic(const std::vector<Leaf>& sl,
+                         const std::vector<Leaf>& dl, int64_t n,
+                         int64_t s_base, int64_t d_base, const Swz& ss,
+                         const Swz& ds, int eb) {
+  GenericArgs g;
+  g.n = uint64_t(n);
+  g.eb = eb;
+  g.wide = n >= (int64_t(1) << 31) ? 1 : 0;
+  fill_side(sl, eb, g.s_ext, g.s_div, g.s_str, g.s_ext64, g.ns);
+  fill_side(dl, eb, g.d_ext, g.d_div, g.d_str, g.d_ext64, g.nd);
+  for (int k = 0; k < g.ns; ++k)
+    if (!g.s_ext[k]) g.wide = 1;
+  for (int k = 0; k < g.nd; ++k)
+    if (!g.d_ext[k]) g.wide = 1;
+  g.s_base = mul_chk(s_base, eb);
+  g.d_base = mul_chk(d_base, eb);
+  g.s_swz = to_bytes(ss, eb);
+  g.d_swz = to_bytes(ds, eb);
+  return g;
+}
+
+GenericArgs generic_for_modes(const std::vector<JMode>& ms, int64_t s_base,
+                              int64_t d_base, const lm_plan& P) {
+  std::vector<Leaf> sl, dl;
+  for (const JMode& m : ms) {
+    sl.push_back({m.e, m.s});
+    dl.push_back({m.e, m.d});
+  }
+  return make_generic(sl, dl, prod_e(ms), s_base, d_base, P.s_swz, P.d_swz,
+                      P.eb);
+}
+
+// ---------------------------------------------------------------------------
+// STAGED: tile choice, chains, smem layout search
+// ---------------------------------------------------------------------------
+
+struct TileMode {
+  int mode;     // index into the piece's joint modes
+  int64_t T;    // tile extent along it (divides the mode's extent)
+};
+
+int64_t tile_bytes_target() {
+  static int64_t v = [] {
+    const char* e = std::getenv("LM_TILE_BYTES");
+    int64_t t = e ? std::atoll(e) : 8192;
+    return std::clamp<int64_t>(t, 1024, 24576);
+  }();
+  return v;
+}
+
+// Largest divisor of e that is <= want and a multiple of `mult`, or 0.
+int64_t divisor_at_most(int64_t e, int64_t want, int64_t mult) {
+  want = std::min(want, e);
+  for (int64_t t = want; t >= 1; --t)
+    if (e % t == 0 && t % mult == 0) return t;
+  return 0;
+}
+
+struct SmemSim {
+  // per candidate pad: linear addresses of every lane access
+  std::vector<int64_t> load_addr;     // [n_lchunks] (16-byte accesses)
+  std::vector<int64_t> gather_addr;   // [n_schunks * V]
+};
+
+// Wavefronts of one warp-wide shared-memory instruction: per phase (lanes
+// whose requests share one 128-byte pass), the largest number of distinct
+// 4-byte words any of the 32 banks must deliver.
+int64_t wavefronts(const int64_t* addr, const bool* valid, int lanes,
+                   int bytes) {
+  const int per_phase = bytes <= 4 ? 32 : 128 / bytes;
+  const int words = bytes <= 4 ? 1 : bytes / 4;
+  int64_t total = 0;
+  for (int p0 = 0; p0 < lanes; p0 += per_phase) {
+    int64_t seen[32][32];
+    int cnt[32] = {0};
+    int worst = 0;
+    bool any = false;
+    for (int l = p0; l < std::min(lanes, p0 + per_phase); ++l) {
+      if (!valid[l]) continue;
+      any = true;
+      for (int w = 0; w < words; ++w) {
+        const int64_t word = (addr[l] >> 2) + w;
+        const int bank = int(word & 31);
+        bool dup = false;
+        for (int q = 0; q < cnt[bank]; ++q)
+          if (seen[bank][q] == word) dup = true;
+        if (!dup && cnt[bank] < 32) seen[bank][cnt[bank]++] = word;
+        worst = std::max(worst, cnt[bank]);
+      }
+    }
+    if (any) total += std::max(worst, 1);
+  }
+  return total;
+}
+
+struct StagedChoice {
+  bool ok = false;
+  int split_mode = -1;     // > = 0: split the box along this mode at split_at
+  int64_t split_at = 0;
+};
+
+}  // namespace
+
+// Try to plan `ms` (a box of the joint domain) on the STAGED path.  Fills
+// pc on success.  May instead request a split of a mode whose extent has no
+// good tile divisor.
+static StagedChoice plan_staged(const std::vector<JMode>& ms, int64_t s_base,
+                                int64_t d_base, const lm_plan& P, Piece& pc) {
+  StagedChoice ch;
+  const int eb = P.eb;
+  const int64_t V = 16 / eb;  // elements per 16-byte chunk
+  const int n = int(ms.size());
+  int a = -1, b = -1;
+  for (int k = 0; k < n; ++k) {
+    if (ms[size_t(k)].s == 1 && a < 0) a = k;
+    if (ms[size_t(k)].d == 1 && b < 0) b = k;
+  }
+  if (a < 0 || b < 0) return ch;
+  const Swz ssb = to_bytes(P.s_swz, eb), dsb = to_bytes(P.d_swz, eb);
+  if ((ssb.on() && ssb.m < 4) || (dsb.on() && dsb.m < 4)) return ch;
+
+  const int64_t target = tile_bytes_target() / eb;  // elements per tile
+  std::vector<int64_t> T(size_t(n), 0);
+  auto tile_elems = [&] {
+    int64_t p = 1;
+    for (int k = 0; k < n; ++k)
+      if (T[size_t(k)]) p *= T[size_t(k)];
+    return p;
+  };
+  // choose a tile extent near `want` for mode k, or request a split
+  auto choose = [&](int k, int64_t want, int64_t mult) -> bool {
+    const int64_t e = ms[size_t(k)].e;
+    want = std::max<int64_t>(want, 1);
+    if (e <= want) {
+      T[size_t(k)] = e;
+      return true;
+    }
+    int64_t t = divisor_at_most(e, want, mult);
+    if (t == 0 || t * 2 <= want) {
+      // no divisor close to `want`: split off the ragged tail of the mode
+      int64_t w = std::max<int64_t>(mult, (want / mult) * mult);
+      if (e / w >= 1 && e % w) {
+        ch.split_mode = k;
+        ch.split_at = e - e % w;
+        return false;
+      }
+      t = divisor_at_most(e, want, 1);
+    }
+    T[size_t(k)] = t;
+    return true;
+  };
+
+  // 1) destination run: about 128 bytes along the dst-fastest modes
+  {
+    int cur = b;
+    int64_t span = 1;
+    const int64_t want = std::max<int64_t>(V, 128 / eb);
+    if (!choose(cur, want, V > 1 ? std::min<int64_t>(V, ms[size_t(cur)].e) : 1))
+      return ch;
+    span = T[size_t(cur)];
+    while (T[size_t(cur)] == ms[size_t(cur)].e && span < want) {
+      int nxt = -1;
+      for (int k = 0; k < n; ++k)
+        if (!T[size_t(k)] && ms[size_t(k)].d == span) nxt = k;
+      if (nxt < 0) break;
+      if (!choose(nxt, (want + span - 1) / span, 1)) return ch;
+      span *= T[size_t(nxt)];
+      cur = nxt;
+    }
+  }
+  // 2) source run: the src-fastest mode, sized to fill the tile target
+  if (!T[size_t(a)]) {
+    const int64_t want =
+        std::max<int64_t>(128 / eb, target / std::max<int64_t>(tile_elems(), 1));
+    if (!choose(a, want, std::min<int64_t>(V, ms[size_t(a)].e))) return ch;
+  }
+  // 3) grow until the tile holds about `target` elements: first along the
+  //    destination's contiguous chain, then the partial src/dst modes, then a
+  //    new outer mode
+  for (int guard = 0; guard < 64 && tile_elems() * 2 <= target; ++guard) {
+    // dst chain continuation
+    int64_t span = 1;
+    int cur = b;
+    std::vector<bool> in_chain(size_t(n), false);
+    for (;;) {
+      in_chain[size_t(cur)] = true;
+      span *= T[size_t(cur)];
+      if (T[size_t(cur)] != ms[size_t(cur)].e) break;
+      int nxt = -1;
+      for (int k = 0; k < n; ++k)
+        if (!in_chain[size_t(k)] && ms[size_t(k)].d == span) nxt = k;
+      if (nxt < 0 || !T[size_t(nxt)]) {
+        if (nxt >= 0) {
+          if (!choose(nxt, std::max<int64_t>(1, target / tile_elems()), 1))
+            return ch;
+          cur = -1;
+        }
+        break;
+      }
+      cur = nxt;
+    }
+    if (cur == -1) continue;
+    // partial modes: double the src-fast one, then the dst-fast one
+    bool grown = false;
+    for (int k : {a, b}) {
+      const int64_t e = ms[size_t(k)].e, t = T[size_t(k)];
+      if (t < e && e % (2 * t) == 0 && tile_elems() * 2 <= target) {
+        T[size_t(k)] = 2 * t;
+        grown = true;
+        break;
+      }
+    }
+    if (grown) continue;
+    // a new outer mode
+    int best = -1;
+    for (int k = 0; k < n; ++k) {
+      if (T[size_t(k)]) continue;
+      if (best < 0 || std::min(ms[size_t(k)].s, ms[size_t(k)].d) <
+                          std::min(ms[size_t(best)].s, ms[size_t(best)].d))
+        best = k;
+    }
+    if (best < 0) break;
+    if (!choose(best, std::max<int64_t>(1, target / tile_elems()), 1))
+      return ch;
+  }
+
+  // ---- chains over the final tile ---------------------------------------
+  std::vector<int> tile_modes;
+  for (int k = 0; k < n; ++k)
+    if (T[size_t(k)]) tile_modes.push_back(k);
+  if (tile_modes.size() > size_t(kMaxTile)) return ch;
+
+  // src chain: from a, the tile mode with the smallest stride at or beyond
+  // the current span, gaps of at most one chunk, through full modes only
+  std::vector<int> s_chain{a};
+  int64_t s_span = T[size_t(a)];
+  {
+    std::vector<bool> used(size_t(n), false);
+    used[size_t(a)] = true;
+    int cur = a;
+    while (T[size_t(cur)] == ms[size_t(cur)].e) {
+      int nxt = -1;
+      for (int k : tile_modes) {
+        if (used[size_t(k)] || ms[size_t(k)].s < s_span) continue;
+        if ((ms[size_t(k)].s - s_span) * eb > 16) continue;
+        if (nxt < 0 || ms[size_t(k)].s < ms[size_t(nxt)].s) nxt = k;
+      }
+      if (nxt < 0) break;
+      used[size_t(nxt)] = true;
+      s_span = ms[size_t(nxt)].s * (T[size_t(nxt)] - 1) + s_span;
+      s_chain.push_back(nxt);
+      cur = nxt;
+    }
+  }
+  // dst chain: exact contiguity
+  std::vector<int> d_chain{b};
+  int64_t d_span = T[size_t(b)];
+  {
+    std::vector<bool> used(size_t(n), false);
+    used[size_t(b)] = true;
+    int cur = b;
+    while (T[size_t(cur)] == ms[size_t(cur)].e) {
+      int nxt = -1;
+      for (int k : tile_modes)
+        if (!used[size_t(k)] && ms[size_t(k)].d == d_span) nxt = k;
+      if (nxt < 0) break;
+      used[size_t(nxt)] = true;
+      d_span *= T[size_t(nxt)];
+      d_chain.push_back(nxt);
+      cur = nxt;
+    }
+  }
+  auto in = [](const std::vector<int>& v, int k) {
+    return std::find(v.begin(), v.end(), k) != v.end();
+  };
+  std::vector<int> s_outer, d_outer;
+  for (int k : tile_modes) {
+    if (!in(s_chain, k)) s_outer.push_back(k);
+    if (!in(d_chain, k)) d_outer.push_back(k);
+  }
+  if (s_outer.size() > size_t(kMaxTile) || d_outer.size() > size_t(kMaxTile) ||
+      d_chain.size() > size_t(kMaxTile))
+    return ch;
+
+  // ---- alignment: every chunk start 16-byte aligned ----------------------
+  const int64_t seg_bytes = ((s_span * eb + 15) / 16) * 16;
+  {
+    // the kernel keeps offsets inside a tile in 32 bits
+    int64_t s_reach = seg_bytes, d_reach = 16;
+    for (int k : tile_modes) {
+      s_reach = add_chk(s_reach, mul_chk(mul_chk(T[size_t(k)] - 1, ms[size_t(k)].s), eb));
+      d_reach = add_chk(d_reach, mul_chk(mul_chk(T[size_t(k)] - 1, ms[size_t(k)].d), eb));
+    }
+    if (s_reach >= (int64_t(1) << 31) || d_reach >= (int64_t(1) << 31)) return ch;
+  }
+  if ((d_span * eb) % 16) return ch;
+  auto al = [&](int64_t elems) { return (elems * eb) % 16 == 0; };
+  if (!al(s_base) || !al(d_base)) return ch;
+  for (int k : s_outer)
+    if (!al(ms[size_t(k)].s)) return ch;
+  for (int k : d_outer)
+    if (!al(ms[size_t(k)].d)) return ch;
+  std::vector<JMode> grid;
+  for (int k = 0; k < n; ++k) {
+    const JMode& m = ms[size_t(k)];
+    const int64_t t = T[size_t(k)] ? T[size_t(k)] : 1;
+    if (t == m.e) continue;
+    grid.push_back({m.e / t, m.s * t, m.d * t});
+    if (!al(m.s * t) || !al(m.d * t)) return ch;
+  }
+  if (grid.size() > size_t(kMaxModes)) return ch;
+  std::sort(grid.begin(), grid.end(),
+            [](const JMode& x, const JMode& y) { return x.d < y.d; });
+  const int64_t n_tiles = prod_e(grid);
+  if (n_tiles >= (int64_t(1) << 32)) return ch;
+
+  // ---- shared-memory layout: segment pitch and XOR swizzle ---------------
+  int64_t n_seg = 1;
+  for (int k : s_outer) n_seg *= T[size_t(k)];
+  const int64_t cps = seg_bytes / 16;
+  const int64_t n_l = n_seg * cps;
+  const int64_t n_s = tile_elems() / V;
+  const int64_t cpd = d_span * eb / 16;
+  const int64_t lpt = (n_l + kThreads - 1) / kThreads;
+  const int64_t spt = (n_s + kThreads - 1) / kThreads;
+  const int max_spt = std::min(8, std::max(1, 32 / int(V)));
+  if (lpt > 8 || spt > max_spt) return ch;
+
+  // smem bytes per coordinate of each tile mode for a given pitch
+  auto smem_m = [&](int64_t pitch, std::vector<int64_t>& m) {
+    m.assign(size_t(n), 0);
+    for (int k : s_chain) m[size_t(k)] = ms[size_t(k)].s * eb;
+    int64_t w = pitch;
+    for (int k : s_outer) {
+      m[size_t(k)] = w;
+      w *= T[size_t(k)];
+    }
+  };
+  // linear smem address of every load chunk and every gathered element
+  auto linear = [&](int64_t pitch, std::vector<int64_t>& la,
+                    std::vector<int64_t>& ga) {
+    std::vector<int64_t> m;
+    smem_m(pitch, m);
+    la.resize(size_t(n_l));
+    for (int64_t j = 0; j < n_l; ++j) la[size_t(j)] = (j / cps) * pitch + (j % cps) * 16;
+    ga.resize(size_t(n_s * V));
+    for (int64_t j = 0; j < n_s; ++j) {
+      int64_t o = j / cpd, p = j % cpd, base = 0;
+      for (int k : d_outer) {
+        base += (o % T[size_t(k)]) * m[size_t(k)];
+        o /= T[size_t(k)];
+      }
+      for (int64_t e = 0; e < V; ++e) {
+        int64_t q = p * V + e, addr = base;
+        for (int k : d_chain) {
+          addr += (q % T[size_t(k)]) * m[size_t(k)];
+          q /= T[size_t(k)];
+        }
+        ga[size_t(j * V + e)] = addr;
+      }
+    }
+  };
+  struct Cand {
+    int64_t pad = 0;
+    Swz z;
+    int64_t cost = -1, bytes = 0;
+  } best, ideal_c;
+  std::vector<int64_t> la, ga, addr(32);
+  bool valid[32];
+  const std::vector<int64_t> pads =
+      n_seg > 1 ? std::vector<int64_t>{0, 16, 32, 48, 64, 80, 96, 112}
+                : std::vector<int64_t>{0};
+  int64_t ideal = 0;
+  for (int64_t pad : pads) {
+    const int64_t pitch = seg_bytes + pad;
+    linear(pitch, la, ga);
+    const int64_t lin_max = (n_seg - 1) * pitch + seg_bytes;
+    std::vector<Swz> zs{Swz{}};
+    for (int bb = 1; bb <= 3; ++bb)
+      for (int ss = bb; ss <= 10; ++ss) zs.push_back(Swz{bb, 4, ss});
+    for (const Swz& z : zs) {
+      const int64_t blk = int64_t(16) << z.b;
+      const int64_t bytes = ((lin_max + blk - 1) / blk) * blk;
+      if (bytes > 24576) continue;
+      int64_t cost = 0, id = 0;
+      for (int w = 0; w < kThreads / 32; ++w) {
+        for (int64_t k = 0; k < lpt; ++k) {
+          for (int l = 0; l < 32; ++l) {
+            const int64_t j = 32 * w + l + k * kThreads;
+            valid[l] = j < n_l;
+            addr[size_t(l)] = valid[l] ? z.apply(la[size_t(j)]) : 0;
+          }
+          cost += wavefronts(addr.data(), valid, 32, 16);
+          int cntv = 0;
+          for (int l = 0; l < 32; ++l) cntv += valid[l];
+          id += (cntv * 16 + 127) / 128;
+        }
+        for (int64_t k = 0; k < spt; ++k)
+          for (int64_t e = 0; e < V; ++e) {
+            int cntv = 0;
+            for (int l = 0; l < 32; ++l) {
+              const int64_t j = 32 * w + l + k * kThreads;
+              valid[l] = j < n_s;
+              cntv += valid[l];
+              addr[size_t(l)] = valid[l] ? z.apply(ga[size_t(j * V + e)]) : 0;
+            }
+            cost += wavefronts(addr.data(), valid, 32, eb);
+            id += cntv ? (cntv * eb + 127) / 128 : 0;
+          }
+      }
+      ideal = id;
+      if (best.cost < 0 || cost < best.cost ||
+          (cost == best.cost && bytes < best.bytes)) {
+        best.pad = pad;
+        best.z = z;
+        best.cost = cost;
+        best.bytes = bytes;
+      }
+    }
+  }
+  if (best.cost < 0) return ch;
+
+  // ---- fill the kernel arguments -----------------------------------------
+  StagedArgs& A = pc.st;
+  A = StagedArgs{};
+  const int64_t pitch = seg_bytes + best.pad;
+  std::vector<int64_t> m;
+  smem_m(pitch, m);
+  A.n_tiles = uint32_t(n_tiles);
+  A.ng = int32_t(grid.size());
+  uint32_t pre = 1;
+  for (size_t k = 0; k < grid.size(); ++k) {
+    A.g_ext[k] = uint32_t(grid[k].e);
+    A.g_pre[k] = make_fastdiv(pre);
+    A.g_div[k] = make_fastdiv(uint32_t(grid[k].e));
+    A.g_s[k] = mul_chk(grid[k].s, eb);
+    A.g_d[k] = mul_chk(grid[k].d, eb);
+    pre *= uint32_t(grid[k].e);
+  }
+  A.s_base = mul_chk(s_base, eb);
+  A.d_base = mul_chk(d_base, eb);
+  A.s_swz = ssb;
+  A.d_swz = dsb;
+  A.n_lchunks = uint32_t(n_l);
+  A.cps = uint32_t(cps);
+  A.cps_div = make_fastdiv(uint32_t(cps));
+  A.nso = int32_t(s_outer.size());
+  for (size_t i = 0; i < s_outer.size(); ++i) {
+    const int k = s_outer[i];
+    A.so_ext[i] = uint32_t(T[size_t(k)]);
+    A.so_div[i] = make_fastdiv(uint32_t(T[size_t(k)]));
+    A.so_s[i] = mul_chk(ms[size_t(k)].s, eb);
+    A.so_m[i] = uint32_t(m[size_t(k)]);
+  }
+  A.n_schunks = uint32_t(n_s);
+  A.cpd = uint32_t(cpd);
+  A.cpd_div = make_fastdiv(uint32_t(cpd));
+  A.ndo = int32_t(d_outer.size());
+  for (size_t i = 0; i < d_outer.size(); ++i) {
+    const int k = d_outer[i];
+    A.do_ext[i] = uint32_t(T[size_t(k)]);
+    A.do_div[i] = make_fastdiv(uint32_t(T[size_t(k)]));
+    A.do_d[i] = mul_chk(ms[size_t(k)].d, eb);
+    A.do_m[i] = uint32_t(m[size_t(k)]);
+  }
+  A.ndi = int32_t(d_chain.size());
+  for (size_t i = 0; i < d_chain.size(); ++i) {
+    const int k = d_chain[i];
+    A.di_ext[i] = uint32_t(T[size_t(k)]);
+    A.di_div[i] = make_fastdiv(uint32_t(T[size_t(k)]));
+    A.di_m[i] = uint32_t(m[size_t(k)]);
+  }
+  A.stage_bytes = uint32_t(best.bytes);
+  A.m_swz = best.z;
+  pc.path = PATH_STAGED;
+  pc.tile_elems = tile_elems();
+  pc.bank_cost = best.cost;
+  pc.bank_ideal = ideal;
+  ch.ok = true;
+  return ch;
+}
+
+// VEC when a unit-stride run shared by both sides gives 16-byte vectors (or
+// narrower vectors when `allow_narrow`).  May request a split of the run.
+static StagedChoice plan_vec(const std::vector<JMode>& ms, int64_t s_base,
+                             int64_t d_base, const lm_plan& P, Piece& pc,
+                             bool allow_narrow) {
+  StagedChoice ch;
+  const int eb = P.eb;
+  int r = -1;
+  for (size_t k = 0; k < ms.size(); ++k)
+    if (ms[k].s == 1 && ms[k].d == 1) r = int(k);
+  if (r < 0) return ch;
+  auto fits = [&](int64_t V, bool check_run) {
+    if (check_run && ms[size_t(r)].e % V) return false;
+    for (size_t k = 0; k < ms.size(); ++k) {
+      if (int(k) == r) continue;
+      if (ms[k].s % V || ms[k].d % V) return false;
+    }
+    if (s_base % V || d_base % V) return false;
+    if (P.s_swz.on() && (int64_t(1) << P.s_swz.m) < V) return false;
+    if (P.d_swz.on() && (int64_t(1) << P.d_swz.m) < V) return false;
+    return true;
+  };
+  const int64_t vmax = 16 / eb;
+  const int64_t e = ms[size_t(r)].e;
+  if (vmax > 1 && e % vmax && e >= 2 * vmax && fits(vmax, false)) {
+    ch.split_mode = r;
+    ch.split_at = e - e % vmax;
+    return ch;
+  }
+  int64_t V = vmax;
+  while (V > 1 && !fits(V, true)) V /= 2;
+  const int vb = int(V * eb);
+  if (vb < 16 && !allow_narrow) return ch;
+  if (vb < 4) return ch;
+  std::vector<JMode> rest;
+  for (size_t k = 0; k < ms.size(); ++k)
+    if (int(k) != r) rest.push_back(ms[k]);
+  std::sort(rest.begin(), rest.end(),
+            [](const JMode& x, const JMode& y) { return x.d < y.d; });
+  if (rest.size() + 1 > size_t(kMaxModes)) return ch;
+  VecArgs& A = pc.vec;
+  A = VecArgs{};
+  const int64_t nvec = prod_e(ms) / V;
+  if (nvec >= (int64_t(1) << 32)) return ch;
+  A.n_vec = uint32_t(nvec);
+  A.nm = int32_t(rest.size() + 1);
+  A.ext[0] = uint32_t(e / V);
+  A.div[0] = make_fastdiv(A.ext[0]);
+  A.s[0] = V * eb;
+  A.d[0] = V * eb;
+  for (size_t k = 0; k < rest.size(); ++k) {
+    A.ext[k + 1] = uint32_t(rest[k].e);
+    A.div[k + 1] = make_fastdiv(uint32_t(rest[k].e));
+    A.s[k + 1] = mul_chk(rest[k].s, eb);
+    A.d[k + 1] = mul_chk(rest[k].d, eb);
+  }
+  A.s_base = mul_chk(s_base, eb);
+  A.d_base = mul_chk(d_base, eb);
+  A.s_swz = to_bytes(P.s_swz, eb);
+  A.d_swz = to_bytes(P.d_swz, eb);
+  pc.path = PATH_VEC;
+  pc.vec_bytes = vb;
+  ch.ok = true;
+  return ch;
+}
+
+static void plan_box(lm_plan& P, std::vector<JMode> ms, int64_t s_base,
+                     int64_t d_base, int depth) {
+  ms = coalesce_joint(ms);
+  const int64_t size = prod_e(ms);
+  if (size == 0) return;
+  if (depth > 24 || ms.size() > size_t(kMaxModes)) {
+    Piece pc;
+    pc.modes = ms;
+    pc.s_base = s_base;
+    pc.d_base = d_base;
+    pc.gen = generic_for_modes(ms, s_base, d_base, P);
+    P.pieces.push_back(std::move(pc));
+    return;
+  }
+  auto split = [&](int k, int64_t at) {
+    std::vector<JMode> lo = ms, hi = ms;
+    lo[size_t(k)].e = at;
+    hi[size_t(k)].e = ms[size_t(k)].e - at;
+    plan_box(P, lo, s_base, d_base, depth + 1);
+    plan_box(P, hi, add_chk(s_base, mul_chk(at, ms[size_t(k)].s)),
+             add_chk(d_base, mul_chk(at, ms[size_t(k)].d)), depth + 1);
+  };
+  if (size >= kMaxPiece) {
+    int k = 0;
+    for (size_t j = 1; j < ms.size(); ++j)
+      if (ms[j].e > ms[size_t(k)].e) k = int(j);
+    split(k, ms[size_t(k)].e / 2);
+    return;
+  }
+  Piece pc;
+  pc.modes = ms;
+  pc.s_base = s_base;
+  pc.d_base = d_base;
+  pc.gen = generic_for_modes(ms, s_base, d_base, P);
+  if (size > kSmall) {
+    StagedChoice c = plan_vec(ms, s_base, d_base, P, pc, false);
+    if (c.split_mode >= 0) return split(c.split_mode, c.split_at);
+    if (!c.ok) {
+      c = plan_staged(ms, s_base, d_base, P, pc);
+      if (c.split_mode >= 0) return split(c.split_mode, c.split_at);
+    }
+    if (!c.ok) c = plan_vec(ms, s_base, d_base, P, pc, true);
+    if (!c.ok) pc.path = PATH_GENERIC;
+  }
+  P.pieces.push_back(std::move(pc));
+}
+
+static std::string describe(const lm_plan& P) {
+  std::ostringstream os;
+  os << "{\"size\":" << P.size << ",\"elem_bytes\":" << P.eb
+     << ",\"joint\":" << (P.joint ? "true" : "false") << ",\"pieces\":[";
+  for (size_t i = 0; i < P.pieces.size(); ++i) {
+    const Piece& pc = P.pieces[i];
+    if (i) os << ',';
+    const char* path = pc.path == PATH_VEC      ? "VEC"
+                       : pc.path == PATH_STAGED ? "STAGED"
+                                                : "GENERIC";
+    os << "{\"path\":\"" << path << "\",\"modes\":[";
+    for (size_t k = 0; k < pc.modes.size(); ++k) {
+      if (k) os << ',';
+      os << '[' << pc.modes[k].e << ',' << pc.modes[k].s << ','
+         << pc.modes[k].d << ']';
+    }
+    os << "],\"s_base\":" << pc.s_base << ",\"d_base\":" << pc.d_base;
+    if (pc.path == PATH_VEC) os << ",\"vec_bytes\":" << pc.vec_bytes;
+    if (pc.path == PATH_STAGED) {
+      const StagedArgs& A = pc.st;
+      os << ",\"tile_elems\":" << pc.tile_elems << ",\"n_tiles\":" << A.n_tiles
+         << ",\"load_chunks\":" << A.n_lchunks
+         << ",\"store_chunks\":" << A.n_schunks
+         << ",\"stage_bytes\":" << A.stage_bytes << ",\"smem_swizzle\":["
+         << A.m_swz.b << ',' << A.m_swz.m << ',' << A.m_swz.s << ']'
+         << ",\"bank_wavefronts\":" << pc.bank_cost
+         << ",\"bank_wavefronts_ideal\":" << pc.bank_ideal;
+    }
+    os << '}';
+  }
+  os << "]}";
+  return os.str();
+}
+
+}  // namespace lm
+
+using lm::fail;
+
+extern "C" {
+
+int lm_plan_copy(const lm_layout* src, const lm_layout* dst, int elem_bytes,
+                 lm_plan** out) {
+  if (out) *out = nullptr;
+  try {
+    if (!src || !dst || !out) fail(LM_E_INVALID);
+    if (elem_bytes != 1 && elem_bytes != 2 && elem_bytes != 4 &&
+        elem_bytes != 8 && elem_bytes != 16)
+      fail(LM_E_INVALID);
+    if (src->size != dst->size) fail(LM_E_INCOMPATIBLE);
+    auto P = std::make_unique<lm_plan>();
+    P->eb = elem_bytes;
+    P->size = src->size;
+    P->src_cosize = src->cosize;
+    P->dst_cosize = dst->cosize;
+    P->s_swz = src->swz;
+    P->d_swz = dst->swz;
+    // byte offsets must fit int64
+    lm::mul_chk(std::max(P->src_cosize, P->dst_cosize), elem_bytes);
+    if (P->size > 0) {
+      if (!lm::affine_injective(dst->leaves)) fail(LM_E_NOT_INJECTIVE);
+      std::vector<lm::JMode> jm;
+      if (lm::refine(src->leaves, dst->leaves, jm)) {
+        P->joint = true;
+        lm::plan_box(*P, jm, 0, 0, 0);
+      } else {
+        P->joint = false;
+        lm::Piece pc;
+        pc.path = lm::PATH_GENERIC;
+        std::vector<lm::Leaf> sl = lm::coalesce_leaves(src->leaves);
+        std::vector<lm::Leaf> dl = lm::coalesce_leaves(dst->leaves);
+        pc.gen = lm::make_generic(sl, dl, P->size, 0, 0, P->s_swz, P->d_swz,
+                                  elem_bytes);
+        P->pieces.push_back(std::move(pc));
+      }
+    }
+    P->describe = lm::describe(*P);
+    *out = P.release();
+    return LM_OK;
+  } catch (const lm::Error& e) {
+    return e.status;
+  } catch (const std::bad_alloc&) {
+    return LM_E_NOMEM;
+  } catch (...) {
+    return LM_E_INVALID;
+  }
+}
+
+int lm_plan_describe(const lm_plan* plan, char* buf, size_t cap) {
+  if (!plan || (!buf && cap)) return LM_E_INVALID;
+  if (cap == 0) return LM_E_BUFFER;
+  const std::string& s = plan->describe;
+  const size_t n = std::min(s.size(), cap - 1);
+  std::memcpy(buf, s.data(), n);
+  buf[n] = '\0';
+  return s.size() + 1 > cap ? LM_E_BUFFER : LM_OK;
+}
+
+int lm_plan_extent(const lm_plan* plan, int64_t* size, int64_t* src_cosize,
+                   int64_t* dst_cosize) {
+  if (!plan) return LM_E_INVALID;
+  if (size) *size = plan->size;
+  if (src_cosize) *src_cosize = plan->src_cosize;
+  if (dst_cosize) *dst_cosize = plan->dst_cosize;
+  return LM_OK;
+}
+
+int lm_plan_launches(const lm_plan* plan, int* launches) {
+  if (!plan || !launches) return LM_E_INVALID;
+  *launches = int(plan->pieces.size());
+  return LM_OK;
+}
+
+void lm_plan_destroy(lm_plan* plan) { delete plan; }
+
+}  // extern "C"

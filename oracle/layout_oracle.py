@@ -67,8 +67,8 @@ def flatten(shape, stride) -> list[tuple[int, int]]:
     if isinstance(shape, int):
         if not isinstance(stride, int):
             raise ValueError("shape and stride nest differently")
-        if shape < 1:
-            raise ValueError("extent must be >= 1")
+        if shape < 0:
+            raise ValueError("extent must be >= 0 (0 makes an empty layout)")
         return [(shape, stride)]
     if isinstance(stride, int) or len(shape) != len(stride):
         raise ValueError("shape and stride nest differently")

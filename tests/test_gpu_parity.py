@@ -1,0 +1,276 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Every comparison is byte-exact (tolerance 0: the copy moves raw bits).  The
+destination is pre-filled with 0xA5 and framed by guard bands, so slots the
+destination layout does not cover, and bytes outside the buffer, must come
+back untouched.  Small cases span several tiles and ragged tails; the
+full-size workloads run with the same plans (and so the same launch
+configuration) that bench.py times and are compared with the oracle in
+full.
+"""
+
+import numpy as np
+import pytest
+
+from oracle import layout_oracle as lo
+from workloads import EVAL_C1, WORKLOADS, seeded_bytes
+
+torch = pytest.importorskip("torch")
+lm = pytest.importorskip("layout_driven_movement_gb300")
+
+pytestmark = pytest.mark.gpu
+
+GUARD = 256
+FILL = 0xA5
+GUARD_FILL = 0x5C
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from layout_driven_movement_gb300 import _build
+    _build.build()
+    lm.lib()
+
+
+def device_buffer(nbytes, fill, offset=0):
+    """A CUDA uint8 view of nbytes at byte `offset` past a 256-byte guard."""
+    raw = torch.full((nbytes + 2 * GUARD + offset,), GUARD_FILL,
+                     dtype=torch.uint8, device="cuda")
+    view = raw[GUARD + offset:GUARD + offset + nbytes]
+    view.fill_(fill)
+    return raw, view
+
+
+def run_case(src_spec, dst_spec, eb, values="bytes", dtype="uint8", seed=7,
+             src_offset=0, dst_offset=0, stream=None, sentinel=None,
+             expect_paths=None):
+    S, D = lm.build_layout(src_spec), lm.build_layout(dst_spec)
+    OS, OD = lo.build(src_spec), lo.build(dst_spec)
+    plan = lm.Plan(S, D, eb)
+    if expect_paths is not None:
+        assert [p["path"] for p in plan.describe()["pieces"]] == expect_paths
+    n_src, n_dst = lo.cosize(OS), lo.cosize(OD)
+    assert S.cosize >= n_src and D.cosize >= n_dst
+    n_src_cap, n_dst_cap = S.cosize, D.cosize
+    if values == "bytes":
+        inp = seeded_bytes("bytes", "uint8", n_src_cap * eb, seed)
+    else:
+        inp = seeded_bytes(values, dtype, n_src_cap, seed)
+    if sentinel is not None:
+        # slots of the source that no logical index reads
+        touched = np.zeros(n_src_cap, dtype=bool)
+        touched[lo.image(OS)] = True
+        v = inp.view(np.dtype((np.void, eb)))
+        pad = np.frombuffer(np.array([sentinel], dtype=np.uint64).tobytes(),
+                            dtype=np.dtype((np.void, eb)))
+        v[~touched] = pad[0]
+    want = np.full(n_dst_cap * eb, FILL, dtype=np.uint8)
+    lo.copy(OS, OD, inp, want, eb)
+
+    s_raw, s_view = device_buffer(n_src_cap * eb, 0, src_offset)
+    s_view.copy_(torch.from_numpy(inp))
+    d_raw, d_view = device_buffer(n_dst_cap * eb, FILL, dst_offset)
+    if stream is None:
+        lm.layout_copy_ptr(plan, s_view.data_ptr(), n_src_cap,
+                           d_view.data_ptr(), n_dst_cap)
+    else:
+        with torch.cuda.stream(stream):
+            lm.layout_copy_ptr(plan, s_view.data_ptr(), n_src_cap,
+                               d_view.data_ptr(), n_dst_cap, stream)
+        stream.synchronize()
+    torch.cuda.synchronize()
+    got = d_view.cpu().numpy()
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, (
+        f"{bad.size} bytes differ, first at byte {bad[:8].tolist()} "
+        f"plan={plan.describe()}")
+    g = d_raw.cpu().numpy()
+    assert (g[:GUARD + dst_offset] == GUARD_FILL).all()
+    assert (g[GUARD + dst_offset + n_dst_cap * eb:] == GUARD_FILL).all()
+    if sentinel is not None:
+        pat = np.frombuffer(np.array([sentinel], dtype=np.uint64).tobytes(),
+                            dtype=np.uint8)[:eb]
+        rows = got.reshape(-1, eb)
+        assert not (rows == pat).all(axis=1).any()
+    return plan
+
+
+# --------------------------------------------------------------------------
+# small cases: several tiles, ragged tails, every element size
+# --------------------------------------------------------------------------
+
+SMALL = [
+    # (name, src, dst, eb)
+    ("c1", WORKLOADS["C1"].src, WORKLOADS["C1"].dst, 4),
+    ("transpose_ragged_f32", ("layout", (200, 136), (1, 200)),
+     ("layout", (200, 136), (136, 1)), 4),
+    ("transpose_1000x1000_f16", ("layout", (1000, 1000), (1, 1000)),
+     ("layout", (1000, 1000), (1000, 1)), 2),
+    ("transpose_prime_u8", ("layout", (97, 131), (1, 97)),
+     ("layout", (97, 131), (131, 1)), 1),
+    ("transpose_b128", ("layout", (50, 60), (1, 50)),
+     ("layout", (50, 60), (60, 1)), 16),
+    ("transpose_f64", ("layout", (300, 257), (1, 300)),
+     ("layout", (300, 257), (257, 1)), 8),
+    ("tiles_swizzled_bf16",
+     ("zipped_divide", ("layout", (512, 384), (384, 1)), (64, 64)),
+     ("swizzle", 3, 4, 3,
+      ("layout", ((64, 64), (8, 6)), ((64, 1), (24576, 4096)))), 2),
+    ("padded_tv_gather_f64",
+     ("concat", WORKLOADS["C4"].src[1], ("layout", 3001, 72)),
+     ("layout", (((4, 8), 2), 3001), (((1, 4), 32), 64)), 8),
+    ("nhwc_to_nchw_f16", ("layout", (3, 40, 7, 9), (2520, 1, 360, 40)),
+     ("layout", (3, 40, 7, 9), (2520, 63, 9, 1)), 2),
+    ("nhwc_to_nchw_big_c", ("layout", (2, 256, 14, 14), (50176, 1, 3584, 256)),
+     ("layout", (2, 256, 14, 14), (50176, 196, 14, 1)), 2),
+    ("head_interleave_f16", ("layout", (2, 1000, 24), (24000, 24, 1)),
+     ("layout", (2, 1000, 24), (1, 48, 2)), 2),
+    ("head_interleave_full_rows", ("layout", (2, 4096, 128), (524288, 128, 1)),
+     ("layout", (2, 4096, 128), (1, 256, 2)), 2),
+    ("identity_vec", ("layout", 100003, 1), ("layout", 100003, 1), 4),
+    ("run_then_transpose", ("layout", (8, 300, 70), (1, 8, 2400)),
+     ("layout", (8, 300, 70), (1, 560, 8)), 2),
+    ("gap_dst_untouched", ("layout", (64, 300), (1, 64)),
+     ("layout", (64, 300), (301, 1)), 4),
+    ("broadcast_src", ("layout", (512, 33), (1, 0)),
+     ("layout", (512, 33), (33, 1)), 4),
+    ("swizzled_src", ("swizzle", 2, 4, 4, ("layout", (128, 96), (96, 1))),
+     ("layout", (128, 96), (1, 128)), 2),
+    ("non_refinable_generic", ("layout", (6, 5), (1, 6)),
+     ("layout", (5, 6), (6, 1)), 4),
+    ("rank5_mixed", ("layout", (3, 4, 5, 6, 7), (1, 3, 12, 60, 360)),
+     ("layout", (3, 4, 5, 6, 7), (840, 210, 42, 7, 1)), 2),
+]
+
+
+@pytest.mark.parametrize("name,src,dst,eb", SMALL, ids=[c[0] for c in SMALL])
+def test_small_parity(name, src, dst, eb):
+    run_case(src, dst, eb)
+
+
+def test_small_parity_paths_cover_every_kernel():
+    seen = set()
+    for _, src, dst, eb in SMALL:
+        p = lm.Plan(lm.build_layout(src), lm.build_layout(dst), eb)
+        seen |= {pc["path"] for pc in p.describe()["pieces"]}
+    assert seen == {"GENERIC", "VEC", "STAGED"}
+
+
+@pytest.mark.parametrize("eb", [1, 2, 4, 8, 16])
+def test_every_element_size_staged_and_vec(eb):
+    run_case(("layout", (96, 80), (1, 96)), ("layout", (96, 80), (80, 1)), eb)
+    run_case(("layout", (64, 90), (1, 70)), ("layout", (64, 90), (1, 64)), eb)
+
+
+@pytest.mark.parametrize("src_off,dst_off", [(4, 0), (0, 8), (1, 3), (16, 16)])
+def test_misaligned_pointers_fall_back(src_off, dst_off):
+    run_case(("layout", (256, 96), (1, 256)), ("layout", (256, 96), (96, 1)),
+             4, src_offset=src_off, dst_offset=dst_off)
+    run_case(("layout", 50000, 1), ("layout", 50000, 1), 2,
+             src_offset=src_off, dst_offset=dst_off)
+
+
+def test_runs_on_side_stream():
+    s = torch.cuda.Stream()
+    run_case(("layout", (640, 320), (1, 640)), ("layout", (640, 320), (320, 1)),
+             4, stream=s)
+
+
+def test_random_bijections():
+    rng = np.random.default_rng(2024)
+    for trial in range(40):
+        nm = int(rng.integers(1, 5))
+        ext = [int(v) for v in rng.integers(1, 70, nm)]
+        def compact(perm, pad):
+            stride = [0] * nm
+            acc = 1
+            for k in perm:
+                stride[k] = acc
+                acc *= ext[k] + (pad if k == perm[0] else 0)
+            return tuple(stride)
+        s = ("layout", tuple(ext),
+             compact(rng.permutation(nm), int(rng.integers(0, 3))))
+        d = ("layout", tuple(ext), compact(rng.permutation(nm), 0))
+        if rng.random() < 0.25:
+            d = ("swizzle", int(rng.integers(1, 4)), int(rng.integers(2, 5)),
+                 3, d)
+        eb = int(rng.choice([1, 2, 4, 8, 16]))
+        run_case(s, d, eb, seed=trial)
+
+
+def test_empty_layout_is_a_no_op():
+    plan = lm.Plan(lm.Layout.parse("(0,5):(1,0)"), lm.Layout.parse("(0,5):(5,1)"), 4)
+    buf = torch.full((64,), FILL, dtype=torch.uint8, device="cuda")
+    lm.layout_copy_ptr(plan, buf.data_ptr(), 0, buf.data_ptr() + 32, 0)
+    torch.cuda.synchronize()
+    assert (buf.cpu() == FILL).all()
+
+
+def test_capacity_and_overlap_errors_on_device_buffers():
+    plan = lm.Plan(lm.Layout.parse("(64,64):(1,64)"),
+                   lm.Layout.parse("(64,64):(64,1)"), 4)
+    a = torch.zeros(4096, dtype=torch.float32, device="cuda")
+    b = torch.zeros(4095, dtype=torch.float32, device="cuda")
+    with pytest.raises(lm.LayoutMoveError) as e:
+        lm.layout_copy(plan, a, b)
+    assert e.value.status == -6
+    with pytest.raises(lm.LayoutMoveError) as e:
+        lm.layout_copy(plan, a, a)
+    assert e.value.status == -7
+
+
+def test_src_capacity_exactly_cosize_staged_tail():
+    """The padded gather loads whole 16-byte chunks; at the very end of the
+    source the last chunk reaches past cosize and is clipped."""
+    run_case(("concat", WORKLOADS["C4"].src[1], ("layout", 4096, 72)),
+             ("layout", (((4, 8), 2), 4096), (((1, 4), 32), 64)), 8,
+             sentinel=0x7FF8DEADBEEF0001)
+
+
+# --------------------------------------------------------------------------
+# layout_eval
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("spec", [
+    EVAL_C1, WORKLOADS["C1"].dst, WORKLOADS["C3"].dst, WORKLOADS["C4"].src,
+    ("layout", (7, 11, 13), (1, 1000, 7)),
+])
+@pytest.mark.parametrize("width", [4, 8])
+def test_layout_eval_device(spec, width):
+    L = lm.build_layout(spec)
+    O = lo.build(spec)
+    dt = torch.int32 if width == 4 else torch.int64
+    table = torch.full((O.size + 3,), -7, dtype=dt, device="cuda")
+    lm.layout_eval_device(L, table)
+    torch.cuda.synchronize()
+    got = table.cpu().numpy()
+    assert (got[O.size:] == -7).all()
+    n = O.size
+    idx = np.arange(n) if n <= 1 << 22 else np.unique(np.concatenate([
+        np.arange(4096), np.arange(n - 4096, n),
+        np.random.default_rng(5).integers(0, n, 1 << 20)]))
+    assert (got[idx] == O.at(idx)).all()
+
+
+def test_layout_eval_c1_blocked_page_values():
+    L = lm.build_layout(EVAL_C1)
+    table = torch.empty(64, dtype=torch.int32, device="cuda")
+    lm.layout_eval_device(L, table)
+    t = table.cpu().numpy()
+    assert sorted(set(t.tolist())) == sorted(set(lo.image(lo.build(EVAL_C1)).tolist()))
+    assert len(set(t.tolist())) == 48 and t.max() == 47
+    # (r=1, c=0) -> 2 and (r=3, c=1)? read as the leaf coordinate (3,0,1,0):
+    # colex index 3 + 4*0 + 8*1 = 11 -> 6 + 1 = 7
+    assert t[1] == 2 and t[3 + 8] == 7
+
+
+# --------------------------------------------------------------------------
+# full-size workloads (the bench's plans), compared in full
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["C1", "C2", "C3", "C4", "C5a", "C5b"])
+def test_full_size_workload(name):
+    w = WORKLOADS[name]
+    sentinel = 0x7FF8DEADBEEF0001 if name == "C4" else None
+    run_case(w.src, w.dst, w.elem_bytes, values=w.values, dtype=w.dtype,
+             seed=w.seed, sentinel=sentinel)

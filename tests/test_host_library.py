@@ -1,0 +1,481 @@
+"""Host side of the C ABI against the oracle (no GPU needed).
+
+The library's layout algebra and its copy planner run on the host; these
+tests compare them with the oracle on exhaustive tiny cases and seeded random
+ones.  The planner is checked by expanding every piece of a plan into its
+(src offset, dst offset) pairs and comparing the union with the oracle's
+pairs {(src(i), dst(i))}: the pieces must partition the copy exactly.
+"""
+
+import itertools
+import re
+
+import numpy as np
+import pytest
+
+from oracle import layout_oracle as lo
+from workloads import WORKLOADS
+
+lm = pytest.importorskip("layout_driven_movement_gb300")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from layout_driven_movement_gb300 import _build
+    _build.build()
+    lm.lib()
+
+
+def fmt(x):
+    return str(x) if isinstance(x, int) else "(" + ",".join(fmt(k) for k in x) + ")"
+
+
+def random_layout(rng, max_modes=3, max_ext=5, max_stride=12, nest=True):
+    n = int(rng.integers(1, max_modes + 1))
+    shape, stride = [], []
+    for _ in range(n):
+        if nest and rng.random() < 0.3:
+            k = int(rng.integers(2, 4))
+            shape.append(tuple(int(v) for v in rng.integers(1, max_ext + 1, k)))
+            stride.append(tuple(int(v) for v in rng.integers(0, max_stride + 1, k)))
+        else:
+            shape.append(int(rng.integers(1, max_ext + 1)))
+            stride.append(int(rng.integers(0, max_stride + 1)))
+    return tuple(shape), tuple(stride)
+
+
+# --------------------------------------------------------------------------
+# the ABI surface
+# --------------------------------------------------------------------------
+
+def test_library_exports_every_declared_symbol():
+    import ctypes
+    import os
+    header = open(os.path.join(os.path.dirname(__file__), "..", "include",
+                               "layoutmove.h")).read()
+    names = set(re.findall(
+        r"^(?:int|void|const char\*)\s+(lm_[a-z_]+)\s*\(", header, re.M))
+    assert len(names) >= 25
+    so = ctypes.CDLL(lm.LIB_PATH)
+    for name in sorted(names):
+        assert hasattr(so, name), name
+    declared = {n for n, _, _ in lm.SIGNATURES}
+    assert names == declared
+
+
+def test_status_strings_and_version():
+    L = lm.lib()
+    assert L.lm_status_string(0) == b"LM_OK"
+    assert L.lm_status_string(-4) == b"LM_E_NOT_INJECTIVE"
+    assert L.lm_status_string(12345) == b"LM_E_UNKNOWN"
+    assert re.match(rb"\d+\.\d+\.\d+", L.lm_version())
+
+
+# --------------------------------------------------------------------------
+# construction, printing, evaluation
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("text", [
+    "(4,2):(2,1)", "((4,2),(2,4)):((2,16),(1,8))", "8:1", "(8):(3)",
+    "Sw<3,4,3> o ((64,64),(128,128)):((64,1),(524288,4096))",
+    "(((4,8),2),1048576):(((1,4),32),64)", "(0,3):(1,0)",
+])
+def test_parse_print_round_trip(text):
+    assert str(lm.Layout.parse(text)) == text
+
+
+def test_parse_static_marks_and_cute_swizzle_print():
+    assert str(lm.Layout.parse("(4,2):(_2,_1)")) == "(4,2):(2,1)"
+    L = lm.Layout.parse("Sw<3,0,3> o _0 o (8,8):(8,1)")
+    assert str(L) == "Sw<3,0,3> o (8,8):(8,1)"
+
+
+@pytest.mark.parametrize("bad", ["", "(4,2)", "(4,2):(1)", "(4,2):(1,2,3)",
+                                 "((4,2):(1,2)", "(4,-2):(1,1)", "a:b",
+                                 "Sw<3,0,2> o 8:1", "(4,2):(2,1) junk"])
+def test_parse_rejects(bad):
+    with pytest.raises(lm.LayoutMoveError) as e:
+        lm.Layout.parse(bad)
+    assert e.value.status == -1
+
+
+def test_make_matches_parse():
+    a = lm.Layout.make([4, 2, 2, 4], [2, 16, 1, 8], [2, 2])
+    assert str(a) == "((4,2),(2,4)):((2,16),(1,8))"
+    assert str(lm.Layout.make([8], [1])) == "8:1"
+    with pytest.raises(lm.LayoutMoveError):
+        lm.Layout.make([4, 2], [1, 4], [3])
+
+
+def test_eval_matches_oracle_random():
+    rng = np.random.default_rng(101)
+    for _ in range(300):
+        shape, stride = random_layout(rng)
+        L = lm.Layout.of(shape, stride)
+        O = lo.Layout(shape, stride)
+        assert L.size == O.size
+        i = np.arange(O.size)
+        want = O.at(i)
+        got = [L(int(k)) for k in i]
+        assert got == want.tolist()
+        if O.size:
+            assert L.cosize == lo.cosize(O)
+        # leaf-coordinate form
+        coord = [int(rng.integers(0, 7)) for _ in O.leaves]
+        assert L.eval_coord(coord) == lo.eval_leaf_coord(O, coord)
+
+
+def test_eval_swizzled_matches_oracle():
+    rng = np.random.default_rng(102)
+    for _ in range(200):
+        shape, stride = random_layout(rng, max_ext=6, max_stride=40)
+        b = int(rng.integers(1, 4))
+        m = int(rng.integers(0, 4))
+        s = int(rng.integers(b, b + 4))
+        L = lm.Layout.of(shape, stride).swizzle(b, m, s)
+        O = lo.Swizzled(b, m, s, lo.Layout(shape, stride))
+        i = np.arange(O.size)
+        assert [L(int(k)) for k in i] == O.at(i).tolist()
+        if O.size:
+            assert L.cosize >= lo.cosize(O)
+            assert L.cosize % (1 << (m + b)) == 0
+
+
+def test_eval_rejects_out_of_range():
+    L = lm.Layout.parse("(4,2):(2,1)")
+    for bad in (-1, 8):
+        with pytest.raises(lm.LayoutMoveError):
+            L(bad)
+
+
+def test_page_layouts_through_library():
+    blocked = lm.Layout.parse("((4,2),(2,4)):((2,16),(1,8))")
+    assert blocked.eval_coord([0, 1, 0, 0]) == 16
+    assert blocked.eval_coord([1, 0, 0, 0]) == 2
+    assert blocked.eval_coord([3, 3, 0, 0]) == 54
+    assert blocked.cosize == 48
+    sw = lm.Layout.parse("(8,8):(8,1)").swizzle(3, 0, 3)
+    for r in range(8):
+        for c in range(8):
+            assert sw(r + 8 * c) == r * 8 + (c ^ r)
+
+
+# --------------------------------------------------------------------------
+# algebra
+# --------------------------------------------------------------------------
+
+def test_compose_page_example_closed_form():
+    P = lm.Layout.parse("(8,8):(1,9)")
+    TV = lm.Layout.parse("((4,8),2):((16,1),8)")
+    assert str(P.compose(TV)) == "((4,8),2):((18,1),9)"
+    col = lm.Layout.parse("(8,8):(1,8)")
+    assert str(col.compose(TV)) == "((4,8),2):((16,1),8)"
+
+
+def test_compose_matches_oracle_random():
+    rng = np.random.default_rng(103)
+    ok = 0
+    for trial in range(600):
+        if trial % 2:
+            # compact outer layouts in random mode order: composable often
+            ext = [int(v) for v in rng.integers(1, 5, int(rng.integers(1, 4)))]
+            order = rng.permutation(len(ext))
+            stride = [0] * len(ext)
+            acc = 1
+            for k in order:
+                stride[k] = acc
+                acc *= ext[k]
+            a_shape, a_stride = tuple(ext), tuple(stride)
+        else:
+            a_shape, a_stride = random_layout(rng, max_stride=6, nest=False)
+        b_shape, b_stride = random_layout(rng, max_ext=4, max_stride=6)
+        A = lm.Layout.of(a_shape, a_stride)
+        B = lm.Layout.of(b_shape, b_stride)
+        OA, OB = lo.Layout(a_shape, a_stride), lo.Layout(b_shape, b_stride)
+        if OA.size == 0:
+            continue
+        try:
+            R = A.compose(B)
+        except lm.LayoutMoveError as e:
+            assert e.status == -3
+            continue
+        ok += 1
+        want = lo.Composed(OA, OB).at(np.arange(OB.size))
+        assert R.size == OB.size
+        assert [R(int(k)) for k in range(OB.size)] == want.tolist(), \
+            (a_shape, a_stride, b_shape, b_stride, str(R))
+    assert ok > 250
+
+
+def test_compose_swizzled_outer_and_rejects_swizzled_inner():
+    A = lm.Layout.parse("(8,8):(8,1)").swizzle(3, 0, 3)
+    B = lm.Layout.parse("(8,8):(1,8)")
+    R = A.compose(B)
+    OA = lo.Swizzled(3, 0, 3, lo.Layout((8, 8), (8, 1)))
+    want = lo.Composed(OA, lo.Layout((8, 8), (1, 8))).at(np.arange(64))
+    assert [R(k) for k in range(64)] == want.tolist()
+    with pytest.raises(lm.LayoutMoveError) as e:
+        B.compose(A)
+    assert e.value.status == -3
+
+
+def test_zipped_divide_page_example_and_c3():
+    Z = lm.Layout.parse("(128,128):(1,128)").zipped_divide([4, 8])
+    assert str(Z) == "((4,8),(32,16)):((1,128),(4,1024))"
+    Z3 = lm.build_layout(WORKLOADS["C3"].src)
+    assert str(Z3) == "((64,64),(128,128)):((8192,1),(524288,64))"
+
+
+def test_zipped_divide_matches_oracle_random():
+    rng = np.random.default_rng(104)
+    ok = 0
+    for _ in range(400):
+        shape, stride = random_layout(rng, max_modes=3, max_ext=6)
+        O = lo.Layout(shape, stride)
+        modes = O.modes()
+        tiler = []
+        for m in modes:
+            divs = [t for t in range(1, m.size + 1) if m.size % t == 0] or [1]
+            tiler.append(int(rng.choice(divs)) if m.size else 1)
+        if O.size == 0:
+            continue
+        L = lm.Layout.of(shape, stride)
+        try:
+            Z = L.zipped_divide(tiler)
+        except lm.LayoutMoveError as e:
+            assert e.status == -3
+            continue
+        ok += 1
+        want = lo.ZippedDivide(O, tiler).at(np.arange(O.size))
+        assert [Z(int(k)) for k in range(O.size)] == want.tolist(), \
+            (shape, stride, tiler, str(Z))
+    assert ok > 200
+
+
+def test_zipped_divide_rejects_non_dividing_tiler():
+    with pytest.raises(lm.LayoutMoveError) as e:
+        lm.Layout.parse("(6,4):(1,6)").zipped_divide([4, 4])
+    assert e.value.status == -3
+    with pytest.raises(lm.LayoutMoveError) as e:
+        lm.Layout.parse("(6,4):(1,6)").zipped_divide([2])
+    assert e.value.status == -1
+
+
+def test_coalesce_keeps_function():
+    rng = np.random.default_rng(105)
+    for _ in range(200):
+        shape, stride = random_layout(rng)
+        L = lm.Layout.of(shape, stride)
+        C = L.coalesce()
+        O = lo.Layout(shape, stride)
+        assert [C(k) for k in range(O.size)] == O.at(np.arange(O.size)).tolist()
+    assert str(lm.Layout.parse("(4,2,3):(1,4,8)").coalesce()) == "24:1"
+
+
+def test_right_inverse_round_trip_and_oracle():
+    rng = np.random.default_rng(106)
+    for _ in range(150):
+        ext = [int(v) for v in rng.integers(1, 6, int(rng.integers(1, 4)))]
+        order = rng.permutation(len(ext))
+        stride = [0] * len(ext)
+        acc = 1
+        for k in order:
+            stride[k] = acc
+            acc *= ext[k]
+        L = lm.Layout.of(tuple(ext), tuple(stride))
+        R = L.right_inverse()
+        O = lo.Layout(tuple(ext), tuple(stride))
+        assert R.size == O.size
+        want = lo.right_inverse_values(O)
+        assert [R(j) for j in range(R.size)] == want.tolist()
+    assert str(lm.Layout.parse("(4,2):(2,1)").right_inverse()) == "(2,4):(4,1)"
+
+
+def test_max_common_vector_matches_oracle():
+    rng = np.random.default_rng(107)
+    for _ in range(300):
+        ext = [int(v) for v in rng.integers(1, 5, int(rng.integers(1, 4)))]
+        def compact(perm, gap=0):
+            stride = [0] * len(ext)
+            acc = 1
+            for k in perm:
+                stride[k] = acc
+                acc *= ext[k] + (gap if k == perm[-1] else 0)
+            return tuple(stride)
+        sa = compact(rng.permutation(len(ext)))
+        sb = compact(rng.permutation(len(ext)), int(rng.integers(0, 2)))
+        A = lm.Layout.of(tuple(ext), sa)
+        B = lm.Layout.of(tuple(ext), sb)
+        if rng.random() < 0.3:
+            b = int(rng.integers(1, 3))
+            m = int(rng.integers(0, 3))
+            s = int(rng.integers(b, b + 3))
+            B = B.swizzle(b, m, s)
+            OB = lo.Swizzled(b, m, s, lo.Layout(tuple(ext), sb))
+        else:
+            OB = lo.Layout(tuple(ext), sb)
+        OA = lo.Layout(tuple(ext), sa)
+        assert A.max_common_vector(B) == lo.max_common_vector(OA, OB)
+    with pytest.raises(lm.LayoutMoveError) as e:
+        lm.Layout.parse("4:1").max_common_vector(lm.Layout.parse("5:1"))
+    assert e.value.status == -2
+
+
+def test_max_common_vector_large_uses_structure():
+    # 2^22 elements: beyond the brute-force limit, answered from joint modes
+    a = lm.Layout.parse("(64,65536):(1,64)")
+    b = lm.Layout.parse("(64,65536):(1,128)")
+    assert a.max_common_vector(b) == 64
+    c = lm.build_layout(WORKLOADS["C3"].src)
+    d = lm.build_layout(WORKLOADS["C3"].dst)
+    assert c.max_common_vector(d) == 64
+
+
+def test_stripmined_layout_matches_oracle():
+    for threads, pitch, strips, k_row in itertools.product(
+            (32, 64, 100), (1, 4, 8), (1, 2, 4), (16, 33)):
+        L = lm.Layout.stripmined(threads, pitch, strips, k_row)
+        t = np.arange(threads)
+        want = lo.stripmined_offset(t, k_row, pitch, strips)
+        assert [L(int(k)) for k in t] == want.tolist()
+
+
+# --------------------------------------------------------------------------
+# the planner
+# --------------------------------------------------------------------------
+
+def plan_pairs(plan: "lm.Plan", s_swz, d_swz):
+    """Expand a joint plan's pieces into its (src, dst) offset pairs."""
+    desc = plan.describe()
+    assert desc["joint"]
+    src, dst = [], []
+    for pc in desc["pieces"]:
+        ms = pc["modes"]
+        n = int(np.prod([m[0] for m in ms])) if ms else 1
+        i = np.arange(n)
+        so = np.full(n, pc["s_base"], dtype=np.int64)
+        do = np.full(n, pc["d_base"], dtype=np.int64)
+        for e, s, d in ms:
+            c = i % e
+            i = i // e
+            so += c * s
+            do += c * d
+        src.append(so)
+        dst.append(do)
+    so = np.concatenate(src) if src else np.zeros(0, np.int64)
+    do = np.concatenate(dst) if dst else np.zeros(0, np.int64)
+    if s_swz:
+        so = lo.swizzle(so, *s_swz)
+    if d_swz:
+        do = lo.swizzle(do, *d_swz)
+    return so, do
+
+
+def check_plan_partition(src_spec, dst_spec, eb):
+    S, D = lm.build_layout(src_spec), lm.build_layout(dst_spec)
+    OS, OD = lo.build(src_spec), lo.build(dst_spec)
+    plan = lm.Plan(S, D, eb)
+    desc = plan.describe()
+    if not desc["joint"]:
+        return desc
+    s_swz = (OS.b, OS.m, OS.s) if isinstance(OS, lo.Swizzled) else None
+    d_swz = (OD.b, OD.m, OD.s) if isinstance(OD, lo.Swizzled) else None
+    so, do = plan_pairs(plan, s_swz, d_swz)
+    i = np.arange(OS.size)
+    want = np.stack([OS.at(i), OD.at(i)], 1)
+    got = np.stack([so, do], 1)
+    assert got.shape == want.shape
+    order_w = np.lexsort((want[:, 0], want[:, 1]))
+    order_g = np.lexsort((got[:, 0], got[:, 1]))
+    assert (want[order_w] == got[order_g]).all()
+    n, sc, dc = plan.extent()
+    assert n == OS.size and sc >= lo.cosize(OS) and dc >= lo.cosize(OD)
+    assert plan.launches == len(desc["pieces"])
+    return desc
+
+
+def test_plan_paths_for_workloads():
+    paths = {}
+    for name, w in WORKLOADS.items():
+        S, D = lm.build_layout(w.src), lm.build_layout(w.dst)
+        paths[name] = [p["path"] for p in lm.Plan(S, D, w.elem_bytes).describe()["pieces"]]
+    assert paths == {"C1": ["GENERIC"], "C2": ["STAGED"], "C3": ["VEC"],
+                     "C4": ["STAGED"], "C5a": ["STAGED"], "C5b": ["STAGED"]}
+
+
+def test_plan_partition_small_workload_shapes():
+    cases = [
+        (WORKLOADS["C1"].src, WORKLOADS["C1"].dst, 4),
+        (("layout", (200, 136), (1, 200)), ("layout", (200, 136), (136, 1)), 4),
+        (("zipped_divide", ("layout", (256, 192), (192, 1)), (64, 64)),
+         ("swizzle", 3, 4, 3, ("layout", ((64, 64), (4, 3)), ((64, 1), (12288, 4096)))), 2),
+        (("concat", WORKLOADS["C4"].src[1], ("layout", 100, 72)),
+         ("layout", (((4, 8), 2), 100), (((1, 4), 32), 64)), 8),
+        (("layout", (3, 40, 7, 9), (2520, 1, 360, 40)),
+         ("layout", (3, 40, 7, 9), (2520, 63, 9, 1)), 2),
+        (("layout", (2, 1000, 24), (24000, 24, 1)),
+         ("layout", (2, 1000, 24), (1, 48, 2)), 2),
+        (("layout", (97, 131), (1, 97)), ("layout", (97, 131), (131, 1)), 1),
+        (("layout", (50, 60), (1, 50)), ("layout", (50, 60), (60, 1)), 16),
+        (("layout", (4096,), (1,)), ("layout", (4096,), (1,)), 4),
+        (("layout", (5000,), (1,)), ("layout", (5000,), (1,)), 2),
+    ]
+    for s, d, eb in cases:
+        check_plan_partition(s, d, eb)
+
+
+def test_plan_partition_random_bijections():
+    rng = np.random.default_rng(108)
+    for _ in range(120):
+        nm = int(rng.integers(1, 5))
+        ext = [int(v) for v in rng.integers(1, 40, nm)]
+        def compact(perm, pad):
+            stride = [0] * nm
+            acc = 1
+            for k in perm:
+                stride[k] = acc
+                acc *= ext[k] + (pad if k == perm[0] else 0)
+            return tuple(stride)
+        s = ("layout", tuple(ext), compact(rng.permutation(nm), int(rng.integers(0, 3))))
+        d = ("layout", tuple(ext), compact(rng.permutation(nm), 0))
+        eb = int(rng.choice([1, 2, 4, 8, 16]))
+        check_plan_partition(s, d, eb)
+
+
+def test_plan_errors():
+    a = lm.Layout.parse("(8,8):(1,8)")
+    with pytest.raises(lm.LayoutMoveError) as e:
+        lm.Plan(a, lm.Layout.parse("(8,4):(1,8)"), 4)
+    assert e.value.status == -2
+    with pytest.raises(lm.LayoutMoveError) as e:
+        lm.Plan(a, lm.Layout.parse("((4,2),(2,4)):((2,16),(1,8))"), 4)
+    assert e.value.status == -4
+    with pytest.raises(lm.LayoutMoveError) as e:
+        lm.Plan(a, a, 3)
+    assert e.value.status == -1
+    with pytest.raises(lm.LayoutMoveError) as e:
+        lm.Plan(a, lm.Layout.parse("(8,8):(0,1)"), 4)
+    assert e.value.status == -4
+
+
+def test_plan_non_refinable_pair_is_generic_and_empty_plan():
+    s = lm.Layout.parse("(2,3):(1,2)")
+    d = lm.Layout.parse("(3,2):(2,1)")
+    desc = lm.Plan(s, d, 4).describe()
+    assert not desc["joint"] and desc["pieces"][0]["path"] == "GENERIC"
+    e = lm.Plan(lm.Layout.parse("(0,4):(1,0)"), lm.Layout.parse("(0,4):(4,1)"), 4)
+    assert e.describe()["pieces"] == [] and e.launches == 0
+
+
+def test_copy_validation_without_gpu():
+    """Host-side checks of lm_layout_copy fire before any CUDA call."""
+    import ctypes as C
+    L = lm.lib()
+    p = lm.Plan(lm.Layout.parse("(64,64):(1,64)"), lm.Layout.parse("(64,64):(64,1)"), 4)
+    assert L.lm_layout_copy(p.handle, C.c_void_p(4096), 4095, C.c_void_p(1 << 30), 4096, None) == -6
+    assert L.lm_layout_copy(p.handle, C.c_void_p(4096), 4096, C.c_void_p(4096 + 100), 4096, None) == -7
+    assert L.lm_layout_copy(p.handle, None, 4096, C.c_void_p(1 << 30), 4096, None) == -1
+    assert L.lm_layout_eval_device(lm.Layout.parse("8:1").handle, C.c_void_p(4096), 3, 8, None) == -1
+    assert L.lm_layout_eval_device(lm.Layout.parse("8:1").handle, C.c_void_p(4096), 4, 7, None) == -6
+    big = lm.Layout.parse("(2,2):(1,4294967296)")
+    assert L.lm_layout_eval_device(big.handle, C.c_void_p(4096), 4, 8, None) == -5
