@@ -88,6 +88,8 @@ class ClockSampler:
         self.window = (0.0, float("inf"))
 
     def __enter__(self):
+        if not self.gpu:
+            return self
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}",
@@ -193,7 +195,8 @@ def run_native(args) -> dict | None:
         dist.barrier()
     import layout_driven_movement_gb300 as lm
     lm.lib()
-    suite = Suite(device)
+    names = tuple(args.workloads.split(",")) if args.workloads else BENCH_SUITE
+    suite = Suite(device, names)
     torch.cuda.synchronize()
     for _ in range(args.warmup):
         suite.step()
@@ -202,8 +205,9 @@ def run_native(args) -> dict | None:
     n = len(suite.items)
     events = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)]
                for _ in range(n)] for _ in range(args.steps)]
-    with ClockSampler(gpu_smi_id(local)) as clk:
-        time.sleep(1.0)             # let the sampler start
+    with ClockSampler(gpu_smi_id(local) if not args.quick else "") as clk:
+        if not args.quick:
+            time.sleep(1.0)         # let the sampler start
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
@@ -238,9 +242,10 @@ def run_native(args) -> dict | None:
             "path": "+".join(p["path"] for p in it["plan"].describe()["pieces"]),
             "bytes": it["bytes"], "median_us": round(ms * 1e3, 2),
             "gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4)}
-    dom = per[DOMINANT]
+    dom_name = DOMINANT if DOMINANT in per else suite.items[0]["name"]
+    dom = per[dom_name]
     dom_ms = sum(dom) / len(dom)
-    achieved = ALGO_BYTES[DOMINANT] / (dom_ms * 1e-3) / 1e9
+    achieved = ALGO_BYTES[dom_name] / (dom_ms * 1e-3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1),
                 "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4),
@@ -251,8 +256,8 @@ def run_native(args) -> dict | None:
     if rank != 0:
         return None
 
-    e2e = measure_e2e(suite, args, torch)
-    cpu = cpu_baseline(suite) if world == 1 else None
+    e2e = measure_e2e(suite, args, torch) if not args.quick else None
+    cpu = cpu_baseline(suite) if world == 1 and not args.quick else None
     clocks = clk.summary()
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT,
@@ -262,8 +267,8 @@ def run_native(args) -> dict | None:
         "dtype": "u8", "data": "synthetic (seeded numpy PCG64, shapes and "
         "value distributions of the five relayouts)",
         "config": {
-            "workload": "relayout suite C2+C3+C4+C5a+C5b, one layout_copy "
-                        "each per step",
+            "workload": "relayout suite " + "+".join(names) +
+                        ", one layout_copy each per step",
             "bytes_per_step": suite.bytes_per_step,
             "element_types": "fp32, bf16, fp64, fp16, fp16 (moved as raw bytes)",
             "l2": "no flush: 1.87 GB/step over five buffer pairs, each reused "
@@ -435,6 +440,10 @@ def main():
     ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workloads", default="",
+                    help="comma-separated subset of the suite (profiling)")
+    ap.add_argument("--quick", action="store_true",
+                    help="skip the clock sampler, e2e and CPU legs (profiling)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":

@@ -198,9 +198,21 @@ struct StagedArgs {
   uint32_t di_ext[kMaxTile];
   FastDiv di_div[kMaxTile];
   uint32_t di_m[kMaxTile];              // smem bytes per coordinate
+  // transpose store (store_mode 1): micro-tiles of R rows (dst-fast mode b)
+  // by one 16-byte chunk (V elements of the src-fast mode a)
+  int32_t store_mode = 0;               // 0 gather, 1 transpose
+  int32_t xr = 0;                       // R, rows per micro-tile
+  uint32_t n_micro = 0;                 // micro-tiles per tile
+  uint32_t n_bc = 1;                    // micro-tiles along b (fastest)
+  FastDiv bc_div;
+  uint32_t x_pitch = 0;                 // smem bytes between rows
+  int64_t x_da = 0;                     // dst bytes per 16-byte chunk of a
+  int64_t x_db = 0;                     // dst bytes per R rows of b
+  int64_t x_vstep = 0;                  // dst bytes between output vectors
   // shared memory
   uint32_t stage_bytes = 0;
   Swz m_swz;                            // smem swizzle, bytes
+  int32_t threads = 256;                // block size
 };
 
 struct EvalArgs {
@@ -229,6 +241,7 @@ struct Piece {
   int64_t s_base = 0, d_base = 0;  // elements
   int vec_bytes = 0;               // VEC: bytes per vector
   int64_t tile_elems = 0;          // STAGED: elements per tile
+  int xr = 0;                      // STAGED transpose: rows per micro-tile
   GenericArgs gen;                 // always filled (fallback)
   VecArgs vec;
   StagedArgs st;

@@ -189,17 +189,19 @@ __global__ void __launch_bounds__(256)
 
 // ---------------------------------------------------------------------------
 // STAGED copy
+//
+// The load side is shared: each thread owns a fixed set of 16-byte chunks of
+// the tile's source image (the same for every tile) and moves them with
+// cp.async into a swizzled shared-memory image, one tile ahead of the store
+// side (two stages).  The store side is a policy:
+//   GatherStore : per-element gathers from shared memory into 16-byte
+//                 destination vectors (any tile structure);
+//   XposeStore  : micro-tiles of R rows x 16 bytes read with 16-byte shared
+//                 loads and transposed in registers (byte permutes), for
+//                 tiles that are a 2-D transpose.
 // ---------------------------------------------------------------------------
 
-constexpr int kStagedThreads = 256;
-constexpr int kMaxLoadSlots = 8;
-
-template <int EB>
-struct StagedTraits {
-  static constexpr int V = 16 / EB;  // elements per 16-byte chunk
-  static constexpr int MaxStore = (32 / V) < 8 ? ((32 / V) > 0 ? 32 / V : 1) : 8;
-  static constexpr int Packed = (V + 1) / 2;  // 16-bit smem addresses, 2/reg
-};
+constexpr int kMaxLoadSlots = 4;
 
 __device__ __forceinline__ void cp_async16(uint32_t smem_addr, const void* g,
                                            int src_bytes) {
@@ -214,6 +216,10 @@ __device__ __forceinline__ void cp_async_commit() {
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(const unsigned char* p) {
+  return *reinterpret_cast<const uint4*>(p);
 }
 
 // Tile origin offsets (bytes).  Lane k of each group of 8 lanes computes
@@ -239,181 +245,273 @@ __device__ __forceinline__ void tile_base(const StagedArgs& a, uint32_t tile,
   db = d;
 }
 
-template <int EB>
-__device__ __forceinline__ uint4 gather16(const unsigned char* sm,
-                                          const uint32_t* packed) {
-  constexpr int V = StagedTraits<EB>::V;
-  auto addr = [&](int e) -> uint32_t {
-    return (packed[e >> 1] >> ((e & 1) * 16)) & 0xffffu;
-  };
-  uint4 r;
-  uint32_t w[4];
-  if constexpr (EB == 16) {
-    r = *reinterpret_cast<const uint4*>(sm + addr(0));
-    return r;
-  } else if constexpr (EB == 8) {
-    const uint2 x = *reinterpret_cast<const uint2*>(sm + addr(0));
-    const uint2 y = *reinterpret_cast<const uint2*>(sm + addr(1));
-    w[0] = x.x;
-    w[1] = x.y;
-    w[2] = y.x;
-    w[3] = y.y;
-  } else if constexpr (EB == 4) {
+struct LoadSlots {
+  int32_t src[kMaxLoadSlots];
+  uint32_t sm[kMaxLoadSlots];
+
+  __device__ __forceinline__ void init(const StagedArgs& a, uint32_t tid,
+                                       uint32_t nt) {
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
-      w[e] = *reinterpret_cast<const uint32_t*>(sm + addr(e));
-  } else if constexpr (EB == 2) {
+    for (int k = 0; k < kMaxLoadSlots; ++k) {
+      const uint32_t j = tid + uint32_t(k) * nt;
+      src[k] = -1;
+      sm[k] = 0;
+      if (j < a.n_lchunks) {
+        const uint32_t seg = fdiv(j, a.cps_div);
+        const uint32_t c = j - seg * a.cps;
+        int64_t srel = int64_t(c) * 16;
+        uint32_t mrel = c * 16u;
+        uint32_t r = seg;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t lo = *reinterpret_cast<const uint16_t*>(sm + addr(2 * i));
-      const uint32_t hi =
-          *reinterpret_cast<const uint16_t*>(sm + addr(2 * i + 1));
-      w[i] = lo | (hi << 16);
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t b0 = sm[addr(4 * i)];
-      const uint32_t b1 = sm[addr(4 * i + 1)];
-      const uint32_t b2 = sm[addr(4 * i + 2)];
-      const uint32_t b3 = sm[addr(4 * i + 3)];
-      w[i] = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+        for (int t = 0; t < kMaxTile; ++t) {
+          if (t >= a.nso) break;
+          const uint32_t rn = fdiv(r, a.so_div[t]);
+          const uint32_t x = r - rn * a.so_ext[t];
+          srel += int64_t(x) * a.so_s[t];
+          mrel += x * a.so_m[t];
+          r = rn;
+        }
+        src[k] = int32_t(srel);
+        sm[k] = swz_apply32(a.m_swz, mrel);
+      }
     }
   }
-  (void)V;
-  r.x = w[0];
-  r.y = w[1];
-  r.z = w[2];
-  r.w = w[3];
-  return r;
-}
+
+  __device__ __forceinline__ void issue(const StagedArgs& a, const char* src_p,
+                                        int64_t src_cap, int64_t base,
+                                        uint32_t sm_stage) const {
+#pragma unroll
+    for (int k = 0; k < kMaxLoadSlots; ++k) {
+      if (src[k] < 0) continue;
+      const int64_t off = swz_apply(a.s_swz, base + src[k]);
+      const int64_t room = src_cap - off;
+      const int nbytes = room >= 16 ? 16 : (room > 0 ? int(room) : 0);
+      cp_async16(sm_stage + sm[k], nbytes ? src_p + off : src_p, nbytes);
+    }
+  }
+};
 
 template <int EB>
-__global__ void __launch_bounds__(kStagedThreads)
+struct GatherStore {
+  static constexpr int V = 16 / EB;
+  static constexpr int MaxS = (16 / V) < 1 ? 1 : ((16 / V) > 4 ? 4 : 16 / V);
+  int32_t dst[MaxS];
+  uint32_t sm[MaxS][V];
+
+  __device__ __forceinline__ void init(const StagedArgs& a, uint32_t tid,
+                                       uint32_t nt) {
+#pragma unroll
+    for (int k = 0; k < MaxS; ++k) {
+      const uint32_t j = tid + uint32_t(k) * nt;
+      dst[k] = -1;
+#pragma unroll
+      for (int e = 0; e < V; ++e) sm[k][e] = 0;
+      if (j < a.n_schunks) {
+        const uint32_t o = fdiv(j, a.cpd_div);
+        const uint32_t p = j - o * a.cpd;
+        int64_t drel = int64_t(p) * 16;
+        uint32_t mb = 0, r = o;
+#pragma unroll
+        for (int t = 0; t < kMaxTile; ++t) {
+          if (t >= a.ndo) break;
+          const uint32_t rn = fdiv(r, a.do_div[t]);
+          const uint32_t x = r - rn * a.do_ext[t];
+          drel += int64_t(x) * a.do_d[t];
+          mb += x * a.do_m[t];
+          r = rn;
+        }
+        dst[k] = int32_t(drel);
+#pragma unroll
+        for (int e = 0; e < V; ++e) {
+          uint32_t q = p * uint32_t(V) + uint32_t(e);
+          uint32_t m = mb;
+#pragma unroll
+          for (int t = 0; t < kMaxTile; ++t) {
+            if (t >= a.ndi) break;
+            const uint32_t qn = fdiv(q, a.di_div[t]);
+            m += (q - qn * a.di_ext[t]) * a.di_m[t];
+            q = qn;
+          }
+          sm[k][e] = swz_apply32(a.m_swz, m);
+        }
+      }
+    }
+  }
+
+  __device__ __forceinline__ void store(const StagedArgs& a,
+                                        const unsigned char* smst, char* dst_p,
+                                        int64_t dbase) const {
+#pragma unroll
+    for (int k = 0; k < MaxS; ++k) {
+      if (dst[k] < 0) continue;
+      uint32_t w[4];
+      if constexpr (EB == 16) {
+        const uint4 v = lds128(smst + sm[k][0]);
+        w[0] = v.x;
+        w[1] = v.y;
+        w[2] = v.z;
+        w[3] = v.w;
+      } else if constexpr (EB == 8) {
+        const uint2 x = *reinterpret_cast<const uint2*>(smst + sm[k][0]);
+        const uint2 y = *reinterpret_cast<const uint2*>(smst + sm[k][1]);
+        w[0] = x.x;
+        w[1] = x.y;
+        w[2] = y.x;
+        w[3] = y.y;
+      } else if constexpr (EB == 4) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          w[e] = *reinterpret_cast<const uint32_t*>(smst + sm[k][e]);
+      } else if constexpr (EB == 2) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t lo = *reinterpret_cast<const uint16_t*>(smst + sm[k][2 * i]);
+          const uint32_t hi = *reinterpret_cast<const uint16_t*>(smst + sm[k][2 * i + 1]);
+          w[i] = __byte_perm(lo, hi, 0x5410);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t b0 = smst[sm[k][4 * i]];
+          const uint32_t b1 = smst[sm[k][4 * i + 1]];
+          const uint32_t b2 = smst[sm[k][4 * i + 2]];
+          const uint32_t b3 = smst[sm[k][4 * i + 3]];
+          w[i] = __byte_perm(__byte_perm(b0, b1, 0x0040),
+                             __byte_perm(b2, b3, 0x0040), 0x5410);
+        }
+      }
+      const int64_t off = swz_apply(a.d_swz, dbase + dst[k]);
+      __stcs(reinterpret_cast<uint4*>(dst_p + off),
+             make_uint4(w[0], w[1], w[2], w[3]));
+    }
+  }
+};
+
+// Register transpose of R rows of V = 16/EB elements: output word W of the
+// column-by-column order (element f = in[f % R][f / R]).  W is a
+// compile-time constant after unrolling, so every index is too.
+template <int EB, int R>
+__device__ __forceinline__ uint32_t xword(const uint32_t (&in)[R][4], int W) {
+  if constexpr (EB == 4) {
+    return in[W % R][W / R];
+  } else if constexpr (EB == 8) {
+    const int f = W / 2;
+    return in[f % R][(f / R) * 2 + (W % 2)];
+  } else if constexpr (EB == 2) {
+    const int f0 = 2 * W, f1 = 2 * W + 1;
+    const int a0 = f0 / R, b0 = f0 % R, a1 = f1 / R, b1 = f1 % R;
+    const uint32_t sel =
+        ((a0 & 1) ? 0x32u : 0x10u) | ((a1 & 1) ? 0x7600u : 0x5400u);
+    return __byte_perm(in[b0][a0 / 2], in[b1][a1 / 2], sel);
+  } else {  // EB == 1
+    uint32_t t[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int f0 = 4 * W + 2 * h, f1 = f0 + 1;
+      const int a0 = f0 / R, b0 = f0 % R, a1 = f1 / R, b1 = f1 % R;
+      const uint32_t sel = uint32_t(a0 % 4) | (uint32_t(4 + a1 % 4) << 4);
+      t[h] = __byte_perm(in[b0][a0 / 4], in[b1][a1 / 4], sel);
+    }
+    return __byte_perm(t[0], t[1], 0x5410);
+  }
+}
+
+template <int EB, int R>
+struct XposeStore {
+  static constexpr int MaxM = R >= 8 ? 1 : 2;
+  int32_t dst[MaxM];
+  uint32_t sm[MaxM][R];
+
+  __device__ __forceinline__ void init(const StagedArgs& a, uint32_t tid,
+                                       uint32_t nt) {
+#pragma unroll
+    for (int k = 0; k < MaxM; ++k) {
+      const uint32_t j = tid + uint32_t(k) * nt;
+      dst[k] = -1;
+#pragma unroll
+      for (int r = 0; r < R; ++r) sm[k][r] = 0;
+      if (j < a.n_micro) {
+        const uint32_t ac = fdiv(j, a.bc_div);
+        const uint32_t bc = j - ac * a.n_bc;
+        dst[k] = int32_t(int64_t(ac) * a.x_da + int64_t(bc) * a.x_db);
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+          sm[k][r] = swz_apply32(a.m_swz,
+                                 (bc * uint32_t(R) + uint32_t(r)) * a.x_pitch +
+                                     ac * 16u);
+      }
+    }
+  }
+
+  __device__ __forceinline__ void store(const StagedArgs& a,
+                                        const unsigned char* smst, char* dst_p,
+                                        int64_t dbase) const {
+#pragma unroll
+    for (int k = 0; k < MaxM; ++k) {
+      if (dst[k] < 0) continue;
+      uint32_t in[R][4];
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const uint4 v = lds128(smst + sm[k][r]);
+        in[r][0] = v.x;
+        in[r][1] = v.y;
+        in[r][2] = v.z;
+        in[r][3] = v.w;
+      }
+      const int64_t base = dbase + dst[k];
+#pragma unroll
+      for (int j = 0; j < R; ++j) {
+        const int64_t off = swz_apply(a.d_swz, base + j * a.x_vstep);
+        __stcs(reinterpret_cast<uint4*>(dst_p + off),
+               make_uint4(xword<EB, R>(in, 4 * j), xword<EB, R>(in, 4 * j + 1),
+                          xword<EB, R>(in, 4 * j + 2),
+                          xword<EB, R>(in, 4 * j + 3)));
+      }
+    }
+  }
+};
+
+template <int EB, class Store>
+__global__ void __launch_bounds__(256)
     lm_staged_kernel(const __grid_constant__ StagedArgs a,
                      const char* __restrict__ src, char* __restrict__ dst,
                      int64_t src_cap) {
   extern __shared__ __align__(128) unsigned char smem[];
-  using Tr = StagedTraits<EB>;
-  constexpr int V = Tr::V;
   const uint32_t tid = threadIdx.x;
   const uint32_t nt = blockDim.x;
-
-  // ---- per-thread slots, the same for every tile -----------------------
-  int32_t l_src[kMaxLoadSlots];
-  uint32_t l_sm[kMaxLoadSlots];
-#pragma unroll
-  for (int k = 0; k < kMaxLoadSlots; ++k) {
-    const uint32_t j = tid + uint32_t(k) * nt;
-    l_src[k] = -1;
-    l_sm[k] = 0;
-    if (j < a.n_lchunks) {
-      const uint32_t seg = fdiv(j, a.cps_div);
-      const uint32_t c = j - seg * a.cps;
-      int64_t srel = int64_t(c) * 16;
-      uint32_t mrel = c * 16u;
-      uint32_t r = seg;
-#pragma unroll
-      for (int t = 0; t < kMaxTile; ++t) {
-        if (t >= a.nso) break;
-        const uint32_t rn = fdiv(r, a.so_div[t]);
-        const uint32_t x = r - rn * a.so_ext[t];
-        srel += int64_t(x) * a.so_s[t];
-        mrel += x * a.so_m[t];
-        r = rn;
-      }
-      l_src[k] = int32_t(srel);
-      l_sm[k] = swz_apply32(a.m_swz, mrel);
-    }
-  }
-  int32_t s_dst[Tr::MaxStore];
-  uint32_t s_sm[Tr::MaxStore][Tr::Packed];
-#pragma unroll
-  for (int k = 0; k < Tr::MaxStore; ++k) {
-    const uint32_t j = tid + uint32_t(k) * nt;
-    s_dst[k] = -1;
-#pragma unroll
-    for (int i = 0; i < Tr::Packed; ++i) s_sm[k][i] = 0;
-    if (j < a.n_schunks) {
-      const uint32_t o = fdiv(j, a.cpd_div);
-      const uint32_t p = j - o * a.cpd;
-      int64_t drel = int64_t(p) * 16;
-      uint32_t mb = 0, r = o;
-#pragma unroll
-      for (int t = 0; t < kMaxTile; ++t) {
-        if (t >= a.ndo) break;
-        const uint32_t rn = fdiv(r, a.do_div[t]);
-        const uint32_t x = r - rn * a.do_ext[t];
-        drel += int64_t(x) * a.do_d[t];
-        mb += x * a.do_m[t];
-        r = rn;
-      }
-      s_dst[k] = int32_t(drel);
-#pragma unroll
-      for (int e = 0; e < V; ++e) {
-        uint32_t q = p * uint32_t(V) + uint32_t(e);
-        uint32_t m = mb;
-#pragma unroll
-        for (int t = 0; t < kMaxTile; ++t) {
-          if (t >= a.ndi) break;
-          const uint32_t qn = fdiv(q, a.di_div[t]);
-          m += (q - qn * a.di_ext[t]) * a.di_m[t];
-          q = qn;
-        }
-        m = swz_apply32(a.m_swz, m);
-        s_sm[k][e >> 1] |= (m & 0xffffu) << ((e & 1) * 16);
-      }
-    }
-  }
+  LoadSlots ls;
+  ls.init(a, tid, nt);
+  Store st;
+  st.init(a, tid, nt);
 
   uint32_t tile = blockIdx.x;
   if (tile >= a.n_tiles) return;
   const uint32_t smem0 = uint32_t(__cvta_generic_to_shared(smem));
-
-  auto issue = [&](uint32_t t, int stage) {
-    int64_t sb, db;
-    tile_base(a, t, sb, db);
-    const int64_t base = a.s_base + sb;
-    const uint32_t sm_stage = smem0 + uint32_t(stage) * a.stage_bytes;
-#pragma unroll
-    for (int k = 0; k < kMaxLoadSlots; ++k) {
-      if (l_src[k] < 0) continue;
-      const int64_t off = swz_apply(a.s_swz, base + l_src[k]);
-      const int64_t room = src_cap - off;
-      const int nbytes = room >= 16 ? 16 : (room > 0 ? int(room) : 0);
-      cp_async16(sm_stage + l_sm[k], nbytes ? src + off : src, nbytes);
-    }
-  };
-
-  int stage = 0;
-  issue(tile, 0);
+  int64_t sb, db;
+  tile_base(a, tile, sb, db);
+  ls.issue(a, src, src_cap, a.s_base + sb, smem0);
   cp_async_commit();
+  int stage = 0;
   for (;;) {
     const uint64_t next64 = uint64_t(tile) + gridDim.x;
     const bool has_next = next64 < a.n_tiles;
+    int64_t nsb = 0, ndb = 0;
     if (has_next) {
-      issue(uint32_t(next64), stage ^ 1);
+      tile_base(a, uint32_t(next64), nsb, ndb);
+      ls.issue(a, src, src_cap, a.s_base + nsb,
+               smem0 + uint32_t(stage ^ 1) * a.stage_bytes);
       cp_async_commit();
       cp_async_wait<1>();
     } else {
       cp_async_wait<0>();
     }
     __syncthreads();
-    int64_t sb, db;
-    tile_base(a, tile, sb, db);
-    const int64_t dbase = a.d_base + db;
-    const unsigned char* sm = smem + size_t(stage) * a.stage_bytes;
-#pragma unroll
-    for (int k = 0; k < Tr::MaxStore; ++k) {
-      if (s_dst[k] < 0) continue;
-      const uint4 v = gather16<EB>(sm, s_sm[k]);
-      const int64_t off = swz_apply(a.d_swz, dbase + s_dst[k]);
-      __stcs(reinterpret_cast<uint4*>(dst + off), v);
-    }
+    st.store(a, smem + size_t(stage) * a.stage_bytes, dst, a.d_base + db);
     __syncthreads();
     if (!has_next) break;
     tile = uint32_t(next64);
     stage ^= 1;
+    db = ndb;
   }
 }
 
@@ -513,7 +611,7 @@ int launch_vec_t(const VecArgs& v, const char* src, char* dst,
   return check_launch();
 }
 
-template <int EB>
+template <int EB, class Store>
 int launch_staged_t(const StagedArgs& a, const char* src, int64_t src_cap,
                     char* dst, cudaStream_t st) {
   // two stages of at most 24 KiB each: within the default 48 KiB of
@@ -522,16 +620,64 @@ int launch_staged_t(const StagedArgs& a, const char* src, int64_t src_cap,
   const DeviceInfo di = device_info();
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-          &per_sm, lm_staged_kernel<EB>, kStagedThreads, size_t(smem)) !=
+          &per_sm, lm_staged_kernel<EB, Store>, a.threads, size_t(smem)) !=
           cudaSuccess ||
       per_sm < 1)
     per_sm = 1;
   const uint64_t cap = uint64_t(di.sms) * uint64_t(per_sm);
   const unsigned grid =
       unsigned(std::max<uint64_t>(1, std::min<uint64_t>(a.n_tiles, cap)));
-  lm_staged_kernel<EB><<<grid, kStagedThreads, size_t(smem), st>>>(
+  lm_staged_kernel<EB, Store><<<grid, a.threads, size_t(smem), st>>>(
       a, src, dst, src_cap);
   return check_launch();
+}
+
+template <int EB>
+int launch_xpose(const StagedArgs& a, const char* src, int64_t cap, char* dst,
+                 cudaStream_t st) {
+  constexpr int V = 16 / EB;
+  switch (a.xr) {
+    case 2:
+      if constexpr (V >= 2)
+        return launch_staged_t<EB, XposeStore<EB, 2>>(a, src, cap, dst, st);
+      break;
+    case 4:
+      if constexpr (V >= 4)
+        return launch_staged_t<EB, XposeStore<EB, 4>>(a, src, cap, dst, st);
+      break;
+    case 8:
+      if constexpr (V >= 8)
+        return launch_staged_t<EB, XposeStore<EB, 8>>(a, src, cap, dst, st);
+      break;
+    case 16:
+      if constexpr (V >= 16)
+        return launch_staged_t<EB, XposeStore<EB, 16>>(a, src, cap, dst, st);
+      break;
+    default:
+      break;
+  }
+  return LM_E_INVALID;
+}
+
+int launch_staged(const StagedArgs& a, int eb, const char* src, int64_t cap,
+                  char* dst, cudaStream_t st) {
+  if (a.store_mode == 1) {
+    switch (eb) {
+      case 1: return launch_xpose<1>(a, src, cap, dst, st);
+      case 2: return launch_xpose<2>(a, src, cap, dst, st);
+      case 4: return launch_xpose<4>(a, src, cap, dst, st);
+      case 8: return launch_xpose<8>(a, src, cap, dst, st);
+      default: return LM_E_INVALID;
+    }
+  }
+  switch (eb) {
+    case 1: return launch_staged_t<1, GatherStore<1>>(a, src, cap, dst, st);
+    case 2: return launch_staged_t<2, GatherStore<2>>(a, src, cap, dst, st);
+    case 4: return launch_staged_t<4, GatherStore<4>>(a, src, cap, dst, st);
+    case 8: return launch_staged_t<8, GatherStore<8>>(a, src, cap, dst, st);
+    case 16: return launch_staged_t<16, GatherStore<16>>(a, src, cap, dst, st);
+    default: return LM_E_INVALID;
+  }
 }
 
 int launch_piece(const lm_plan& P, const Piece& pc, const char* src,
@@ -547,16 +693,8 @@ int launch_piece(const lm_plan& P, const Piece& pc, const char* src,
       default: break;
     }
   }
-  if (pc.path == PATH_STAGED && ((ps | pd) % 16) == 0) {
-    switch (P.eb) {
-      case 1: return launch_staged_t<1>(pc.st, src, src_cap_bytes, dst, st);
-      case 2: return launch_staged_t<2>(pc.st, src, src_cap_bytes, dst, st);
-      case 4: return launch_staged_t<4>(pc.st, src, src_cap_bytes, dst, st);
-      case 8: return launch_staged_t<8>(pc.st, src, src_cap_bytes, dst, st);
-      case 16: return launch_staged_t<16>(pc.st, src, src_cap_bytes, dst, st);
-      default: break;
-    }
-  }
+  if (pc.path == PATH_STAGED && ((ps | pd) % 16) == 0)
+    return launch_staged(pc.st, P.eb, src, src_cap_bytes, dst, st);
   return launch_generic(pc.gen, src, dst, st);
 }
 

@@ -136,6 +136,16 @@ struct TileMode {
   int64_t T;    // tile extent along it (divides the mode's extent)
 };
 
+// LM_TRANSPOSE=0 plans 2-D transposes with the per-element gather store
+// instead of register micro-tiles (for comparing the two).
+bool transpose_disabled() {
+  static bool v = [] {
+    const char* e = std::getenv("LM_TRANSPOSE");
+    return e && e[0] == '0';
+  }();
+  return v;
+}
+
 int64_t tile_bytes_target() {
   static int64_t v = [] {
     const char* e = std::getenv("LM_TILE_BYTES");
@@ -152,12 +162,6 @@ int64_t divisor_at_most(int64_t e, int64_t want, int64_t mult) {
     if (e % t == 0 && t % mult == 0) return t;
   return 0;
 }
-
-struct SmemSim {
-  // per candidate pad: linear addresses of every lane access
-  std::vector<int64_t> load_addr;     // [n_lchunks] (16-byte accesses)
-  std::vector<int64_t> gather_addr;   // [n_schunks * V]
-};
 
 // Wavefronts of one warp-wide shared-memory instruction: per phase (lanes
 // whose requests share one 128-byte pass), the largest number of distinct
@@ -190,6 +194,82 @@ int64_t wavefronts(const int64_t* addr, const bool* valid, int lanes,
   return total;
 }
 
+
+// The shared-memory image of a tile: n_seg segments of seg_bytes, placed at a
+// pitch of seg_bytes + pad, then XOR-swizzled in 16-byte units.  Loads write
+// 16-byte chunks; the store side reads `per` accesses of `width` bytes for
+// each of n_reads slots.  Chooses the pad and swizzle with the fewest
+// simulated wavefronts over every warp of one tile.
+struct SmemLayout {
+  int64_t pad = 0;
+  Swz z;
+  int64_t bytes = 0, cost = -1, ideal = 0;
+};
+
+template <class ReadAddr>
+SmemLayout search_smem(int threads, int64_t n_seg, int64_t seg_bytes,
+                       int64_t n_reads, int per, int width,
+                       const ReadAddr& read_addr) {
+  SmemLayout best;
+  const int64_t cps = seg_bytes / 16;
+  const int64_t n_l = n_seg * cps;
+  const int64_t lpt = (n_l + threads - 1) / threads;
+  const int64_t spt = (n_reads + threads - 1) / threads;
+  const std::vector<int64_t> pads =
+      n_seg > 1 ? std::vector<int64_t>{0, 16, 32, 48, 64, 80, 96, 112}
+                : std::vector<int64_t>{0};
+  std::vector<Swz> zs{Swz{}};
+  for (int bb = 1; bb <= 3; ++bb)
+    for (int ss = bb; ss <= 10; ++ss) zs.push_back(Swz{bb, 4, ss});
+  std::vector<int64_t> addr(32);
+  bool valid[32];
+  for (int64_t pad : pads) {
+    const int64_t pitch = seg_bytes + pad;
+    const int64_t lin_max = (n_seg - 1) * pitch + seg_bytes;
+    for (const Swz& z : zs) {
+      const int64_t blk = int64_t(16) << z.b;
+      const int64_t bytes = ((lin_max + blk - 1) / blk) * blk;
+      if (bytes > 24576) continue;
+      int64_t cost = 0, id = 0;
+      for (int w = 0; w < threads / 32; ++w) {
+        for (int64_t k = 0; k < lpt; ++k) {
+          int cnt = 0;
+          for (int l = 0; l < 32; ++l) {
+            const int64_t j = 32 * w + l + k * threads;
+            valid[l] = j < n_l;
+            cnt += valid[l];
+            addr[size_t(l)] =
+                valid[l] ? z.apply((j / cps) * pitch + (j % cps) * 16) : 0;
+          }
+          cost += wavefronts(addr.data(), valid, 32, 16);
+          id += (cnt * 16 + 127) / 128;
+        }
+        for (int64_t k = 0; k < spt; ++k)
+          for (int e = 0; e < per; ++e) {
+            int cnt = 0;
+            for (int l = 0; l < 32; ++l) {
+              const int64_t j = 32 * w + l + k * threads;
+              valid[l] = j < n_reads;
+              cnt += valid[l];
+              addr[size_t(l)] = valid[l] ? z.apply(read_addr(j, e, pitch)) : 0;
+            }
+            cost += wavefronts(addr.data(), valid, 32, width);
+            id += cnt ? (cnt * width + 127) / 128 : 0;
+          }
+      }
+      if (best.cost < 0 || cost < best.cost ||
+          (cost == best.cost && bytes < best.bytes)) {
+        best.pad = pad;
+        best.z = z;
+        best.cost = cost;
+        best.bytes = bytes;
+        best.ideal = id;
+      }
+    }
+  }
+  return best;
+}
+
 struct StagedChoice {
   bool ok = false;
   int split_mode = -1;     // > = 0: split the box along this mode at split_at
@@ -197,6 +277,187 @@ struct StagedChoice {
 };
 
 }  // namespace
+
+// Grid over tiles (colex, fastest first) and the piece's global placement.
+static void fill_grid(StagedArgs& A, const std::vector<JMode>& grid,
+                      int64_t s_base, int64_t d_base, int eb, const Swz& ssb,
+                      const Swz& dsb) {
+  A.n_tiles = uint32_t(prod_e(grid));
+  A.ng = int32_t(grid.size());
+  uint32_t pre = 1;
+  for (size_t k = 0; k < grid.size(); ++k) {
+    A.g_ext[k] = uint32_t(grid[k].e);
+    A.g_pre[k] = make_fastdiv(pre);
+    A.g_div[k] = make_fastdiv(uint32_t(grid[k].e));
+    A.g_s[k] = mul_chk(grid[k].s, eb);
+    A.g_d[k] = mul_chk(grid[k].d, eb);
+    pre *= uint32_t(grid[k].e);
+  }
+  A.s_base = mul_chk(s_base, eb);
+  A.d_base = mul_chk(d_base, eb);
+  A.s_swz = ssb;
+  A.d_swz = dsb;
+}
+
+// Bytes per tile for a box of `total_bytes`: 16 KiB, smaller for small boxes
+// so that there are at least ~8 tiles per SM (152 SMs) to balance.
+static int64_t tile_target(int64_t total_bytes) {
+  int64_t t = 16384;
+  while (t > 2048 && total_bytes / t < 152 * 8) t /= 2;
+  return t;
+}
+
+// STAGED with the transpose store.  The tile is T_a x T_b over the src-fast
+// mode a (unit source stride) and the dst-fast mode b (unit destination
+// stride); the shared-memory image holds one row of T_a elements per b.
+// Micro-tiles are R rows by one 16-byte chunk: R = V when b's runs hold
+// whole 16-byte vectors, or R = extent(b) < V when b is short and a
+// continues its destination run (an interleave).
+static StagedChoice plan_transpose(const std::vector<JMode>& ms,
+                                   int64_t s_base, int64_t d_base,
+                                   const lm_plan& P, Piece& pc) {
+  StagedChoice ch;
+  const int eb = P.eb;
+  if (eb > 8) return ch;
+  const int64_t V = 16 / eb;
+  const int n = int(ms.size());
+  int a = -1, b = -1;
+  for (int k = 0; k < n; ++k) {
+    if (ms[size_t(k)].s == 1 && a < 0) a = k;
+    if (ms[size_t(k)].d == 1 && b < 0) b = k;
+  }
+  if (a < 0 || b < 0 || a == b) return ch;
+  const Swz ssb = to_bytes(P.s_swz, eb), dsb = to_bytes(P.d_swz, eb);
+  if ((ssb.on() && ssb.m < 4) || (dsb.on() && dsb.m < 4)) return ch;
+  const JMode ma = ms[size_t(a)], mb = ms[size_t(b)];
+  int64_t R;
+  if (mb.e >= V) {
+    R = V;
+  } else if (V % mb.e == 0 && ma.d == mb.e) {
+    R = mb.e;
+  } else {
+    return ch;
+  }
+  // ragged extents: split off the tail that is not a whole chunk/vector
+  if (ma.e % V) {
+    if (ma.e >= 2 * V) {
+      ch.split_mode = a;
+      ch.split_at = ma.e - ma.e % V;
+    }
+    return ch;
+  }
+  if (R == V && mb.e % V) {
+    if (mb.e >= 2 * V) {
+      ch.split_mode = b;
+      ch.split_at = mb.e - mb.e % V;
+    }
+    return ch;
+  }
+  const int64_t target = tile_target(mul_chk(prod_e(ms), eb)) / eb;
+  int64_t Ta, Tb;
+  if (R == V) {
+    Ta = divisor_at_most(ma.e, std::max<int64_t>(V, 256 / eb), V);
+    if (!Ta) return ch;
+    const int64_t want_b = std::max<int64_t>(V, target / Ta);
+    Tb = divisor_at_most(mb.e, want_b, V);
+    if (Tb * 2 <= want_b && mb.e > want_b) {
+      int64_t w = V;
+      while (w * 2 <= want_b) w *= 2;
+      if (mb.e % w) {
+        ch.split_mode = b;
+        ch.split_at = mb.e - mb.e % w;
+        return ch;
+      }
+      Tb = w;
+    }
+  } else {
+    Tb = mb.e;
+    const int64_t want_a = std::max<int64_t>(V, target / Tb);
+    Ta = divisor_at_most(ma.e, want_a, V);
+    if (Ta * 2 <= want_a && ma.e > want_a) {
+      int64_t w = V;
+      while (w * 2 <= want_a) w *= 2;
+      if (ma.e % w) {
+        ch.split_mode = a;
+        ch.split_at = ma.e - ma.e % w;
+        return ch;
+      }
+      Ta = w;
+    }
+  }
+  const int64_t n_bc = Tb / R, n_ac = Ta / V;
+  const int64_t n_micro = n_bc * n_ac;
+  const int64_t seg_bytes = Ta * eb;
+  const int64_t cps = seg_bytes / 16;
+  // one micro-tile per thread where possible; enough threads for the loads
+  auto r32 = [](int64_t v) { return ((v + 31) / 32) * 32; };
+  const int64_t threads = std::clamp<int64_t>(
+      std::max(r32(std::min<int64_t>(n_micro, 256)), r32((Tb * cps + 3) / 4)),
+      32, 256);
+  const int64_t max_m = R >= 8 ? 1 : 2;  // micro-tiles per thread
+  if (n_micro > max_m * threads || Tb * cps > threads * 4) return ch;
+
+  // alignment of every 16-byte access
+  auto al = [&](int64_t elems) { return (elems * eb) % 16 == 0; };
+  if (!al(s_base) || !al(d_base) || !al(mb.s)) return ch;
+  if (R == V && !al(ma.d)) return ch;
+  std::vector<JMode> grid;
+  for (int k = 0; k < n; ++k) {
+    const JMode& m = ms[size_t(k)];
+    const int64_t t = k == a ? Ta : (k == b ? Tb : 1);
+    if (t == m.e) continue;
+    grid.push_back({m.e / t, m.s * t, m.d * t});
+    if (!al(m.s * t) || !al(m.d * t)) return ch;
+  }
+  if (grid.size() > size_t(kMaxModes)) return ch;
+  std::sort(grid.begin(), grid.end(),
+            [](const JMode& x, const JMode& y) { return x.d < y.d; });
+  if (prod_e(grid) >= (int64_t(1) << 32)) return ch;
+  const int64_t s_reach = add_chk(mul_chk(mul_chk(Tb - 1, mb.s), eb), seg_bytes);
+  const int64_t d_reach = add_chk(mul_chk(mul_chk(Ta - 1, ma.d), eb), Tb * eb);
+  if (s_reach >= (int64_t(1) << 31) || d_reach >= (int64_t(1) << 31))
+    return ch;
+
+  auto read_addr = [&](int64_t j, int r, int64_t pitch) {
+    const int64_t bc = j % n_bc, ac = j / n_bc;
+    return (bc * R + r) * pitch + ac * 16;
+  };
+  const SmemLayout best = search_smem(int(threads), Tb, seg_bytes, n_micro,
+                                      int(R), 16, read_addr);
+  if (best.cost < 0) return ch;
+
+  StagedArgs& A = pc.st;
+  A = StagedArgs{};
+  fill_grid(A, grid, s_base, d_base, eb, ssb, dsb);
+  const int64_t pitch = seg_bytes + best.pad;
+  A.n_lchunks = uint32_t(Tb * cps);
+  A.cps = uint32_t(cps);
+  A.cps_div = make_fastdiv(uint32_t(cps));
+  A.nso = 1;
+  A.so_ext[0] = uint32_t(Tb);
+  A.so_div[0] = make_fastdiv(uint32_t(Tb));
+  A.so_s[0] = mul_chk(mb.s, eb);
+  A.so_m[0] = uint32_t(pitch);
+  A.store_mode = 1;
+  A.xr = int32_t(R);
+  A.n_micro = uint32_t(n_micro);
+  A.n_bc = uint32_t(n_bc);
+  A.bc_div = make_fastdiv(uint32_t(n_bc));
+  A.x_pitch = uint32_t(pitch);
+  A.x_da = mul_chk(V * ma.d, eb);
+  A.x_db = R * eb;
+  A.x_vstep = R == V ? mul_chk(ma.d, eb) : 16;
+  A.stage_bytes = uint32_t(best.bytes);
+  A.m_swz = best.z;
+  A.threads = int32_t(threads);
+  pc.path = PATH_STAGED;
+  pc.xr = int(R);
+  pc.tile_elems = Ta * Tb;
+  pc.bank_cost = best.cost;
+  pc.bank_ideal = best.ideal;
+  ch.ok = true;
+  return ch;
+}
 
 // Try to plan `ms` (a box of the joint domain) on the STAGED path.  Fills
 // pc on success.  May instead request a split of a mode whose extent has no
@@ -418,10 +679,8 @@ static StagedChoice plan_staged(const std::vector<JMode>& ms, int64_t s_base,
   const int64_t n_l = n_seg * cps;
   const int64_t n_s = tile_elems() / V;
   const int64_t cpd = d_span * eb / 16;
-  const int64_t lpt = (n_l + kThreads - 1) / kThreads;
-  const int64_t spt = (n_s + kThreads - 1) / kThreads;
-  const int max_spt = std::min(8, std::max(1, 32 / int(V)));
-  if (lpt > 8 || spt > max_spt) return ch;
+  const int max_s = std::max(1, std::min(4, 16 / int(V)));
+  if (n_l > kThreads * 4 || n_s > int64_t(kThreads) * max_s) return ch;
 
   // smem bytes per coordinate of each tile mode for a given pitch
   auto smem_m = [&](int64_t pitch, std::vector<int64_t>& m) {
@@ -433,88 +692,28 @@ static StagedChoice plan_staged(const std::vector<JMode>& ms, int64_t s_base,
       w *= T[size_t(k)];
     }
   };
-  // linear smem address of every load chunk and every gathered element
-  auto linear = [&](int64_t pitch, std::vector<int64_t>& la,
-                    std::vector<int64_t>& ga) {
-    std::vector<int64_t> m;
-    smem_m(pitch, m);
-    la.resize(size_t(n_l));
-    for (int64_t j = 0; j < n_l; ++j) la[size_t(j)] = (j / cps) * pitch + (j % cps) * 16;
-    ga.resize(size_t(n_s * V));
-    for (int64_t j = 0; j < n_s; ++j) {
-      int64_t o = j / cpd, p = j % cpd, base = 0;
-      for (int k : d_outer) {
-        base += (o % T[size_t(k)]) * m[size_t(k)];
-        o /= T[size_t(k)];
-      }
-      for (int64_t e = 0; e < V; ++e) {
-        int64_t q = p * V + e, addr = base;
-        for (int k : d_chain) {
-          addr += (q % T[size_t(k)]) * m[size_t(k)];
-          q /= T[size_t(k)];
-        }
-        ga[size_t(j * V + e)] = addr;
-      }
+  // linear smem address of element e of store chunk j
+  int64_t cached_pitch = -1;
+  std::vector<int64_t> mcache;
+  auto gather_addr = [&](int64_t j, int e, int64_t pitch) {
+    if (pitch != cached_pitch) {
+      smem_m(pitch, mcache);
+      cached_pitch = pitch;
     }
+    int64_t o = j / cpd, p = j % cpd, addr = 0;
+    for (int k : d_outer) {
+      addr += (o % T[size_t(k)]) * mcache[size_t(k)];
+      o /= T[size_t(k)];
+    }
+    int64_t q = p * V + e;
+    for (int k : d_chain) {
+      addr += (q % T[size_t(k)]) * mcache[size_t(k)];
+      q /= T[size_t(k)];
+    }
+    return addr;
   };
-  struct Cand {
-    int64_t pad = 0;
-    Swz z;
-    int64_t cost = -1, bytes = 0;
-  } best, ideal_c;
-  std::vector<int64_t> la, ga, addr(32);
-  bool valid[32];
-  const std::vector<int64_t> pads =
-      n_seg > 1 ? std::vector<int64_t>{0, 16, 32, 48, 64, 80, 96, 112}
-                : std::vector<int64_t>{0};
-  int64_t ideal = 0;
-  for (int64_t pad : pads) {
-    const int64_t pitch = seg_bytes + pad;
-    linear(pitch, la, ga);
-    const int64_t lin_max = (n_seg - 1) * pitch + seg_bytes;
-    std::vector<Swz> zs{Swz{}};
-    for (int bb = 1; bb <= 3; ++bb)
-      for (int ss = bb; ss <= 10; ++ss) zs.push_back(Swz{bb, 4, ss});
-    for (const Swz& z : zs) {
-      const int64_t blk = int64_t(16) << z.b;
-      const int64_t bytes = ((lin_max + blk - 1) / blk) * blk;
-      if (bytes > 24576) continue;
-      int64_t cost = 0, id = 0;
-      for (int w = 0; w < kThreads / 32; ++w) {
-        for (int64_t k = 0; k < lpt; ++k) {
-          for (int l = 0; l < 32; ++l) {
-            const int64_t j = 32 * w + l + k * kThreads;
-            valid[l] = j < n_l;
-            addr[size_t(l)] = valid[l] ? z.apply(la[size_t(j)]) : 0;
-          }
-          cost += wavefronts(addr.data(), valid, 32, 16);
-          int cntv = 0;
-          for (int l = 0; l < 32; ++l) cntv += valid[l];
-          id += (cntv * 16 + 127) / 128;
-        }
-        for (int64_t k = 0; k < spt; ++k)
-          for (int64_t e = 0; e < V; ++e) {
-            int cntv = 0;
-            for (int l = 0; l < 32; ++l) {
-              const int64_t j = 32 * w + l + k * kThreads;
-              valid[l] = j < n_s;
-              cntv += valid[l];
-              addr[size_t(l)] = valid[l] ? z.apply(ga[size_t(j * V + e)]) : 0;
-            }
-            cost += wavefronts(addr.data(), valid, 32, eb);
-            id += cntv ? (cntv * eb + 127) / 128 : 0;
-          }
-      }
-      ideal = id;
-      if (best.cost < 0 || cost < best.cost ||
-          (cost == best.cost && bytes < best.bytes)) {
-        best.pad = pad;
-        best.z = z;
-        best.cost = cost;
-        best.bytes = bytes;
-      }
-    }
-  }
+  const SmemLayout best =
+      search_smem(kThreads, n_seg, seg_bytes, n_s, int(V), eb, gather_addr);
   if (best.cost < 0) return ch;
 
   // ---- fill the kernel arguments -----------------------------------------
@@ -523,21 +722,7 @@ static StagedChoice plan_staged(const std::vector<JMode>& ms, int64_t s_base,
   const int64_t pitch = seg_bytes + best.pad;
   std::vector<int64_t> m;
   smem_m(pitch, m);
-  A.n_tiles = uint32_t(n_tiles);
-  A.ng = int32_t(grid.size());
-  uint32_t pre = 1;
-  for (size_t k = 0; k < grid.size(); ++k) {
-    A.g_ext[k] = uint32_t(grid[k].e);
-    A.g_pre[k] = make_fastdiv(pre);
-    A.g_div[k] = make_fastdiv(uint32_t(grid[k].e));
-    A.g_s[k] = mul_chk(grid[k].s, eb);
-    A.g_d[k] = mul_chk(grid[k].d, eb);
-    pre *= uint32_t(grid[k].e);
-  }
-  A.s_base = mul_chk(s_base, eb);
-  A.d_base = mul_chk(d_base, eb);
-  A.s_swz = ssb;
-  A.d_swz = dsb;
+  fill_grid(A, grid, s_base, d_base, eb, ssb, dsb);
   A.n_lchunks = uint32_t(n_l);
   A.cps = uint32_t(cps);
   A.cps_div = make_fastdiv(uint32_t(cps));
@@ -569,10 +754,12 @@ static StagedChoice plan_staged(const std::vector<JMode>& ms, int64_t s_base,
   }
   A.stage_bytes = uint32_t(best.bytes);
   A.m_swz = best.z;
+  A.store_mode = 0;
+  A.threads = kThreads;
   pc.path = PATH_STAGED;
   pc.tile_elems = tile_elems();
   pc.bank_cost = best.cost;
-  pc.bank_ideal = ideal;
+  pc.bank_ideal = best.ideal;
   ch.ok = true;
   return ch;
 }
@@ -680,6 +867,10 @@ static void plan_box(lm_plan& P, std::vector<JMode> ms, int64_t s_base,
   if (size > kSmall) {
     StagedChoice c = plan_vec(ms, s_base, d_base, P, pc, false);
     if (c.split_mode >= 0) return split(c.split_mode, c.split_at);
+    if (!c.ok && !transpose_disabled()) {
+      c = plan_transpose(ms, s_base, d_base, P, pc);
+      if (c.split_mode >= 0) return split(c.split_mode, c.split_at);
+    }
     if (!c.ok) {
       c = plan_staged(ms, s_base, d_base, P, pc);
       if (c.split_mode >= 0) return split(c.split_mode, c.split_at);
@@ -713,6 +904,8 @@ static std::string describe(const lm_plan& P) {
       os << ",\"tile_elems\":" << pc.tile_elems << ",\"n_tiles\":" << A.n_tiles
          << ",\"load_chunks\":" << A.n_lchunks
          << ",\"store_chunks\":" << A.n_schunks
+         << ",\"store\":\"" << (A.store_mode ? "transpose" : "gather")
+         << "\",\"rows\":" << A.xr << ",\"threads\":" << A.threads
          << ",\"stage_bytes\":" << A.stage_bytes << ",\"smem_swizzle\":["
          << A.m_swz.b << ',' << A.m_swz.m << ',' << A.m_swz.s << ']'
          << ",\"bank_wavefronts\":" << pc.bank_cost

@@ -152,8 +152,12 @@ def test_small_parity_paths_cover_every_kernel():
     seen = set()
     for _, src, dst, eb in SMALL:
         p = lm.Plan(lm.build_layout(src), lm.build_layout(dst), eb)
-        seen |= {pc["path"] for pc in p.describe()["pieces"]}
-    assert seen == {"GENERIC", "VEC", "STAGED"}
+        for pc in p.describe()["pieces"]:
+            seen.add(pc["path"] if pc["path"] != "STAGED"
+                     else "STAGED/" + pc["store"] + str(pc["rows"]))
+    assert {"GENERIC", "VEC", "STAGED/gather0"} <= seen
+    assert {"STAGED/transpose2", "STAGED/transpose4",
+            "STAGED/transpose8"} <= seen, seen
 
 
 @pytest.mark.parametrize("eb", [1, 2, 4, 8, 16])
