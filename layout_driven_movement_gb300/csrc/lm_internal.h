@@ -164,6 +164,20 @@ struct VecArgs {
   int64_t s[kMaxModes], d[kMaxModes];   // bytes per coordinate step
   int64_t s_base = 0, d_base = 0;       // bytes
   Swz s_swz, d_swz;                     // in bytes
+  // tiled form (tiled == 1): tiles of tile_vecs vectors over the first nt
+  // modes (tile extents t_ext), a grid of n_tiles tiles over the rest
+  int32_t tiled = 0;
+  int32_t unroll = 4;                   // vectors per thread per tile (4|8)
+  uint32_t tile_vecs = 0;
+  int32_t nt = 0;
+  uint32_t t_ext[kMaxModes];
+  FastDiv t_div[kMaxModes];
+  int64_t t_s[kMaxModes], t_d[kMaxModes];
+  uint32_t n_tiles = 0;
+  int32_t ng = 0;
+  uint32_t g_ext[kMaxModes];
+  FastDiv g_pre[kMaxModes], g_div[kMaxModes];
+  int64_t g_s[kMaxModes], g_d[kMaxModes];
 };
 
 struct StagedArgs {
@@ -213,6 +227,7 @@ struct StagedArgs {
   uint32_t stage_bytes = 0;
   Swz m_swz;                            // smem swizzle, bytes
   int32_t threads = 256;                // block size
+  int32_t stages = 2;                   // cp.async pipeline depth (2 or 3)
 };
 
 struct EvalArgs {

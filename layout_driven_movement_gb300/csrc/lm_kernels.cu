@@ -22,6 +22,8 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstdlib>
+#include <utility>
 #include <cstring>
 #include <mutex>
 
@@ -60,6 +62,17 @@ template <>
 struct VecT<1> {
   using T = uint8_t;
 };
+
+// Programmatic dependent launch: a kernel lets the next kernel on its stream
+// start as soon as all of its own blocks are resident, and waits for the
+// previous kernel to complete (and its writes to be visible) before its
+// first global memory access.  Without the launch attribute both are no-ops.
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() {
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+}
 
 __device__ __forceinline__ int64_t swz_apply(const Swz& z, int64_t o) {
   return z.b > 0 ? (o ^ ((o >> z.s) & (((int64_t(1) << z.b) - 1) << z.m))) : o;
@@ -104,6 +117,8 @@ __device__ __forceinline__ int64_t side_offset64(uint64_t q, int n,
 template <typename OUT>
 __global__ void __launch_bounds__(256)
     lm_eval_kernel(const __grid_constant__ EvalArgs a, OUT* __restrict__ table) {
+  pdl_trigger();
+  pdl_wait();
   const uint64_t stride = uint64_t(gridDim.x) * blockDim.x;
   for (uint64_t i = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < a.n;
        i += stride) {
@@ -126,6 +141,8 @@ __global__ void __launch_bounds__(256)
     lm_generic_kernel(const __grid_constant__ GenericArgs a,
                       const char* __restrict__ src, char* __restrict__ dst) {
   using T = typename VecT<EB>::T;
+  pdl_trigger();
+  pdl_wait();
   const uint64_t stride = uint64_t(gridDim.x) * blockDim.x;
   for (uint64_t i = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < a.n;
        i += stride) {
@@ -155,6 +172,8 @@ __global__ void __launch_bounds__(256)
     lm_vec_kernel(const __grid_constant__ VecArgs a,
                   const char* __restrict__ src, char* __restrict__ dst) {
   using T = typename VecT<VB>::T;
+  pdl_trigger();
+  pdl_wait();
   const uint64_t nthreads = uint64_t(gridDim.x) * blockDim.x;
   for (uint64_t q0 = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x;
        q0 < a.n_vec; q0 += kVecUnroll * nthreads) {
@@ -187,6 +206,103 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// Tile origin offsets (bytes) over a grid of ng modes.  Lane k of each group
+// of 8 lanes computes grid coordinate k in parallel (tile / product of the
+// faster extents, mod the extent); a 3-step butterfly of warp shuffles sums
+// the contributions, so every lane of the warp ends with both totals.
+__device__ __forceinline__ void grid_base(int ng, const uint32_t* ext,
+                                          const FastDiv* pre,
+                                          const FastDiv* div,
+                                          const int64_t* gs, const int64_t* gd,
+                                          uint32_t tile, int64_t& sb,
+                                          int64_t& db) {
+  const int k = threadIdx.x & 7;
+  int64_t s = 0, d = 0;
+  if (k < ng) {
+    uint32_t c = fdiv(tile, pre[k]);
+    c -= fdiv(c, div[k]) * ext[k];
+    s = int64_t(c) * gs[k];
+    d = int64_t(c) * gd[k];
+  }
+#pragma unroll
+  for (int off = 4; off > 0; off >>= 1) {
+    s += __shfl_xor_sync(0xffffffffu, s, off);
+    d += __shfl_xor_sync(0xffffffffu, d, off);
+  }
+  sb = s;
+  db = d;
+}
+
+// VEC, tiled: each thread owns U vectors of a tile (the same
+// offsets in every tile, computed once); the next tile's vectors are loaded
+// into registers before the current tile's are stored.
+template <int VB, int U>
+__global__ void __launch_bounds__(256)
+    lm_vec_tiled_kernel(const __grid_constant__ VecArgs a,
+                        const char* __restrict__ src, char* __restrict__ dst) {
+  using T = typename VecT<VB>::T;
+  const uint32_t tid = threadIdx.x, nt = blockDim.x;
+  int32_t so[U], dof[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    uint32_t j = tid + uint32_t(u) * nt;
+    so[u] = -1;
+    dof[u] = 0;
+    if (j < a.tile_vecs) {
+      int64_t s = 0, d = 0;
+#pragma unroll
+      for (int k = 0; k < kMaxModes; ++k) {
+        if (k >= a.nt) break;
+        const uint32_t jn = fdiv(j, a.t_div[k]);
+        const int64_t c = int64_t(j - jn * a.t_ext[k]);
+        s += c * a.t_s[k];
+        d += c * a.t_d[k];
+        j = jn;
+      }
+      so[u] = int32_t(s);
+      dof[u] = int32_t(d);
+    }
+  }
+  pdl_trigger();
+  pdl_wait();
+  uint32_t tile = blockIdx.x;
+  if (tile >= a.n_tiles) return;
+  int64_t sb, db;
+  grid_base(a.ng, a.g_ext, a.g_pre, a.g_div, a.g_s, a.g_d, tile, sb, db);
+  T cur[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u)
+    if (so[u] >= 0)
+      cur[u] = __ldcs(reinterpret_cast<const T*>(
+          src + swz_apply(a.s_swz, a.s_base + sb + so[u])));
+  for (;;) {
+    const uint64_t next64 = uint64_t(tile) + gridDim.x;
+    const bool has_next = next64 < a.n_tiles;
+    T nxt[U];
+    int64_t nsb = 0, ndb = 0;
+    if (has_next) {
+      grid_base(a.ng, a.g_ext, a.g_pre, a.g_div, a.g_s, a.g_d,
+                uint32_t(next64), nsb, ndb);
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (so[u] >= 0)
+          nxt[u] = __ldcs(reinterpret_cast<const T*>(
+              src + swz_apply(a.s_swz, a.s_base + nsb + so[u])));
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (so[u] >= 0)
+        __stcs(reinterpret_cast<T*>(
+                   dst + swz_apply(a.d_swz, a.d_base + db + dof[u])),
+               cur[u]);
+    if (!has_next) break;
+#pragma unroll
+    for (int u = 0; u < U; ++u) cur[u] = nxt[u];
+    tile = uint32_t(next64);
+    db = ndb;
+  }
+}
+
 // ---------------------------------------------------------------------------
 // STAGED copy
 //
@@ -201,7 +317,6 @@ __global__ void __launch_bounds__(256)
 //                 tiles that are a 2-D transpose.
 // ---------------------------------------------------------------------------
 
-constexpr int kMaxLoadSlots = 4;
 
 __device__ __forceinline__ void cp_async16(uint32_t smem_addr, const void* g,
                                            int src_bytes) {
@@ -245,14 +360,15 @@ __device__ __forceinline__ void tile_base(const StagedArgs& a, uint32_t tile,
   db = d;
 }
 
+template <int L>
 struct LoadSlots {
-  int32_t src[kMaxLoadSlots];
-  uint32_t sm[kMaxLoadSlots];
+  int32_t src[L];
+  uint32_t sm[L];
 
   __device__ __forceinline__ void init(const StagedArgs& a, uint32_t tid,
                                        uint32_t nt) {
 #pragma unroll
-    for (int k = 0; k < kMaxLoadSlots; ++k) {
+    for (int k = 0; k < L; ++k) {
       const uint32_t j = tid + uint32_t(k) * nt;
       src[k] = -1;
       sm[k] = 0;
@@ -281,7 +397,7 @@ struct LoadSlots {
                                         int64_t src_cap, int64_t base,
                                         uint32_t sm_stage) const {
 #pragma unroll
-    for (int k = 0; k < kMaxLoadSlots; ++k) {
+    for (int k = 0; k < L; ++k) {
       if (src[k] < 0) continue;
       const int64_t off = swz_apply(a.s_swz, base + src[k]);
       const int64_t room = src_cap - off;
@@ -293,6 +409,7 @@ struct LoadSlots {
 
 template <int EB>
 struct GatherStore {
+  static constexpr int kLoadSlots = 4;
   static constexpr int V = 16 / EB;
   static constexpr int MaxS = (16 / V) < 1 ? 1 : ((16 / V) > 4 ? 4 : 16 / V);
   int32_t dst[MaxS];
@@ -418,9 +535,10 @@ __device__ __forceinline__ uint32_t xword(const uint32_t (&in)[R][4], int W) {
 
 template <int EB, int R>
 struct XposeStore {
+  static constexpr int kLoadSlots = R >= 8 ? 8 : 4;
   static constexpr int MaxM = R >= 8 ? 1 : 2;
   int32_t dst[MaxM];
-  uint32_t sm[MaxM][R];
+  uint32_t lin[MaxM];  // unswizzled smem byte offset of row 0, chunk ac
 
   __device__ __forceinline__ void init(const StagedArgs& a, uint32_t tid,
                                        uint32_t nt) {
@@ -428,17 +546,12 @@ struct XposeStore {
     for (int k = 0; k < MaxM; ++k) {
       const uint32_t j = tid + uint32_t(k) * nt;
       dst[k] = -1;
-#pragma unroll
-      for (int r = 0; r < R; ++r) sm[k][r] = 0;
+      lin[k] = 0;
       if (j < a.n_micro) {
         const uint32_t ac = fdiv(j, a.bc_div);
         const uint32_t bc = j - ac * a.n_bc;
         dst[k] = int32_t(int64_t(ac) * a.x_da + int64_t(bc) * a.x_db);
-#pragma unroll
-        for (int r = 0; r < R; ++r)
-          sm[k][r] = swz_apply32(a.m_swz,
-                                 (bc * uint32_t(R) + uint32_t(r)) * a.x_pitch +
-                                     ac * 16u);
+        lin[k] = bc * uint32_t(R) * a.x_pitch + ac * 16u;
       }
     }
   }
@@ -452,7 +565,8 @@ struct XposeStore {
       uint32_t in[R][4];
 #pragma unroll
       for (int r = 0; r < R; ++r) {
-        const uint4 v = lds128(smst + sm[k][r]);
+        const uint4 v = lds128(
+            smst + swz_apply32(a.m_swz, lin[k] + uint32_t(r) * a.x_pitch));
         in[r][0] = v.x;
         in[r][1] = v.y;
         in[r][2] = v.z;
@@ -471,7 +585,11 @@ struct XposeStore {
   }
 };
 
-template <int EB, class Store>
+// NS-stage pipeline: the loads of the NS-1 tiles after the current one are
+// in flight while the current tile is stored.  Every iteration commits one
+// cp.async group (possibly empty), so waiting until at most NS-1 groups are
+// pending means the current tile's group has landed.
+template <int EB, class Store, int NS>
 __global__ void __launch_bounds__(256)
     lm_staged_kernel(const __grid_constant__ StagedArgs a,
                      const char* __restrict__ src, char* __restrict__ dst,
@@ -479,40 +597,53 @@ __global__ void __launch_bounds__(256)
   extern __shared__ __align__(128) unsigned char smem[];
   const uint32_t tid = threadIdx.x;
   const uint32_t nt = blockDim.x;
-  LoadSlots ls;
+  LoadSlots<Store::kLoadSlots> ls;
   ls.init(a, tid, nt);
   Store st;
   st.init(a, tid, nt);
+  pdl_trigger();
+  pdl_wait();
 
-  uint32_t tile = blockIdx.x;
+  uint64_t tile = blockIdx.x;
   if (tile >= a.n_tiles) return;
+  const uint64_t G = gridDim.x;
   const uint32_t smem0 = uint32_t(__cvta_generic_to_shared(smem));
-  int64_t sb, db;
-  tile_base(a, tile, sb, db);
-  ls.issue(a, src, src_cap, a.s_base + sb, smem0);
-  cp_async_commit();
+  int64_t dq[NS];  // dst bases of the tiles in flight, oldest first
+#pragma unroll
+  for (int i = 0; i < NS - 1; ++i) {
+    const uint64_t t = tile + uint64_t(i) * G;
+    dq[i] = 0;
+    if (t < a.n_tiles) {
+      int64_t sb;
+      tile_base(a, uint32_t(t), sb, dq[i]);
+      ls.issue(a, src, src_cap, a.s_base + sb,
+               smem0 + uint32_t(i) * a.stage_bytes);
+    }
+    cp_async_commit();
+  }
   int stage = 0;
   for (;;) {
-    const uint64_t next64 = uint64_t(tile) + gridDim.x;
-    const bool has_next = next64 < a.n_tiles;
-    int64_t nsb = 0, ndb = 0;
-    if (has_next) {
-      tile_base(a, uint32_t(next64), nsb, ndb);
-      ls.issue(a, src, src_cap, a.s_base + nsb,
-               smem0 + uint32_t(stage ^ 1) * a.stage_bytes);
-      cp_async_commit();
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
+    const uint64_t ahead = tile + uint64_t(NS - 1) * G;
+    dq[NS - 1] = 0;
+    if (ahead < a.n_tiles) {
+      int64_t sb;
+      tile_base(a, uint32_t(ahead), sb, dq[NS - 1]);
+      const int s_ahead = (stage + NS - 1) % NS;
+      ls.issue(a, src, src_cap, a.s_base + sb,
+               smem0 + uint32_t(s_ahead) * a.stage_bytes);
     }
+    cp_async_commit();
+    cp_async_wait<NS - 1>();
     __syncthreads();
-    st.store(a, smem + size_t(stage) * a.stage_bytes, dst, a.d_base + db);
+    st.store(a, smem + size_t(stage) * a.stage_bytes, dst, a.d_base + dq[0]);
     __syncthreads();
-    if (!has_next) break;
-    tile = uint32_t(next64);
-    stage ^= 1;
-    db = ndb;
+    tile += G;
+    if (tile >= a.n_tiles) break;
+    stage = (stage + 1) % NS;
+#pragma unroll
+    for (int i = 0; i < NS - 1; ++i) dq[i] = dq[i + 1];
   }
+  cp_async_wait<0>();
 }
 
 // ---------------------------------------------------------------------------
@@ -537,6 +668,32 @@ DeviceInfo device_info() {
   return cache[dev];
 }
 
+bool pdl_enabled() {
+  static bool v = [] {
+    const char* e = std::getenv("LM_PDL");
+    return !(e && e[0] == '0');
+  }();
+  return v;
+}
+
+// Launch with the programmatic-stream-serialization attribute (see
+// pdl_wait); LM_PDL=0 launches plainly.
+template <typename... Params, typename... Args>
+cudaError_t launch_k(void (*kern)(Params...), unsigned grid, unsigned block,
+                     size_t smem, cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 int check_launch() {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
@@ -553,7 +710,7 @@ int launch_generic_t(const GenericArgs& g, const char* src, char* dst,
   const uint64_t want = (g.n + 255) / 256;
   const uint64_t cap = uint64_t(di.sms) * 16;
   const unsigned grid = unsigned(std::max<uint64_t>(1, std::min(want, cap)));
-  lm_generic_kernel<EB><<<grid, 256, 0, st>>>(g, src, dst);
+  launch_k(lm_generic_kernel<EB>, grid, 256, 0, st, g, src, dst);
   return check_launch();
 }
 
@@ -599,37 +756,65 @@ int launch_generic(const GenericArgs& g0, const char* src, char* dst,
   }
 }
 
+template <int VB, int U>
+int launch_vec_tiled(const VecArgs& v, const char* src, char* dst,
+                     cudaStream_t st) {
+  const DeviceInfo di = device_info();
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+          &per_sm, lm_vec_tiled_kernel<VB, U>, 256, 0) != cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  const uint64_t cap = uint64_t(di.sms) * uint64_t(per_sm);
+  const unsigned grid =
+      unsigned(std::max<uint64_t>(1, std::min<uint64_t>(v.n_tiles, cap)));
+  launch_k(lm_vec_tiled_kernel<VB, U>, grid, 256, 0, st, v, src, dst);
+  return check_launch();
+}
+
 template <int VB>
 int launch_vec_t(const VecArgs& v, const char* src, char* dst,
                  cudaStream_t st) {
   const DeviceInfo di = device_info();
+  if (v.tiled) {
+    if (v.unroll == 8) return launch_vec_tiled<VB, 8>(v, src, dst, st);
+    return launch_vec_tiled<VB, 4>(v, src, dst, st);
+  }
   const uint64_t want = (uint64_t(v.n_vec) + 256 * kVecUnroll - 1) /
                         (256 * kVecUnroll);
   const uint64_t cap = uint64_t(di.sms) * 8;
   const unsigned grid = unsigned(std::max<uint64_t>(1, std::min(want, cap)));
-  lm_vec_kernel<VB><<<grid, 256, 0, st>>>(v, src, dst);
+  launch_k(lm_vec_kernel<VB>, grid, 256, 0, st, v, src, dst);
+  return check_launch();
+}
+
+template <int EB, class Store, int NS>
+int launch_staged_ns(const StagedArgs& a, const char* src, int64_t src_cap,
+                     char* dst, cudaStream_t st) {
+  // NS stages of at most 48 KiB / NS each: within the default 48 KiB of
+  // dynamic shared memory, so no per-device attribute is needed
+  const int smem = int(NS * a.stage_bytes);
+  const DeviceInfo di = device_info();
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+          &per_sm, lm_staged_kernel<EB, Store, NS>, a.threads,
+          size_t(smem)) != cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  const uint64_t cap = uint64_t(di.sms) * uint64_t(per_sm);
+  const unsigned grid =
+      unsigned(std::max<uint64_t>(1, std::min<uint64_t>(a.n_tiles, cap)));
+  launch_k(lm_staged_kernel<EB, Store, NS>, grid, unsigned(a.threads),
+           size_t(smem), st, a, src, dst, src_cap);
   return check_launch();
 }
 
 template <int EB, class Store>
 int launch_staged_t(const StagedArgs& a, const char* src, int64_t src_cap,
                     char* dst, cudaStream_t st) {
-  // two stages of at most 24 KiB each: within the default 48 KiB of
-  // dynamic shared memory, so no per-device attribute is needed
-  const int smem = int(2 * a.stage_bytes);
-  const DeviceInfo di = device_info();
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-          &per_sm, lm_staged_kernel<EB, Store>, a.threads, size_t(smem)) !=
-          cudaSuccess ||
-      per_sm < 1)
-    per_sm = 1;
-  const uint64_t cap = uint64_t(di.sms) * uint64_t(per_sm);
-  const unsigned grid =
-      unsigned(std::max<uint64_t>(1, std::min<uint64_t>(a.n_tiles, cap)));
-  lm_staged_kernel<EB, Store><<<grid, a.threads, size_t(smem), st>>>(
-      a, src, dst, src_cap);
-  return check_launch();
+  if (a.stages == 3 && 3 * a.stage_bytes <= 49152)
+    return launch_staged_ns<EB, Store, 3>(a, src, src_cap, dst, st);
+  return launch_staged_ns<EB, Store, 2>(a, src, src_cap, dst, st);
 }
 
 template <int EB>
@@ -720,11 +905,11 @@ int launch_eval(const lm_layout& L, void* table, int offset_bytes,
   const unsigned grid = unsigned(
       std::max<uint64_t>(1, std::min<uint64_t>(want, uint64_t(di.sms) * 16)));
   if (offset_bytes == 4)
-    lm_eval_kernel<int32_t>
-        <<<grid, 256, 0, st>>>(a, static_cast<int32_t*>(table));
+    launch_k(lm_eval_kernel<int32_t>, grid, 256, 0, st, a,
+             static_cast<int32_t*>(table));
   else
-    lm_eval_kernel<int64_t>
-        <<<grid, 256, 0, st>>>(a, static_cast<int64_t*>(table));
+    launch_k(lm_eval_kernel<int64_t>, grid, 256, 0, st, a,
+             static_cast<int64_t*>(table));
   return check_launch();
 }
 

@@ -146,6 +146,22 @@ bool transpose_disabled() {
   return v;
 }
 
+int env_int(const char* name, int dflt) {
+  const char* e = std::getenv(name);
+  return e ? std::atoi(e) : dflt;
+}
+// cp.async pipeline depth of STAGED kernels (LM_STAGES, 2 or 3)
+int staged_stages() {
+  static int v = env_int("LM_STAGES", 2) == 3 ? 3 : 2;
+  return v;
+}
+// 16-byte vectors per thread per tile of the tiled VEC kernel
+// (LM_VEC_UNROLL, 4 or 8)
+int vec_unroll() {
+  static int v = env_int("LM_VEC_UNROLL", 4) == 8 ? 8 : 4;
+  return v;
+}
+
 int64_t tile_bytes_target() {
   static int64_t v = [] {
     const char* e = std::getenv("LM_TILE_BYTES");
@@ -390,12 +406,14 @@ static StagedChoice plan_transpose(const std::vector<JMode>& ms,
   const int64_t seg_bytes = Ta * eb;
   const int64_t cps = seg_bytes / 16;
   // one micro-tile per thread where possible; enough threads for the loads
+  // (these limits match XposeStore: micro-tiles and load chunks per thread)
+  const int64_t max_m = R >= 8 ? 1 : 2, max_l = R >= 8 ? 8 : 4;
   auto r32 = [](int64_t v) { return ((v + 31) / 32) * 32; };
   const int64_t threads = std::clamp<int64_t>(
-      std::max(r32(std::min<int64_t>(n_micro, 256)), r32((Tb * cps + 3) / 4)),
+      std::max(r32(std::min<int64_t>(n_micro, 256)),
+               r32((Tb * cps + max_l - 1) / max_l)),
       32, 256);
-  const int64_t max_m = R >= 8 ? 1 : 2;  // micro-tiles per thread
-  if (n_micro > max_m * threads || Tb * cps > threads * 4) return ch;
+  if (n_micro > max_m * threads || Tb * cps > threads * max_l) return ch;
 
   // alignment of every 16-byte access
   auto al = [&](int64_t elems) { return (elems * eb) % 16 == 0; };
@@ -450,6 +468,7 @@ static StagedChoice plan_transpose(const std::vector<JMode>& ms,
   A.stage_bytes = uint32_t(best.bytes);
   A.m_swz = best.z;
   A.threads = int32_t(threads);
+  A.stages = staged_stages();
   pc.path = PATH_STAGED;
   pc.xr = int(R);
   pc.tile_elems = Ta * Tb;
@@ -756,6 +775,7 @@ static StagedChoice plan_staged(const std::vector<JMode>& ms, int64_t s_base,
   A.m_swz = best.z;
   A.store_mode = 0;
   A.threads = kThreads;
+  A.stages = staged_stages();
   pc.path = PATH_STAGED;
   pc.tile_elems = tile_elems();
   pc.bank_cost = best.cost;
@@ -824,6 +844,62 @@ static StagedChoice plan_vec(const std::vector<JMode>& ms, int64_t s_base,
   A.d_base = mul_chk(d_base, eb);
   A.s_swz = to_bytes(P.s_swz, eb);
   A.d_swz = to_bytes(P.d_swz, eb);
+  // tiled form: about 1024 vectors per tile over the leading modes, so each
+  // thread's offsets inside a tile are computed once
+  {
+    std::vector<JMode> vm;  // vector units: the run first, then the rest
+    vm.push_back({e / V, V, V});
+    for (const JMode& m : rest) vm.push_back(m);
+    const int64_t want = 256 * vec_unroll();
+    int64_t tile = 1;
+    std::vector<int64_t> T;
+    for (size_t k = 0; k < vm.size(); ++k) {
+      if (tile * vm[k].e <= want) {
+        T.push_back(vm[k].e);
+        tile *= vm[k].e;
+        continue;
+      }
+      const int64_t t = divisor_at_most(vm[k].e, want / tile, 1);
+      T.push_back(t);
+      tile *= t;
+      break;
+    }
+    int64_t s_reach = vb, d_reach = vb;
+    for (size_t k = 0; k < T.size(); ++k) {
+      s_reach = add_chk(s_reach, mul_chk(mul_chk(T[k] - 1, vm[k].s), eb));
+      d_reach = add_chk(d_reach, mul_chk(mul_chk(T[k] - 1, vm[k].d), eb));
+    }
+    std::vector<JMode> grid;
+    for (size_t k = 0; k < vm.size(); ++k) {
+      const int64_t t = k < T.size() ? T[k] : 1;
+      if (t != vm[k].e) grid.push_back({vm[k].e / t, vm[k].s * t, vm[k].d * t});
+    }
+    if (tile >= 256 && s_reach < (int64_t(1) << 31) &&
+        d_reach < (int64_t(1) << 31) && grid.size() <= size_t(kMaxModes) &&
+        prod_e(grid) < (int64_t(1) << 32)) {
+      A.tiled = 1;
+      A.unroll = vec_unroll();
+      A.tile_vecs = uint32_t(tile);
+      A.nt = int32_t(T.size());
+      for (size_t k = 0; k < T.size(); ++k) {
+        A.t_ext[k] = uint32_t(T[k]);
+        A.t_div[k] = make_fastdiv(uint32_t(T[k]));
+        A.t_s[k] = mul_chk(vm[k].s, eb);
+        A.t_d[k] = mul_chk(vm[k].d, eb);
+      }
+      A.n_tiles = uint32_t(prod_e(grid));
+      A.ng = int32_t(grid.size());
+      uint32_t pre = 1;
+      for (size_t k = 0; k < grid.size(); ++k) {
+        A.g_ext[k] = uint32_t(grid[k].e);
+        A.g_pre[k] = make_fastdiv(pre);
+        A.g_div[k] = make_fastdiv(uint32_t(grid[k].e));
+        A.g_s[k] = mul_chk(grid[k].s, eb);
+        A.g_d[k] = mul_chk(grid[k].d, eb);
+        pre *= uint32_t(grid[k].e);
+      }
+    }
+  }
   pc.path = PATH_VEC;
   pc.vec_bytes = vb;
   ch.ok = true;
@@ -898,7 +974,10 @@ static std::string describe(const lm_plan& P) {
          << pc.modes[k].d << ']';
     }
     os << "],\"s_base\":" << pc.s_base << ",\"d_base\":" << pc.d_base;
-    if (pc.path == PATH_VEC) os << ",\"vec_bytes\":" << pc.vec_bytes;
+    if (pc.path == PATH_VEC)
+      os << ",\"vec_bytes\":" << pc.vec_bytes << ",\"tiled\":"
+         << (pc.vec.tiled ? "true" : "false") << ",\"tile_vecs\":"
+         << pc.vec.tile_vecs << ",\"n_tiles\":" << pc.vec.n_tiles;
     if (pc.path == PATH_STAGED) {
       const StagedArgs& A = pc.st;
       os << ",\"tile_elems\":" << pc.tile_elems << ",\"n_tiles\":" << A.n_tiles
@@ -906,6 +985,7 @@ static std::string describe(const lm_plan& P) {
          << ",\"store_chunks\":" << A.n_schunks
          << ",\"store\":\"" << (A.store_mode ? "transpose" : "gather")
          << "\",\"rows\":" << A.xr << ",\"threads\":" << A.threads
+         << ",\"stages\":" << A.stages
          << ",\"stage_bytes\":" << A.stage_bytes << ",\"smem_swizzle\":["
          << A.m_swz.b << ',' << A.m_swz.m << ',' << A.m_swz.s << ']'
          << ",\"bank_wavefronts\":" << pc.bank_cost

@@ -138,6 +138,8 @@ SMALL = [
      ("layout", (128, 96), (1, 128)), 2),
     ("non_refinable_generic", ("layout", (6, 5), (1, 6)),
      ("layout", (5, 6), (6, 1)), 4),
+    ("vec_untiled_prime", ("layout", (8, 2053), (1, 8)),
+     ("layout", (8, 2053), (1, 16)), 2),
     ("rank5_mixed", ("layout", (3, 4, 5, 6, 7), (1, 3, 12, 60, 360)),
      ("layout", (3, 4, 5, 6, 7), (840, 210, 42, 7, 1)), 2),
 ]
