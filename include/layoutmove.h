@@ -57,7 +57,8 @@ typedef enum lm_status {
   LM_E_CAPACITY = -6,          /* a buffer is smaller than the layout needs   */
   LM_E_OVERLAP = -7,           /* src and dst byte ranges overlap             */
   LM_E_CUDA = -8,              /* a CUDA call failed; see lm_last_cuda_error  */
-  LM_E_TIMEOUT = -9,           /* reserved: a bounded device wait gave up     */
+  LM_E_TIMEOUT = -9,           /* a bounded device wait gave up (see
+                                  lm_device_status)                           */
   LM_E_NOMEM = -10,            /* host allocation failed                      */
   LM_E_BUFFER = -11            /* a text output buffer is too small           */
 } lm_status;
@@ -244,6 +245,25 @@ const char* lm_status_string(int status);
 /* The cudaError_t of the last LM_E_CUDA returned on this thread (0 if
  * none). */
 int lm_last_cuda_error(void);
+
+/* Synchronise cuda_stream (a cudaStream_t, NULL for the legacy stream),
+ * then report in *status whether a kernel of this library on the current
+ * device gave up a bounded wait since the last reset: LM_OK, or
+ * LM_E_TIMEOUT (the bulk-copy STAGED kernels bound every mbarrier wait at
+ * about a second; a block that gives up records it here, drains its own
+ * copies and exits, leaving its part of the destination unwritten).  The
+ * record is per device, shared by every stream and sticky; reset != 0
+ * clears it after reading.  Errors: LM_E_INVALID (NULL status), LM_E_CUDA. */
+int lm_device_status(void* cuda_stream, int reset, int* status);
+
+/* Self-test of the bounded device wait (no counterpart on the source
+ * pages).  Clears the status record, launches one warp that waits on an
+ * mbarrier -- with arrive == 0 nothing ever arrives, so the wait gives up
+ * after about a second -- and returns the resulting status in *status
+ * (LM_E_TIMEOUT when arrive == 0, LM_OK otherwise), clearing the record
+ * again.  Never hangs and never faults; blocks the calling thread for about
+ * a second when arrive == 0.  Errors: LM_E_INVALID, LM_E_CUDA. */
+int lm_selftest_bounded_wait(int arrive, void* cuda_stream, int* status);
 
 /* Library version, "major.minor.patch". */
 const char* lm_version(void);

@@ -18,7 +18,7 @@ from typing import Iterable, Sequence
 
 __all__ = [
     "LayoutMoveError", "Layout", "Plan", "lib", "layout_copy",
-    "layout_eval_device", "build_layout", "STATUS",
+    "layout_eval_device", "build_layout", "device_status", "STATUS",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -68,6 +68,8 @@ SIGNATURES = [
     ("lm_plan_destroy", None, [_P]),
     ("lm_status_string", C.c_char_p, [C.c_int]),
     ("lm_last_cuda_error", C.c_int, []),
+    ("lm_device_status", C.c_int, [_P, C.c_int, _IP]),
+    ("lm_selftest_bounded_wait", C.c_int, [C.c_int, _P, _IP]),
     ("lm_version", C.c_char_p, []),
 ]
 
@@ -364,6 +366,15 @@ def layout_eval_device(layout: Layout, table, stream=None) -> None:
                                        table.element_size(), table.numel(),
                                        _stream_handle(stream)),
            "lm_layout_eval_device")
+
+
+def device_status(stream=None, reset: bool = False) -> int:
+    """Synchronise the stream and return LM_OK (0) or LM_E_TIMEOUT (-9) if a
+    kernel of the library gave up a bounded wait since the last reset."""
+    st = C.c_int()
+    _check(lib().lm_device_status(_stream_handle(stream), int(reset),
+                                  C.byref(st)), "lm_device_status")
+    return st.value
 
 
 def build_layout(spec) -> Layout:

@@ -217,8 +217,13 @@ struct StagedArgs {
   int32_t store_mode = 0;               // 0 gather, 1 transpose
   int32_t xr = 0;                       // R, rows per micro-tile
   uint32_t n_micro = 0;                 // micro-tiles per tile
-  uint32_t n_bc = 1;                    // micro-tiles along b (fastest)
+  uint32_t n_bc = 1;                    // micro-tiles along b
   FastDiv bc_div;
+  uint32_t n_ac = 1;                    // micro-tiles along a
+  FastDiv ac_div;
+  int32_t x_acfast = 0;                 // 1: micro-tile index runs along a
+                                        //    first (conflict-free rows
+                                        //    without a swizzle)
   uint32_t x_pitch = 0;                 // smem bytes between rows
   int64_t x_da = 0;                     // dst bytes per 16-byte chunk of a
   int64_t x_db = 0;                     // dst bytes per R rows of b
@@ -228,6 +233,13 @@ struct StagedArgs {
   Swz m_swz;                            // smem swizzle, bytes
   int32_t threads = 256;                // block size
   int32_t stages = 2;                   // cp.async pipeline depth (2 or 3)
+  // bulk-copy form (bulk == 1): one cp.async.bulk per source segment into an
+  // unswizzled image, mbarrier pipeline; needs the whole source reach
+  // (src_reach bytes from the buffer start) inside the caller's capacity
+  int32_t bulk = 0;
+  int32_t bulk_stages = 3;
+  uint32_t n_seg = 0, seg_bytes = 0;
+  int64_t src_reach = 0;
 };
 
 struct EvalArgs {

@@ -25,6 +25,7 @@
 #include <cstdlib>
 #include <utility>
 #include <cstring>
+#include <map>
 #include <mutex>
 
 #include "lm_internal.h"
@@ -548,8 +549,14 @@ struct XposeStore {
       dst[k] = -1;
       lin[k] = 0;
       if (j < a.n_micro) {
-        const uint32_t ac = fdiv(j, a.bc_div);
-        const uint32_t bc = j - ac * a.n_bc;
+        uint32_t ac, bc;
+        if (a.x_acfast) {
+          bc = fdiv(j, a.ac_div);
+          ac = j - bc * a.n_ac;
+        } else {
+          ac = fdiv(j, a.bc_div);
+          bc = j - ac * a.n_bc;
+        }
         dst[k] = int32_t(int64_t(ac) * a.x_da + int64_t(bc) * a.x_db);
         lin[k] = bc * uint32_t(R) * a.x_pitch + ac * 16u;
       }
@@ -644,6 +651,201 @@ __global__ void __launch_bounds__(256)
     for (int i = 0; i < NS - 1; ++i) dq[i] = dq[i + 1];
   }
   cp_async_wait<0>();
+}
+
+// ---------------------------------------------------------------------------
+// STAGED copy, bulk-copy form
+//
+// Warp 0 is the producer: per tile it announces the tile's byte count on the
+// stage's "full" mbarrier and its lanes issue one cp.async.bulk per source
+// segment (row) straight into the stage's padded shared-memory image.  Every
+// warp consumes: it waits on "full", runs the store policy on the stage and
+// arrives on the stage's "empty" mbarrier, which the producer waits on before
+// refilling the stage NS tiles later.  No block-wide barrier sits in the
+// tile loop.
+//
+// Every wait is bounded (kWaitCycles of clock64, about a second): a wait
+// that gives up sets bit 0 of g_lm_device_status, the producer then waits,
+// again bounded, for the copies it still has in flight, and the block
+// returns.  The host reads the word with lm_device_status.
+// ---------------------------------------------------------------------------
+
+__device__ unsigned int g_lm_device_status = 0;
+constexpr long long kWaitCycles = 2000000000LL;
+constexpr int kBulkSegsPerLane = 4;  // up to 128 segments per tile
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar),
+               "r"(count)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar,
+                                                      uint32_t bytes) {
+  asm volatile(
+      "mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar),
+      "r"(bytes)
+      : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for the phase with the given parity to complete.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try(bar, parity))
+    if (clock64() - t0 > kWaitCycles) return false;
+  return true;
+}
+// The same, agreed by the whole warp (every lane waits, so every lane has
+// acquired the phase; the warp proceeds only if all lanes saw it complete).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity));
+}
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst_smem, const void* src,
+                                         uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1], %2, [%3];\n" ::"r"(dst_smem),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+template <int EB, class Store, int NS>
+__global__ void __launch_bounds__(256)
+    lm_bulk_kernel(const __grid_constant__ StagedArgs a,
+                   const char* __restrict__ src, char* __restrict__ dst) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const uint32_t tid = threadIdx.x, nt = blockDim.x;
+  const uint32_t warp = tid >> 5, lane = tid & 31, n_warps = nt >> 5;
+  const uint32_t bars = uint32_t(__cvta_generic_to_shared(smem));
+  auto full = [&](uint32_t s) { return bars + 8u * s; };
+  auto empty = [&](uint32_t s) { return bars + 8u * (NS + s); };
+  unsigned char* stages = smem + 128;
+  const uint32_t stage0 = bars + 128;
+
+  Store st;
+  st.init(a, tid, nt);
+  // producer slots: segments lane, lane + 32, ... (source and smem offsets)
+  int32_t seg_src[kBulkSegsPerLane];
+  uint32_t seg_sm[kBulkSegsPerLane];
+  if (warp == 0) {
+#pragma unroll
+    for (int k = 0; k < kBulkSegsPerLane; ++k) {
+      const uint32_t g = lane + 32u * uint32_t(k);
+      seg_src[k] = -1;
+      seg_sm[k] = 0;
+      if (g < a.n_seg) {
+        int64_t srel = 0;
+        uint32_t mrel = 0, r = g;
+#pragma unroll
+        for (int t = 0; t < kMaxTile; ++t) {
+          if (t >= a.nso) break;
+          const uint32_t rn = fdiv(r, a.so_div[t]);
+          const uint32_t x = r - rn * a.so_ext[t];
+          srel += int64_t(x) * a.so_s[t];
+          mrel += x * a.so_m[t];
+          r = rn;
+        }
+        seg_src[k] = int32_t(srel);
+        seg_sm[k] = mrel;
+      }
+    }
+  }
+  if (tid == 0) {
+#pragma unroll
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), n_warps);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  __syncthreads();
+  pdl_trigger();
+  pdl_wait();
+
+  if (blockIdx.x >= a.n_tiles) return;
+  const uint32_t G = gridDim.x;
+  const uint32_t n_local = (a.n_tiles - blockIdx.x + G - 1) / G;
+  const uint32_t tile_bytes = a.n_seg * a.seg_bytes;
+  bool ok = true;
+  uint32_t issued = 0;  // tiles the producer has issued
+
+  // producer: tile number i of this block into stage i % NS
+  auto issue = [&](uint32_t i) -> bool {
+    const uint32_t s = i % NS;
+    if (i >= uint32_t(NS) && !warp_wait(empty(s), ((i / NS) - 1) & 1))
+      return false;
+    int64_t sb, db;
+    tile_base(a, blockIdx.x + i * G, sb, db);
+    if (lane == 0) mbar_arrive_expect_tx(full(s), tile_bytes);
+    __syncwarp();
+    const char* base = src + a.s_base + sb;
+    const uint32_t sdst = stage0 + s * a.stage_bytes;
+#pragma unroll
+    for (int k = 0; k < kBulkSegsPerLane; ++k)
+      if (seg_src[k] >= 0)
+        bulk_g2s(sdst + seg_sm[k], base + seg_src[k], a.seg_bytes, full(s));
+    return true;
+  };
+
+  if (warp == 0)
+    for (uint32_t i = 0; i < uint32_t(NS - 1) && i < n_local && ok; ++i) {
+      ok = issue(i);
+      issued += ok ? 1u : 0u;
+    }
+  uint32_t i = 0;
+  for (; i < n_local; ++i) {
+    if (warp == 0 && ok && i + NS - 1 < n_local) {
+      ok = issue(i + NS - 1);
+      issued += ok ? 1u : 0u;
+    }
+    const uint32_t s = i % NS;
+    if (!ok || !warp_wait(full(s), (i / NS) & 1)) {
+      ok = false;
+      break;
+    }
+    int64_t sb, db;
+    tile_base(a, blockIdx.x + i * G, sb, db);
+    st.store(a, stages + size_t(s) * a.stage_bytes, dst, a.d_base + db);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty(s));
+  }
+  if (!ok) {
+    if (lane == 0) atomicOr(&g_lm_device_status, 1u);
+    if (warp == 0)  // drain this block's copies still in flight
+      for (uint32_t j = i; j < issued; ++j)
+        warp_wait(full(j % NS), (j / NS) & 1);
+  }
+}
+
+// Self-test of the bounded wait: one warp waits on an mbarrier that, with
+// arrive == 0, nothing ever arrives at.  The wait gives up after kWaitCycles
+// and records the timeout exactly as the copy kernels do.
+__global__ void lm_selftest_wait_kernel(int arrive) {
+  __shared__ __align__(8) unsigned long long bar;
+  const uint32_t b = uint32_t(__cvta_generic_to_shared(&bar));
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  __syncthreads();
+  if (arrive && threadIdx.x == 0) mbar_arrive(b);
+  const bool ok = warp_wait(b, 0);
+  if (!ok && threadIdx.x == 0) atomicOr(&g_lm_device_status, 1u);
 }
 
 // ---------------------------------------------------------------------------
@@ -809,9 +1011,57 @@ int launch_staged_ns(const StagedArgs& a, const char* src, int64_t src_cap,
   return check_launch();
 }
 
+// Dynamic shared memory above 48 KiB needs an opt-in per device and kernel
+// (cached per device and kernel address).
+template <typename K>
+bool allow_smem(K kern, int bytes) {
+  if (bytes <= 49152) return true;
+  static std::mutex mu;
+  static std::map<std::pair<int, const void*>, int> done;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  const auto key = std::make_pair(dev, reinterpret_cast<const void*>(kern));
+  std::lock_guard<std::mutex> g(mu);
+  auto it = done.find(key);
+  if (it == done.end() || it->second < bytes) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             bytes) != cudaSuccess)
+      return false;
+    done[key] = bytes;
+  }
+  return true;
+}
+
+template <int EB, class Store, int NS>
+int launch_bulk_ns(const StagedArgs& a, const char* src, char* dst,
+                   cudaStream_t st) {
+  const int smem = int(128 + NS * a.stage_bytes);
+  if (!allow_smem(lm_bulk_kernel<EB, Store, NS>, smem)) return LM_E_CUDA;
+  const DeviceInfo di = device_info();
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+          &per_sm, lm_bulk_kernel<EB, Store, NS>, a.threads, size_t(smem)) !=
+          cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  const uint64_t cap = uint64_t(di.sms) * uint64_t(per_sm);
+  const unsigned grid =
+      unsigned(std::max<uint64_t>(1, std::min<uint64_t>(a.n_tiles, cap)));
+  launch_k(lm_bulk_kernel<EB, Store, NS>, grid, unsigned(a.threads),
+           size_t(smem), st, a, src, dst);
+  return check_launch();
+}
+
 template <int EB, class Store>
 int launch_staged_t(const StagedArgs& a, const char* src, int64_t src_cap,
                     char* dst, cudaStream_t st) {
+  if (a.bulk && src_cap >= a.src_reach) {
+    switch (a.bulk_stages) {
+      case 2: return launch_bulk_ns<EB, Store, 2>(a, src, dst, st);
+      case 4: return launch_bulk_ns<EB, Store, 4>(a, src, dst, st);
+      default: return launch_bulk_ns<EB, Store, 3>(a, src, dst, st);
+    }
+  }
   if (a.stages == 3 && 3 * a.stage_bytes <= 49152)
     return launch_staged_ns<EB, Store, 3>(a, src, src_cap, dst, st);
   return launch_staged_ns<EB, Store, 2>(a, src, src_cap, dst, st);
@@ -972,5 +1222,36 @@ int lm_layout_eval_device(const lm_layout* layout, void* table_dev,
 }
 
 int lm_last_cuda_error(void) { return lm::g_last_cuda; }
+
+int lm_selftest_bounded_wait(int arrive, void* cuda_stream, int* status) {
+  if (!status) return LM_E_INVALID;
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  int before = 0;
+  int rc = lm_device_status(cuda_stream, 1, &before);
+  if (rc != LM_OK) return rc;
+  lm::lm_selftest_wait_kernel<<<1, 32, 0, st>>>(arrive);
+  rc = lm::check_launch();
+  if (rc != LM_OK) return rc;
+  return lm_device_status(cuda_stream, 1, status);
+}
+
+int lm_device_status(void* cuda_stream, int reset, int* status) {
+  if (!status) return LM_E_INVALID;
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  unsigned int word = 0;
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e == cudaSuccess)
+    e = cudaMemcpyFromSymbol(&word, lm::g_lm_device_status, sizeof(word));
+  if (e == cudaSuccess && reset && word) {
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(lm::g_lm_device_status, &zero, sizeof(zero));
+  }
+  if (e != cudaSuccess) {
+    lm::set_cuda_error(int(e));
+    return LM_E_CUDA;
+  }
+  *status = word ? LM_E_TIMEOUT : LM_OK;
+  return LM_OK;
+}
 
 }  // extern "C"

@@ -162,6 +162,31 @@ int vec_unroll() {
   return v;
 }
 
+// Bulk-copy (TMA) loads for STAGED tiles (LM_BULK=0 turns them off) and
+// their pipeline depth (LM_BULK_STAGES, 2..4).
+bool bulk_enabled() {
+  static bool v = env_int("LM_BULK", 1) != 0;
+  return v;
+}
+int bulk_stages() {
+  static int v = std::clamp(env_int("LM_BULK_STAGES", 2), 2, 4);
+  return v;
+}
+// Bulk copies pay off for long rows: the bf16/fp32 transposes' 128-256 byte
+// rows ran faster with per-thread cp.async (measured on GB300), the 9 KiB
+// segments of the padded TV gather faster with one bulk copy.
+constexpr int64_t kBulkMinSegment = 1024;
+
+// Largest byte offset + 1 the loads of any tile reach from the buffer start.
+int64_t src_reach(const StagedArgs& A) {
+  int64_t r = add_chk(A.s_base, int64_t(A.seg_bytes));
+  for (int k = 0; k < A.ng; ++k)
+    r = add_chk(r, mul_chk(int64_t(A.g_ext[k]) - 1, A.g_s[k]));
+  for (int k = 0; k < A.nso; ++k)
+    r = add_chk(r, mul_chk(int64_t(A.so_ext[k]) - 1, A.so_s[k]));
+  return r;
+}
+
 int64_t tile_bytes_target() {
   static int64_t v = [] {
     const char* e = std::getenv("LM_TILE_BYTES");
@@ -225,7 +250,7 @@ struct SmemLayout {
 template <class ReadAddr>
 SmemLayout search_smem(int threads, int64_t n_seg, int64_t seg_bytes,
                        int64_t n_reads, int per, int width,
-                       const ReadAddr& read_addr) {
+                       const ReadAddr& read_addr, bool allow_swizzle = true) {
   SmemLayout best;
   const int64_t cps = seg_bytes / 16;
   const int64_t n_l = n_seg * cps;
@@ -235,8 +260,9 @@ SmemLayout search_smem(int threads, int64_t n_seg, int64_t seg_bytes,
       n_seg > 1 ? std::vector<int64_t>{0, 16, 32, 48, 64, 80, 96, 112}
                 : std::vector<int64_t>{0};
   std::vector<Swz> zs{Swz{}};
-  for (int bb = 1; bb <= 3; ++bb)
-    for (int ss = bb; ss <= 10; ++ss) zs.push_back(Swz{bb, 4, ss});
+  if (allow_swizzle)
+    for (int bb = 1; bb <= 3; ++bb)
+      for (int ss = bb; ss <= 10; ++ss) zs.push_back(Swz{bb, 4, ss});
   std::vector<int64_t> addr(32);
   bool valid[32];
   for (int64_t pad : pads) {
@@ -436,12 +462,18 @@ static StagedChoice plan_transpose(const std::vector<JMode>& ms,
   if (s_reach >= (int64_t(1) << 31) || d_reach >= (int64_t(1) << 31))
     return ch;
 
+  const bool bulk = bulk_enabled() && !ssb.on() && Tb <= 128 &&
+                    seg_bytes >= kBulkMinSegment;
+  // without a swizzle (bulk copies write rows linearly) run the micro-tile
+  // index along a first: 8 lanes then read 8 consecutive chunks of a row
+  const bool acfast = bulk && n_ac >= 8;
   auto read_addr = [&](int64_t j, int r, int64_t pitch) {
-    const int64_t bc = j % n_bc, ac = j / n_bc;
+    const int64_t bc = acfast ? j / n_ac : j % n_bc;
+    const int64_t ac = acfast ? j % n_ac : j / n_bc;
     return (bc * R + r) * pitch + ac * 16;
   };
   const SmemLayout best = search_smem(int(threads), Tb, seg_bytes, n_micro,
-                                      int(R), 16, read_addr);
+                                      int(R), 16, read_addr, !bulk);
   if (best.cost < 0) return ch;
 
   StagedArgs& A = pc.st;
@@ -461,6 +493,9 @@ static StagedChoice plan_transpose(const std::vector<JMode>& ms,
   A.n_micro = uint32_t(n_micro);
   A.n_bc = uint32_t(n_bc);
   A.bc_div = make_fastdiv(uint32_t(n_bc));
+  A.n_ac = uint32_t(n_ac);
+  A.ac_div = make_fastdiv(uint32_t(n_ac));
+  A.x_acfast = acfast ? 1 : 0;
   A.x_pitch = uint32_t(pitch);
   A.x_da = mul_chk(V * ma.d, eb);
   A.x_db = R * eb;
@@ -469,6 +504,13 @@ static StagedChoice plan_transpose(const std::vector<JMode>& ms,
   A.m_swz = best.z;
   A.threads = int32_t(threads);
   A.stages = staged_stages();
+  if (bulk) {
+    A.bulk = 1;
+    A.bulk_stages = bulk_stages();
+    A.n_seg = uint32_t(Tb);
+    A.seg_bytes = uint32_t(seg_bytes);
+    A.src_reach = src_reach(A);
+  }
   pc.path = PATH_STAGED;
   pc.xr = int(R);
   pc.tile_elems = Ta * Tb;
@@ -731,8 +773,10 @@ static StagedChoice plan_staged(const std::vector<JMode>& ms, int64_t s_base,
     }
     return addr;
   };
-  const SmemLayout best =
-      search_smem(kThreads, n_seg, seg_bytes, n_s, int(V), eb, gather_addr);
+  const bool bulk = bulk_enabled() && !ssb.on() && n_seg <= 128 &&
+                    seg_bytes >= kBulkMinSegment;
+  const SmemLayout best = search_smem(kThreads, n_seg, seg_bytes, n_s,
+                                      int(V), eb, gather_addr, !bulk);
   if (best.cost < 0) return ch;
 
   // ---- fill the kernel arguments -----------------------------------------
@@ -776,6 +820,13 @@ static StagedChoice plan_staged(const std::vector<JMode>& ms, int64_t s_base,
   A.store_mode = 0;
   A.threads = kThreads;
   A.stages = staged_stages();
+  if (bulk) {
+    A.bulk = 1;
+    A.bulk_stages = bulk_stages();
+    A.n_seg = uint32_t(n_seg);
+    A.seg_bytes = uint32_t(seg_bytes);
+    A.src_reach = src_reach(A);
+  }
   pc.path = PATH_STAGED;
   pc.tile_elems = tile_elems();
   pc.bank_cost = best.cost;
@@ -985,7 +1036,9 @@ static std::string describe(const lm_plan& P) {
          << ",\"store_chunks\":" << A.n_schunks
          << ",\"store\":\"" << (A.store_mode ? "transpose" : "gather")
          << "\",\"rows\":" << A.xr << ",\"threads\":" << A.threads
-         << ",\"stages\":" << A.stages
+         << ",\"stages\":" << (A.bulk ? A.bulk_stages : A.stages)
+         << ",\"bulk\":"
+         << (A.bulk ? "true" : "false")
          << ",\"stage_bytes\":" << A.stage_bytes << ",\"smem_swizzle\":["
          << A.m_swz.b << ',' << A.m_swz.m << ',' << A.m_swz.s << ']'
          << ",\"bank_wavefronts\":" << pc.bank_cost

@@ -43,7 +43,7 @@ def device_buffer(nbytes, fill, offset=0):
 
 def run_case(src_spec, dst_spec, eb, values="bytes", dtype="uint8", seed=7,
              src_offset=0, dst_offset=0, stream=None, sentinel=None,
-             expect_paths=None):
+             expect_paths=None, src_round16=False):
     S, D = lm.build_layout(src_spec), lm.build_layout(dst_spec)
     OS, OD = lo.build(src_spec), lo.build(dst_spec)
     plan = lm.Plan(S, D, eb)
@@ -52,6 +52,8 @@ def run_case(src_spec, dst_spec, eb, values="bytes", dtype="uint8", seed=7,
     n_src, n_dst = lo.cosize(OS), lo.cosize(OD)
     assert S.cosize >= n_src and D.cosize >= n_dst
     n_src_cap, n_dst_cap = S.cosize, D.cosize
+    if src_round16:   # the source buffer rounded up to a 16-byte multiple
+        n_src_cap = -(-(n_src_cap * eb) // 16) * 16 // eb
     if values == "bytes":
         inp = seeded_bytes("bytes", "uint8", n_src_cap * eb, seed)
     else:
@@ -138,6 +140,8 @@ SMALL = [
      ("layout", (128, 96), (1, 128)), 2),
     ("non_refinable_generic", ("layout", (6, 5), (1, 6)),
      ("layout", (5, 6), (6, 1)), 4),
+    ("transpose_tall_f32", ("layout", (2048, 96), (1, 2048)),
+     ("layout", (2048, 96), (96, 1)), 4),
     ("vec_untiled_prime", ("layout", (8, 2053), (1, 8)),
      ("layout", (8, 2053), (1, 16)), 2),
     ("rank5_mixed", ("layout", (3, 4, 5, 6, 7), (1, 3, 12, 60, 360)),
@@ -279,4 +283,65 @@ def test_full_size_workload(name):
     w = WORKLOADS[name]
     sentinel = 0x7FF8DEADBEEF0001 if name == "C4" else None
     run_case(w.src, w.dst, w.elem_bytes, values=w.values, dtype=w.dtype,
-             seed=w.seed, sentinel=sentinel)
+             seed=w.seed, sentinel=sentinel, src_round16=True)
+    assert lm.device_status() == 0
+
+
+# --------------------------------------------------------------------------
+# the two load paths of STAGED and the bounded waits of the bulk path
+# --------------------------------------------------------------------------
+
+VARIANT_CASES = ["transpose_ragged_f32", "transpose_1000x1000_f16",
+                 "padded_tv_gather_f64", "head_interleave_full_rows",
+                 "tiles_swizzled_bf16", "identity_vec", "transpose_tall_f32"]
+
+
+def test_bulk_path_is_planned_for_long_segments():
+    for name, bulk in (("C2", False), ("C4", True), ("C5a", False),
+                       ("C5b", True)):
+        w = WORKLOADS[name]
+        d = lm.Plan(lm.build_layout(w.src), lm.build_layout(w.dst),
+                    w.elem_bytes).describe()
+        assert all(p["bulk"] == bulk for p in d["pieces"]), (name, d)
+
+
+@pytest.mark.parametrize("env", [{"LM_BULK": "0"},
+                                 {"LM_BULK": "0", "LM_STAGES": "3"},
+                                 {"LM_BULK_STAGES": "2"},
+                                 {"LM_BULK_STAGES": "4", "LM_VEC_UNROLL": "8"}])
+def test_pipeline_variants_parity(env):
+    """The cp.async load path (LM_BULK=0, 2 or 3 stages) and other bulk
+    pipeline depths, in a fresh process since the knobs are read once."""
+    import os
+    import subprocess
+    import sys
+    here = os.path.dirname(os.path.abspath(__file__))
+    code = (
+        "import sys; sys.path[:0] = [%r, %r]\n"
+        "import test_gpu_parity as t\n"
+        "t.lm.lib()\n"
+        "cases = {c[0]: c for c in t.SMALL}\n"
+        "for n in %r:\n"
+        "    _, s, d, eb = cases[n]\n"
+        "    p = t.run_case(s, d, eb)\n"
+        "    bulk = [pc.get('bulk') for pc in p.describe()['pieces']]\n"
+        "    if %r == '0': assert not any(bulk), (n, bulk)\n"
+        "print('ok')\n" % (here, os.path.dirname(here), VARIANT_CASES,
+                           env.get("LM_BULK", "1")))
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True,
+                       text=True, env={**os.environ, **env}, timeout=600)
+    assert r.returncode == 0 and "ok" in r.stdout, r.stdout + r.stderr
+
+
+def test_bounded_wait_gives_up_and_reports():
+    import ctypes as C
+    st = C.c_int(123)
+    L = lm.lib()
+    assert L.lm_selftest_bounded_wait(1, None, C.byref(st)) == 0
+    assert st.value == 0
+    assert L.lm_selftest_bounded_wait(0, None, C.byref(st)) == 0
+    assert st.value == -9                    # LM_E_TIMEOUT, after ~1 s
+    assert lm.device_status() == 0           # the self-test cleared it
+    # the context is still usable
+    run_case(("layout", (96, 80), (1, 96)), ("layout", (96, 80), (80, 1)), 4)
+    assert lm.device_status() == 0
