@@ -75,6 +75,17 @@ __device__ __forceinline__ void pdl_wait() {
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
 }
 
+// Streaming global accesses: every byte is read once and written once, so
+// both are marked evict-first in L1/L2.
+template <class T>
+__device__ __forceinline__ T ld_stream(const T* p) {
+  return __ldcs(p);
+}
+template <class T>
+__device__ __forceinline__ void st_stream(T* p, const T& v) {
+  __stcs(p, v);
+}
+
 __device__ __forceinline__ int64_t swz_apply(const Swz& z, int64_t o) {
   return z.b > 0 ? (o ^ ((o >> z.s) & (((int64_t(1) << z.b) - 1) << z.m))) : o;
 }
@@ -198,12 +209,12 @@ __global__ void __launch_bounds__(256)
         }
         s = swz_apply(a.s_swz, s);
         doff[u] = swz_apply(a.d_swz, d);
-        v[u] = __ldcs(reinterpret_cast<const T*>(src + s));
+        v[u] = ld_stream(reinterpret_cast<const T*>(src + s));
       }
     }
 #pragma unroll
     for (int u = 0; u < kVecUnroll; ++u)
-      if (doff[u] >= 0) __stcs(reinterpret_cast<T*>(dst + doff[u]), v[u]);
+      if (doff[u] >= 0) st_stream(reinterpret_cast<T*>(dst + doff[u]), v[u]);
   }
 }
 
@@ -274,7 +285,7 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
   for (int u = 0; u < U; ++u)
     if (so[u] >= 0)
-      cur[u] = __ldcs(reinterpret_cast<const T*>(
+      cur[u] = ld_stream(reinterpret_cast<const T*>(
           src + swz_apply(a.s_swz, a.s_base + sb + so[u])));
   for (;;) {
     const uint64_t next64 = uint64_t(tile) + gridDim.x;
@@ -287,13 +298,13 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
       for (int u = 0; u < U; ++u)
         if (so[u] >= 0)
-          nxt[u] = __ldcs(reinterpret_cast<const T*>(
+          nxt[u] = ld_stream(reinterpret_cast<const T*>(
               src + swz_apply(a.s_swz, a.s_base + nsb + so[u])));
     }
 #pragma unroll
     for (int u = 0; u < U; ++u)
       if (so[u] >= 0)
-        __stcs(reinterpret_cast<T*>(
+        st_stream(reinterpret_cast<T*>(
                    dst + swz_apply(a.d_swz, a.d_base + db + dof[u])),
                cur[u]);
     if (!has_next) break;
@@ -410,7 +421,7 @@ struct LoadSlots {
 
 template <int EB>
 struct GatherStore {
-  static constexpr int kLoadSlots = 4;
+  static constexpr int kLoadSlots = EB >= 8 ? 8 : 4;
   static constexpr int V = 16 / EB;
   static constexpr int MaxS = (16 / V) < 1 ? 1 : ((16 / V) > 4 ? 4 : 16 / V);
   int32_t dst[MaxS];
@@ -499,7 +510,7 @@ struct GatherStore {
         }
       }
       const int64_t off = swz_apply(a.d_swz, dbase + dst[k]);
-      __stcs(reinterpret_cast<uint4*>(dst_p + off),
+      st_stream(reinterpret_cast<uint4*>(dst_p + off),
              make_uint4(w[0], w[1], w[2], w[3]));
     }
   }
@@ -583,7 +594,7 @@ struct XposeStore {
 #pragma unroll
       for (int j = 0; j < R; ++j) {
         const int64_t off = swz_apply(a.d_swz, base + j * a.x_vstep);
-        __stcs(reinterpret_cast<uint4*>(dst_p + off),
+        st_stream(reinterpret_cast<uint4*>(dst_p + off),
                make_uint4(xword<EB, R>(in, 4 * j), xword<EB, R>(in, 4 * j + 1),
                           xword<EB, R>(in, 4 * j + 2),
                           xword<EB, R>(in, 4 * j + 3)));
@@ -870,6 +881,31 @@ DeviceInfo device_info() {
   return cache[dev];
 }
 
+// Blocks launched: several waves beat one persistent wave (measured on
+// GB300): blocks that finish are replaced at once, so the memory system
+// stays busy to the end.  VEC grids are LM_WAVES_VEC (default 8) times the
+// resident blocks.
+uint64_t env_waves(const char* name, uint64_t dflt) {
+  const char* e = std::getenv(name);
+  const long long w = e ? std::atoll(e) : (long long)dflt;
+  return uint64_t(w < 1 ? 1 : w);
+}
+uint64_t waves_vec() {
+  static uint64_t v = env_waves("LM_WAVES_VEC", 8);
+  return v;
+}
+// STAGED grids give each block about this many tiles (LM_TILES_PER_BLOCK):
+// enough for the two-stage pipeline to overlap a tile's loads with the
+// previous tile's stores, few enough that blocks turn over often.
+uint64_t tiles_per_block() {
+  static uint64_t v = env_waves("LM_TILES_PER_BLOCK", 2);
+  return v;
+}
+uint64_t staged_grid(uint64_t n_tiles, uint64_t resident) {
+  const uint64_t want = (n_tiles + tiles_per_block() - 1) / tiles_per_block();
+  return std::max<uint64_t>(1, std::min<uint64_t>(want, resident * 64));
+}
+
 bool pdl_enabled() {
   static bool v = [] {
     const char* e = std::getenv("LM_PDL");
@@ -967,7 +1003,7 @@ int launch_vec_tiled(const VecArgs& v, const char* src, char* dst,
           &per_sm, lm_vec_tiled_kernel<VB, U>, 256, 0) != cudaSuccess ||
       per_sm < 1)
     per_sm = 1;
-  const uint64_t cap = uint64_t(di.sms) * uint64_t(per_sm);
+  const uint64_t cap = uint64_t(di.sms) * uint64_t(per_sm) * waves_vec();
   const unsigned grid =
       unsigned(std::max<uint64_t>(1, std::min<uint64_t>(v.n_tiles, cap)));
   launch_k(lm_vec_tiled_kernel<VB, U>, grid, 256, 0, st, v, src, dst);
@@ -1003,9 +1039,8 @@ int launch_staged_ns(const StagedArgs& a, const char* src, int64_t src_cap,
           size_t(smem)) != cudaSuccess ||
       per_sm < 1)
     per_sm = 1;
-  const uint64_t cap = uint64_t(di.sms) * uint64_t(per_sm);
-  const unsigned grid =
-      unsigned(std::max<uint64_t>(1, std::min<uint64_t>(a.n_tiles, cap)));
+  const unsigned grid = unsigned(
+      staged_grid(a.n_tiles, uint64_t(di.sms) * uint64_t(per_sm)));
   launch_k(lm_staged_kernel<EB, Store, NS>, grid, unsigned(a.threads),
            size_t(smem), st, a, src, dst, src_cap);
   return check_launch();
@@ -1044,9 +1079,8 @@ int launch_bulk_ns(const StagedArgs& a, const char* src, char* dst,
           cudaSuccess ||
       per_sm < 1)
     per_sm = 1;
-  const uint64_t cap = uint64_t(di.sms) * uint64_t(per_sm);
-  const unsigned grid =
-      unsigned(std::max<uint64_t>(1, std::min<uint64_t>(a.n_tiles, cap)));
+  const unsigned grid = unsigned(
+      staged_grid(a.n_tiles, uint64_t(di.sms) * uint64_t(per_sm)));
   launch_k(lm_bulk_kernel<EB, Store, NS>, grid, unsigned(a.threads),
            size_t(smem), st, a, src, dst);
   return check_launch();

@@ -187,10 +187,30 @@ int64_t src_reach(const StagedArgs& A) {
   return r;
 }
 
+// Order of the tile grid (and of the VEC modes): by destination stride
+// (LM_GRID_ORDER=d, default) or by source stride (LM_GRID_ORDER=s).
+bool order_by_src() {
+  static bool v = [] {
+    const char* e = std::getenv("LM_GRID_ORDER");
+    return e && e[0] == 's';
+  }();
+  return v;
+}
+bool mode_before(const JMode& x, const JMode& y) {
+  return order_by_src() ? (x.s < y.s || (x.s == y.s && x.d < y.d))
+                        : (x.d < y.d || (x.d == y.d && x.s < y.s));
+}
+// Bytes of one shared-memory row (along the source-fast mode) of a
+// transpose tile (LM_XPOSE_ROW_BYTES, default 256).
+int64_t xpose_row_bytes() {
+  static int64_t v = std::clamp(env_int("LM_XPOSE_ROW_BYTES", 256), 64, 4096);
+  return v;
+}
+
 int64_t tile_bytes_target() {
   static int64_t v = [] {
     const char* e = std::getenv("LM_TILE_BYTES");
-    int64_t t = e ? std::atoll(e) : 8192;
+    int64_t t = e ? std::atoll(e) : 16384;
     return std::clamp<int64_t>(t, 1024, 24576);
   }();
   return v;
@@ -398,7 +418,7 @@ static StagedChoice plan_transpose(const std::vector<JMode>& ms,
   const int64_t target = tile_target(mul_chk(prod_e(ms), eb)) / eb;
   int64_t Ta, Tb;
   if (R == V) {
-    Ta = divisor_at_most(ma.e, std::max<int64_t>(V, 256 / eb), V);
+    Ta = divisor_at_most(ma.e, std::max<int64_t>(V, xpose_row_bytes() / eb), V);
     if (!Ta) return ch;
     const int64_t want_b = std::max<int64_t>(V, target / Ta);
     Tb = divisor_at_most(mb.e, want_b, V);
@@ -454,8 +474,7 @@ static StagedChoice plan_transpose(const std::vector<JMode>& ms,
     if (!al(m.s * t) || !al(m.d * t)) return ch;
   }
   if (grid.size() > size_t(kMaxModes)) return ch;
-  std::sort(grid.begin(), grid.end(),
-            [](const JMode& x, const JMode& y) { return x.d < y.d; });
+  std::sort(grid.begin(), grid.end(), mode_before);
   if (prod_e(grid) >= (int64_t(1) << 32)) return ch;
   const int64_t s_reach = add_chk(mul_chk(mul_chk(Tb - 1, mb.s), eb), seg_bytes);
   const int64_t d_reach = add_chk(mul_chk(mul_chk(Ta - 1, ma.d), eb), Tb * eb);
@@ -728,8 +747,7 @@ static StagedChoice plan_staged(const std::vector<JMode>& ms, int64_t s_base,
     if (!al(m.s * t) || !al(m.d * t)) return ch;
   }
   if (grid.size() > size_t(kMaxModes)) return ch;
-  std::sort(grid.begin(), grid.end(),
-            [](const JMode& x, const JMode& y) { return x.d < y.d; });
+  std::sort(grid.begin(), grid.end(), mode_before);
   const int64_t n_tiles = prod_e(grid);
   if (n_tiles >= (int64_t(1) << 32)) return ch;
 
@@ -740,8 +758,10 @@ static StagedChoice plan_staged(const std::vector<JMode>& ms, int64_t s_base,
   const int64_t n_l = n_seg * cps;
   const int64_t n_s = tile_elems() / V;
   const int64_t cpd = d_span * eb / 16;
+  // (these limits match GatherStore: load chunks and store chunks per thread)
   const int max_s = std::max(1, std::min(4, 16 / int(V)));
-  if (n_l > kThreads * 4 || n_s > int64_t(kThreads) * max_s) return ch;
+  const int max_l = eb >= 8 ? 8 : 4;
+  if (n_l > kThreads * max_l || n_s > int64_t(kThreads) * max_s) return ch;
 
   // smem bytes per coordinate of each tile mode for a given pitch
   auto smem_m = [&](int64_t pitch, std::vector<int64_t>& m) {
@@ -872,8 +892,7 @@ static StagedChoice plan_vec(const std::vector<JMode>& ms, int64_t s_base,
   std::vector<JMode> rest;
   for (size_t k = 0; k < ms.size(); ++k)
     if (int(k) != r) rest.push_back(ms[k]);
-  std::sort(rest.begin(), rest.end(),
-            [](const JMode& x, const JMode& y) { return x.d < y.d; });
+  std::sort(rest.begin(), rest.end(), mode_before);
   if (rest.size() + 1 > size_t(kMaxModes)) return ch;
   VecArgs& A = pc.vec;
   A = VecArgs{};
