@@ -236,6 +236,8 @@ struct StagedArgs {
   // bulk-copy form (bulk == 1): one cp.async.bulk per source segment into an
   // unswizzled image, mbarrier pipeline; needs the whole source reach
   // (src_reach bytes from the buffer start) inside the caller's capacity
+  int64_t load_reach = 0;               // largest byte a tile's loads reach
+                                        // past the tile origin, + 1
   int32_t bulk = 0;
   int32_t bulk_stages = 3;
   uint32_t n_seg = 0, seg_bytes = 0;

@@ -337,6 +337,12 @@ __device__ __forceinline__ void cp_async16(uint32_t smem_addr, const void* g,
       "l"(g), "r"(src_bytes)
       : "memory");
 }
+__device__ __forceinline__ void cp_async16_full(uint32_t smem_addr,
+                                                const void* g) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_addr),
+               "l"(g)
+               : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;\n" ::: "memory");
 }
@@ -408,6 +414,14 @@ struct LoadSlots {
   __device__ __forceinline__ void issue(const StagedArgs& a, const char* src_p,
                                         int64_t src_cap, int64_t base,
                                         uint32_t sm_stage) const {
+    if (a.s_swz.b == 0 && base + a.load_reach <= src_cap) {
+      // common case: no source swizzle, the whole tile inside the buffer
+      const char* p = src_p + base;
+#pragma unroll
+      for (int k = 0; k < L; ++k)
+        if (src[k] >= 0) cp_async16_full(sm_stage + sm[k], p + src[k]);
+      return;
+    }
 #pragma unroll
     for (int k = 0; k < L; ++k) {
       if (src[k] < 0) continue;
@@ -509,9 +523,10 @@ struct GatherStore {
                              __byte_perm(b2, b3, 0x0040), 0x5410);
         }
       }
-      const int64_t off = swz_apply(a.d_swz, dbase + dst[k]);
+      const int64_t off =
+          a.d_swz.b ? swz_apply(a.d_swz, dbase + dst[k]) : dbase + dst[k];
       st_stream(reinterpret_cast<uint4*>(dst_p + off),
-             make_uint4(w[0], w[1], w[2], w[3]));
+                make_uint4(w[0], w[1], w[2], w[3]));
     }
   }
 };
@@ -550,7 +565,7 @@ struct XposeStore {
   static constexpr int kLoadSlots = R >= 8 ? 8 : 4;
   static constexpr int MaxM = R >= 8 ? 1 : 2;
   int32_t dst[MaxM];
-  uint32_t lin[MaxM];  // unswizzled smem byte offset of row 0, chunk ac
+  uint32_t sm[MaxM][R];  // swizzled smem address of each row's chunk
 
   __device__ __forceinline__ void init(const StagedArgs& a, uint32_t tid,
                                        uint32_t nt) {
@@ -558,7 +573,8 @@ struct XposeStore {
     for (int k = 0; k < MaxM; ++k) {
       const uint32_t j = tid + uint32_t(k) * nt;
       dst[k] = -1;
-      lin[k] = 0;
+#pragma unroll
+      for (int r = 0; r < R; ++r) sm[k][r] = 0;
       if (j < a.n_micro) {
         uint32_t ac, bc;
         if (a.x_acfast) {
@@ -569,7 +585,10 @@ struct XposeStore {
           bc = j - ac * a.n_bc;
         }
         dst[k] = int32_t(int64_t(ac) * a.x_da + int64_t(bc) * a.x_db);
-        lin[k] = bc * uint32_t(R) * a.x_pitch + ac * 16u;
+        const uint32_t lin = bc * uint32_t(R) * a.x_pitch + ac * 16u;
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+          sm[k][r] = swz_apply32(a.m_swz, lin + uint32_t(r) * a.x_pitch);
       }
     }
   }
@@ -577,27 +596,39 @@ struct XposeStore {
   __device__ __forceinline__ void store(const StagedArgs& a,
                                         const unsigned char* smst, char* dst_p,
                                         int64_t dbase) const {
+    const int32_t vstep = int32_t(a.x_vstep);
 #pragma unroll
     for (int k = 0; k < MaxM; ++k) {
       if (dst[k] < 0) continue;
       uint32_t in[R][4];
 #pragma unroll
       for (int r = 0; r < R; ++r) {
-        const uint4 v = lds128(
-            smst + swz_apply32(a.m_swz, lin[k] + uint32_t(r) * a.x_pitch));
+        const uint4 v = lds128(smst + sm[k][r]);
         in[r][0] = v.x;
         in[r][1] = v.y;
         in[r][2] = v.z;
         in[r][3] = v.w;
       }
-      const int64_t base = dbase + dst[k];
+      if (a.d_swz.b == 0) {
+        char* p = dst_p + (dbase + dst[k]);
 #pragma unroll
-      for (int j = 0; j < R; ++j) {
-        const int64_t off = swz_apply(a.d_swz, base + j * a.x_vstep);
-        st_stream(reinterpret_cast<uint4*>(dst_p + off),
-               make_uint4(xword<EB, R>(in, 4 * j), xword<EB, R>(in, 4 * j + 1),
-                          xword<EB, R>(in, 4 * j + 2),
-                          xword<EB, R>(in, 4 * j + 3)));
+        for (int j = 0; j < R; ++j)
+          st_stream(reinterpret_cast<uint4*>(p + j * vstep),
+                    make_uint4(xword<EB, R>(in, 4 * j),
+                               xword<EB, R>(in, 4 * j + 1),
+                               xword<EB, R>(in, 4 * j + 2),
+                               xword<EB, R>(in, 4 * j + 3)));
+      } else {
+        const int64_t base = dbase + dst[k];
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+          const int64_t off = swz_apply(a.d_swz, base + j * vstep);
+          st_stream(reinterpret_cast<uint4*>(dst_p + off),
+                    make_uint4(xword<EB, R>(in, 4 * j),
+                               xword<EB, R>(in, 4 * j + 1),
+                               xword<EB, R>(in, 4 * j + 2),
+                               xword<EB, R>(in, 4 * j + 3)));
+        }
       }
     }
   }

@@ -369,6 +369,13 @@ static int64_t tile_target(int64_t total_bytes) {
   return t;
 }
 
+static int64_t load_reach(const StagedArgs& A, int64_t seg_bytes) {
+  int64_t r = seg_bytes;
+  for (int k = 0; k < A.nso; ++k)
+    r = add_chk(r, mul_chk(int64_t(A.so_ext[k]) - 1, A.so_s[k]));
+  return r;
+}
+
 // STAGED with the transpose store.  The tile is T_a x T_b over the src-fast
 // mode a (unit source stride) and the dst-fast mode b (unit destination
 // stride); the shared-memory image holds one row of T_a elements per b.
@@ -519,10 +526,12 @@ static StagedChoice plan_transpose(const std::vector<JMode>& ms,
   A.x_da = mul_chk(V * ma.d, eb);
   A.x_db = R * eb;
   A.x_vstep = R == V ? mul_chk(ma.d, eb) : 16;
+  if (A.x_vstep * R >= (int64_t(1) << 31)) return ch;  // kept in 32 bits
   A.stage_bytes = uint32_t(best.bytes);
   A.m_swz = best.z;
   A.threads = int32_t(threads);
   A.stages = staged_stages();
+  A.load_reach = load_reach(A, seg_bytes);
   if (bulk) {
     A.bulk = 1;
     A.bulk_stages = bulk_stages();
@@ -539,6 +548,7 @@ static StagedChoice plan_transpose(const std::vector<JMode>& ms,
   return ch;
 }
 
+// Bytes past a tile's origin that its loads reach (one past the last byte).
 // Try to plan `ms` (a box of the joint domain) on the STAGED path.  Fills
 // pc on success.  May instead request a split of a mode whose extent has no
 // good tile divisor.
@@ -840,6 +850,7 @@ static StagedChoice plan_staged(const std::vector<JMode>& ms, int64_t s_base,
   A.store_mode = 0;
   A.threads = kThreads;
   A.stages = staged_stages();
+  A.load_reach = load_reach(A, seg_bytes);
   if (bulk) {
     A.bulk = 1;
     A.bulk_stages = bulk_stages();
