@@ -201,6 +201,19 @@ void lm_layout_destroy(lm_layout* layout);
 int lm_plan_copy(const lm_layout* src, const lm_layout* dst, int elem_bytes,
                  lm_plan** out);
 
+/* Shard `rank` (0 <= rank < world) of the same copy, for running one copy on
+ * several devices or streams: every logical index is independent, so the
+ * shards need no exchange.  A pair with a common refinement is split along
+ * its joint mode with the largest destination stride into `world` balanced
+ * contiguous ranges (each shard writes one region of the destination; the
+ * mode is the largest-stride one with at least `world` coordinates); other
+ * pairs split the logical index range.  The shards of ranks 0..world-1
+ * partition the copy exactly; each is an ordinary plan over the full
+ * layouts (same buffers, same capacities).  world == 1 is lm_plan_copy.
+ * Errors: as lm_plan_copy, and LM_E_INVALID for a bad rank or world. */
+int lm_plan_copy_shard(const lm_layout* src, const lm_layout* dst,
+                       int elem_bytes, int rank, int world, lm_plan** out);
+
 /* One-line JSON description: pieces, path, modes, vector width, tile. */
 int lm_plan_describe(const lm_plan* plan, char* buf, size_t cap);
 

@@ -60,6 +60,8 @@ SIGNATURES = [
     ("lm_layout_stripmined", C.c_int, [_I64, _I64, _I64, _I64, C.POINTER(_P)]),
     ("lm_layout_destroy", None, [_P]),
     ("lm_plan_copy", C.c_int, [_P, _P, C.c_int, C.POINTER(_P)]),
+    ("lm_plan_copy_shard", C.c_int,
+     [_P, _P, C.c_int, C.c_int, C.c_int, C.POINTER(_P)]),
     ("lm_plan_describe", C.c_int, [_P, C.c_char_p, C.c_size_t]),
     ("lm_plan_extent", C.c_int, [_P, _I64P, _I64P, _I64P]),
     ("lm_layout_copy", C.c_int, [_P, _P, _I64, _P, _I64, _P]),
@@ -277,10 +279,18 @@ class Plan:
 
     __slots__ = ("_h", "elem_bytes")
 
-    def __init__(self, src: Layout, dst: Layout, elem_bytes: int):
+    def __init__(self, src: Layout, dst: Layout, elem_bytes: int,
+                 rank: int = 0, world: int = 1):
+        """The copy plan, or with world > 1 the plan of shard `rank`."""
         out = C.c_void_p()
-        _check(lib().lm_plan_copy(src.handle, dst.handle, int(elem_bytes),
-                                  C.byref(out)), "lm_plan_copy")
+        if world == 1:
+            _check(lib().lm_plan_copy(src.handle, dst.handle, int(elem_bytes),
+                                      C.byref(out)), "lm_plan_copy")
+        else:
+            _check(lib().lm_plan_copy_shard(src.handle, dst.handle,
+                                            int(elem_bytes), int(rank),
+                                            int(world), C.byref(out)),
+                   "lm_plan_copy_shard")
         self._h = out
         self.elem_bytes = int(elem_bytes)
 

@@ -145,6 +145,7 @@ constexpr int kMaxTile = 6;     // modes of a staged tile per role
 
 struct GenericArgs {
   uint64_t n = 0;            // elements in the piece
+  uint64_t i0 = 0;           // logical index of the piece's first element
   int32_t ns = 0, nd = 0;    // leaves per side
   int32_t eb = 1;            // element bytes moved per element (1..16)
   int32_t wide = 0;          // 1 if n >= 2^32 (64-bit index arithmetic)

@@ -159,12 +159,13 @@ __global__ void __launch_bounds__(256)
   for (uint64_t i = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < a.n;
        i += stride) {
     int64_t so, dof;
+    const uint64_t ig = i + a.i0;
     if (a.wide) {
-      so = side_offset64(i, a.ns, a.s_ext64, a.s_str);
-      dof = side_offset64(i, a.nd, a.d_ext64, a.d_str);
+      so = side_offset64(ig, a.ns, a.s_ext64, a.s_str);
+      dof = side_offset64(ig, a.nd, a.d_ext64, a.d_str);
     } else {
-      so = side_offset32(uint32_t(i), a.ns, a.s_ext, a.s_div, a.s_str);
-      dof = side_offset32(uint32_t(i), a.nd, a.d_ext, a.d_div, a.d_str);
+      so = side_offset32(uint32_t(ig), a.ns, a.s_ext, a.s_div, a.s_str);
+      dof = side_offset32(uint32_t(ig), a.nd, a.d_ext, a.d_div, a.d_str);
     }
     so = swz_apply(a.s_swz, a.s_base + so);
     dof = swz_apply(a.d_swz, a.d_base + dof);
@@ -1012,7 +1013,8 @@ int launch_generic(const GenericArgs& g0, const char* src, char* dst,
     shift(g.s_ext, g.s_div, g.s_str, g.s_ext64, g.ns);
     shift(g.d_ext, g.d_div, g.d_str, g.d_ext64, g.nd);
     g.n *= uint64_t(g.eb);
-    if (g.n >= (uint64_t(1) << 31)) g.wide = 1;
+    g.i0 *= uint64_t(g.eb);
+    if (g.n + g.i0 >= (uint64_t(1) << 31)) g.wide = 1;
     g.eb = 1;
   }
   switch (g.eb) {

@@ -1055,6 +1055,9 @@ static std::string describe(const lm_plan& P) {
          << pc.modes[k].d << ']';
     }
     os << "],\"s_base\":" << pc.s_base << ",\"d_base\":" << pc.d_base;
+    if (!P.joint)
+      os << ",\"index_begin\":" << pc.gen.i0 << ",\"index_count\":"
+         << pc.gen.n;
     if (pc.path == PATH_VEC)
       os << ",\"vec_bytes\":" << pc.vec_bytes << ",\"tiled\":"
          << (pc.vec.tiled ? "true" : "false") << ",\"tile_vecs\":"
@@ -1086,11 +1089,20 @@ using lm::fail;
 
 extern "C" {
 
-int lm_plan_copy(const lm_layout* src, const lm_layout* dst, int elem_bytes,
-                 lm_plan** out) {
+}  // extern "C"
+
+namespace lm {
+
+// Plan shard `rank` of `world` of the copy (world == 1: the whole copy).
+// Joint plans split the joint mode with the largest destination stride
+// among those with at least `world` coordinates into `world` balanced
+// ranges; other pairs split the logical index range.
+static int plan_copy_impl(const lm_layout* src, const lm_layout* dst,
+                          int elem_bytes, int rank, int world, lm_plan** out) {
   if (out) *out = nullptr;
   try {
-    if (!src || !dst || !out) fail(LM_E_INVALID);
+    if (!src || !dst || !out || world < 1 || rank < 0 || rank >= world)
+      fail(LM_E_INVALID);
     if (elem_bytes != 1 && elem_bytes != 2 && elem_bytes != 4 &&
         elem_bytes != 8 && elem_bytes != 16)
       fail(LM_E_INVALID);
@@ -1103,34 +1115,74 @@ int lm_plan_copy(const lm_layout* src, const lm_layout* dst, int elem_bytes,
     P->s_swz = src->swz;
     P->d_swz = dst->swz;
     // byte offsets must fit int64
-    lm::mul_chk(std::max(P->src_cosize, P->dst_cosize), elem_bytes);
+    mul_chk(std::max(P->src_cosize, P->dst_cosize), elem_bytes);
     if (P->size > 0) {
-      if (!lm::affine_injective(dst->leaves)) fail(LM_E_NOT_INJECTIVE);
-      std::vector<lm::JMode> jm;
-      if (lm::refine(src->leaves, dst->leaves, jm)) {
+      if (!affine_injective(dst->leaves)) fail(LM_E_NOT_INJECTIVE);
+      std::vector<JMode> jm;
+      if (refine(src->leaves, dst->leaves, jm)) {
         P->joint = true;
-        lm::plan_box(*P, jm, 0, 0, 0);
+        jm = coalesce_joint(jm);
+        int64_t s_base = 0, d_base = 0;
+        if (world > 1 && !jm.empty()) {
+          // the largest-stride mode that has at least `world` coordinates,
+          // else the longest mode
+          size_t k = jm.size();
+          for (size_t j = 0; j < jm.size(); ++j)
+            if (jm[j].e >= world && (k == jm.size() || jm[j].d > jm[k].d))
+              k = j;
+          if (k == jm.size()) {
+            k = 0;
+            for (size_t j = 1; j < jm.size(); ++j)
+              if (jm[j].e > jm[k].e) k = j;
+          }
+          const int64_t e = jm[k].e;
+          const int64_t lo = e * rank / world, hi = e * (rank + 1) / world;
+          s_base = mul_chk(lo, jm[k].s);
+          d_base = mul_chk(lo, jm[k].d);
+          jm[k].e = hi - lo;
+        }
+        plan_box(*P, jm, s_base, d_base, 0);
       } else {
         P->joint = false;
-        lm::Piece pc;
-        pc.path = lm::PATH_GENERIC;
-        std::vector<lm::Leaf> sl = lm::coalesce_leaves(src->leaves);
-        std::vector<lm::Leaf> dl = lm::coalesce_leaves(dst->leaves);
-        pc.gen = lm::make_generic(sl, dl, P->size, 0, 0, P->s_swz, P->d_swz,
-                                  elem_bytes);
-        P->pieces.push_back(std::move(pc));
+        const int64_t lo = P->size * rank / world;
+        const int64_t hi = P->size * (rank + 1) / world;
+        if (hi > lo) {
+          Piece pc;
+          pc.path = PATH_GENERIC;
+          std::vector<Leaf> sl = coalesce_leaves(src->leaves);
+          std::vector<Leaf> dl = coalesce_leaves(dst->leaves);
+          pc.gen = make_generic(sl, dl, hi - lo, 0, 0, P->s_swz, P->d_swz,
+                                elem_bytes);
+          pc.gen.i0 = uint64_t(lo);
+          if (uint64_t(hi) >= (uint64_t(1) << 31)) pc.gen.wide = 1;
+          P->pieces.push_back(std::move(pc));
+        }
       }
     }
-    P->describe = lm::describe(*P);
+    P->describe = describe(*P);
     *out = P.release();
     return LM_OK;
-  } catch (const lm::Error& e) {
+  } catch (const Error& e) {
     return e.status;
   } catch (const std::bad_alloc&) {
     return LM_E_NOMEM;
   } catch (...) {
     return LM_E_INVALID;
   }
+}
+
+}  // namespace lm
+
+extern "C" {
+
+int lm_plan_copy(const lm_layout* src, const lm_layout* dst, int elem_bytes,
+                 lm_plan** out) {
+  return lm::plan_copy_impl(src, dst, elem_bytes, 0, 1, out);
+}
+
+int lm_plan_copy_shard(const lm_layout* src, const lm_layout* dst,
+                       int elem_bytes, int rank, int world, lm_plan** out) {
+  return lm::plan_copy_impl(src, dst, elem_bytes, rank, world, out);
 }
 
 int lm_plan_describe(const lm_plan* plan, char* buf, size_t cap) {

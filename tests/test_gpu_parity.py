@@ -345,3 +345,25 @@ def test_bounded_wait_gives_up_and_reports():
     # the context is still usable
     run_case(("layout", (96, 80), (1, 96)), ("layout", (96, 80), (80, 1)), 4)
     assert lm.device_status() == 0
+
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_shards_compose_the_full_copy(world):
+    """All shards of a copy, run one after another on the same buffers, give
+    the oracle's full result (the shards of a multi-device run, on one)."""
+    for name in ("C2", "C4", "C5b"):
+        w = WORKLOADS[name]
+        S, D = lm.build_layout(w.src), lm.build_layout(w.dst)
+        OS, OD = lo.build(w.src), lo.build(w.dst)
+        eb = w.elem_bytes
+        n_src = -(-(S.cosize * eb) // 16) * 16 // eb
+        inp = seeded_bytes(w.values, w.dtype, n_src, w.seed)
+        want = np.full(D.cosize * eb, FILL, dtype=np.uint8)
+        lo.copy(OS, OD, inp, want, eb)
+        src = torch.from_numpy(inp).cuda()
+        dst = torch.full((D.cosize * eb,), FILL, dtype=torch.uint8,
+                         device="cuda")
+        for r in range(world):
+            lm.layout_copy(lm.Plan(S, D, eb, rank=r, world=world), src, dst)
+        torch.cuda.synchronize()
+        assert np.array_equal(dst.cpu().numpy(), want), name
