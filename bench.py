@@ -254,8 +254,15 @@ def run_native(args) -> dict | None:
     for it in suite.items:
         ms = statistics.median(per[it["name"]])
         gbs = it["bytes"] / (ms * 1e-3) / 1e9
+        pieces = it["plan"].describe()["pieces"]
         per_cfg[it["name"]] = {
-            "path": "+".join(p["path"] for p in it["plan"].describe()["pieces"]),
+            "path": "+".join(p["path"] for p in pieces),
+            "kernel": kernel_name(it["plan"], it["w"].elem_bytes),
+            # shared-memory wavefronts per tile predicted by the planner's
+            # bank-conflict simulation, against the conflict-free minimum
+            "smem_wavefronts_per_tile": [
+                [p.get("bank_wavefronts"), p.get("bank_wavefronts_ideal")]
+                for p in pieces if p["path"] == "STAGED"],
             "bytes": it["bytes"], "median_us": round(ms * 1e3, 2),
             "gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4)}
     dom_name = DOMINANT if DOMINANT in per else suite.items[0]["name"]
