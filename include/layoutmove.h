@@ -170,6 +170,30 @@ int lm_layout_right_inverse(const lm_layout* layout, lm_layout** r);
 int lm_layout_max_common_vector(const lm_layout* a, const lm_layout* b,
                                 int64_t* k);
 
+/* complement(L, cotarget): the layout R, strides increasing, with (L, R)
+ * one-to-one and reaching every offset below cotarget when L's strides nest.
+ * Walking L's leaves by increasing stride d (extent e), the gap between the
+ * offsets reached so far (c, starting at 1) and d becomes a leaf d/c : c,
+ * then c = e*d; a last leaf ceil(cotarget/c) : c runs R up to cotarget.
+ * The operation the products of "CUTE布局代数" §4.1 rest on.
+ * Errors: LM_E_INVALID (cotarget < 1), LM_E_NOT_REPRESENTABLE (swizzled L,
+ * a stride that does not nest: d not a multiple of c, or d < c). */
+int lm_layout_complement(const lm_layout* layout, int64_t cotarget,
+                         lm_layout** r);
+
+/* logical_product(A, B) = (A, complement(A, size(A)*cosize(B)) o B): B
+ * repeats A, its coordinates stepping over whole copies of A
+ * ("CUTE布局代数" §4.1).  blocked_product(A, B): the same modes zipped, mode
+ * k = (A's mode k, the product's mode k), so a rank-r tile A laid out in the
+ * order of a rank-r grid B; the page's 4x8 tile over a 2x5 grid gives shape
+ * ((4,2),(8,5)).  Errors: LM_E_INVALID (blocked: ranks differ),
+ * LM_E_NOT_REPRESENTABLE (swizzled operands, complement or composition not
+ * representable). */
+int lm_layout_logical_product(const lm_layout* a, const lm_layout* b,
+                              lm_layout** r);
+int lm_layout_blocked_product(const lm_layout* a, const lm_layout* b,
+                              lm_layout** r);
+
 /* The stripmined thread map of the PitchLinearStripminedThreadMap article
  * (hotelren.com, §2.2) as a layout over thread ids:
  * (pitch, strips, ceil(threads/(pitch*strips))):(1, k_row,

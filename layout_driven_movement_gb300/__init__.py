@@ -57,6 +57,9 @@ SIGNATURES = [
     ("lm_layout_coalesce", C.c_int, [_P, C.POINTER(_P)]),
     ("lm_layout_right_inverse", C.c_int, [_P, C.POINTER(_P)]),
     ("lm_layout_max_common_vector", C.c_int, [_P, _P, _I64P]),
+    ("lm_layout_complement", C.c_int, [_P, _I64, C.POINTER(_P)]),
+    ("lm_layout_logical_product", C.c_int, [_P, _P, C.POINTER(_P)]),
+    ("lm_layout_blocked_product", C.c_int, [_P, _P, C.POINTER(_P)]),
     ("lm_layout_stripmined", C.c_int, [_I64, _I64, _I64, _I64, C.POINTER(_P)]),
     ("lm_layout_destroy", None, [_P]),
     ("lm_plan_copy", C.c_int, [_P, _P, C.c_int, C.POINTER(_P)]),
@@ -259,6 +262,20 @@ class Layout:
         _check(lib().lm_layout_coalesce(self._h, C.byref(out)),
                "lm_layout_coalesce")
         return Layout(out.value)
+
+    def complement(self, cotarget: int) -> "Layout":
+        out = C.c_void_p()
+        _check(lib().lm_layout_complement(self._h, int(cotarget),
+                                          C.byref(out)), "lm_layout_complement")
+        return Layout(out.value)
+
+    def logical_product(self, other: "Layout") -> "Layout":
+        return self._binary(lib().lm_layout_logical_product, other,
+                            "lm_layout_logical_product")
+
+    def blocked_product(self, other: "Layout") -> "Layout":
+        return self._binary(lib().lm_layout_blocked_product, other,
+                            "lm_layout_blocked_product")
 
     def right_inverse(self) -> "Layout":
         out = C.c_void_p()

@@ -598,6 +598,75 @@ static int64_t max_common_vector(const lm_layout& A, const lm_layout& B) {
   return k;
 }
 
+// ---------------------------------------------------------------------------
+// complement and products ("CUTE布局代数" §4.1)
+// ---------------------------------------------------------------------------
+
+// complement(A, M): the stride-sorted layout R such that (A, R) is one-to-one
+// and reaches every offset below M when A's strides nest: walking A's leaves
+// by increasing stride, each gap between the offsets A already reaches
+// (current) and the next leaf's stride becomes a leaf of R, and a last leaf
+// runs R up to M.
+static std::vector<Leaf> complement_leaves(const lm_layout& A, int64_t M) {
+  if (A.swz.on()) fail(LM_E_NOT_REPRESENTABLE);
+  std::vector<Leaf> ls;
+  for (const Leaf& l : A.leaves) {
+    if (l.e == 0) fail(LM_E_NOT_REPRESENTABLE);
+    if (l.e > 1 && l.d > 0) ls.push_back(l);
+  }
+  std::sort(ls.begin(), ls.end(), [](const Leaf& x, const Leaf& y) {
+    return x.d < y.d || (x.d == y.d && x.e < y.e);
+  });
+  std::vector<Leaf> out;
+  int64_t cur = 1;
+  for (const Leaf& l : ls) {
+    if (l.d < cur || l.d % cur) fail(LM_E_NOT_REPRESENTABLE);
+    if (l.d / cur > 1) out.push_back({l.d / cur, cur});
+    cur = mul_chk(l.e, l.d);
+  }
+  const int64_t rest = (M + cur - 1) / cur;
+  if (rest > 1) out.push_back({rest, cur});
+  std::vector<Leaf> co = coalesce_leaves(out);
+  if (co.empty()) co.push_back({1, 0});
+  return co;
+}
+
+static lm_layout complement(const lm_layout& A, int64_t M) {
+  lm_layout R;
+  R.root = leaves_node(complement_leaves(A, M));
+  finalize(R);
+  return R;
+}
+
+// logical_product(A, B) = (A, complement(A, size(A) * cosize(B)) o B)
+static lm_layout logical_product(const lm_layout& A, const lm_layout& B) {
+  if (A.swz.on() || B.swz.on()) fail(LM_E_NOT_REPRESENTABLE);
+  const lm_layout C = complement(A, mul_chk(A.size, B.cosize));
+  const lm_layout P = compose(C, B);
+  lm_layout R;
+  R.root = Node::make_tuple({A.root, P.root});
+  finalize(R);
+  return R;
+}
+
+// blocked_product(A, B): the modes of logical_product zipped, mode k being
+// (A's mode k, the product's mode k): tiles A laid out in the order of B.
+static lm_layout blocked_product(const lm_layout& A, const lm_layout& B) {
+  if (A.swz.on() || B.swz.on()) fail(LM_E_NOT_REPRESENTABLE);
+  const std::vector<Node> am = top_modes(A), bm = top_modes(B);
+  if (am.size() != bm.size()) fail(LM_E_INVALID);
+  const lm_layout C = complement(A, mul_chk(A.size, B.cosize));
+  const lm_layout P = compose(C, B);
+  const std::vector<Node> pm = top_modes(P);
+  std::vector<Node> kids;
+  for (size_t k = 0; k < am.size(); ++k)
+    kids.push_back(Node::make_tuple({am[k], pm[k]}));
+  lm_layout R;
+  R.root = Node::make_tuple(std::move(kids));
+  finalize(R);
+  return R;
+}
+
 static lm_layout stripmined(int64_t threads, int64_t pitch, int64_t strips,
                             int64_t k_row) {
   if (threads < 1 || pitch < 1 || strips < 1 || k_row < 1) fail(LM_E_INVALID);
@@ -840,6 +909,33 @@ int lm_layout_max_common_vector(const lm_layout* a, const lm_layout* b,
   return guard([&] {
     if (!a || !b || !k) fail(LM_E_INVALID);
     *k = lm::max_common_vector(*a, *b);
+  });
+}
+
+int lm_layout_complement(const lm_layout* layout, int64_t cotarget,
+                         lm_layout** r) {
+  if (r) *r = nullptr;
+  return guard([&] {
+    if (!layout || !r || cotarget < 1) fail(LM_E_INVALID);
+    *r = publish(lm::complement(*layout, cotarget));
+  });
+}
+
+int lm_layout_logical_product(const lm_layout* a, const lm_layout* b,
+                              lm_layout** r) {
+  if (r) *r = nullptr;
+  return guard([&] {
+    if (!a || !b || !r) fail(LM_E_INVALID);
+    *r = publish(lm::logical_product(*a, *b));
+  });
+}
+
+int lm_layout_blocked_product(const lm_layout* a, const lm_layout* b,
+                              lm_layout** r) {
+  if (r) *r = nullptr;
+  return guard([&] {
+    if (!a || !b || !r) fail(LM_E_INVALID);
+    *r = publish(lm::blocked_product(*a, *b));
   });
 }
 

@@ -53,7 +53,8 @@ __all__ = [
     "swizzle", "eval_leaf_coord", "eval_2d", "cosize", "is_injective",
     "inverse_map", "right_inverse_values", "max_common_vector",
     "pitch_linear_offset", "stripmined_offset", "copy", "copy_loop",
-    "parse", "build", "image",
+    "parse", "build", "image", "complement", "LogicalProduct",
+    "BlockedProduct",
 ]
 
 
@@ -348,6 +349,91 @@ def max_common_vector(a, b) -> int:
     while k < n and inv_a[k] >= 0 and inv_a[k] == inv_b[k]:
         k += 1
     return k
+
+
+# ---------------------------------------------------------------------------
+# complement and products ("CUTE布局代数" §4.1)
+# ---------------------------------------------------------------------------
+
+def complement(layout: Layout, cotarget: int) -> Layout:
+    """The layout that fills in what ``layout`` leaves out, up to cotarget.
+
+    The pages name the products of §4.1 without defining them; the
+    complement they rest on is taken as: walk the leaves by increasing
+    stride; whenever the next stride d exceeds the span c reached so far,
+    the gap contributes a leaf (d // c):c; the span becomes extent * d; a
+    last leaf ceil(cotarget / c):c reaches cotarget.  Leaves of extent 1 or
+    stride 0 add nothing.  A stride that is not a multiple of the span
+    reached so far has no such complement (ValueError)."""
+    leaves = sorted(((e, d) for e, d in layout.leaves if e > 1 and d > 0),
+                    key=lambda ed: (ed[1], ed[0]))
+    shape, stride = [], []
+    span = 1
+    for e, d in leaves:
+        if d < span or d % span:
+            raise ValueError("strides do not nest: no complement")
+        if d // span > 1:
+            shape.append(d // span)
+            stride.append(span)
+        span = e * d
+    rest = -(-cotarget // span)
+    if rest > 1:
+        shape.append(rest)
+        stride.append(span)
+    if not shape:
+        return Layout(1, 0)
+    return Layout(tuple(shape), tuple(stride))
+
+
+class LogicalProduct:
+    """logical_product(A, B): the layout (A, complement(A, size(A) *
+    cosize(B)) o B) -- A repeated at the positions B lists, each step of B
+    skipping one whole copy of A."""
+
+    def __init__(self, a: Layout, b: Layout):
+        self.a = a
+        self.rest = Composed(complement(a, a.size * cosize(b)), b)
+        self.size = a.size * b.size
+
+    def at(self, i, extended: bool = False) -> np.ndarray:
+        x = _as_index(i)
+        return self.a.at(x % self.a.size) + self.rest.at(x // self.a.size)
+
+    __call__ = at
+
+
+class BlockedProduct:
+    """blocked_product(A, B) for layouts of equal rank r: mode k of the
+    result is (mode k of A, mode k of complement(A, size(A)*cosize(B)) o B),
+    so the tile A is laid out at every grid position of B.  The page's
+    example, a 4x8 tile over a 2x5 grid, makes a layout of shape
+    ((4,2),(8,5))."""
+
+    def __init__(self, a: Layout, b: Layout):
+        self.a_modes = a.modes()
+        self.b_modes = b.modes()
+        if len(self.a_modes) != len(self.b_modes):
+            raise ValueError("blocked_product needs operands of equal rank")
+        self.a = a
+        self.c = complement(a, a.size * cosize(b))
+        self.b = b
+        self.size = a.size * b.size
+
+    def at(self, i, extended: bool = False) -> np.ndarray:
+        x = _as_index(i)
+        a_idx = np.zeros_like(x)
+        b_idx = np.zeros_like(x)
+        a_w = b_w = 1
+        for am, bm in zip(self.a_modes, self.b_modes):
+            xk = x % (am.size * bm.size)        # this mode's coordinate
+            x = x // (am.size * bm.size)
+            a_idx = a_idx + (xk % am.size) * a_w   # A's part, colex in A
+            b_idx = b_idx + (xk // am.size) * b_w  # B's part, colex in B
+            a_w *= am.size
+            b_w *= bm.size
+        return self.a.at(a_idx) + self.c.at(self.b.at(b_idx), extended=True)
+
+    __call__ = at
 
 
 # ---------------------------------------------------------------------------

@@ -331,6 +331,49 @@ def test_max_common_vector_large_uses_structure():
     assert c.max_common_vector(d) == 64
 
 
+def test_complement_and_products_match_oracle():
+    assert str(lm.Layout.parse("(2,2):(1,6)").complement(24)) == "(3,2):(2,12)"
+    assert str(lm.Layout.parse("4:1").complement(24)) == "6:4"
+    tile = lm.Layout.parse("(4,8):(1,4)")
+    grid = lm.Layout.parse("(2,5):(1,2)")
+    bp = tile.blocked_product(grid)
+    assert str(bp) == "((4,2),(8,5)):((1,32),(4,64))"
+    rng = np.random.default_rng(109)
+    ok = 0
+    for _ in range(200):
+        n = int(rng.integers(1, 3))
+        ext = [int(v) for v in rng.integers(1, 4, n)]
+        stride, span = [], 1
+        for e in ext:
+            span *= int(rng.integers(1, 3))
+            stride.append(span)
+            span *= e
+        A_spec = (tuple(ext), tuple(stride))
+        B_spec = (tuple(int(v) for v in rng.integers(1, 4, n)),
+                  tuple(int(v) for v in rng.integers(0, 3, n)))
+        A, B = lm.Layout.of(*A_spec), lm.Layout.of(*B_spec)
+        OA, OB = lo.Layout(*A_spec), lo.Layout(*B_spec)
+        M = span * int(rng.integers(1, 3))
+        C = A.complement(M)
+        OC = lo.complement(OA, M)
+        assert [C(k) for k in range(C.size)] == lo.image(OC).tolist()
+        for fn, ofn in (("logical_product", lo.LogicalProduct),
+                        ("blocked_product", lo.BlockedProduct)):
+            try:
+                R = getattr(A, fn)(B)
+            except lm.LayoutMoveError as e:
+                assert e.status == -3
+                continue
+            ok += 1
+            O = ofn(OA, OB)
+            assert R.size == O.size
+            assert [R(k) for k in range(R.size)] == \
+                O.at(np.arange(O.size)).tolist(), (A_spec, B_spec, fn, str(R))
+    assert ok > 100
+    with pytest.raises(lm.LayoutMoveError):
+        lm.Layout.parse("(2,3):(1,3)").complement(12)
+
+
 def test_stripmined_layout_matches_oracle():
     for threads, pitch, strips, k_row in itertools.product(
             (32, 64, 100), (1, 4, 8), (1, 2, 4), (16, 33)):

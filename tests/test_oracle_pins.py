@@ -521,6 +521,85 @@ def test_workload_closed_forms_small_samples():
 
 
 # --------------------------------------------------------------------------
+# complement and products ("CUTE布局代数" §4.1)
+# --------------------------------------------------------------------------
+
+def pin_complement_worked_examples():
+    """Worked by hand from the definition (gap leaves in stride order, then
+    a leaf up to the cotarget)."""
+    cases = [((4, 1, 24), (6, 4)),              # 4:1 -> the other 6 copies
+             ((6, 4, 24), (4, 1)),              # 6:4 -> the 4 inside
+             ((4, 2, 16), ((2, 2), (1, 8)))]     # gap of 1 below 2, then 8
+    for (e, d, m), (shape, stride) in cases:
+        C = lo.complement(lo.Layout(e, d), m)
+        want = lo.Layout(shape, stride)
+        assert C.size == want.size
+        assert (C.at(np.arange(C.size)) == want.at(np.arange(C.size))).all()
+    C = lo.complement(lo.Layout((2, 2), (1, 6)), 24)
+    assert (C.at(np.arange(6)) == lo.Layout((3, 2), (2, 12)).at(np.arange(6))).all()
+    full = lo.complement(lo.Layout((4, 6), (1, 4)), 24)
+    assert full.size == 1
+
+
+def test_complement_worked_examples():
+    pin_complement_worked_examples()
+
+
+def test_complement_invariants():
+    """(A, complement(A, M)) never repeats an offset, and covers [0, M)
+    exactly when M is a multiple of A's span."""
+    rng = np.random.default_rng(21)
+    for _ in range(100):
+        n = int(rng.integers(1, 4))
+        ext = [int(v) for v in rng.integers(1, 5, n)]
+        stride, span = [], 1
+        for e in ext:                        # nested strides with gaps
+            span *= int(rng.integers(1, 3))
+            stride.append(span)
+            span *= e
+        A = lo.Layout(tuple(ext), tuple(stride))
+        M = span * int(rng.integers(1, 4))
+        C = lo.complement(A, M)
+        both = lo.Concat(A, C)
+        img = lo.image(both)
+        assert np.unique(img).size == img.size
+        assert sorted(img.tolist()) == list(range(M))
+    with pytest.raises(ValueError):
+        lo.complement(lo.Layout((2, 3), (1, 3)), 12)     # 3 is not 2-nested
+
+
+def pin_blocked_product_page_example():
+    """A 4x8 tile (column-major) over a 2x5 grid: the page's shape
+    ((4,2),(8,5)).  Worked by hand: the complement of the 32-element tile is
+    10:32, so grid coordinate (g0, g1) starts at 32*(g0 + 2*g1):
+    ((4,2),(8,5)):((1,32),(4,64))."""
+    T = lo.Layout((4, 8), (1, 4))
+    G = lo.Layout((2, 5), (1, 2))
+    P = lo.BlockedProduct(T, G)
+    closed = lo.Layout(((4, 2), (8, 5)), ((1, 32), (4, 64)))
+    i = np.arange(P.size)
+    assert P.size == 320
+    assert (P.at(i) == closed.at(i)).all()
+
+
+def test_blocked_product_page_example():
+    pin_blocked_product_page_example()
+
+
+def test_logical_product_fills_the_gaps():
+    """(2,2):(1,4) reaches {0,1,4,5}; its product with 2:1 repeats it at +2,
+    giving ((2,2),2):((1,4),2), a bijection onto [0,8)."""
+    P = lo.LogicalProduct(lo.Layout((2, 2), (1, 4)), lo.Layout(2, 1))
+    closed = lo.Layout(((2, 2), 2), ((1, 4), 2))
+    i = np.arange(8)
+    assert (P.at(i) == closed.at(i)).all()
+    assert sorted(P.at(i).tolist()) == list(range(8))
+    # a contiguous tile repeated contiguously: (4):(1) x (3):(1) = (4,3):(1,4)
+    Q = lo.LogicalProduct(lo.Layout(4, 1), lo.Layout(3, 1))
+    assert (Q.at(np.arange(12)) == np.arange(12)).all()
+
+
+# --------------------------------------------------------------------------
 # the pins catch plausible mistakes planted in the oracle
 # --------------------------------------------------------------------------
 
@@ -553,6 +632,14 @@ def _transposed_swizzle(offset, b, m, s):
     return o ^ ((o << s) & (((1 << b) - 1) << (m + s)))
 
 
+def _complement_no_gap_leaf(layout, cotarget):
+    # forgets the gap leaves: only the final leaf up to the cotarget
+    span = 1
+    for e, d in layout.leaves:
+        span = max(span, e * d)
+    return lo.Layout(-(-cotarget // span), span)
+
+
 def _strips_times_pitch(thread_id, k_row, pitch, strips):
     t = np.asarray(thread_id, dtype=np.int64)
     div, mod = t // pitch, t % pitch
@@ -564,7 +651,8 @@ PINS = [pin_rowmajor_grid, pin_colmajor_grid, pin_blocked_leaf_coordinates,
         pin_stripmined_page_values, pin_stripmined_is_colex_layout,
         pin_column_major_composition_is_identity,
         pin_padded_composition_closed_form, pin_zipped_divide_closed_form,
-        pin_swizzle_page_formula, pin_copy_transpose]
+        pin_swizzle_page_formula, pin_copy_transpose,
+        pin_complement_worked_examples, pin_blocked_product_page_example]
 
 
 @pytest.mark.parametrize("target,bad", [
@@ -573,6 +661,7 @@ PINS = [pin_rowmajor_grid, pin_colmajor_grid, pin_blocked_leaf_coordinates,
     ("swizzle", _wrong_shift_swizzle),
     ("swizzle", _transposed_swizzle),
     ("stripmined_offset", _strips_times_pitch),
+    ("complement", _complement_no_gap_leaf),
 ])
 def test_pins_catch_planted_mistakes(monkeypatch, target, bad):
     monkeypatch.setattr(lo, target, bad)
