@@ -258,11 +258,15 @@ def run_native(args) -> dict | None:
         per_cfg[it["name"]] = {
             "path": "+".join(p["path"] for p in pieces),
             "kernel": kernel_name(it["plan"], it["w"].elem_bytes),
-            # shared-memory wavefronts per tile predicted by the planner's
-            # bank-conflict simulation, against the conflict-free minimum
-            "smem_wavefronts_per_tile": [
-                [p.get("bank_wavefronts"), p.get("bank_wavefronts_ideal")]
-                for p in pieces if p["path"] == "STAGED"],
+            # shared-memory wavefronts per launch predicted by the planner's
+            # bank-conflict simulation ([predicted, conflict-free minimum]):
+            # the store side's shared loads, and the 16-byte tile writes
+            # (cp.async, or the bulk copy engine when "bulk" is set)
+            "smem_read_wavefronts": staged_sum(
+                pieces, "bank_read_wavefronts", "bank_read_wavefronts_ideal"),
+            "smem_write_wavefronts": staged_sum(
+                pieces, "bank_wavefronts", "bank_wavefronts_ideal",
+                minus=("bank_read_wavefronts", "bank_read_wavefronts_ideal")),
             "bytes": it["bytes"], "median_us": round(ms * 1e3, 2),
             "gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4)}
     dom_name = DOMINANT if DOMINANT in per else suite.items[0]["name"]
@@ -310,6 +314,20 @@ def run_native(args) -> dict | None:
         "gpu_launches": suite.launches_per_step * args.steps,
     }
     return line
+
+
+def staged_sum(pieces, key, ideal_key, minus=None):
+    """A per-tile planner figure summed over the STAGED pieces' tiles."""
+    got = [0, 0]
+    for p in pieces:
+        if p["path"] != "STAGED":
+            continue
+        a, b = p[key], p[ideal_key]
+        if minus:
+            a, b = a - p[minus[0]], b - p[minus[1]]
+        got[0] += a * p["n_tiles"]
+        got[1] += b * p["n_tiles"]
+    return got if any(p["path"] == "STAGED" for p in pieces) else None
 
 
 def kernel_name(plan, eb: int) -> str:

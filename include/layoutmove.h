@@ -202,6 +202,24 @@ int lm_layout_blocked_product(const lm_layout* a, const lm_layout* b,
 int lm_layout_stripmined(int64_t threads, int64_t pitch, int64_t strips,
                          int64_t k_row, lm_layout** r);
 
+/* Shared-memory bank wavefronts of a warp-by-warp access pattern: the
+ * check "CUTLASS Layout可视化" §5.2 and §6.4 ask of a tile layout (do one
+ * warp's offsets, taken mod 32 banks, spread out?), counted.  Access i,
+ * colex over the domain of `access`, is made by lane i % 32 of warp access
+ * i / 32 and reads access_bytes at byte address access(i) * elem_bytes.
+ * Model: 32 banks of 4 bytes; 16-byte accesses are served 8 lanes at a
+ * time, 8-byte ones 16 at a time, narrower ones a whole warp at a time;
+ * within such a group the cost is the largest number of distinct 4-byte
+ * words that one bank holds (lanes reading one word share it).  *wavefronts
+ * = the sum over all groups; *ideal = the conflict-free minimum, a group's
+ * bytes over 128 (at least 1).  The copy planner chooses its shared tile's
+ * pad and swizzle with the same model.
+ * Errors: LM_E_INVALID (null pointers, elem_bytes or access_bytes not a
+ * power of two in 1..16, size(access) > 2^24, an address not a multiple of
+ * access_bytes or negative), LM_E_OVERFLOW. */
+int lm_smem_wavefronts(const lm_layout* access, int elem_bytes,
+                       int access_bytes, int64_t* wavefronts, int64_t* ideal);
+
 void lm_layout_destroy(lm_layout* layout);
 
 /* ---------------------------------------------------------------------------

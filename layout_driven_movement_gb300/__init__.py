@@ -61,6 +61,7 @@ SIGNATURES = [
     ("lm_layout_logical_product", C.c_int, [_P, _P, C.POINTER(_P)]),
     ("lm_layout_blocked_product", C.c_int, [_P, _P, C.POINTER(_P)]),
     ("lm_layout_stripmined", C.c_int, [_I64, _I64, _I64, _I64, C.POINTER(_P)]),
+    ("lm_smem_wavefronts", C.c_int, [_P, C.c_int, C.c_int, _I64P, _I64P]),
     ("lm_layout_destroy", None, [_P]),
     ("lm_plan_copy", C.c_int, [_P, _P, C.c_int, C.POINTER(_P)]),
     ("lm_plan_copy_shard", C.c_int,
@@ -230,6 +231,16 @@ class Layout:
         _check(lib().lm_layout_eval_coord(self._h, len(coord), _i64s(coord),
                                           C.byref(v)), "lm_layout_eval_coord")
         return v.value
+
+    def smem_wavefronts(self, elem_bytes: int,
+                        access_bytes: int | None = None) -> tuple[int, int]:
+        """(wavefronts, conflict-free minimum) of warps reading shared
+        memory at this layout's offsets, 32 consecutive indices a warp."""
+        w, i = C.c_int64(), C.c_int64()
+        ab = elem_bytes if access_bytes is None else access_bytes
+        _check(lib().lm_smem_wavefronts(self._h, elem_bytes, ab, C.byref(w),
+                                        C.byref(i)), "lm_smem_wavefronts")
+        return w.value, i.value
 
     # -- algebra --------------------------------------------------------
     def _binary(self, fn, other, what) -> "Layout":

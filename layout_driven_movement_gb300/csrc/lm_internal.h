@@ -276,6 +276,7 @@ struct Piece {
   VecArgs vec;
   StagedArgs st;
   int64_t bank_cost = 0, bank_ideal = 0;  // STAGED: simulated smem wavefronts
+  int64_t bank_read = 0, bank_read_ideal = 0;  // of which the store side's reads
 };
 
 }  // namespace lm

@@ -265,7 +265,18 @@ struct SmemLayout {
   int64_t pad = 0;
   Swz z;
   int64_t bytes = 0, cost = -1, ideal = 0;
+  int64_t read_cost = 0, read_ideal = 0;  // the store side's reads alone
 };
+
+// LM_SMEM_SEARCH=0 keeps the plain image (no pad, no swizzle): a tuning and
+// validation knob that shows the conflicts the search removes.
+bool smem_search_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("LM_SMEM_SEARCH");
+    return !(v && v[0] == '0');
+  }();
+  return on;
+}
 
 template <class ReadAddr>
 SmemLayout search_smem(int threads, int64_t n_seg, int64_t seg_bytes,
@@ -276,11 +287,13 @@ SmemLayout search_smem(int threads, int64_t n_seg, int64_t seg_bytes,
   const int64_t n_l = n_seg * cps;
   const int64_t lpt = (n_l + threads - 1) / threads;
   const int64_t spt = (n_reads + threads - 1) / threads;
+  const bool search = smem_search_enabled();
   const std::vector<int64_t> pads =
-      n_seg > 1 ? std::vector<int64_t>{0, 16, 32, 48, 64, 80, 96, 112}
-                : std::vector<int64_t>{0};
+      n_seg > 1 && search
+          ? std::vector<int64_t>{0, 16, 32, 48, 64, 80, 96, 112}
+          : std::vector<int64_t>{0};
   std::vector<Swz> zs{Swz{}};
-  if (allow_swizzle)
+  if (allow_swizzle && search)
     for (int bb = 1; bb <= 3; ++bb)
       for (int ss = bb; ss <= 10; ++ss) zs.push_back(Swz{bb, 4, ss});
   std::vector<int64_t> addr(32);
@@ -292,7 +305,7 @@ SmemLayout search_smem(int threads, int64_t n_seg, int64_t seg_bytes,
       const int64_t blk = int64_t(16) << z.b;
       const int64_t bytes = ((lin_max + blk - 1) / blk) * blk;
       if (bytes > 24576) continue;
-      int64_t cost = 0, id = 0;
+      int64_t cost = 0, id = 0, rcost = 0, rid = 0;
       for (int w = 0; w < threads / 32; ++w) {
         for (int64_t k = 0; k < lpt; ++k) {
           int cnt = 0;
@@ -315,10 +328,12 @@ SmemLayout search_smem(int threads, int64_t n_seg, int64_t seg_bytes,
               cnt += valid[l];
               addr[size_t(l)] = valid[l] ? z.apply(read_addr(j, e, pitch)) : 0;
             }
-            cost += wavefronts(addr.data(), valid, 32, width);
-            id += cnt ? (cnt * width + 127) / 128 : 0;
+            rcost += wavefronts(addr.data(), valid, 32, width);
+            rid += cnt ? (cnt * width + 127) / 128 : 0;
           }
       }
+      cost += rcost;
+      id += rid;
       if (best.cost < 0 || cost < best.cost ||
           (cost == best.cost && bytes < best.bytes)) {
         best.pad = pad;
@@ -326,6 +341,8 @@ SmemLayout search_smem(int threads, int64_t n_seg, int64_t seg_bytes,
         best.cost = cost;
         best.bytes = bytes;
         best.ideal = id;
+        best.read_cost = rcost;
+        best.read_ideal = rid;
       }
     }
   }
@@ -544,6 +561,8 @@ static StagedChoice plan_transpose(const std::vector<JMode>& ms,
   pc.tile_elems = Ta * Tb;
   pc.bank_cost = best.cost;
   pc.bank_ideal = best.ideal;
+  pc.bank_read = best.read_cost;
+  pc.bank_read_ideal = best.read_ideal;
   ch.ok = true;
   return ch;
 }
@@ -862,6 +881,8 @@ static StagedChoice plan_staged(const std::vector<JMode>& ms, int64_t s_base,
   pc.tile_elems = tile_elems();
   pc.bank_cost = best.cost;
   pc.bank_ideal = best.ideal;
+  pc.bank_read = best.read_cost;
+  pc.bank_read_ideal = best.read_ideal;
   ch.ok = true;
   return ch;
 }
@@ -1075,7 +1096,9 @@ static std::string describe(const lm_plan& P) {
          << ",\"stage_bytes\":" << A.stage_bytes << ",\"smem_swizzle\":["
          << A.m_swz.b << ',' << A.m_swz.m << ',' << A.m_swz.s << ']'
          << ",\"bank_wavefronts\":" << pc.bank_cost
-         << ",\"bank_wavefronts_ideal\":" << pc.bank_ideal;
+         << ",\"bank_wavefronts_ideal\":" << pc.bank_ideal
+         << ",\"bank_read_wavefronts\":" << pc.bank_read
+         << ",\"bank_read_wavefronts_ideal\":" << pc.bank_read_ideal;
     }
     os << '}';
   }
@@ -1088,6 +1111,55 @@ static std::string describe(const lm_plan& P) {
 using lm::fail;
 
 extern "C" {
+
+// Shared-memory wavefronts of the accesses `access` describes: access i
+// (colex over its domain) is lane i % 32 of warp access i / 32 and reads
+// access_bytes at byte address access(i) * elem_bytes.  Same bank model as
+// the planner's layout search (32 banks of 4 bytes; 16-byte accesses served
+// 8 lanes at a time, 8-byte ones 16 at a time; one word read by several
+// lanes is a broadcast).
+int lm_smem_wavefronts(const lm_layout* access, int elem_bytes,
+                       int access_bytes, int64_t* wavefronts, int64_t* ideal) {
+  auto pow2_le16 = [](int v) { return v >= 1 && v <= 16 && !(v & (v - 1)); };
+  if (!access || !wavefronts || !ideal || !pow2_le16(elem_bytes) ||
+      !pow2_le16(access_bytes))
+    return LM_E_INVALID;
+  if (access->size > (int64_t(1) << 24)) return LM_E_INVALID;
+  try {
+    int64_t total = 0, best = 0;
+    std::vector<int64_t> addr(32);
+    bool valid[32];
+    for (int64_t w0 = 0; w0 < access->size; w0 += 32) {
+      int cnt = 0;
+      for (int l = 0; l < 32; ++l) {
+        const int64_t i = w0 + l;
+        valid[l] = i < access->size;
+        addr[size_t(l)] = 0;
+        if (!valid[l]) continue;
+        ++cnt;
+        const int64_t off = access->swz.apply(
+            lm::eval_affine(access->leaves, i));
+        const int64_t a = lm::mul_chk(off, elem_bytes);
+        if (a < 0 || a % access_bytes) return LM_E_INVALID;
+        addr[size_t(l)] = a;
+      }
+      total += lm::wavefronts(addr.data(), valid, 32, access_bytes);
+      // per phase: its lanes' bytes over 128, at least one
+      const int per_phase = access_bytes <= 4 ? 32 : 128 / access_bytes;
+      for (int p0 = 0; p0 < cnt; p0 += per_phase) {
+        const int n = std::min(cnt - p0, per_phase);
+        best += std::max<int64_t>(1, (int64_t(n) * access_bytes + 127) / 128);
+      }
+    }
+    *wavefronts = total;
+    *ideal = best;
+    return LM_OK;
+  } catch (const lm::Error& e) {
+    return e.status;
+  } catch (const std::bad_alloc&) {
+    return LM_E_NOMEM;
+  }
+}
 
 }  // extern "C"
 

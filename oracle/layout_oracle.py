@@ -33,7 +33,10 @@ fusion, no reordering):
   element bytes ("CUTE布局代数" §5.1, make_copy(gmem_layout, smem_layout));
 * the thread maps are the pitch-linear map and the stripmined get_offset map
   of the PitchLinearStripminedThreadMap article (hotelren.com/news/5252042,
-  §1.2 and §2.2).
+  §1.2 and §2.2);
+* a warp's shared-memory access costs one pass per distinct word that its
+  busiest bank must serve, 32 banks of 4 bytes ("CUTLASS Layout可视化"
+  §5.2).
 
 Every function here is pinned by ``tests/test_oracle_pins.py`` against
 values printed on the pages, closed forms, textbook special cases and
@@ -458,6 +461,35 @@ def stripmined_offset(thread_id, k_row: int, pitch: int, strips: int):
     strip = above % strips
     group = above // strips
     return in_pitch + strip * k_row + group * (pitch * strips * k_row)
+
+
+# ---------------------------------------------------------------------------
+# shared-memory banks ("CUTLASS Layout可视化" §5.2, §6.4)
+# ---------------------------------------------------------------------------
+
+def smem_wavefronts(byte_addr, access_bytes: int) -> tuple[int, int]:
+    """§5.2: shared memory is 32 banks of 4 bytes; lanes of one warp that
+    touch different 4-byte words of the same bank are served one after the
+    other, lanes that read the same word share it.  Accesses of 8 or 16
+    bytes per lane are served 16 or 8 lanes at a time (128 bytes).  Access
+    i belongs to warp i // 32.  Returns (wavefronts, conflict-free minimum)
+    summed over every group of lanes served together."""
+    addr = [int(a) for a in np.asarray(byte_addr, dtype=np.int64).ravel()]
+    per_group = 32 if access_bytes <= 4 else 128 // access_bytes
+    words_per_lane = max(1, access_bytes // 4)
+    total = ideal = 0
+    for w0 in range(0, len(addr), 32):
+        warp = addr[w0:w0 + 32]
+        for g0 in range(0, len(warp), per_group):
+            group = warp[g0:g0 + per_group]
+            words_in_bank = {}
+            for a in group:
+                for k in range(words_per_lane):
+                    word = a // 4 + k
+                    words_in_bank.setdefault(word % 32, set()).add(word)
+            total += max(len(v) for v in words_in_bank.values())
+            ideal += max(1, -(-len(group) * access_bytes // 128))
+    return total, ideal
 
 
 # ---------------------------------------------------------------------------

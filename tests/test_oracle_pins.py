@@ -600,6 +600,51 @@ def test_logical_product_fills_the_gaps():
 
 
 # --------------------------------------------------------------------------
+# shared-memory banks ("CUTLASS Layout可视化" §4.3, §5.2)
+# --------------------------------------------------------------------------
+
+def _column_read(rows, row_pitch, eb=4, swz=None):
+    """Byte addresses of lanes 0..rows-1 reading column 0 of a row-major
+    tile with `row_pitch` elements per row."""
+    off = np.arange(rows, dtype=np.int64) * row_pitch
+    if swz:
+        off = lo.swizzle(off, *swz)
+    return off * eb
+
+
+def pin_bank_closed_forms():
+    """Closed forms of the 32-bank model:
+    * 32 lanes on consecutive fp32 words: one bank each, 1 wavefront;
+    * all lanes on one word: a broadcast, 1;
+    * a column of a 32-wide fp32 tile: every row in the column's bank, 32
+      (the page's serialisation to 1/32);
+    * a column of an 8-wide fp32 tile, 32 rows: banks c, c+8, c+16, c+24,
+      eight rows each, so 8;
+    * the same tile padded to 9 per row (the page's N -> N+1): 9 is odd, so
+      the 32 rows land in 32 banks, 1;
+    * 16-byte vectors on 32 consecutive chunks: 512 bytes, 4 passes of 128;
+    * 8-byte lanes at a stride of 16 bytes: each half warp spans 256 bytes,
+      so 2 passes per half, 4 in all (ideal 2);
+    * Swizzle<3,0,3> on the 8-wide tile: rows r and r+4 share the bank
+      group 8*(r mod 4) and differ in column bits, so 32 rows fall in 8
+      banks, 4 deep; 8 rows of an 8x8 tile reach 8 banks, 1."""
+    assert lo.smem_wavefronts(np.arange(32) * 4, 4) == (1, 1)
+    assert lo.smem_wavefronts(np.zeros(32, np.int64), 4) == (1, 1)
+    assert lo.smem_wavefronts(_column_read(32, 32), 4) == (32, 1)
+    assert lo.smem_wavefronts(_column_read(32, 8), 4) == (8, 1)
+    assert lo.smem_wavefronts(_column_read(32, 9), 4) == (1, 1)
+    assert lo.smem_wavefronts(np.arange(32) * 16, 16) == (4, 4)
+    assert lo.smem_wavefronts(np.arange(32) * 16, 8) == (4, 2)
+    assert lo.smem_wavefronts(_column_read(32, 8, swz=(3, 0, 3)), 4) == (4, 1)
+    assert lo.smem_wavefronts(_column_read(8, 8, swz=(3, 0, 3)), 4) == (1, 1)
+    assert lo.smem_wavefronts(_column_read(8, 8), 4) == (2, 1)
+
+
+def test_bank_closed_forms():
+    pin_bank_closed_forms()
+
+
+# --------------------------------------------------------------------------
 # the pins catch plausible mistakes planted in the oracle
 # --------------------------------------------------------------------------
 
@@ -640,6 +685,37 @@ def _complement_no_gap_leaf(layout, cotarget):
     return lo.Layout(-(-cotarget // span), span)
 
 
+def _sixteen_banks(byte_addr, access_bytes):
+    # banks taken mod 16 instead of mod 32
+    addr = [int(a) for a in np.asarray(byte_addr, dtype=np.int64).ravel()]
+    per = 32 if access_bytes <= 4 else 128 // access_bytes
+    total = ideal = 0
+    for w0 in range(0, len(addr), 32):
+        warp = addr[w0:w0 + 32]
+        for g0 in range(0, len(warp), per):
+            banks = {}
+            for a in warp[g0:g0 + per]:
+                for k in range(max(1, access_bytes // 4)):
+                    banks.setdefault((a // 4 + k) % 16, set()).add(a // 4 + k)
+            total += max(len(v) for v in banks.values())
+            ideal += max(1, -(-len(warp[g0:g0 + per]) * access_bytes // 128))
+    return total, ideal
+
+
+def _no_broadcast(byte_addr, access_bytes):
+    # counts every lane, not every distinct word
+    addr = [int(a) for a in np.asarray(byte_addr, dtype=np.int64).ravel()]
+    total = ideal = 0
+    for w0 in range(0, len(addr), 32):
+        banks = {}
+        for a in addr[w0:w0 + 32]:
+            banks[(a // 4) % 32] = banks.get((a // 4) % 32, 0) + 1
+        total += max(banks.values())
+        ideal += 1
+    return total, ideal
+
+
+
 def _strips_times_pitch(thread_id, k_row, pitch, strips):
     t = np.asarray(thread_id, dtype=np.int64)
     div, mod = t // pitch, t % pitch
@@ -652,7 +728,8 @@ PINS = [pin_rowmajor_grid, pin_colmajor_grid, pin_blocked_leaf_coordinates,
         pin_column_major_composition_is_identity,
         pin_padded_composition_closed_form, pin_zipped_divide_closed_form,
         pin_swizzle_page_formula, pin_copy_transpose,
-        pin_complement_worked_examples, pin_blocked_product_page_example]
+        pin_complement_worked_examples, pin_blocked_product_page_example,
+        pin_bank_closed_forms]
 
 
 @pytest.mark.parametrize("target,bad", [
@@ -662,6 +739,8 @@ PINS = [pin_rowmajor_grid, pin_colmajor_grid, pin_blocked_leaf_coordinates,
     ("swizzle", _transposed_swizzle),
     ("stripmined_offset", _strips_times_pitch),
     ("complement", _complement_no_gap_leaf),
+    ("smem_wavefronts", _sixteen_banks),
+    ("smem_wavefronts", _no_broadcast),
 ])
 def test_pins_catch_planted_mistakes(monkeypatch, target, bad):
     monkeypatch.setattr(lo, target, bad)
