@@ -34,6 +34,9 @@ fusion, no reordering):
 * the thread maps are the pitch-linear map and the stripmined get_offset map
   of the PitchLinearStripminedThreadMap article (hotelren.com/news/5252042,
   §1.2 and §2.2);
+* a thread's part of a tile under local_partition is one element of every
+  thread-layout-shaped block, at the thread's coordinate in the block
+  ("CUTLASS Layout可视化" §5.3);
 * a warp's shared-memory access costs one pass per distinct word that its
   busiest bank must serve, 32 banks of 4 bytes ("CUTLASS Layout可视化"
   §5.2).
@@ -461,6 +464,58 @@ def stripmined_offset(thread_id, k_row: int, pitch: int, strips: int):
     strip = above % strips
     group = above // strips
     return in_pitch + strip * k_row + group * (pitch * strips * k_row)
+
+
+# ---------------------------------------------------------------------------
+# thread partitions ("CUTLASS Layout可视化" §5.3)
+# ---------------------------------------------------------------------------
+
+def thread_coordinate(thr: Layout, thr_idx: int) -> list[int]:
+    """The per-mode coordinate (a 1-D index into each top mode of thr) that
+    the thread layout maps to thread number thr_idx, found by trying every
+    coordinate.  thr must reach thr_idx exactly once."""
+    hits = np.nonzero(thr.at(np.arange(thr.size)) == thr_idx)[0]
+    if len(hits) != 1:
+        raise ValueError("the thread layout must reach the thread once")
+    i = int(hits[0])
+    coord = []
+    for m in thr.modes():
+        coord.append(i % m.size)
+        i //= m.size
+    return coord
+
+
+def local_partition(layout, thr: Layout, thr_idx: int) -> np.ndarray:
+    """§5.3's local_partition(tile, thread_layout, thread_idx): the
+    elements of `layout` that thread thr_idx owns.  With T_k the size of the
+    thread layout's mode k (1 past its rank) and c the thread's coordinate,
+    the thread owns, in every mode k, the coordinates x_k = c_k + T_k * r_k:
+    one element of every T_0 x T_1 x ... block, at the thread's place in the
+    block.  Returns their offsets, r taken colex (r_0 fastest); a swizzled
+    layout's swizzle applies to each whole offset."""
+    base = layout.inner if isinstance(layout, Swizzled) else layout
+    modes = base.modes()
+    tm = thr.modes()
+    if len(tm) > len(modes):
+        raise ValueError("thread layout of higher rank than the tile")
+    c = thread_coordinate(thr, thr_idx) + [0] * (len(modes) - len(tm))
+    t = [m.size for m in tm] + [1] * (len(modes) - len(tm))
+    for m, tk in zip(modes, t):
+        if m.size % tk:
+            raise ValueError("thread layout extents must divide the tile")
+    rest = [m.size // tk for m, tk in zip(modes, t)]
+    out = []
+    for r_flat in range(prod(rest)):
+        off = 0
+        for m, ck, tk, nk in zip(modes, c, t, rest):
+            rk = r_flat % nk
+            r_flat //= nk
+            off += int(m.at(ck + tk * rk))
+        out.append(off)
+    off = np.array(out, dtype=np.int64)
+    if isinstance(layout, Swizzled):
+        off = swizzle(off, layout.b, layout.m, layout.s)
+    return off
 
 
 # ---------------------------------------------------------------------------

@@ -645,6 +645,61 @@ def test_bank_closed_forms():
 
 
 # --------------------------------------------------------------------------
+# local_partition ("CUTLASS Layout可视化" §5.3)
+# --------------------------------------------------------------------------
+
+def pin_local_partition_closed_form():
+    """8x8 row-major tile (8,8):(8,1) over a column-major 4x2 thread
+    layout (4,2):(1,4).  Thread 5 sits at row 1, column 1 of the thread
+    layout, so it owns rows 1, 5 and columns 1, 3, 5, 7: offsets 8*row+col
+    with the row index fastest.  Thread 2 (row 2, column 0) owns rows 2, 6
+    and columns 0, 2, 4, 6."""
+    tile = lo.Layout((8, 8), (8, 1))
+    thr = lo.Layout((4, 2), (1, 4))
+    assert lo.local_partition(tile, thr, 5).tolist() == [
+        9, 41, 11, 43, 13, 45, 15, 47]
+    assert lo.local_partition(tile, thr, 2).tolist() == [
+        16, 48, 18, 50, 20, 52, 22, 54]
+    # a row-major thread layout (2,4):(4,1): thread 5 is row 1, column 1
+    thr_r = lo.Layout((2, 4), (4, 1))
+    assert lo.local_partition(tile, thr_r, 5).tolist() == [
+        9, 25, 41, 57, 13, 29, 45, 61]
+
+
+def test_local_partition_closed_form():
+    pin_local_partition_closed_form()
+
+
+def test_local_partition_tiles_the_layout():
+    """The parts of all threads partition the tile's offsets; one thread
+    owns the whole tile; a thread layout as large as the tile gives each
+    thread the single element at its coordinate; the swizzle rides along."""
+    cases = [
+        (lo.Layout((16, 12), (12, 1)), lo.Layout((4, 3), (3, 1))),
+        (lo.Layout(((2, 4), 6), ((1, 12), 2)), lo.Layout((8, 2), (1, 8))),
+        (lo.Layout((32, 8), (8, 1)), lo.Layout(32, 1)),
+        (lo.Layout((6, 10, 4), (40, 1, 10)), lo.Layout((3, 5), (5, 1))),
+    ]
+    for tile, thr in cases:
+        parts = [lo.local_partition(tile, thr, t) for t in range(thr.size)]
+        assert len({len(p) for p in parts}) == 1
+        got = np.sort(np.concatenate(parts))
+        want = np.sort(tile.at(np.arange(tile.size)))
+        assert (got == want).all()
+    tile = lo.Layout((8, 8), (8, 1))
+    assert (lo.local_partition(tile, lo.Layout(1, 0), 0)
+            == tile.at(np.arange(64))).all()
+    full = lo.Layout((8, 8), (1, 8))
+    for t in range(64):
+        assert lo.local_partition(tile, full, t).tolist() == [
+            8 * (t % 8) + t // 8]
+    sw = lo.Swizzled(3, 0, 3, tile)
+    thr = lo.Layout((4, 2), (1, 4))
+    assert (lo.local_partition(sw, thr, 5)
+            == lo.swizzle(lo.local_partition(tile, thr, 5), 3, 0, 3)).all()
+
+
+# --------------------------------------------------------------------------
 # the pins catch plausible mistakes planted in the oracle
 # --------------------------------------------------------------------------
 
@@ -716,6 +771,23 @@ def _no_broadcast(byte_addr, access_bytes):
 
 
 
+def _partition_blocked(layout, thr, thr_idx):
+    # gives each thread a contiguous block instead of a strided share
+    base = layout.inner if isinstance(layout, lo.Swizzled) else layout
+    modes = base.modes()
+    c = lo.thread_coordinate(thr, thr_idx) + [0] * (len(modes) - len(thr.modes()))
+    t = [m.size for m in thr.modes()] + [1] * (len(modes) - len(thr.modes()))
+    rest = [m.size // tk for m, tk in zip(modes, t)]
+    out = []
+    for r_flat in range(int(np.prod(rest))):
+        off = 0
+        for m, ck, nk in zip(modes, c, rest):
+            off += int(m.at(ck * nk + r_flat % nk))
+            r_flat //= nk
+        out.append(off)
+    return np.array(out, dtype=np.int64)
+
+
 def _strips_times_pitch(thread_id, k_row, pitch, strips):
     t = np.asarray(thread_id, dtype=np.int64)
     div, mod = t // pitch, t % pitch
@@ -729,7 +801,7 @@ PINS = [pin_rowmajor_grid, pin_colmajor_grid, pin_blocked_leaf_coordinates,
         pin_padded_composition_closed_form, pin_zipped_divide_closed_form,
         pin_swizzle_page_formula, pin_copy_transpose,
         pin_complement_worked_examples, pin_blocked_product_page_example,
-        pin_bank_closed_forms]
+        pin_bank_closed_forms, pin_local_partition_closed_form]
 
 
 @pytest.mark.parametrize("target,bad", [
@@ -741,6 +813,7 @@ PINS = [pin_rowmajor_grid, pin_colmajor_grid, pin_blocked_leaf_coordinates,
     ("complement", _complement_no_gap_leaf),
     ("smem_wavefronts", _sixteen_banks),
     ("smem_wavefronts", _no_broadcast),
+    ("local_partition", _partition_blocked),
 ])
 def test_pins_catch_planted_mistakes(monkeypatch, target, bad):
     monkeypatch.setattr(lo, target, bad)
