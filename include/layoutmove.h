@@ -194,6 +194,23 @@ int lm_layout_logical_product(const lm_layout* a, const lm_layout* b,
 int lm_layout_blocked_product(const lm_layout* a, const lm_layout* b,
                               lm_layout** r);
 
+/* local_partition(layout, thr, thr_idx): the part of a tile that thread
+ * thr_idx owns under the thread layout thr, as in the
+ * local_partition(sA, thread_layout, thread_idx) call of "CUTLASS Layout
+ * 可视化" §5.3.  thr must map its domain one-to-one onto [0, size(thr))
+ * (strides 1, e0, e0*e1, ... in some order) and have rank <= rank(layout);
+ * with T_k the size of thr's mode k (1 past its rank) and c the coordinate
+ * thr maps to thr_idx, the thread owns the mode coordinates c_k + T_k*r_k.
+ * *part is the layout of r (colex, no swizzle; the rest mode of
+ * zipped_divide(layout, T)), *base the offset at r = 0, so value v sits at
+ * Swz(*base + part(v)), Swz being layout's swizzle (none: identity).
+ * Errors: LM_E_INVALID (NULL, thr not a compact bijection or swizzled,
+ * thr_idx outside [0, size(thr)), rank(thr) > rank(layout)),
+ * LM_E_NOT_REPRESENTABLE (a T_k does not divide mode k). */
+int lm_layout_local_partition(const lm_layout* layout, const lm_layout* thr,
+                              int64_t thr_idx, lm_layout** part,
+                              int64_t* base);
+
 /* The stripmined thread map of the PitchLinearStripminedThreadMap article
  * (hotelren.com, §2.2) as a layout over thread ids:
  * (pitch, strips, ceil(threads/(pitch*strips))):(1, k_row,

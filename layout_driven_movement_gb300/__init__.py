@@ -60,6 +60,8 @@ SIGNATURES = [
     ("lm_layout_complement", C.c_int, [_P, _I64, C.POINTER(_P)]),
     ("lm_layout_logical_product", C.c_int, [_P, _P, C.POINTER(_P)]),
     ("lm_layout_blocked_product", C.c_int, [_P, _P, C.POINTER(_P)]),
+    ("lm_layout_local_partition", C.c_int,
+     [_P, _P, _I64, C.POINTER(_P), _I64P]),
     ("lm_layout_stripmined", C.c_int, [_I64, _I64, _I64, _I64, C.POINTER(_P)]),
     ("lm_smem_wavefronts", C.c_int, [_P, C.c_int, C.c_int, _I64P, _I64P]),
     ("lm_layout_destroy", None, [_P]),
@@ -231,6 +233,16 @@ class Layout:
         _check(lib().lm_layout_eval_coord(self._h, len(coord), _i64s(coord),
                                           C.byref(v)), "lm_layout_eval_coord")
         return v.value
+
+    def local_partition(self, thr: "Layout",
+                        thr_idx: int) -> tuple["Layout", int]:
+        """(part, base): thread thr_idx's values sit at
+        swizzle(base + part(v))."""
+        out, base = C.c_void_p(), C.c_int64()
+        _check(lib().lm_layout_local_partition(self._h, thr._h, int(thr_idx),
+                                               C.byref(out), C.byref(base)),
+               "lm_layout_local_partition")
+        return Layout(out.value), base.value
 
     def smem_wavefronts(self, elem_bytes: int,
                         access_bytes: int | None = None) -> tuple[int, int]:

@@ -101,6 +101,8 @@ int64_t eval_affine(const std::vector<Leaf>& leaves, int64_t idx);
 std::string to_string(const lm_layout& L);
 std::vector<Leaf> coalesce_leaves(const std::vector<Leaf>& leaves);
 bool affine_injective(std::vector<Leaf> leaves);
+bool compact_bijection(const std::vector<Leaf>& leaves);
+std::vector<int64_t> thread_coordinate(const lm_layout& thr, int64_t t);
 
 // ---------------------------------------------------------------------------
 // Fast division by an invariant 32-bit divisor: Granlund & Montgomery,

@@ -667,6 +667,78 @@ static lm_layout blocked_product(const lm_layout& A, const lm_layout& B) {
   return R;
 }
 
+// ---------------------------------------------------------------------------
+// local_partition ("CUTLASS Layout可视化" §5.3)
+// ---------------------------------------------------------------------------
+
+// True when the layout maps its domain one-to-one onto [0, size): its
+// leaves, sorted by stride, have strides 1, e0, e0*e1, ...
+bool compact_bijection(const std::vector<Leaf>& leaves) {
+  std::vector<Leaf> ls;
+  for (const Leaf& l : leaves)
+    if (l.e > 1) ls.push_back(l);
+  std::sort(ls.begin(), ls.end(),
+            [](const Leaf& a, const Leaf& b) { return a.d < b.d; });
+  int64_t next = 1;
+  for (const Leaf& l : ls) {
+    if (l.d != next) return false;
+    next = mul_chk(next, l.e);
+  }
+  return true;
+}
+
+// The per-mode coordinate (a colex index into each top mode) that the thread
+// layout maps to thread number t.
+std::vector<int64_t> thread_coordinate(const lm_layout& thr, int64_t t) {
+  if (thr.swz.on() || !compact_bijection(thr.leaves)) fail(LM_E_INVALID);
+  if (t < 0 || t >= thr.size) fail(LM_E_INVALID);
+  std::vector<int64_t> c;
+  for (const Node& m : top_modes(thr)) {
+    int64_t ck = 0, w = 1;
+    for (const Leaf& l : flatten(m)) {
+      if (l.e > 1) ck += ((t / l.d) % l.e) * w;
+      w *= l.e;
+    }
+    c.push_back(ck);
+  }
+  return c;
+}
+
+// Thread t's part: zipped_divide by the thread layout's mode sizes, the tile
+// mode fixed at the thread's coordinate.  Returns the rest mode (the
+// values, no swizzle) and the tile mode's offset at the coordinate in *base.
+static lm_layout local_partition(const lm_layout& L, const lm_layout& thr,
+                                 int64_t t, int64_t* base) {
+  const std::vector<int64_t> c = thread_coordinate(thr, t);
+  const std::vector<Node> lm_modes = top_modes(L);
+  const std::vector<Node> tm = top_modes(thr);
+  if (tm.size() > lm_modes.size()) fail(LM_E_INVALID);
+  std::vector<int64_t> tiler, cc;
+  for (size_t k = 0; k < lm_modes.size(); ++k) {
+    int64_t tk = 1;
+    if (k < tm.size())
+      for (const Leaf& l : flatten(tm[k])) tk = mul_chk(tk, l.e);
+    tiler.push_back(tk);
+    cc.push_back(k < c.size() ? c[k] : 0);
+  }
+  lm_layout A = L;
+  A.swz = Swz{};
+  finalize(A);
+  const lm_layout Z = zipped_divide(A, int(tiler.size()), tiler.data());
+  lm_layout tile, part;
+  tile.root = Z.root.kids[0];
+  part.root = Z.root.kids[1];
+  finalize(tile);
+  finalize(part);
+  int64_t idx = 0, w = 1;
+  for (size_t k = 0; k < cc.size(); ++k) {
+    idx += cc[k] * w;
+    w *= tiler[k];
+  }
+  *base = eval_affine(tile.leaves, idx);
+  return part;
+}
+
 static lm_layout stripmined(int64_t threads, int64_t pitch, int64_t strips,
                             int64_t k_row) {
   if (threads < 1 || pitch < 1 || strips < 1 || k_row < 1) fail(LM_E_INVALID);
@@ -936,6 +1008,19 @@ int lm_layout_blocked_product(const lm_layout* a, const lm_layout* b,
   return guard([&] {
     if (!a || !b || !r) fail(LM_E_INVALID);
     *r = publish(lm::blocked_product(*a, *b));
+  });
+}
+
+int lm_layout_local_partition(const lm_layout* layout, const lm_layout* thr,
+                              int64_t thr_idx, lm_layout** part,
+                              int64_t* base) {
+  if (part) *part = nullptr;
+  return guard([&] {
+    if (!layout || !thr || !part || !base) fail(LM_E_INVALID);
+    int64_t b = 0;
+    lm_layout P = lm::local_partition(*layout, *thr, thr_idx, &b);
+    *base = b;
+    *part = publish(std::move(P));
   });
 }
 

@@ -522,3 +522,43 @@ def test_copy_validation_without_gpu():
     assert L.lm_layout_eval_device(lm.Layout.parse("8:1").handle, C.c_void_p(4096), 4, 7, None) == -6
     big = lm.Layout.parse("(2,2):(1,4294967296)")
     assert L.lm_layout_eval_device(big.handle, C.c_void_p(4096), 4, 8, None) == -5
+
+
+def test_local_partition_matches_oracle():
+    """Thread parts from lm_layout_local_partition equal the oracle's, for
+    nested tiles, thread layouts of lower rank, and a swizzled tile."""
+    cases = [("(8,8):(8,1)", "(4,2):(1,4)"),
+             ("(8,8):(8,1)", "(2,4):(4,1)"),
+             ("(16,12):(12,1)", "(4,3):(3,1)"),
+             ("((2,4),6):((1,12),2)", "(8,2):(1,8)"),
+             ("(32,8):(8,1)", "32:1"),
+             ("(6,10,4):(40,1,10)", "(3,5):(5,1)"),
+             ("(64,64):(1,64)", "((8,4),(2,4)):((1,64),(8,16))")]
+    for tile_t, thr_t in cases:
+        tile, thr = lm.Layout.parse(tile_t), lm.Layout.parse(thr_t)
+        ot, othr = lo.parse(tile_t), lo.parse(thr_t)
+        for t in range(thr.size):
+            part, base = tile.local_partition(thr, t)
+            got = [base + part(v) for v in range(part.size)]
+            assert got == lo.local_partition(ot, othr, t).tolist(), (tile_t, t)
+    sw = lm.Layout.parse("(32,8):(8,1)").swizzle(3, 0, 3)
+    thr = lm.Layout.parse("(8,4):(4,1)")
+    osw = lo.Swizzled(3, 0, 3, lo.parse("(32,8):(8,1)"))
+    for t in range(32):
+        part, base = sw.local_partition(thr, t)
+        got = lo.swizzle(np.array([base + part(v) for v in range(part.size)]),
+                         3, 0, 3)
+        assert got.tolist() == lo.local_partition(osw, lo.parse("(8,4):(4,1)"),
+                                                  t).tolist()
+
+
+def test_local_partition_rejects():
+    tile = lm.Layout.parse("(8,8):(8,1)")
+    bad = [("(4,2):(1,2)", 0, -1),        # not a bijection onto [0, 8)
+           ("(4,2):(1,4)", 8, -1),        # thread out of range
+           ("(4,2,2):(1,4,8)", 0, -1),    # rank above the tile's
+           ("(3,2):(1,3)", 0, -3)]        # 3 does not divide 8
+    for thr_t, t, code in bad:
+        with pytest.raises(lm.LayoutMoveError) as e:
+            tile.local_partition(lm.Layout.parse(thr_t), t)
+        assert e.value.status == code, thr_t
