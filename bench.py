@@ -45,7 +45,26 @@ UNIT = "GB/s"
 # algorithmic bytes per copy (read + written), SURVEY 8(d)
 ALGO_BYTES = {"C2": 134_217_728, "C3": 268_435_456, "C4": 1_140_850_688,
               "C5a": 205_520_896, "C5b": 16_777_216}
-DOMINANT = "C4"          # largest share of the step: lm_staged_kernel<8>
+DOMINANT = "C4"          # largest share of the step: lm_bulk_kernel<8>
+
+# The thread-value tile copy (lm_tv_copy) on full-size workloads: shared
+# tile layout, thread layouts of the load and store phases, and the tiler
+# that zipped_divide applies to both sides first (None: the workload's
+# layouts are tiled already).  Reported beside the suite, not part of the
+# headline.
+TV_CONFIGS = {
+    # bf16 64x64 tiles, 16-byte vectors along the contiguous columns in both
+    # phases, 128-byte XOR swizzle on the shared rows
+    "C3": ("Sw<3,3,6> o (64,64):(64,1)", "(32,8):(8,1)", "(32,8):(8,1)",
+           None),
+    # fp32 64x64 transposes: 4-byte accesses in both phases, a 5-bit XOR so
+    # a warp reading a shared row or column touches 32 banks
+    "C2": ("Sw<5,0,6> o (64,64):(1,64)", "(32,8):(1,32)", "(8,32):(32,1)",
+           (64, 64)),
+    # the same with 16-byte loads; the store phase then conflicts 4 ways
+    "C2v": ("Sw<3,2,6> o (64,64):(1,64)", "(16,16):(1,16)", "(8,32):(32,1)",
+            (64, 64)),
+}
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -285,6 +304,7 @@ def run_native(args) -> dict | None:
     if rank != 0:
         return None
 
+    tv = measure_tv(suite, args, torch, peak) if not args.quick else {}
     e2e = measure_e2e(suite, args, torch) if not args.quick else None
     cpu = cpu_baseline(suite) if world == 1 and not args.quick else None
     clocks = clk.summary()
@@ -306,6 +326,7 @@ def run_native(args) -> dict | None:
             "breakdown": "per_config: a second pass of " + str(k2) +
                          " steps with CUDA events around every copy",
             "per_config": per_cfg,
+            "tv_copy": tv,
         },
         "clocks": clocks,
         "roofline": roofline,
@@ -359,6 +380,56 @@ def measured_traffic(kernel: str):
         return rec["dram_bytes_per_launch"]
     except Exception:
         return None
+
+
+def measure_tv(suite, args, torch, peak) -> dict:
+    """Time lm_tv_copy on the suite's full-size buffers (TV_CONFIGS), the
+    copies of one round back to back with events around each."""
+    lm = suite.lm
+    items = {it["name"]: it for it in suite.items}
+    runs = []
+    for key, (smem, tl, ts, tiler) in TV_CONFIGS.items():
+        it = items.get(key[:2])
+        if it is None:
+            continue
+        S, D = it["S"], it["D"]
+        if tiler:
+            S, D = S.zipped_divide(list(tiler)), D.zipped_divide(list(tiler))
+        plan = lm.TVPlan(S, lm.Layout.parse(smem), D, lm.Layout.parse(tl),
+                         lm.Layout.parse(ts), it["w"].elem_bytes)
+        runs.append((key, it, plan))
+    if not runs:
+        return {}
+    rounds = min(args.steps, 300)
+    for _ in range(3):
+        for _, it, plan in runs:
+            lm.tv_copy(plan, it["src"], it["dst"])
+    ev = [[(torch.cuda.Event(enable_timing=True),
+            torch.cuda.Event(enable_timing=True)) for _ in runs]
+          for _ in range(rounds)]
+    torch.cuda.synchronize()
+    for r in range(rounds):
+        for k, (_, it, plan) in enumerate(runs):
+            ev[r][k][0].record()
+            lm.tv_copy(plan, it["src"], it["dst"])
+            ev[r][k][1].record()
+    torch.cuda.synchronize()
+    out = {}
+    for k, (key, it, plan) in enumerate(runs):
+        ms = statistics.median(ev[r][k][0].elapsed_time(ev[r][k][1])
+                               for r in range(rounds))
+        gbs = it["bytes"] / (ms * 1e-3) / 1e9
+        d = plan.describe()
+        out[key] = {
+            "smem": TV_CONFIGS[key][0], "thr_load": TV_CONFIGS[key][1],
+            "thr_store": TV_CONFIGS[key][2],
+            "vec_bytes": [d["load"]["vec_bytes"], d["store"]["vec_bytes"]],
+            "smem_wavefronts_per_tile": [
+                [d["load"]["smem_wavefronts"], d["load"]["smem_wavefronts_ideal"]],
+                [d["store"]["smem_wavefronts"], d["store"]["smem_wavefronts_ideal"]]],
+            "median_us": round(ms * 1e3, 2), "gbs": round(gbs, 1),
+            "frac_of_peak": round(gbs / peak, 4)}
+    return out
 
 
 def measure_e2e(suite, args, torch) -> dict:

@@ -43,6 +43,7 @@ extern "C" {
 
 typedef struct lm_layout lm_layout; /* opaque, freed by lm_layout_destroy */
 typedef struct lm_plan lm_plan;     /* opaque, freed by lm_plan_destroy   */
+typedef struct lm_tv_plan lm_tv_plan; /* opaque, freed by lm_tv_plan_destroy */
 
 typedef enum lm_status {
   LM_OK = 0,
@@ -310,6 +311,57 @@ int lm_layout_eval_device(const lm_layout* layout, void* table_dev,
                           void* cuda_stream);
 
 void lm_plan_destroy(lm_plan* plan);
+
+/* ---------------------------------------------------------------------------
+ * Thread-value partitioned tile copies through shared memory
+ * ------------------------------------------------------------------------- */
+
+/* Plan a copy out[dst(i)] = in[src(i)] that stages every tile in shared
+ * memory with caller-chosen layouts: the global-to-shared copy
+ * make_copy(gmem_layout, smem_layout) of "CUTE布局代数" §5.1, each thread
+ * moving its local_partition of the tile ("CUTLASS Layout可视化" §5.3).
+ * src and dst: layouts over the same domain whose mode 0 is the tile (its
+ * own modes are the tile modes, as zipped_divide returns) and whose other
+ * top modes number the tiles; the grid modes are refined jointly.  smem:
+ * the shared tile, one mode per tile mode with the same sizes, injective,
+ * at most 232448 bytes, swizzle allowed.  thr_load / thr_store: thread
+ * layouts (compact bijections onto [0, size), at most 1024 threads, rank
+ * at most the tile's) of the load phase (src -> smem) and the store phase
+ * (smem -> dst).  A phase moves vectors of vec_*_bytes (0: the widest of
+ * 16, 8, ..., elem_bytes that works) along one tile mode: that many
+ * consecutive coordinates must be contiguous and aligned on both of its
+ * sides; the thread layout then partitions the tile with that mode counted
+ * in vectors, at most 128 vectors per thread.  lm_tv_plan_describe gives
+ * the choices and the shared-memory wavefronts the bank model of
+ * lm_smem_wavefronts predicts per tile for each phase.
+ * Errors: LM_E_INVALID (NULL, elem_bytes, limits above, empty tile),
+ * LM_E_INCOMPATIBLE (sizes or tile modes differ, grids do not refine),
+ * LM_E_NOT_INJECTIVE (smem or dst), LM_E_NOT_REPRESENTABLE (no vector
+ * width fits, a thread extent does not divide its mode, or the offsets are
+ * not base(thread) + value-offset), LM_E_OVERFLOW. */
+int lm_tv_plan_create(const lm_layout* src, const lm_layout* smem,
+                      const lm_layout* dst, const lm_layout* thr_load,
+                      const lm_layout* thr_store, int elem_bytes,
+                      int vec_load_bytes, int vec_store_bytes,
+                      lm_tv_plan** out);
+
+/* JSON description of a plan (same buffer rules as lm_plan_describe). */
+int lm_tv_plan_describe(const lm_tv_plan* plan, char* buf, size_t cap);
+
+/* Copy the plan's lm_tv_args (layoutmove_tv.h) into args, cap bytes long,
+ * for consumer kernels that call the device functions of layoutmove_tv.cuh.
+ * Errors: LM_E_INVALID, LM_E_BUFFER (cap < sizeof(lm_tv_args)). */
+int lm_tv_plan_args(const lm_tv_plan* plan, void* args, size_t cap);
+
+/* Enqueue the copy on cuda_stream: one block per tile at a time, the load
+ * phase, a barrier, the store phase.  Buffers as for lm_layout_copy; src
+ * must be aligned to the load phase's vector bytes and dst to the store
+ * phase's.  Errors: LM_E_INVALID, LM_E_CAPACITY, LM_E_OVERLAP, LM_E_CUDA. */
+int lm_tv_copy(const lm_tv_plan* plan, const void* src_dev,
+               int64_t src_capacity_elems, void* dst_dev,
+               int64_t dst_capacity_elems, void* cuda_stream);
+
+void lm_tv_plan_destroy(lm_tv_plan* plan);
 
 /* Static, NUL-terminated name of a status code. */
 const char* lm_status_string(int status);

@@ -19,6 +19,7 @@ from typing import Iterable, Sequence
 __all__ = [
     "LayoutMoveError", "Layout", "Plan", "lib", "layout_copy",
     "layout_eval_device", "build_layout", "device_status", "STATUS",
+    "TVPlan", "tv_copy",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -74,6 +75,12 @@ SIGNATURES = [
     ("lm_plan_launches", C.c_int, [_P, _IP]),
     ("lm_layout_eval_device", C.c_int, [_P, _P, C.c_int, _I64, _P]),
     ("lm_plan_destroy", None, [_P]),
+    ("lm_tv_plan_create", C.c_int,
+     [_P, _P, _P, _P, _P, C.c_int, C.c_int, C.c_int, C.POINTER(_P)]),
+    ("lm_tv_plan_describe", C.c_int, [_P, C.c_char_p, C.c_size_t]),
+    ("lm_tv_plan_args", C.c_int, [_P, _P, C.c_size_t]),
+    ("lm_tv_copy", C.c_int, [_P, _P, _I64, _P, _I64, _P]),
+    ("lm_tv_plan_destroy", None, [_P]),
     ("lm_status_string", C.c_char_p, [C.c_int]),
     ("lm_last_cuda_error", C.c_int, []),
     ("lm_device_status", C.c_int, [_P, C.c_int, _IP]),
@@ -368,6 +375,47 @@ class Plan:
         return v.value
 
 
+class TVPlan:
+    """A copy staged tile by tile through a caller-chosen shared layout,
+    each phase a local_partition by a caller-chosen thread layout."""
+
+    __slots__ = ("_h", "elem_bytes")
+
+    def __init__(self, src: Layout, smem: Layout, dst: Layout,
+                 thr_load: Layout, thr_store: Layout, elem_bytes: int,
+                 vec_load_bytes: int = 0, vec_store_bytes: int = 0):
+        out = C.c_void_p()
+        _check(lib().lm_tv_plan_create(src.handle, smem.handle, dst.handle,
+                                       thr_load.handle, thr_store.handle,
+                                       int(elem_bytes), int(vec_load_bytes),
+                                       int(vec_store_bytes), C.byref(out)),
+               "lm_tv_plan_create")
+        self._h = out
+        self.elem_bytes = int(elem_bytes)
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h and _lib is not None:
+            _lib.lm_tv_plan_destroy(h)
+            self._h = None
+
+    @property
+    def handle(self):
+        return self._h
+
+    def describe(self) -> dict:
+        buf = C.create_string_buffer(4096)
+        _check(lib().lm_tv_plan_describe(self._h, buf, 4096),
+               "lm_tv_plan_describe")
+        return json.loads(buf.value.decode())
+
+    def args_bytes(self) -> bytes:
+        """The lm_tv_args block (layoutmove_tv.h) for consumer kernels."""
+        buf = C.create_string_buffer(8192)
+        _check(lib().lm_tv_plan_args(self._h, buf, 8192), "lm_tv_plan_args")
+        return buf.raw
+
+
 def _stream_handle(stream) -> C.c_void_p:
     if stream is None:
         import torch
@@ -396,6 +444,15 @@ def layout_copy(plan: Plan, src, dst, stream=None) -> None:
     _check(lib().lm_layout_copy(plan.handle, C.c_void_p(sp), scap,
                                 C.c_void_p(dp), dcap, _stream_handle(stream)),
            "lm_layout_copy")
+
+
+def tv_copy(plan: TVPlan, src, dst, stream=None) -> None:
+    """Enqueue the tile-staged copy of ``plan`` (see TVPlan) on ``stream``."""
+    sp, scap = _dev_buffer(src, plan.elem_bytes)
+    dp, dcap = _dev_buffer(dst, plan.elem_bytes)
+    _check(lib().lm_tv_copy(plan.handle, C.c_void_p(sp), scap,
+                            C.c_void_p(dp), dcap, _stream_handle(stream)),
+           "lm_tv_copy")
 
 
 def layout_copy_ptr(plan: Plan, src_ptr: int, src_cap: int, dst_ptr: int,

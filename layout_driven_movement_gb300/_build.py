@@ -39,7 +39,7 @@ def _sources():
 def _newest_input() -> float:
     files = _sources() + [os.path.join(CSRC, f) for f in os.listdir(CSRC)
                           if f.endswith(".h")]
-    files.append(os.path.join(INCLUDE, "layoutmove.h"))
+    files += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE)]
     files.append(os.path.abspath(__file__))
     return max(os.path.getmtime(f) for f in files)
 

@@ -8,6 +8,7 @@
 #include <vector>
 
 #include "layoutmove.h"
+#include "layoutmove_tv.h"
 
 #if defined(__CUDACC__)
 #define LM_HD __host__ __device__ __forceinline__
@@ -292,7 +293,20 @@ struct lm_plan {
   std::string describe;
 };
 
+// A thread-value partitioned tile copy (lm_tv.cpp plans it, lm_tv.cu runs it).
+struct lm_tv_plan {
+  lm_tv_args args{};
+  int64_t src_cosize = 0, dst_cosize = 0;  // elements
+  std::string describe;
+};
+
 namespace lm {
+// Shared-memory wavefronts of one warp access (lm_plan.cpp): addr in bytes,
+// `bytes` per lane.
+int64_t warp_wavefronts(const int64_t* addr, const bool* valid, int bytes);
+int launch_tv(const lm_tv_plan& plan, const char* src, char* dst,
+              void* stream);  // lm_tv.cu
+
 // implemented in lm_kernels.cu
 int launch_piece(const lm_plan& plan, const Piece& pc, const char* src,
                  int64_t src_cap_bytes, char* dst, void* stream);

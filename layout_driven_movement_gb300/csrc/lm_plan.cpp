@@ -349,6 +349,14 @@ SmemLayout search_smem(int threads, int64_t n_seg, int64_t seg_bytes,
   return best;
 }
 
+}  // namespace
+
+int64_t warp_wavefronts(const int64_t* addr, const bool* valid, int bytes) {
+  return wavefronts(addr, valid, 32, bytes);
+}
+
+namespace {
+
 struct StagedChoice {
   bool ok = false;
   int split_mode = -1;     // > = 0: split the box along this mode at split_at

@@ -1,0 +1,136 @@
+// The thread-value partitioned tile copy: one block per tile at a time
+// (grid-stride over tiles), load phase into the shared tile, store phase out
+// of it, both through the device functions of layoutmove_tv.cuh -- the
+// building block this kernel exists to run and test.
+
+#include <cuda_runtime.h>
+
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "layoutmove_tv.cuh"
+#include "lm_internal.h"
+
+namespace lm {
+namespace {
+
+template <int VL, int VS>
+__global__ void __launch_bounds__(1024)
+    lm_tv_kernel(const __grid_constant__ lm_tv_args a,
+                 const char* __restrict__ src, char* __restrict__ dst) {
+  extern __shared__ __align__(16) char tile_smem[];
+  const int t = int(threadIdx.x);
+  for (int64_t tile = blockIdx.x; tile < a.n_tiles; tile += gridDim.x) {
+    int64_t sb, db;
+    lm_tv::tile_bases(a, tile, &sb, &db);
+    lm_tv::load_tile<VL>(a, src, tile_smem, sb, t);
+    lm_tv::wait_copies();
+    __syncthreads();
+    lm_tv::store_tile<VS>(a, tile_smem, dst, db, t);
+    __syncthreads();
+  }
+}
+
+typedef void (*TvKernel)(const lm_tv_args, const char*, char*);
+
+template <int VL>
+TvKernel pick_store(int vs) {
+  switch (vs) {
+    case 1: return lm_tv_kernel<VL, 1>;
+    case 2: return lm_tv_kernel<VL, 2>;
+    case 4: return lm_tv_kernel<VL, 4>;
+    case 8: return lm_tv_kernel<VL, 8>;
+    case 16: return lm_tv_kernel<VL, 16>;
+  }
+  return nullptr;
+}
+
+TvKernel pick(int vl, int vs) {
+  switch (vl) {
+    case 1: return pick_store<1>(vs);
+    case 2: return pick_store<2>(vs);
+    case 4: return pick_store<4>(vs);
+    case 8: return pick_store<8>(vs);
+    case 16: return pick_store<16>(vs);
+  }
+  return nullptr;
+}
+
+int fail_cuda(cudaError_t e) {
+  set_cuda_error(int(e));
+  return LM_E_CUDA;
+}
+
+}  // namespace
+
+int launch_tv(const lm_tv_plan& plan, const char* src, char* dst,
+              void* stream) {
+  const lm_tv_args& a = plan.args;
+  if (a.n_tiles == 0) return LM_OK;
+  TvKernel k = pick(a.load.vec_bytes, a.store.vec_bytes);
+  if (!k) return LM_E_INVALID;
+  const int smem = a.smem_bytes;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e);
+  if (smem > 49152) {
+    static std::mutex mu;
+    static std::map<std::pair<int, const void*>, int> done;
+    std::lock_guard<std::mutex> g(mu);
+    const auto key = std::make_pair(dev, reinterpret_cast<const void*>(k));
+    auto it = done.find(key);
+    if (it == done.end() || it->second < smem) {
+      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               smem);
+      if (e != cudaSuccess) return fail_cuda(e);
+      done[key] = smem;
+    }
+  }
+  int sms = 0, per_sm = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return fail_cuda(e);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k,
+                                                    a.block_threads,
+                                                    size_t(smem));
+  if (e != cudaSuccess) return fail_cuda(e);
+  if (per_sm < 1) return LM_E_INVALID;  // the block cannot be resident
+  const int64_t resident = int64_t(sms) * per_sm;
+  const unsigned grid = unsigned(a.n_tiles < resident ? a.n_tiles : resident);
+  k<<<grid, unsigned(a.block_threads), size_t(smem),
+      static_cast<cudaStream_t>(stream)>>>(a, src, dst);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return fail_cuda(e);
+  return LM_OK;
+}
+
+}  // namespace lm
+
+extern "C" int lm_tv_copy(const lm_tv_plan* plan, const void* src_dev,
+                          int64_t src_capacity_elems, void* dst_dev,
+                          int64_t dst_capacity_elems, void* cuda_stream) {
+  try {
+    if (!plan) return LM_E_INVALID;
+    const lm_tv_args& a = plan->args;
+    if (a.n_tiles == 0) return LM_OK;
+    if (!src_dev || !dst_dev) return LM_E_INVALID;
+    if (src_capacity_elems < plan->src_cosize ||
+        dst_capacity_elems < plan->dst_cosize)
+      return LM_E_CAPACITY;
+    const int64_t eb = a.elem_bytes;
+    const uintptr_t s0 = reinterpret_cast<uintptr_t>(src_dev);
+    const uintptr_t d0 = reinterpret_cast<uintptr_t>(dst_dev);
+    if (s0 % uintptr_t(a.load.vec_bytes) || d0 % uintptr_t(a.store.vec_bytes) ||
+        s0 % uintptr_t(eb) || d0 % uintptr_t(eb))
+      return LM_E_INVALID;
+    const uintptr_t s1 = s0 + uintptr_t(lm::mul_chk(plan->src_cosize, eb));
+    const uintptr_t d1 = d0 + uintptr_t(lm::mul_chk(plan->dst_cosize, eb));
+    if (s0 < d1 && d0 < s1) return LM_E_OVERLAP;
+    return lm::launch_tv(*plan, static_cast<const char*>(src_dev),
+                         static_cast<char*>(dst_dev), cuda_stream);
+  } catch (const lm::Error& e) {
+    return e.status;
+  } catch (...) {
+    return LM_E_INVALID;
+  }
+}

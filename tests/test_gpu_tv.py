@@ -1,0 +1,145 @@
+"""GPU parity of the thread-value partitioned tile copy (lm_tv_copy).
+
+Each tile goes global -> shared -> global through the device functions of
+include/layoutmove_tv.cuh, every thread moving its local_partition of the
+tile ("CUTLASS Layout可视化" §5.3).  The shared layout and the thread
+layouts only decide who moves what and where it waits, so the result must
+be the oracle's out[dst(i)] = in[src(i)], byte for byte, with untouched
+destination slots and guard bands intact.
+"""
+
+import numpy as np
+import pytest
+
+from oracle import layout_oracle as lo
+from workloads import WORKLOADS, seeded_bytes
+from tv_cases import CASES, zd
+
+torch = pytest.importorskip("torch")
+lm = pytest.importorskip("layout_driven_movement_gb300")
+
+pytestmark = pytest.mark.gpu
+
+GUARD = 256
+FILL = 0xA5
+GUARD_FILL = 0x5C
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from layout_driven_movement_gb300 import _build
+    _build.build()
+    lm.lib()
+
+
+def device_buffer(nbytes, fill):
+    raw = torch.full((nbytes + 2 * GUARD,), GUARD_FILL, dtype=torch.uint8,
+                     device="cuda")
+    view = raw[GUARD:GUARD + nbytes]
+    view.fill_(fill)
+    return raw, view
+
+
+def run_tv(src_spec, smem_spec, dst_spec, thr_l, thr_s, eb, vl=0, vs=0,
+           seed=11, expect=None):
+    S, D = lm.build_layout(src_spec), lm.build_layout(dst_spec)
+    M = lm.build_layout(smem_spec)
+    plan = lm.TVPlan(S, M, D, lm.Layout.parse(thr_l), lm.Layout.parse(thr_s),
+                     eb, vl, vs)
+    desc = plan.describe()
+    if expect:
+        for k, v in expect.items():
+            phase, key = k.split(".")
+            assert desc[phase][key] == v, (k, desc)
+    OS, OD = lo.build(src_spec), lo.build(dst_spec)
+    n_src, n_dst = S.cosize, D.cosize
+    inp = seeded_bytes("bytes", "uint8", n_src * eb, seed)
+    want = np.full(n_dst * eb, FILL, dtype=np.uint8)
+    lo.copy(OS, OD, inp, want, eb)
+    s_raw, s_view = device_buffer(n_src * eb, 0)
+    s_view.copy_(torch.from_numpy(inp))
+    d_raw, d_view = device_buffer(n_dst * eb, FILL)
+    lm.tv_copy(plan, s_view, d_view)
+    torch.cuda.synchronize()
+    got = d_view.cpu().numpy()
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, f"{bad.size} bytes differ, first {bad[:8]} {desc}"
+    g = d_raw.cpu().numpy()
+    assert (g[:GUARD] == GUARD_FILL).all()
+    assert (g[GUARD + n_dst * eb:] == GUARD_FILL).all()
+    return desc
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_tv_copy_matches_oracle(case):
+    _, src, smem, dst, tl, ts, eb, expect = case
+    run_tv(src, smem, dst, tl, ts, eb, expect=expect)
+
+
+def test_tv_forced_vector_widths():
+    src = zd((128, 96), (1, 128), (32, 32))
+    dst = zd((128, 96), (96, 1), (32, 32))
+    smem = ("layout", (32, 32), (1, 32))
+    for vl in (4, 8, 16):
+        tl = {4: "(32,8):(1,32)", 8: "(16,16):(1,16)", 16: "(8,32):(1,8)"}[vl]
+        run_tv(src, smem, dst, tl, "(32,8):(8,1)", 4, vl, 4,
+               expect={"load.vec_bytes": vl})
+
+
+def test_tv_empty_grid_is_a_no_op():
+    S = lm.Layout.parse("((32,32),0):((1,32),1024)")
+    M = lm.Layout.parse("(32,32):(1,32)")
+    thr = lm.Layout.parse("(8,32):(1,8)")
+    plan = lm.TVPlan(S, M, S, thr, thr, 4)
+    assert plan.describe()["n_tiles"] == 0
+    a = torch.zeros(16, device="cuda")
+    b = torch.full((16,), 7.0, device="cuda")
+    lm.tv_copy(plan, a, b)
+    torch.cuda.synchronize()
+    assert (b == 7.0).all()
+
+
+def test_tv_rejects_on_device_buffers():
+    src = lm.build_layout(zd((64, 64), (1, 64), (32, 32)))
+    dst = lm.build_layout(zd((64, 64), (64, 1), (32, 32)))
+    M = lm.Layout.parse("(32,32):(1,32)")
+    plan = lm.TVPlan(src, M, dst, lm.Layout.parse("(8,32):(1,8)"),
+                     lm.Layout.parse("(32,8):(8,1)"), 4)
+    a = torch.zeros(4096, device="cuda")
+    b = torch.zeros(4096, device="cuda")
+    with pytest.raises(lm.LayoutMoveError) as e:
+        lm.tv_copy(plan, a[:4000], b)
+    assert e.value.status == -6          # capacity
+    with pytest.raises(lm.LayoutMoveError) as e:
+        lm.tv_copy(plan, a, a)
+    assert e.value.status == -7          # overlap
+    big = torch.zeros(4100, device="cuda")
+    with pytest.raises(lm.LayoutMoveError) as e:
+        lm.tv_copy(plan, big[1:4097], b)  # 16-byte vectors need alignment
+    assert e.value.status == -1
+
+
+def test_tv_full_size_tiles_swizzled_bf16():
+    """The 8192x8192 bf16 swizzled tiling through the building block, with
+    the shapes bench.py times; compared in full with the oracle."""
+    w = WORKLOADS["C3"]
+    desc = run_tv(w.src, ("swizzle", 3, 3, 6, ("layout", (64, 64), (64, 1))),
+                  w.dst, "(32,8):(8,1)", "(32,8):(8,1)", 2, seed=3,
+                  expect={"load.vec_bytes": 16, "store.vec_bytes": 16})
+    assert desc["n_tiles"] == 128 * 128
+
+
+@pytest.mark.parametrize("smem,tl,ts", [
+    (("swizzle", 5, 0, 6, ("layout", (64, 64), (1, 64))), "(32,8):(1,32)",
+     "(8,32):(32,1)"),
+    (("swizzle", 3, 2, 6, ("layout", (64, 64), (1, 64))), "(16,16):(1,16)",
+     "(8,32):(32,1)"),
+])
+def test_tv_full_size_transpose_f32(smem, tl, ts):
+    """The 4096x4096 fp32 transpose in 64x64 tiles, with the layouts
+    bench.py times; compared in full with the oracle."""
+    w = WORKLOADS["C2"]
+    src = ("zipped_divide", w.src, (64, 64))
+    dst = ("zipped_divide", w.dst, (64, 64))
+    desc = run_tv(src, smem, dst, tl, ts, 4, seed=4)
+    assert desc["n_tiles"] == 64 * 64

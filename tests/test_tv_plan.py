@@ -1,0 +1,277 @@
+"""Host side of the thread-value partitioned tile copy (no GPU).
+
+The plan's argument block (include/layoutmove_tv.h) is read back through a
+ctypes mirror of the struct, and the device functions of layoutmove_tv.cuh
+are replayed in numpy from their documented arithmetic: every address they
+would form is checked against its buffer (global offsets inside the
+layout's cosize, shared offsets inside the shared tile, both aligned to the
+vector), every shared byte is written exactly once per tile before it is
+read, and the replayed result must equal the oracle's copy.  The bank
+figures of the plan are checked against the oracle's bank model applied to
+the oracle's local_partition of the shared tile.
+"""
+
+import ctypes as C
+
+import numpy as np
+import pytest
+
+from oracle import layout_oracle as lo
+from workloads import seeded_bytes
+from tv_cases import CASES
+
+lm = pytest.importorskip("layout_driven_movement_gb300")
+
+MAXL, MAXV, MAXG = 6, 128, 8
+
+
+class Phase(C.Structure):
+    _fields_ = [("n_thr", C.c_int32), ("n_val", C.c_int32),
+                ("vec_bytes", C.c_int32), ("n_leaves", C.c_int32),
+                ("leaf_ext", C.c_int32 * MAXL),
+                ("leaf_stride", C.c_int32 * MAXL),
+                ("from_step", C.c_int32 * MAXL),
+                ("to_step", C.c_int32 * MAXL),
+                ("from_val", C.c_int32 * MAXV), ("to_val", C.c_int32 * MAXV)]
+
+
+class Args(C.Structure):
+    _fields_ = [("elem_bytes", C.c_int32), ("smem_bytes", C.c_int32),
+                ("block_threads", C.c_int32), ("n_grid", C.c_int32),
+                ("n_tiles", C.c_int64), ("grid_ext", C.c_int64 * MAXG),
+                ("grid_src", C.c_int64 * MAXG), ("grid_dst", C.c_int64 * MAXG),
+                ("src_swz", C.c_int32 * 3), ("smem_swz", C.c_int32 * 3),
+                ("dst_swz", C.c_int32 * 3), ("reserved", C.c_int32),
+                ("load", Phase), ("store", Phase)]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from layout_driven_movement_gb300 import _build
+    _build.build()
+    lm.lib()
+
+
+def args_of(plan):
+    raw = plan.args_bytes()
+    return Args.from_buffer_copy(raw[:C.sizeof(Args)])
+
+
+def swz(o, z):
+    return lo.swizzle(o, z[0], z[1], z[2]) if z[0] else o
+
+
+def thread_bases(p, t):
+    f = np.zeros_like(t)
+    g = np.zeros_like(t)
+    for j in range(p.n_leaves):
+        c = (t // p.leaf_stride[j]) % p.leaf_ext[j]
+        f = f + c * p.from_step[j]
+        g = g + c * p.to_step[j]
+    return f, g
+
+
+def replay(a, src_bytes, dst_bytes, src_cos, dst_cos):
+    """The kernel's loop over tiles, phase by phase, in numpy."""
+    eb = a.elem_bytes
+    for tile in range(a.n_tiles):
+        sb = db = 0
+        rem = tile
+        for k in range(a.n_grid):
+            c = rem % a.grid_ext[k]
+            rem //= a.grid_ext[k]
+            sb += c * a.grid_src[k]
+            db += c * a.grid_dst[k]
+        smem = np.zeros(a.smem_bytes, np.uint8)
+        written = np.zeros(a.smem_bytes, np.int32)
+        for phase, load in ((a.load, True), (a.store, False)):
+            t = np.arange(phase.n_thr, dtype=np.int64)
+            bf, bt = thread_bases(phase, t)
+            vb = phase.vec_bytes
+            assert vb % eb == 0
+            for v in range(phase.n_val):
+                if load:
+                    g = swz((sb + bf + phase.from_val[v]).astype(np.int64),
+                            a.src_swz)
+                    s = swz((bt + phase.to_val[v]).astype(np.int64),
+                            a.smem_swz)
+                    cos = src_cos
+                else:
+                    s = swz((bf + phase.from_val[v]).astype(np.int64),
+                            a.smem_swz)
+                    g = swz((db + bt + phase.to_val[v]).astype(np.int64),
+                            a.dst_swz)
+                    cos = dst_cos
+                assert (g >= 0).all() and ((g * eb + vb) <= cos * eb).all()
+                assert (s >= 0).all() and ((s * eb + vb) <= a.smem_bytes).all()
+                assert ((g * eb) % vb == 0).all() and ((s * eb) % vb == 0).all()
+                for u in range(vb):
+                    gi, si = g * eb + u, s * eb + u
+                    if load:
+                        smem[si] = src_bytes[gi]
+                        np.add.at(written, si, 1)
+                    else:
+                        assert (written[si] == 1).all()
+                        dst_bytes[gi] = smem[si]
+        assert written.max() <= 1
+
+
+TV_CASES = [
+    ("(256,192):(1,256)", "(256,192):(192,1)", (32, 32), "(32,32):(1,32)",
+     None, "(8,32):(1,8)", "(32,8):(8,1)", 4),
+    ("(256,192):(1,256)", "(256,192):(192,1)", (32, 32), "(32,32):(1,33)",
+     None, "(32,8):(1,32)", "(8,32):(32,1)", 4),
+    ("(256,192):(1,256)", "(256,192):(192,1)", (32, 32), "(32,32):(1,32)",
+     (3, 2, 5), "(8,32):(1,8)", "(32,8):(8,1)", 4),
+    ("(512,384):(384,1)", "(512,384):(384,1)", (64, 64), "(64,64):(64,1)",
+     (3, 3, 6), "(32,8):(8,1)", "(32,8):(8,1)", 2),
+    ("(96,80):(1,96)", "(96,80):(80,1)", (32, 16), "(32,16):(16,1)", None,
+     "(2,16):(16,1)", "(32,4):(1,32)", 1),
+    ("(40,24):(24,1)", "(40,24):(1,40)", (8, 8), "(8,8):(8,1)", None,
+     "(8,8):(8,1)", "(8,8):(1,8)", 16),
+    ("(128,64):(1,128)", "(128,64):(64,1)", (32, 32), "(32,32):(1,32)", None,
+     "(16,16):(1,16)", "(32,2):(2,1)", 8),
+]
+
+
+def build_case(src_t, dst_t, tile, smem_t, smem_swz, tl, ts, eb):
+    S = lm.Layout.parse(src_t).zipped_divide(list(tile))
+    D = lm.Layout.parse(dst_t).zipped_divide(list(tile))
+    M = lm.Layout.parse(smem_t)
+    OM = lo.parse(smem_t)
+    if smem_swz:
+        M = M.swizzle(*smem_swz)
+        OM = lo.Swizzled(*smem_swz, OM)
+    plan = lm.TVPlan(S, M, D, lm.Layout.parse(tl), lm.Layout.parse(ts), eb)
+    OS = lo.ZippedDivide(lo.parse(src_t), tile)
+    OD = lo.ZippedDivide(lo.parse(dst_t), tile)
+    return plan, S, D, OS, OD, OM
+
+
+@pytest.mark.parametrize("case", TV_CASES)
+def test_replayed_kernel_matches_oracle(case):
+    plan, S, D, OS, OD, _ = build_case(*case)
+    eb = case[-1]
+    a = args_of(plan)
+    d = plan.describe()
+    assert a.n_tiles == d["n_tiles"]
+    assert a.load.vec_bytes == d["load"]["vec_bytes"]
+    assert a.store.n_val == d["store"]["values"]
+    assert a.block_threads % 32 == 0
+    assert a.block_threads >= max(a.load.n_thr, a.store.n_thr)
+    inp = seeded_bytes("bytes", "uint8", S.cosize * eb, 5)
+    want = np.full(D.cosize * eb, 0xA5, np.uint8)
+    lo.copy(OS, OD, inp, want, eb)
+    got = np.full(D.cosize * eb, 0xA5, np.uint8)
+    replay(a, inp, got, S.cosize, D.cosize)
+    assert (got == want).all()
+
+
+def test_args_block_size_is_checked():
+    plan = build_case(*TV_CASES[0])[0]
+    buf = C.create_string_buffer(C.sizeof(Args))
+    assert lm.lib().lm_tv_plan_args(plan.handle, buf, C.sizeof(Args)) == 0
+    assert lm.lib().lm_tv_plan_args(plan.handle, buf,
+                                    C.sizeof(Args) - 1) == -11
+
+
+@pytest.mark.parametrize("case", TV_CASES)
+def test_bank_figures_match_oracle_partition(case):
+    """Per phase, the shared side's offsets of lane l, value q are the
+    oracle's local_partition of the shared tile (grouped into vectors along
+    the phase's vector mode) for thread l; their bank wavefronts, summed over
+    warps and values, must equal the plan's figure."""
+    plan, S, D, OS, OD, OM = build_case(*case)
+    eb = case[-1]
+    d = plan.describe()
+    base = OM.inner if isinstance(OM, lo.Swizzled) else OM
+    for name, thr_t in (("load", case[5]), ("store", case[6])):
+        ph = d[name]
+        v = ph["vec_bytes"] // eb
+        g = ph["vec_mode"]
+        modes = base.modes()
+        # the shared tile counted in vectors along mode g
+        grouped = []
+        for k, m in enumerate(modes):
+            if k == g and v > 1:
+                grouped.append(lo.Composed(m, lo.Layout(m.size // v, v)))
+            else:
+                grouped.append(m)
+        unit = _Modes(grouped)
+        thr = lo.parse(thr_t)
+        parts = np.stack([lo.local_partition(unit, thr, t)
+                          for t in range(thr.size)])  # (threads, values)
+        if isinstance(OM, lo.Swizzled):
+            parts = lo.swizzle(parts, OM.b, OM.m, OM.s)
+        total = ideal = 0
+        for w0 in range(0, thr.size, 32):
+            for q in range(parts.shape[1]):
+                wf, idl = lo.smem_wavefronts(parts[w0:w0 + 32, q] * eb,
+                                             ph["vec_bytes"])
+                total += wf
+                ideal += idl
+        assert (total, ideal) == (ph["smem_wavefronts"],
+                                  ph["smem_wavefronts_ideal"]), name
+
+
+class _Modes:
+    """Oracle-side layout whose top modes are given objects (for grouping a
+    mode into vectors); evaluated like the oracle's Layout."""
+
+    def __init__(self, modes):
+        self._modes = modes
+        self.size = int(np.prod([m.size for m in modes]))
+
+    def modes(self):
+        return self._modes
+
+    def at(self, i, extended=False):
+        x = np.asarray(i, dtype=np.int64)
+        off = np.zeros_like(x)
+        for m in self._modes:
+            off = off + m.at(x % m.size)
+            x = x // m.size
+        return off
+
+
+def test_tv_plan_errors():
+    S = lm.Layout.parse("(64,64):(1,64)").zipped_divide([32, 32])
+    D = lm.Layout.parse("(64,64):(64,1)").zipped_divide([32, 32])
+    M = lm.Layout.parse("(32,32):(1,32)")
+    t = lm.Layout.parse("(8,32):(1,8)")
+    cases = [
+        ((S, M, D, t, t, 3), -1),                                  # elem size
+        ((S, lm.Layout.parse("(32,16):(1,32)"), D, t, t, 4), -2),  # smem size
+        ((S, lm.Layout.parse("(32,32):(1,16)"), D, t, t, 4), -4),  # smem overlap
+        ((S, M, D, lm.Layout.parse("(8,32):(1,4)"), t, 4), -1),    # thr not bijective
+        ((S, M, D, lm.Layout.parse("(3,32):(1,3)"), t, 4), -3),    # 3 does not divide
+        ((S, M, D, lm.Layout.parse("(2048,1):(1,1)"), t, 4), -1),  # > 1024 threads
+        ((S, M, D, lm.Layout.parse("(1,1):(1,1)"), t, 4), -1),     # > 128 values
+        ((S, lm.Layout.parse("(256,256):(1,256)"), D, t, t, 4), -2),
+    ]
+    for (a, m, d, tl, ts, eb), code in cases:
+        with pytest.raises(lm.LayoutMoveError) as e:
+            lm.TVPlan(a, m, d, tl, ts, eb)
+        assert e.value.status == code, (str(m), str(tl), e.value.status)
+    with pytest.raises(lm.LayoutMoveError) as e:
+        lm.TVPlan(S, M, D, t, t, 4, vec_load_bytes=32)
+    assert e.value.status == -1
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_replayed_gpu_cases_match_oracle(case):
+    """The GPU parity cases, replayed on the host first."""
+    _, src, smem, dst, tl, ts, eb, expect = case
+    S, D = lm.build_layout(src), lm.build_layout(dst)
+    plan = lm.TVPlan(S, lm.build_layout(smem), D, lm.Layout.parse(tl),
+                     lm.Layout.parse(ts), eb)
+    d = plan.describe()
+    for k, v in (expect or {}).items():
+        phase, key = k.split(".")
+        assert d[phase][key] == v, (k, d)
+    inp = seeded_bytes("bytes", "uint8", S.cosize * eb, 9)
+    want = np.full(D.cosize * eb, 0xA5, np.uint8)
+    lo.copy(lo.build(src), lo.build(dst), inp, want, eb)
+    got = np.full(D.cosize * eb, 0xA5, np.uint8)
+    replay(args_of(plan), inp, got, S.cosize, D.cosize)
+    assert (got == want).all()
