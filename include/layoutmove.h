@@ -238,6 +238,31 @@ int lm_layout_stripmined(int64_t threads, int64_t pitch, int64_t strips,
 int lm_smem_wavefronts(const lm_layout* access, int elem_bytes,
                        int access_bytes, int64_t* wavefronts, int64_t* ideal);
 
+/* Choose Pitch and Strips of the stripmined thread map (the
+ * PitchLinearStripminedThreadMap article, hotelren.com, §2.2) for `threads`
+ * threads, each moving vec_elems consecutive elements, over a tile of
+ * `rows` rows of k_row elements of elem_bytes: the tile's rows lie ld
+ * elements apart in global memory, and go to shared memory at smem(row,
+ * col) (a rank-2 layout of sizes (rows, k_row), swizzle allowed; NULL:
+ * row-major, k_row per row).  Thread t of the pass, with the map counted in
+ * vectors (R = k_row / vec_elems per row), takes row (t/P)%S + (t/(P*S))*P*S
+ * and vector column t%P.  Candidates: P and S powers of two, P <= R,
+ * S <= rows, P*S <= threads, every thread's row inside the tile.  The
+ * article's guidance (§4.1-§4.2: Pitch from the vector width and coalescing,
+ * Strips against bank conflicts) becomes a cost, compared in this order:
+ * the 128-byte global segments each warp touches (summed over warps,
+ * *segments), the shared-memory wavefronts of the same accesses under the
+ * bank model of lm_smem_wavefronts (*wavefronts), then the larger P, then
+ * the larger S.  Errors: LM_E_INVALID (arguments out of range: threads not
+ * in 1..1024, vec_elems not dividing k_row, vector bytes not a power of two
+ * up to 16, ld < k_row, smem of other sizes, a misaligned shared address),
+ * LM_E_NOT_REPRESENTABLE (no candidate keeps every thread inside the
+ * tile). */
+int lm_stripmined_tune(int64_t threads, int64_t k_row, int64_t rows,
+                       int64_t ld, int elem_bytes, int vec_elems,
+                       const lm_layout* smem, int64_t* pitch, int64_t* strips,
+                       int64_t* segments, int64_t* wavefronts);
+
 void lm_layout_destroy(lm_layout* layout);
 
 /* ---------------------------------------------------------------------------

@@ -4,20 +4,25 @@
 // A building block for kernels that stage tiles through shared memory: with
 // the lm_tv_args a plan produced (lm_tv_plan_args), a block
 //
-//     lm_tv::load_tile<VL>(a, src, smem, src_tile_base, threadIdx.x);
-//     lm_tv::wait_copies();
-//     __syncthreads();
-//     ... use the shared tile ...
-//     lm_tv::store_tile<VS>(a, smem, dst, dst_tile_base, threadIdx.x);
+//     const lm_tv::Bases b = lm_tv::thread_bases(a, threadIdx.x);  // once
+//     for (each tile) {
+//       lm_tv::tile_bases(a, tile, &src_base, &dst_base);
+//       lm_tv::load_tile<VL>(a, b, src, smem, src_base, threadIdx.x);
+//       lm_tv::wait_copies();
+//       __syncthreads();
+//       ... use the shared tile ...
+//       lm_tv::store_tile<VS>(a, b, smem, dst, dst_base, threadIdx.x);
+//       __syncthreads();
+//     }
 //
-// where VL / VS are a.load.vec_bytes / a.store.vec_bytes and the tile bases
-// come from lm_tv::tile_bases.  Thread t moves its local_partition of the
-// grouped tile ("CUTLASS Layout可视化" §5.3): value v of the load phase goes
-// from src[Swz_src(src_tile_base + base_from(t) + from_val[v])] to
-// smem[Swz_smem(base_to(t) + to_val[v])], in elements.  4-, 8- and 16-byte
-// loads use cp.async (asynchronous: wait_copies() before the tile is read);
-// narrower ones plain loads and stores.  `src` and `dst` must be aligned to
-// the phase's vector bytes, `smem` to 16 bytes.
+// where VL / VS are a.load.vec_bytes / a.store.vec_bytes.  Thread t moves
+// its local_partition of the grouped tile ("CUTLASS Layout可视化" §5.3):
+// value v of the load phase goes from src[Swz_src(src_base + base_from(t) +
+// from_val[v])] to smem[Swz_smem(base_to(t) + to_val[v])], in elements.
+// 4-, 8- and 16-byte loads use cp.async (asynchronous: wait_copies() before
+// the tile is read, or commit_copies() / wait_copies_but<N>() to keep later
+// tiles' loads in flight); narrower ones plain loads and stores.  `src` and `dst`
+// must be aligned to the phase's vector bytes, `smem` to 16 bytes.
 //
 // Pass the arguments as `const __grid_constant__ lm_tv_args` so the value
 // tables are read from the parameter bank rather than copied per thread.
@@ -37,24 +42,45 @@ __device__ __forceinline__ int64_t swizzle(int64_t o, const int32_t* z) {
   return o ^ ((o >> z[2]) & mask);
 }
 
+__device__ __forceinline__ uint32_t fast_div(uint32_t n,
+                                             const lm_tv_fastdiv& f) {
+  const uint32_t t = __umulhi(f.m, n);
+  return (t + ((n - t) >> f.s1)) >> f.s2;
+}
+
 // Element offsets of tile `tile` (colex over the grid modes) in src and dst.
 __device__ __forceinline__ void tile_bases(const lm_tv_args& a, int64_t tile,
                                            int64_t* src_base,
                                            int64_t* dst_base) {
   int64_t s = 0, d = 0;
-  for (int k = 0; k < a.n_grid; ++k) {
-    const int64_t c = tile % a.grid_ext[k];
-    tile /= a.grid_ext[k];
-    s += c * a.grid_src[k];
-    d += c * a.grid_dst[k];
+  if (a.grid_fast) {
+    uint32_t rem = uint32_t(tile);
+    for (int k = 0; k < a.n_grid; ++k) {
+      const uint32_t q = fast_div(rem, a.grid_div[k]);
+      const uint32_t c = rem - q * a.grid_div[k].d;
+      rem = q;
+      s += int64_t(c) * a.grid_src[k];
+      d += int64_t(c) * a.grid_dst[k];
+    }
+  } else {
+    for (int k = 0; k < a.n_grid; ++k) {
+      const int64_t c = tile % a.grid_ext[k];
+      tile /= a.grid_ext[k];
+      s += c * a.grid_src[k];
+      d += c * a.grid_dst[k];
+    }
   }
   *src_base = s;
   *dst_base = d;
 }
 
-// base_from(t), base_to(t) of one phase.
-__device__ __forceinline__ void thread_bases(const lm_tv_phase& p, int t,
-                                             int32_t* from, int32_t* to) {
+// A thread's base offsets in both phases (computed once per thread).
+struct Bases {
+  int32_t load_from, load_to, store_from, store_to;
+};
+
+__device__ __forceinline__ void phase_bases(const lm_tv_phase& p, int t,
+                                            int32_t* from, int32_t* to) {
   int32_t f = 0, g = 0;
   for (int j = 0; j < p.n_leaves; ++j) {
     const int32_t c = (t / p.leaf_stride[j]) % p.leaf_ext[j];
@@ -63,6 +89,19 @@ __device__ __forceinline__ void thread_bases(const lm_tv_phase& p, int t,
   }
   *from = f;
   *to = g;
+}
+
+__device__ __forceinline__ Bases thread_bases(const lm_tv_args& a, int t) {
+  Bases b;
+  phase_bases(a.load, t, &b.load_from, &b.load_to);
+  phase_bases(a.store, t, &b.store_from, &b.store_to);
+  return b;
+}
+
+// Swizzle of an offset inside the shared tile (32-bit).
+__device__ __forceinline__ int32_t swizzle32(int32_t o, const int32_t* z) {
+  if (z[0] == 0) return o;
+  return o ^ ((o >> z[2]) & (((1 << z[0]) - 1) << z[1]));
 }
 
 template <int VB> struct Word;
@@ -94,21 +133,30 @@ __device__ __forceinline__ void wait_copies() {
   asm volatile("cp.async.wait_all;\n" ::: "memory");
 }
 
+// Pipelining: close the group of copies issued so far, and wait until at
+// most N of the closed groups are still in flight.
+__device__ __forceinline__ void commit_copies() {
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void wait_copies_but() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
 // Load phase: this thread's values of the tile at src_tile_base.
 template <int VB>
-__device__ __forceinline__ void load_tile(const lm_tv_args& a,
+__device__ __forceinline__ void load_tile(const lm_tv_args& a, const Bases& b,
                                           const char* src, char* smem,
                                           int64_t src_tile_base, int t) {
   const lm_tv_phase& p = a.load;
   if (t >= p.n_thr) return;
-  int32_t bf, bt;
-  thread_bases(p, t, &bf, &bt);
   const int64_t eb = a.elem_bytes;
-  const int64_t gbase = src_tile_base + bf;
+  const int64_t gbase = src_tile_base + b.load_from;
 #pragma unroll 4
   for (int v = 0; v < p.n_val; ++v) {
     const int64_t go = swizzle(gbase + p.from_val[v], a.src_swz);
-    const int64_t so = swizzle(int64_t(bt) + p.to_val[v], a.smem_swz);
+    const int32_t so = swizzle32(b.load_to + p.to_val[v], a.smem_swz);
     copy_to_shared<VB>(smem + so * eb, src + go * eb);
   }
 }
@@ -116,19 +164,17 @@ __device__ __forceinline__ void load_tile(const lm_tv_args& a,
 // Store phase: this thread's values of the shared tile to the tile at
 // dst_tile_base.
 template <int VB>
-__device__ __forceinline__ void store_tile(const lm_tv_args& a,
+__device__ __forceinline__ void store_tile(const lm_tv_args& a, const Bases& b,
                                            const char* smem, char* dst,
                                            int64_t dst_tile_base, int t) {
   typedef typename Word<VB>::T T;
   const lm_tv_phase& p = a.store;
   if (t >= p.n_thr) return;
-  int32_t bf, bt;
-  thread_bases(p, t, &bf, &bt);
   const int64_t eb = a.elem_bytes;
-  const int64_t gbase = dst_tile_base + bt;
+  const int64_t gbase = dst_tile_base + b.store_to;
 #pragma unroll 4
   for (int v = 0; v < p.n_val; ++v) {
-    const int64_t so = swizzle(int64_t(bf) + p.from_val[v], a.smem_swz);
+    const int32_t so = swizzle32(b.store_from + p.from_val[v], a.smem_swz);
     const int64_t go = swizzle(gbase + p.to_val[v], a.dst_swz);
     *reinterpret_cast<T*>(dst + go * eb) =
         *reinterpret_cast<const T*>(smem + so * eb);

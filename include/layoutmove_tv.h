@@ -16,7 +16,7 @@
  * lm_tv_plan_args (layoutmove.h) fills this struct on the host; the device
  * functions of layoutmove_tv.cuh read it.  Plain C, no CUDA types: a
  * consumer kernel takes it as a `const __grid_constant__ lm_tv_args`
- * parameter (about 2.6 KB).
+ * parameter (about 2.7 KB).
  */
 #ifndef LAYOUTMOVE_TV_H
 #define LAYOUTMOVE_TV_H
@@ -26,6 +26,14 @@
 #define LM_TV_MAX_THR_LEAVES 6   /* thread-layout leaves of extent > 1   */
 #define LM_TV_MAX_VALUES 128     /* vectors per thread per tile           */
 #define LM_TV_MAX_GRID 8         /* joint modes of the grid of tiles      */
+
+/* Division by an invariant divisor d (1 <= d < 2^31) with a multiply and
+ * shifts (Granlund & Montgomery, "Division by invariant integers using
+ * multiplication", PLDI 1994, round-up method): for any 32-bit n,
+ * t = mulhi(m, n), n / d = (t + ((n - t) >> s1)) >> s2. */
+typedef struct lm_tv_fastdiv {
+  uint32_t d, m, s1, s2;
+} lm_tv_fastdiv;
 
 typedef struct lm_tv_phase {
   int32_t n_thr;       /* threads 0 .. n_thr-1 take part                 */
@@ -49,10 +57,12 @@ typedef struct lm_tv_args {
   int64_t grid_ext[LM_TV_MAX_GRID];  /* tile index: colex over these        */
   int64_t grid_src[LM_TV_MAX_GRID];  /* elements per grid coordinate, src   */
   int64_t grid_dst[LM_TV_MAX_GRID];  /* elements per grid coordinate, dst   */
+  lm_tv_fastdiv grid_div[LM_TV_MAX_GRID];  /* by grid_ext, when grid_fast   */
   int32_t src_swz[3];     /* Swizzle<B,M,S> of each side; B == 0: none       */
   int32_t smem_swz[3];
   int32_t dst_swz[3];
-  int32_t reserved;
+  int32_t grid_fast;      /* n_tiles < 2^32 and every grid_ext < 2^31: tile
+                             coordinates by grid_div in 32 bits             */
   lm_tv_phase load;       /* source (global) -> shared tile                 */
   lm_tv_phase store;      /* shared tile -> destination (global)            */
 } lm_tv_args;

@@ -19,7 +19,7 @@ from typing import Iterable, Sequence
 __all__ = [
     "LayoutMoveError", "Layout", "Plan", "lib", "layout_copy",
     "layout_eval_device", "build_layout", "device_status", "STATUS",
-    "TVPlan", "tv_copy",
+    "TVPlan", "tv_copy", "stripmined_tune",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -65,6 +65,9 @@ SIGNATURES = [
      [_P, _P, _I64, C.POINTER(_P), _I64P]),
     ("lm_layout_stripmined", C.c_int, [_I64, _I64, _I64, _I64, C.POINTER(_P)]),
     ("lm_smem_wavefronts", C.c_int, [_P, C.c_int, C.c_int, _I64P, _I64P]),
+    ("lm_stripmined_tune", C.c_int,
+     [_I64, _I64, _I64, _I64, C.c_int, C.c_int, _P, _I64P, _I64P, _I64P,
+      _I64P]),
     ("lm_layout_destroy", None, [_P]),
     ("lm_plan_copy", C.c_int, [_P, _P, C.c_int, C.POINTER(_P)]),
     ("lm_plan_copy_shard", C.c_int,
@@ -444,6 +447,22 @@ def layout_copy(plan: Plan, src, dst, stream=None) -> None:
     _check(lib().lm_layout_copy(plan.handle, C.c_void_p(sp), scap,
                                 C.c_void_p(dp), dcap, _stream_handle(stream)),
            "lm_layout_copy")
+
+
+def stripmined_tune(threads: int, k_row: int, rows: int, elem_bytes: int,
+                    vec_elems: int = 1, ld: int | None = None,
+                    smem: Layout | None = None) -> dict:
+    """Pitch and Strips of the stripmined map for one pass over a tile (see
+    lm_stripmined_tune): {"pitch", "strips", "segments", "wavefronts"}."""
+    p, s, g, w = C.c_int64(), C.c_int64(), C.c_int64(), C.c_int64()
+    _check(lib().lm_stripmined_tune(int(threads), int(k_row), int(rows),
+                                    int(k_row if ld is None else ld),
+                                    int(elem_bytes), int(vec_elems),
+                                    smem.handle if smem is not None else None,
+                                    C.byref(p), C.byref(s), C.byref(g),
+                                    C.byref(w)), "lm_stripmined_tune")
+    return {"pitch": p.value, "strips": s.value, "segments": g.value,
+            "wavefronts": w.value}
 
 
 def tv_copy(plan: TVPlan, src, dst, stream=None) -> None:

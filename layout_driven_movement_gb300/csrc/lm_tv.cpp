@@ -325,12 +325,20 @@ lm_tv_plan plan_tv(const lm_layout& src, const lm_layout& smem,
   A.smem_bytes = int32_t(smem_bytes);
   A.n_grid = int32_t(g2.size());
   A.n_tiles = 1;
+  bool small = true;
   for (size_t k = 0; k < g2.size(); ++k) {
     A.grid_ext[k] = g2[k].e;
     A.grid_src[k] = g2[k].s;
     A.grid_dst[k] = g2[k].d;
     A.n_tiles = mul_chk(A.n_tiles, g2[k].e);
+    if (g2[k].e >= (int64_t(1) << 31)) small = false;
   }
+  A.grid_fast = small && A.n_tiles < (int64_t(1) << 32) ? 1 : 0;
+  if (A.grid_fast)
+    for (size_t k = 0; k < g2.size(); ++k) {
+      const FastDiv f = make_fastdiv(uint32_t(g2[k].e));
+      A.grid_div[k] = lm_tv_fastdiv{f.d, f.m, f.s1, f.s2};
+    }
   int64_t tile_size = 1;
   for (int64_t x : n) tile_size *= x;
   if (tile_size == 0) fail(LM_E_INVALID);  // a tile holds elements

@@ -1,7 +1,8 @@
-// The thread-value partitioned tile copy: one block per tile at a time
-// (grid-stride over tiles), load phase into the shared tile, store phase out
-// of it, both through the device functions of layoutmove_tv.cuh -- the
-// building block this kernel exists to run and test.
+// The thread-value partitioned tile copy: grid-stride over tiles, load
+// phase into a shared tile, store phase out of it, both through the device
+// functions of layoutmove_tv.cuh -- the building block this kernel exists
+// to run and test.  With two shared tiles (`two`), the loads of a block's
+// next tile are in flight while it stores the current one.
 
 #include <cuda_runtime.h>
 
@@ -18,21 +19,46 @@ namespace {
 template <int VL, int VS>
 __global__ void __launch_bounds__(1024)
     lm_tv_kernel(const __grid_constant__ lm_tv_args a,
-                 const char* __restrict__ src, char* __restrict__ dst) {
+                 const char* __restrict__ src, char* __restrict__ dst,
+                 int two) {
   extern __shared__ __align__(16) char tile_smem[];
   const int t = int(threadIdx.x);
-  for (int64_t tile = blockIdx.x; tile < a.n_tiles; tile += gridDim.x) {
-    int64_t sb, db;
-    lm_tv::tile_bases(a, tile, &sb, &db);
-    lm_tv::load_tile<VL>(a, src, tile_smem, sb, t);
-    lm_tv::wait_copies();
+  const int64_t step = gridDim.x;
+  int64_t tile = blockIdx.x;
+  if (tile >= a.n_tiles) return;  // whole block
+  const lm_tv::Bases b = lm_tv::thread_bases(a, t);
+  int64_t sb, db;
+  lm_tv::tile_bases(a, tile, &sb, &db);
+  if (two) {
+    lm_tv::load_tile<VL>(a, b, src, tile_smem, sb, t);
+    lm_tv::commit_copies();
+  }
+  for (int i = 0; tile < a.n_tiles; ++i, tile += step) {
+    char* cur = tile_smem + (two ? (i & 1) * a.smem_bytes : 0);
+    const int64_t next = tile + step;
+    int64_t nsb = 0, ndb = 0;
+    if (next < a.n_tiles) lm_tv::tile_bases(a, next, &nsb, &ndb);
+    if (two) {
+      // the other tile was last read before the barrier that ended the
+      // previous iteration
+      if (next < a.n_tiles)
+        lm_tv::load_tile<VL>(a, b, src,
+                             tile_smem + ((i + 1) & 1) * a.smem_bytes, nsb, t);
+      lm_tv::commit_copies();
+      lm_tv::wait_copies_but<1>();  // this tile's group has landed
+    } else {
+      lm_tv::load_tile<VL>(a, b, src, cur, sb, t);
+      lm_tv::wait_copies();
+    }
     __syncthreads();
-    lm_tv::store_tile<VS>(a, tile_smem, dst, db, t);
+    lm_tv::store_tile<VS>(a, b, cur, dst, db, t);
     __syncthreads();
+    sb = nsb;
+    db = ndb;
   }
 }
 
-typedef void (*TvKernel)(const lm_tv_args, const char*, char*);
+typedef void (*TvKernel)(const lm_tv_args, const char*, char*, int);
 
 template <int VL>
 TvKernel pick_store(int vs) {
@@ -70,10 +96,12 @@ int launch_tv(const lm_tv_plan& plan, const char* src, char* dst,
   if (a.n_tiles == 0) return LM_OK;
   TvKernel k = pick(a.load.vec_bytes, a.store.vec_bytes);
   if (!k) return LM_E_INVALID;
-  const int smem = a.smem_bytes;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail_cuda(e);
+  // two shared tiles when they fit beside each other
+  int two = 2 * int64_t(a.smem_bytes) <= 232448 && a.n_tiles > 1 ? 1 : 0;
+  const int smem = a.smem_bytes * (two ? 2 : 1);
   if (smem > 49152) {
     static std::mutex mu;
     static std::map<std::pair<int, const void*>, int> done;
@@ -98,7 +126,7 @@ int launch_tv(const lm_tv_plan& plan, const char* src, char* dst,
   const int64_t resident = int64_t(sms) * per_sm;
   const unsigned grid = unsigned(a.n_tiles < resident ? a.n_tiles : resident);
   k<<<grid, unsigned(a.block_threads), size_t(smem),
-      static_cast<cudaStream_t>(stream)>>>(a, src, dst);
+      static_cast<cudaStream_t>(stream)>>>(a, src, dst, two);
   e = cudaGetLastError();
   if (e != cudaSuccess) return fail_cuda(e);
   return LM_OK;

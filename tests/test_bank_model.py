@@ -133,3 +133,99 @@ def test_smem_wavefronts_rejects():
         lm.Layout.parse("32:1").smem_wavefronts(4, 8)  # 4-byte aligned only
     with pytest.raises(lm.LayoutMoveError):
         lm.Layout.parse("(4096,4097):(1,4096)").smem_wavefronts(4)  # > 2^24
+
+
+def _tune_by_oracle(threads, k_row, rows, ld, eb, vec, smem_text=None,
+                    smem_swz=None):
+    """The search lm_stripmined_tune documents, recomputed from the oracle's
+    stripmined map, its layout evaluation and its bank model."""
+    from oracle import layout_oracle as lo
+    R = k_row // vec
+    sm = None
+    if smem_text:
+        sm = lo.parse(smem_text)
+        if smem_swz:
+            sm = lo.Swizzled(*smem_swz, sm)
+    best = None
+    P = 1
+    while P <= R and P <= threads:
+        S = 1
+        while S <= rows and P * S <= threads:
+            t = np.arange(threads)
+            off = lo.stripmined_offset(t, R, P, S)   # in vectors
+            row, vcol = off // R, off % R
+            if (row < rows).all():
+                col = vcol * vec
+                g = (row * ld + col) * eb // 128
+                s_off = (sm.at(row + rows * col) if sm is not None
+                         else row * k_row + col)
+                seg = wf = 0
+                for w0 in range(0, threads, 32):
+                    seg += len(set(g[w0:w0 + 32].tolist()))
+                    wf += lo.smem_wavefronts(s_off[w0:w0 + 32] * eb,
+                                             vec * eb)[0]
+                key = (seg, wf, -P, -S)
+                if best is None or key < best[0]:
+                    best = (key, P, S, seg, wf)
+            S *= 2
+        P *= 2
+    return {"pitch": best[1], "strips": best[2], "segments": best[3],
+            "wavefronts": best[4]}
+
+
+@pytest.mark.parametrize("args", [
+    (128, 64, 64, 64, 4, 4, None, None),
+    (128, 32, 64, 32, 4, 4, "(64,32):(32,1)", None),
+    (32, 16, 16, 16, 4, 1, None, None),
+    (256, 64, 64, 4096, 4, 1, "(64,64):(64,1)", None),
+    (256, 64, 64, 4096, 4, 1, "(64,64):(1,64)", None),
+    (256, 64, 64, 4096, 4, 1, "(64,64):(1,64)", (5, 0, 6)),
+    (128, 64, 32, 64, 2, 8, "(32,64):(64,1)", (3, 3, 6)),
+    (96, 24, 96, 100, 8, 2, None, None),
+    (64, 128, 8, 128, 1, 16, None, None),
+])
+def test_stripmined_tune_matches_oracle_search(args):
+    threads, k_row, rows, ld, eb, vec, smem_text, swz = args
+    smem = None
+    if smem_text:
+        smem = lm.Layout.parse(smem_text)
+        if swz:
+            smem = smem.swizzle(*swz)
+    got = lm.stripmined_tune(threads, k_row, rows, eb, vec, ld=ld, smem=smem)
+    assert got == _tune_by_oracle(threads, k_row, rows, ld, eb, vec,
+                                  smem_text, swz)
+
+
+def test_stripmined_tune_follows_the_article_in_closed_form():
+    """fp32 with 16-byte vectors over 64-float rows: Pitch covers a row
+    (16 vectors, 256 bytes), Strips = threads / Pitch, every access at the
+    conflict-free and fully coalesced minimum ([TM] §4.2: Pitch from the
+    vector width, Strips from threads over Pitch)."""
+    got = lm.stripmined_tune(128, 64, 64, 4, 4)
+    assert got == {"pitch": 16, "strips": 8, "segments": 16,
+                   "wavefronts": 16}
+    # a shared tile stored column-major: the same coalesced choice, and the
+    # bank model charges the column-wise shared writes
+    col = lm.stripmined_tune(256, 64, 64, 4, 1, ld=4096,
+                             smem=lm.Layout.parse("(64,64):(1,64)"))
+    assert col["pitch"] == 64 and col["segments"] == 8
+    assert col["wavefronts"] == 8 * 32
+    xor = lm.stripmined_tune(256, 64, 64, 4, 1, ld=4096,
+                             smem=lm.Layout.parse("(64,64):(1,64)").swizzle(
+                                 5, 0, 6))
+    assert xor["pitch"] == 64 and xor["wavefronts"] == 8
+
+
+def test_stripmined_tune_rejects():
+    for a in [(0, 64, 64, 4, 4), (2048, 64, 64, 4, 4), (128, 63, 64, 4, 4),
+              (128, 64, 64, 4, 8), (128, 64, 64, 3, 1)]:
+        with pytest.raises(lm.LayoutMoveError):
+            lm.stripmined_tune(*a)
+    with pytest.raises(lm.LayoutMoveError):
+        lm.stripmined_tune(128, 64, 64, 4, 4, ld=32)
+    with pytest.raises(lm.LayoutMoveError):
+        lm.stripmined_tune(128, 64, 64, 4, 4,
+                           smem=lm.Layout.parse("(32,64):(64,1)"))
+    with pytest.raises(lm.LayoutMoveError) as e:
+        lm.stripmined_tune(1024, 64, 2, 4, 4)   # no pass fits 2 rows
+    assert e.value.status == -3

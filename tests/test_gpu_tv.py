@@ -143,3 +143,45 @@ def test_tv_full_size_transpose_f32(smem, tl, ts):
     dst = ("zipped_divide", w.dst, (64, 64))
     desc = run_tv(src, smem, dst, tl, ts, 4, seed=4)
     assert desc["n_tiles"] == 64 * 64
+
+
+def test_consumer_kernel_built_apart_uses_the_building_block(tmp_path):
+    """A kernel of its own (tests/consumer/tv_consumer.cu), compiled here
+    against include/layoutmove_tv.cuh, takes the plan's argument block and
+    stages bf16 tiles with load_tile / store_tile, complementing every byte
+    in shared memory in between: the result is the oracle's copy of the
+    complemented input."""
+    import ctypes
+    import os
+    import shutil
+    import subprocess
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    so = str(tmp_path / "tv_consumer.so")
+    subprocess.run([nvcc, "-gencode", "arch=compute_103a,code=sm_103a",
+                    "-O3", "-std=c++17", "-shared", "-Xcompiler", "-fPIC",
+                    "-cudart", "static", f"-I{root}/include",
+                    os.path.join(root, "tests", "consumer", "tv_consumer.cu"),
+                    "-o", so], check=True, capture_output=True, timeout=600)
+    cons = ctypes.CDLL(so)
+    cons.tv_consumer_launch.restype = ctypes.c_int
+    cons.tv_consumer_launch.argtypes = [ctypes.c_void_p] * 3 + [
+        ctypes.c_int, ctypes.c_void_p]
+    src_spec = zd((512, 384), (384, 1), (64, 64))
+    dst_spec = ("swizzle", 3, 4, 3,
+                ("layout", ((64, 64), (8, 6)), ((64, 1), (24576, 4096))))
+    S, D = lm.build_layout(src_spec), lm.build_layout(dst_spec)
+    plan = lm.TVPlan(S, lm.Layout.parse("Sw<3,3,6> o (64,64):(64,1)"), D,
+                     lm.Layout.parse("(32,8):(8,1)"),
+                     lm.Layout.parse("(32,8):(8,1)"), 2)
+    args = ctypes.create_string_buffer(plan.args_bytes(), 8192)
+    inp = seeded_bytes("bytes", "uint8", S.cosize * 2, 21)
+    want = np.full(D.cosize * 2, FILL, dtype=np.uint8)
+    lo.copy(lo.build(src_spec), lo.build(dst_spec), ~inp, want, 2)
+    src = torch.from_numpy(inp).cuda()
+    dst = torch.full((D.cosize * 2,), FILL, dtype=torch.uint8, device="cuda")
+    rc = cons.tv_consumer_launch(args, src.data_ptr(), dst.data_ptr(), 20,
+                                 torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert np.array_equal(dst.cpu().numpy(), want)

@@ -35,13 +35,19 @@ class Phase(C.Structure):
                 ("from_val", C.c_int32 * MAXV), ("to_val", C.c_int32 * MAXV)]
 
 
+class FastDiv(C.Structure):
+    _fields_ = [("d", C.c_uint32), ("m", C.c_uint32), ("s1", C.c_uint32),
+                ("s2", C.c_uint32)]
+
+
 class Args(C.Structure):
     _fields_ = [("elem_bytes", C.c_int32), ("smem_bytes", C.c_int32),
                 ("block_threads", C.c_int32), ("n_grid", C.c_int32),
                 ("n_tiles", C.c_int64), ("grid_ext", C.c_int64 * MAXG),
                 ("grid_src", C.c_int64 * MAXG), ("grid_dst", C.c_int64 * MAXG),
+                ("grid_div", FastDiv * MAXG),
                 ("src_swz", C.c_int32 * 3), ("smem_swz", C.c_int32 * 3),
-                ("dst_swz", C.c_int32 * 3), ("reserved", C.c_int32),
+                ("dst_swz", C.c_int32 * 3), ("grid_fast", C.c_int32),
                 ("load", Phase), ("store", Phase)]
 
 
@@ -78,8 +84,16 @@ def replay(a, src_bytes, dst_bytes, src_cos, dst_cos):
         sb = db = 0
         rem = tile
         for k in range(a.n_grid):
-            c = rem % a.grid_ext[k]
-            rem //= a.grid_ext[k]
+            if a.grid_fast:   # the device's 32-bit multiply-shift division
+                f = a.grid_div[k]
+                t = (f.m * rem) >> 32
+                q = (t + ((rem - t) >> f.s1)) >> f.s2
+                assert f.d == a.grid_ext[k] and q == rem // f.d
+                c = rem - q * f.d
+                rem = q
+            else:
+                c = rem % a.grid_ext[k]
+                rem //= a.grid_ext[k]
             sb += c * a.grid_src[k]
             db += c * a.grid_dst[k]
         smem = np.zeros(a.smem_bytes, np.uint8)
