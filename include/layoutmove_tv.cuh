@@ -17,8 +17,8 @@
 //
 // where VL / VS are a.load.vec_bytes / a.store.vec_bytes.  Thread t moves
 // its local_partition of the grouped tile ("CUTLASS Layout可视化" §5.3):
-// value v of the load phase goes from src[Swz_src(src_base + base_from(t) +
-// from_val[v])] to smem[Swz_smem(base_to(t) + to_val[v])], in elements.
+// value v of the load phase goes from src + Swz_src(src_base + base_from(t)
+// + from_val[v]) to smem + Swz_smem(base_to(t) + to_val[v]), all in bytes.
 // 4-, 8- and 16-byte loads use cp.async (asynchronous: wait_copies() before
 // the tile is read, or commit_copies() / wait_copies_but<N>() to keep later
 // tiles' loads in flight); narrower ones plain loads and stores.  `src` and `dst`
@@ -35,7 +35,7 @@
 
 namespace lm_tv {
 
-// Swizzle<B,M,S> on an element offset ("CUTLASS Layout可视化" §4.3).
+// Swizzle<B,M,S> on a byte offset ("CUTLASS Layout可视化" §4.3).
 __device__ __forceinline__ int64_t swizzle(int64_t o, const int32_t* z) {
   if (z[0] == 0) return o;
   const int64_t mask = ((int64_t(1) << z[0]) - 1) << z[1];
@@ -48,7 +48,7 @@ __device__ __forceinline__ uint32_t fast_div(uint32_t n,
   return (t + ((n - t) >> f.s1)) >> f.s2;
 }
 
-// Element offsets of tile `tile` (colex over the grid modes) in src and dst.
+// Byte offsets of tile `tile` (colex over the grid modes) in src and dst.
 __device__ __forceinline__ void tile_bases(const lm_tv_args& a, int64_t tile,
                                            int64_t* src_base,
                                            int64_t* dst_base) {
@@ -151,13 +151,12 @@ __device__ __forceinline__ void load_tile(const lm_tv_args& a, const Bases& b,
                                           int64_t src_tile_base, int t) {
   const lm_tv_phase& p = a.load;
   if (t >= p.n_thr) return;
-  const int64_t eb = a.elem_bytes;
   const int64_t gbase = src_tile_base + b.load_from;
 #pragma unroll 4
   for (int v = 0; v < p.n_val; ++v) {
     const int64_t go = swizzle(gbase + p.from_val[v], a.src_swz);
     const int32_t so = swizzle32(b.load_to + p.to_val[v], a.smem_swz);
-    copy_to_shared<VB>(smem + so * eb, src + go * eb);
+    copy_to_shared<VB>(smem + so, src + go);
   }
 }
 
@@ -170,14 +169,12 @@ __device__ __forceinline__ void store_tile(const lm_tv_args& a, const Bases& b,
   typedef typename Word<VB>::T T;
   const lm_tv_phase& p = a.store;
   if (t >= p.n_thr) return;
-  const int64_t eb = a.elem_bytes;
   const int64_t gbase = dst_tile_base + b.store_to;
 #pragma unroll 4
   for (int v = 0; v < p.n_val; ++v) {
     const int32_t so = swizzle32(b.store_from + p.from_val[v], a.smem_swz);
     const int64_t go = swizzle(gbase + p.to_val[v], a.dst_swz);
-    *reinterpret_cast<T*>(dst + go * eb) =
-        *reinterpret_cast<const T*>(smem + so * eb);
+    *reinterpret_cast<T*>(dst + go) = *reinterpret_cast<const T*>(smem + so);
   }
 }
 

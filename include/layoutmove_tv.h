@@ -8,10 +8,12 @@
  * the source layout into the shared layout, the store phase from the shared
  * layout to the destination layout.  Each phase groups `vec` consecutive
  * coordinates of one tile mode into a vector, partitions the grouped tile by
- * its thread layout and gives thread t, for its value v, the element offsets
+ * its thread layout and gives thread t, for its value v, the byte offsets
  *     from = base_from(t) + from_val[v],   to = base_to(t) + to_val[v]
- * (in elements, before the side's swizzle), where base(t) sums, over the
- * thread layout's leaves j, ((t / leaf_stride[j]) % leaf_ext[j]) * step[j].
+ * (before the side's swizzle), where base(t) sums, over the thread layout's
+ * leaves j, ((t / leaf_stride[j]) % leaf_ext[j]) * step[j].  Every offset,
+ * step and stride below is in bytes, and every swizzle acts on byte
+ * offsets (an element swizzle Swizzle<B,M,S> becomes <B, M+log2(eb), S>).
  *
  * lm_tv_plan_args (layoutmove.h) fills this struct on the host; the device
  * functions of layoutmove_tv.cuh read it.  Plain C, no CUDA types: a
@@ -42,10 +44,10 @@ typedef struct lm_tv_phase {
   int32_t n_leaves;    /* thread-layout leaves used by base(t)           */
   int32_t leaf_ext[LM_TV_MAX_THR_LEAVES];
   int32_t leaf_stride[LM_TV_MAX_THR_LEAVES];
-  int32_t from_step[LM_TV_MAX_THR_LEAVES];  /* elements per coordinate unit */
+  int32_t from_step[LM_TV_MAX_THR_LEAVES];  /* bytes per coordinate unit    */
   int32_t to_step[LM_TV_MAX_THR_LEAVES];
-  int32_t from_val[LM_TV_MAX_VALUES];       /* elements past base_from(t)   */
-  int32_t to_val[LM_TV_MAX_VALUES];         /* elements past base_to(t)     */
+  int32_t from_val[LM_TV_MAX_VALUES];       /* bytes past base_from(t)      */
+  int32_t to_val[LM_TV_MAX_VALUES];         /* bytes past base_to(t)        */
 } lm_tv_phase;
 
 typedef struct lm_tv_args {
@@ -55,10 +57,11 @@ typedef struct lm_tv_args {
   int32_t n_grid;         /* joint modes of the grid of tiles               */
   int64_t n_tiles;
   int64_t grid_ext[LM_TV_MAX_GRID];  /* tile index: colex over these        */
-  int64_t grid_src[LM_TV_MAX_GRID];  /* elements per grid coordinate, src   */
-  int64_t grid_dst[LM_TV_MAX_GRID];  /* elements per grid coordinate, dst   */
+  int64_t grid_src[LM_TV_MAX_GRID];  /* bytes per grid coordinate, src      */
+  int64_t grid_dst[LM_TV_MAX_GRID];  /* bytes per grid coordinate, dst      */
   lm_tv_fastdiv grid_div[LM_TV_MAX_GRID];  /* by grid_ext, when grid_fast   */
-  int32_t src_swz[3];     /* Swizzle<B,M,S> of each side; B == 0: none       */
+  int32_t src_swz[3];     /* Swizzle<B,M,S> of each side on byte offsets;
+                             B == 0: none                                   */
   int32_t smem_swz[3];
   int32_t dst_swz[3];
   int32_t grid_fast;      /* n_tiles < 2^32 and every grid_ext < 2^31: tile

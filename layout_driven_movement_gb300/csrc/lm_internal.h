@@ -182,6 +182,11 @@ struct VecArgs {
   uint32_t g_ext[kMaxModes];
   FastDiv g_pre[kMaxModes], g_div[kMaxModes];
   int64_t g_s[kMaxModes], g_d[kMaxModes];
+  // in-register interleave (PATH_ZIP): each vector index names zip_rows
+  // source vectors zip_s_row bytes apart and zip_rows consecutive
+  // destination vectors
+  int32_t zip_rows = 0;
+  int64_t zip_s_row = 0;
 };
 
 struct StagedArgs {
@@ -262,7 +267,7 @@ struct EvalArgs {
 // ---------------------------------------------------------------------------
 // The lowered plan.
 // ---------------------------------------------------------------------------
-enum Path : int { PATH_GENERIC = 0, PATH_VEC = 1, PATH_STAGED = 2 };
+enum Path : int { PATH_GENERIC = 0, PATH_VEC = 1, PATH_STAGED = 2, PATH_ZIP = 3 };
 
 struct JMode {
   int64_t e, s, d;  // extent, src stride, dst stride (elements)

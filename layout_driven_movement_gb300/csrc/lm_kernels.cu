@@ -561,6 +561,69 @@ __device__ __forceinline__ uint32_t xword(const uint32_t (&in)[R][4], int W) {
   }
 }
 
+// ---------------------------------------------------------------------------
+// ZIP copy: interleave of R source rows without shared memory.  Vector q of
+// the piece names R source vectors (rows zip_s_row bytes apart, the same
+// 16-byte column) and R consecutive destination vectors; the R x V block is
+// transposed in registers.  A warp's loads of one row and its stores are
+// both contiguous.
+// ---------------------------------------------------------------------------
+
+constexpr int kZipUnroll = 2;
+
+template <int EB, int R>
+__global__ void __launch_bounds__(256)
+    lm_zip_kernel(const __grid_constant__ VecArgs a,
+                  const char* __restrict__ src, char* __restrict__ dst) {
+  pdl_trigger();
+  pdl_wait();
+  const uint64_t nthreads = uint64_t(gridDim.x) * blockDim.x;
+  for (uint64_t q0 = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+       q0 < a.n_vec; q0 += kZipUnroll * nthreads) {
+    uint32_t in[kZipUnroll][R][4];
+    int64_t doff[kZipUnroll];
+#pragma unroll
+    for (int u = 0; u < kZipUnroll; ++u) {
+      const uint64_t q64 = q0 + u * nthreads;
+      doff[u] = -1;
+      if (q64 < a.n_vec) {
+        uint32_t q = uint32_t(q64);
+        int64_t s = a.s_base, d = a.d_base;
+#pragma unroll
+        for (int k = 0; k < kMaxModes; ++k) {
+          if (k >= a.nm) break;
+          const uint32_t qn = fdiv(q, a.div[k]);
+          const int64_t c = int64_t(q - qn * a.ext[k]);
+          s += c * a.s[k];
+          d += c * a.d[k];
+          q = qn;
+        }
+        doff[u] = d;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const uint4 v =
+              ld_stream(reinterpret_cast<const uint4*>(src + s + r * a.zip_s_row));
+          in[u][r][0] = v.x;
+          in[u][r][1] = v.y;
+          in[u][r][2] = v.z;
+          in[u][r][3] = v.w;
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kZipUnroll; ++u) {
+      if (doff[u] < 0) continue;
+#pragma unroll
+      for (int j = 0; j < R; ++j)
+        st_stream(reinterpret_cast<uint4*>(dst + doff[u] + 16 * j),
+                  make_uint4(xword<EB, R>(in[u], 4 * j),
+                             xword<EB, R>(in[u], 4 * j + 1),
+                             xword<EB, R>(in[u], 4 * j + 2),
+                             xword<EB, R>(in[u], 4 * j + 3)));
+    }
+  }
+}
+
 template <int EB, int R>
 struct XposeStore {
   static constexpr int kLoadSlots = R >= 8 ? 8 : 4;
@@ -1043,6 +1106,31 @@ int launch_vec_tiled(const VecArgs& v, const char* src, char* dst,
   return check_launch();
 }
 
+template <int EB, int R>
+int launch_zip_t(const VecArgs& v, const char* src, char* dst,
+                 cudaStream_t st) {
+  const DeviceInfo di = device_info();
+  const uint64_t want = (uint64_t(v.n_vec) + 256 * kZipUnroll - 1) /
+                        (256 * kZipUnroll);
+  const uint64_t cap = uint64_t(di.sms) * 8 * uint64_t(waves_vec());
+  const unsigned grid = unsigned(std::max<uint64_t>(1, std::min(want, cap)));
+  launch_k(lm_zip_kernel<EB, R>, grid, 256, 0, st, v, src, dst);
+  return check_launch();
+}
+
+int launch_zip(const VecArgs& v, int eb, const char* src, char* dst,
+               cudaStream_t st) {
+  switch (eb * 100 + v.zip_rows) {
+    case 402: return launch_zip_t<4, 2>(v, src, dst, st);
+    case 202: return launch_zip_t<2, 2>(v, src, dst, st);
+    case 204: return launch_zip_t<2, 4>(v, src, dst, st);
+    case 102: return launch_zip_t<1, 2>(v, src, dst, st);
+    case 104: return launch_zip_t<1, 4>(v, src, dst, st);
+    case 108: return launch_zip_t<1, 8>(v, src, dst, st);
+    default: return LM_E_INVALID;
+  }
+}
+
 template <int VB>
 int launch_vec_t(const VecArgs& v, const char* src, char* dst,
                  cudaStream_t st) {
@@ -1197,6 +1285,8 @@ int launch_piece(const lm_plan& P, const Piece& pc, const char* src,
   }
   if (pc.path == PATH_STAGED && ((ps | pd) % 16) == 0)
     return launch_staged(pc.st, P.eb, src, src_cap_bytes, dst, st);
+  if (pc.path == PATH_ZIP && ((ps | pd) % 16) == 0)
+    return launch_zip(pc.vec, P.eb, src, dst, st);
   return launch_generic(pc.gen, src, dst, st);
 }
 

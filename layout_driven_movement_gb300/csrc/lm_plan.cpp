@@ -407,6 +407,61 @@ static int64_t load_reach(const StagedArgs& A, int64_t seg_bytes) {
 // Micro-tiles are R rows by one 16-byte chunk: R = V when b's runs hold
 // whole 16-byte vectors, or R = extent(b) < V when b is short and a
 // continues its destination run (an interleave).
+// LM_ZIP=0 keeps short interleaves on the shared-memory transpose.
+static bool zip_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("LM_ZIP");
+    return !(v && v[0] == '0');
+  }();
+  return on;
+}
+
+// The in-register interleave: the destination-fast mode b is short (R
+// coordinates, destination stride 1) and the source-fast mode a continues
+// it in the destination (stride R).  Vector j of a names R source vectors
+// (b's rows) and R consecutive destination vectors; no shared memory.
+static bool plan_zip(const std::vector<JMode>& ms, int a, int b, int64_t R,
+                     int64_t s_base, int64_t d_base, const lm_plan& P,
+                     Piece& pc) {
+  const int64_t eb = P.eb, V = 16 / eb;
+  const JMode ma = ms[size_t(a)], mb = ms[size_t(b)];
+  auto al = [](int64_t bytes) { return bytes % 16 == 0; };
+  if (ma.e % V || ma.d != R || mb.d != 1 || mb.e != R) return false;
+  if (!al(s_base * eb) || !al(d_base * eb) || !al(mb.s * eb)) return false;
+  std::vector<JMode> rest;
+  for (int k = 0; k < int(ms.size()); ++k) {
+    if (k == a || k == b) continue;
+    if (!al(ms[size_t(k)].s * eb) || !al(ms[size_t(k)].d * eb)) return false;
+    rest.push_back(ms[size_t(k)]);
+  }
+  if (rest.size() + 1 > size_t(kMaxModes)) return false;
+  std::sort(rest.begin(), rest.end(), mode_before);
+  const int64_t nvec = prod_e(ms) / (V * R);
+  if (nvec >= (int64_t(1) << 32)) return false;
+  VecArgs& A = pc.vec;
+  A = VecArgs{};
+  A.n_vec = uint32_t(nvec);
+  A.nm = int32_t(rest.size() + 1);
+  A.ext[0] = uint32_t(ma.e / V);
+  A.div[0] = make_fastdiv(A.ext[0]);
+  A.s[0] = 16;
+  A.d[0] = 16 * R;
+  for (size_t k = 0; k < rest.size(); ++k) {
+    A.ext[k + 1] = uint32_t(rest[k].e);
+    A.div[k + 1] = make_fastdiv(A.ext[k + 1]);
+    A.s[k + 1] = mul_chk(rest[k].s, eb);
+    A.d[k + 1] = mul_chk(rest[k].d, eb);
+  }
+  A.s_base = mul_chk(s_base, eb);
+  A.d_base = mul_chk(d_base, eb);
+  A.zip_rows = int32_t(R);
+  A.zip_s_row = mul_chk(mb.s, eb);
+  pc.vec_bytes = 16;
+  pc.path = PATH_ZIP;
+  pc.xr = int(R);
+  return true;
+}
+
 static StagedChoice plan_transpose(const std::vector<JMode>& ms,
                                    int64_t s_base, int64_t d_base,
                                    const lm_plan& P, Piece& pc) {
@@ -445,6 +500,11 @@ static StagedChoice plan_transpose(const std::vector<JMode>& ms,
       ch.split_mode = b;
       ch.split_at = mb.e - mb.e % V;
     }
+    return ch;
+  }
+  if (R < V && zip_enabled() && !ssb.on() && !dsb.on() &&
+      plan_zip(ms, a, b, R, s_base, d_base, P, pc)) {
+    ch.ok = true;
     return ch;
   }
   const int64_t target = tile_target(mul_chk(prod_e(ms), eb)) / eb;
@@ -1076,6 +1136,7 @@ static std::string describe(const lm_plan& P) {
     if (i) os << ',';
     const char* path = pc.path == PATH_VEC      ? "VEC"
                        : pc.path == PATH_STAGED ? "STAGED"
+                       : pc.path == PATH_ZIP    ? "ZIP"
                                                 : "GENERIC";
     os << "{\"path\":\"" << path << "\",\"modes\":[";
     for (size_t k = 0; k < pc.modes.size(); ++k) {
@@ -1091,6 +1152,9 @@ static std::string describe(const lm_plan& P) {
       os << ",\"vec_bytes\":" << pc.vec_bytes << ",\"tiled\":"
          << (pc.vec.tiled ? "true" : "false") << ",\"tile_vecs\":"
          << pc.vec.tile_vecs << ",\"n_tiles\":" << pc.vec.n_tiles;
+    if (pc.path == PATH_ZIP)
+      os << ",\"vec_bytes\":16,\"rows\":" << pc.vec.zip_rows
+         << ",\"n_vec\":" << pc.vec.n_vec;
     if (pc.path == PATH_STAGED) {
       const StagedArgs& A = pc.st;
       os << ",\"tile_elems\":" << pc.tile_elems << ",\"n_tiles\":" << A.n_tiles

@@ -212,16 +212,19 @@ int plan_phase(const Side& from, const Side& to, const std::vector<int64_t>& n,
   P.n_val = int32_t(n_val);
   P.vec_bytes = int32_t(v * eb);
   P.n_leaves = int32_t(tl.size());
+  // the device side works in bytes
   for (size_t j = 0; j < tl.size(); ++j) {
-    if (!fits32(sf[j]) || !fits32(st[j])) return LM_E_OVERFLOW;
+    const int64_t a = mul_chk(sf[j], eb), b = mul_chk(st[j], eb);
+    if (!fits32(a) || !fits32(b)) return LM_E_OVERFLOW;
     P.leaf_ext[j] = int32_t(tl[j].e);
     P.leaf_stride[j] = int32_t(tl[j].d);
-    P.from_step[j] = int32_t(sf[j]);
-    P.to_step[j] = int32_t(st[j]);
+    P.from_step[j] = int32_t(a);
+    P.to_step[j] = int32_t(b);
   }
   for (int64_t q = 0; q < n_val; ++q) {
     // base(0) is folded into the value table
-    const int64_t a = vf[size_t(q)] + bf[0], b = vt[size_t(q)] + bt[0];
+    const int64_t a = mul_chk(vf[size_t(q)] + bf[0], eb);
+    const int64_t b = mul_chk(vt[size_t(q)] + bt[0], eb);
     if (!fits32(a) || !fits32(b)) return LM_E_OVERFLOW;
     P.from_val[q] = int32_t(a);
     P.to_val[q] = int32_t(b);
@@ -232,7 +235,7 @@ int plan_phase(const Side& from, const Side& to, const std::vector<int64_t>& n,
 
 // Simulated shared-memory wavefronts of one tile for one phase's shared
 // side (`from` when reading the tile, `to` when writing it).
-int64_t phase_wavefronts(const lm_tv_phase& P, const Swz& z, int eb,
+int64_t phase_wavefronts(const lm_tv_phase& P, const Swz& z,
                          bool shared_is_to, int64_t* ideal) {
   int64_t total = 0, id = 0;
   std::vector<int64_t> addr(32);
@@ -253,7 +256,7 @@ int64_t phase_wavefronts(const lm_tv_phase& P, const Swz& z, int eb,
           h += c * P.to_step[j];
         }
         const int64_t o = shared_is_to ? h + P.to_val[q] : f + P.from_val[q];
-        addr[size_t(l)] = z.apply(o) * eb;
+        addr[size_t(l)] = z.apply(o);  // bytes, byte swizzle
       }
       total += warp_wavefronts(addr.data(), valid, P.vec_bytes);
       const int per = P.vec_bytes <= 4 ? 32 : 128 / P.vec_bytes;
@@ -264,6 +267,17 @@ int64_t phase_wavefronts(const lm_tv_phase& P, const Swz& z, int eb,
   }
   *ideal = id;
   return total;
+}
+
+// A swizzle of element offsets as the same swizzle of byte offsets: the
+// XORed bits move up by log2(eb), the shift stays.
+Swz bytes_swz(const Swz& z, int eb) {
+  Swz r = z;
+  if (!z.on()) return r;
+  int k = 0;
+  while ((1 << k) < eb) ++k;
+  r.m = z.m + k;
+  return r;
 }
 
 void set_swz(int32_t* out, const Swz& z) {
@@ -328,8 +342,8 @@ lm_tv_plan plan_tv(const lm_layout& src, const lm_layout& smem,
   bool small = true;
   for (size_t k = 0; k < g2.size(); ++k) {
     A.grid_ext[k] = g2[k].e;
-    A.grid_src[k] = g2[k].s;
-    A.grid_dst[k] = g2[k].d;
+    A.grid_src[k] = mul_chk(g2[k].s, eb);
+    A.grid_dst[k] = mul_chk(g2[k].d, eb);
     A.n_tiles = mul_chk(A.n_tiles, g2[k].e);
     if (g2[k].e >= (int64_t(1) << 31)) small = false;
   }
@@ -343,9 +357,9 @@ lm_tv_plan plan_tv(const lm_layout& src, const lm_layout& smem,
   for (int64_t x : n) tile_size *= x;
   if (tile_size == 0) fail(LM_E_INVALID);  // a tile holds elements
   if (src.size == 0) A.n_tiles = 0;
-  set_swz(A.src_swz, src.swz);
-  set_swz(A.smem_swz, smem.swz);
-  set_swz(A.dst_swz, dst.swz);
+  set_swz(A.src_swz, bytes_swz(src.swz, eb));
+  set_swz(A.smem_swz, bytes_swz(smem.swz, eb));
+  set_swz(A.dst_swz, bytes_swz(dst.swz, eb));
 
   Side S, M, D;
   S.off = tile_offsets(tsrc);
@@ -368,8 +382,9 @@ lm_tv_plan plan_tv(const lm_layout& src, const lm_layout& smem,
   P.src_cosize = src.cosize;
   P.dst_cosize = dst.cosize;
   int64_t wl_ideal = 0, ws_ideal = 0;
-  const int64_t wl = phase_wavefronts(A.load, smem.swz, eb, true, &wl_ideal);
-  const int64_t ws = phase_wavefronts(A.store, smem.swz, eb, false, &ws_ideal);
+  const Swz zb = bytes_swz(smem.swz, eb);
+  const int64_t wl = phase_wavefronts(A.load, zb, true, &wl_ideal);
+  const int64_t ws = phase_wavefronts(A.store, zb, false, &ws_ideal);
   std::ostringstream os;
   os << "{\"path\":\"TV\",\"n_tiles\":" << A.n_tiles
      << ",\"tile_elems\":" << tile_size << ",\"smem_bytes\":" << A.smem_bytes

@@ -129,6 +129,20 @@ SMALL = [
      ("layout", (2, 1000, 24), (1, 48, 2)), 2),
     ("head_interleave_full_rows", ("layout", (2, 4096, 128), (524288, 128, 1)),
      ("layout", (2, 4096, 128), (1, 256, 2)), 2),
+    # in-register interleaves of 4 and 8 rows, fp32 pairs, a batch mode
+    ("interleave_4_rows_f16", ("layout", (4, 3000, 8), (24000, 8, 1)),
+     ("layout", (4, 3000, 8), (1, 32, 4)), 2),
+    ("interleave_8_rows_u8", ("layout", (8, 5000), (5008, 1)),
+     ("layout", (8, 5000), (1, 8)), 1),
+    ("interleave_pairs_f32", ("layout", (2, 7, 1024), (1024, 2048, 1)),
+     ("layout", (2, 7, 1024), (1, 2048, 2)), 4),
+    ("interleave_ragged_run_f16", ("layout", (2, 5003), (5008, 1)),
+     ("layout", (2, 5003), (1, 2)), 2),
+    ("interleave_unaligned_rows_f16", ("layout", (2, 4000), (4001, 1)),
+     ("layout", (2, 4000), (1, 2)), 2),
+    # a swizzled destination keeps the 2-row interleave in shared memory
+    ("interleave_swizzled_dst_f16", ("layout", (2, 4096), (4096, 1)),
+     ("swizzle", 2, 3, 6, ("layout", (2, 4096), (1, 2))), 2),
     ("identity_vec", ("layout", 100003, 1), ("layout", 100003, 1), 4),
     ("run_then_transpose", ("layout", (8, 300, 70), (1, 8, 2400)),
      ("layout", (8, 300, 70), (1, 560, 8)), 2),
@@ -161,7 +175,7 @@ def test_small_parity_paths_cover_every_kernel():
         for pc in p.describe()["pieces"]:
             seen.add(pc["path"] if pc["path"] != "STAGED"
                      else "STAGED/" + pc["store"] + str(pc["rows"]))
-    assert {"GENERIC", "VEC", "STAGED/gather0"} <= seen
+    assert {"GENERIC", "VEC", "ZIP", "STAGED/gather0"} <= seen
     assert {"STAGED/transpose2", "STAGED/transpose4",
             "STAGED/transpose8"} <= seen, seen
 
@@ -293,22 +307,45 @@ def test_full_size_workload(name):
 
 VARIANT_CASES = ["transpose_ragged_f32", "transpose_1000x1000_f16",
                  "padded_tv_gather_f64", "head_interleave_full_rows",
-                 "tiles_swizzled_bf16", "identity_vec", "transpose_tall_f32"]
+                 "tiles_swizzled_bf16", "identity_vec", "transpose_tall_f32",
+                 "interleave_4_rows_f16", "interleave_8_rows_u8"]
 
 
 def test_bulk_path_is_planned_for_long_segments():
-    for name, bulk in (("C2", False), ("C4", True), ("C5a", False),
-                       ("C5b", True)):
+    for name, bulk in (("C2", False), ("C4", True), ("C5a", False)):
         w = WORKLOADS[name]
         d = lm.Plan(lm.build_layout(w.src), lm.build_layout(w.dst),
                     w.elem_bytes).describe()
         assert all(p["bulk"] == bulk for p in d["pieces"]), (name, d)
 
 
+def test_short_interleaves_plan_the_register_path():
+    """The 2-head interleave and the small interleave cases move through
+    registers (ZIP, no shared memory); rows not 16-byte aligned stay on the
+    shared-memory transpose."""
+    cases = {c[0]: c for c in SMALL}
+    for name, rows in (("head_interleave_f16", 2), ("interleave_4_rows_f16", 4),
+                       ("interleave_8_rows_u8", 8), ("interleave_pairs_f32", 2)):
+        _, s, d, eb = cases[name]
+        pieces = lm.Plan(lm.build_layout(s), lm.build_layout(d),
+                         eb).describe()["pieces"]
+        assert [p["path"] for p in pieces] == ["ZIP"], (name, pieces)
+        assert pieces[0]["rows"] == rows
+    _, s, d, eb = cases["interleave_unaligned_rows_f16"]
+    paths = [p["path"] for p in lm.Plan(lm.build_layout(s), lm.build_layout(d),
+                                        eb).describe()["pieces"]]
+    assert "ZIP" not in paths
+    w = WORKLOADS["C5b"]
+    pieces = lm.Plan(lm.build_layout(w.src), lm.build_layout(w.dst),
+                     w.elem_bytes).describe()["pieces"]
+    assert [p["path"] for p in pieces] == ["ZIP"]
+
+
 @pytest.mark.parametrize("env", [{"LM_BULK": "0"},
                                  {"LM_BULK": "0", "LM_STAGES": "3"},
                                  {"LM_BULK_STAGES": "2"},
-                                 {"LM_BULK_STAGES": "4", "LM_VEC_UNROLL": "8"}])
+                                 {"LM_BULK_STAGES": "4", "LM_VEC_UNROLL": "8"},
+                                 {"LM_ZIP": "0"}])
 def test_pipeline_variants_parity(env):
     """The cp.async load path (LM_BULK=0, 2 or 3 stages) and other bulk
     pipeline depths, in a fresh process since the knobs are read once."""

@@ -443,7 +443,7 @@ def test_plan_paths_for_workloads():
         S, D = lm.build_layout(w.src), lm.build_layout(w.dst)
         paths[name] = [p["path"] for p in lm.Plan(S, D, w.elem_bytes).describe()["pieces"]]
     assert paths == {"C1": ["GENERIC"], "C2": ["STAGED"], "C3": ["VEC"],
-                     "C4": ["STAGED"], "C5a": ["STAGED"], "C5b": ["STAGED"]}
+                     "C4": ["STAGED"], "C5a": ["STAGED"], "C5b": ["ZIP"]}
 
 
 def test_plan_partition_small_workload_shapes():

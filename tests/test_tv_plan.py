@@ -116,11 +116,12 @@ def replay(a, src_bytes, dst_bytes, src_cos, dst_cos):
                     g = swz((db + bt + phase.to_val[v]).astype(np.int64),
                             a.dst_swz)
                     cos = dst_cos
-                assert (g >= 0).all() and ((g * eb + vb) <= cos * eb).all()
-                assert (s >= 0).all() and ((s * eb + vb) <= a.smem_bytes).all()
-                assert ((g * eb) % vb == 0).all() and ((s * eb) % vb == 0).all()
+                # byte offsets
+                assert (g >= 0).all() and ((g + vb) <= cos * eb).all()
+                assert (s >= 0).all() and ((s + vb) <= a.smem_bytes).all()
+                assert (g % vb == 0).all() and (s % vb == 0).all()
                 for u in range(vb):
-                    gi, si = g * eb + u, s * eb + u
+                    gi, si = g + u, s + u
                     if load:
                         smem[si] = src_bytes[gi]
                         np.add.at(written, si, 1)
