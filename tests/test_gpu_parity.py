@@ -329,7 +329,9 @@ def test_short_interleaves_plan_the_register_path():
         _, s, d, eb = cases[name]
         pieces = lm.Plan(lm.build_layout(s), lm.build_layout(d),
                          eb).describe()["pieces"]
-        assert [p["path"] for p in pieces] == ["ZIP"], (name, pieces)
+        # a run that is not a whole number of vectors leaves a GENERIC tail
+        assert pieces[0]["path"] == "ZIP", (name, pieces)
+        assert all(p["path"] == "GENERIC" for p in pieces[1:]), (name, pieces)
         assert pieces[0]["rows"] == rows
     _, s, d, eb = cases["interleave_unaligned_rows_f16"]
     paths = [p["path"] for p in lm.Plan(lm.build_layout(s), lm.build_layout(d),
