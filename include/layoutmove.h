@@ -44,6 +44,7 @@ extern "C" {
 typedef struct lm_layout lm_layout; /* opaque, freed by lm_layout_destroy */
 typedef struct lm_plan lm_plan;     /* opaque, freed by lm_plan_destroy   */
 typedef struct lm_tv_plan lm_tv_plan; /* opaque, freed by lm_tv_plan_destroy */
+typedef struct lm_exchange lm_exchange; /* opaque, lm_exchange_destroy       */
 
 typedef enum lm_status {
   LM_OK = 0,
@@ -336,6 +337,59 @@ int lm_layout_eval_device(const lm_layout* layout, void* table_dev,
                           void* cuda_stream);
 
 void lm_plan_destroy(lm_plan* plan);
+
+/* ---------------------------------------------------------------------------
+ * Relayouts whose source and destination are both sharded across ranks
+ * ------------------------------------------------------------------------- */
+
+/* Plan rank `rank` of `world` of out[dst(i)] = in[src(i)] when every rank
+ * holds only part of the source and must produce only part of the
+ * destination: with the joint modes of the pair (as lm_plan_copy forms
+ * them), rank r holds the source elements of range r of the joint mode with
+ * the largest source stride ("in" mode) and produces the destination
+ * elements of range r of the mode with the largest destination stride
+ * ("out" mode); ranges are balanced (coordinates e*r/world up to
+ * e*(r+1)/world), and both modes need at least `world` coordinates.  The
+ * local shard buffers hold the global layouts' offsets from the shard's
+ * first to its last, rebased to 0 (src_local / dst_local elements; for the
+ * row-sharded transpose of a row-major matrix, the rows themselves).  Rank
+ * p sends rank q the box where p's input range meets q's output range,
+ * packed contiguously in the joint modes' colex order; the exchange is one
+ * all-to-all of those buffers, done by the caller's collective.  The pages
+ * do not shard: this is the copy of "CUTE布局代数" §5.1 (make_copy of a
+ * layout pair) split over ranks, and only the placement of the shards
+ * needs the exchange, every logical index being independent.
+ * Errors: LM_E_INVALID (NULL, elem_bytes, rank/world, an empty copy, no
+ * joint mode with `world` coordinates), LM_E_INCOMPATIBLE (sizes differ or
+ * no common refinement), LM_E_NOT_REPRESENTABLE (a swizzled side),
+ * LM_E_NOT_INJECTIVE. */
+int lm_plan_exchange(const lm_layout* src, const lm_layout* dst,
+                     int elem_bytes, int rank, int world, lm_exchange** out);
+
+/* JSON: joint modes, in/out modes, the local shard extents, and per peer
+ * the box sent and received (count, base offset, modes). */
+int lm_exchange_describe(const lm_exchange* x, char* buf, size_t cap);
+
+/* Elements of the local source and destination shards, and per peer
+ * (arrays of `world`, either may be NULL) the elements sent and received. */
+int lm_exchange_sizes(const lm_exchange* x, int64_t* src_local,
+                      int64_t* dst_local, int64_t* send_counts,
+                      int64_t* recv_counts);
+
+/* Enqueue the pack of the box bound for `peer` from the local source shard
+ * into `send` (its compact image), or the unpack of the box received from
+ * `peer` into the local destination shard: layout copies through
+ * lm_layout_copy, with its buffer rules.  A peer with nothing to exchange
+ * is a no-op.  Errors: LM_E_INVALID, LM_E_CAPACITY, LM_E_OVERLAP,
+ * LM_E_CUDA. */
+int lm_exchange_pack(const lm_exchange* x, int peer, const void* src_local,
+                     int64_t src_capacity_elems, void* send,
+                     int64_t send_capacity_elems, void* cuda_stream);
+int lm_exchange_unpack(const lm_exchange* x, int peer, const void* recv,
+                       int64_t recv_capacity_elems, void* dst_local,
+                       int64_t dst_capacity_elems, void* cuda_stream);
+
+void lm_exchange_destroy(lm_exchange* x);
 
 /* ---------------------------------------------------------------------------
  * Thread-value partitioned tile copies through shared memory

@@ -19,7 +19,7 @@ from typing import Iterable, Sequence
 __all__ = [
     "LayoutMoveError", "Layout", "Plan", "lib", "layout_copy",
     "layout_eval_device", "build_layout", "device_status", "STATUS",
-    "TVPlan", "tv_copy", "stripmined_tune",
+    "TVPlan", "tv_copy", "stripmined_tune", "Exchange", "exchange_copy",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -78,6 +78,13 @@ SIGNATURES = [
     ("lm_plan_launches", C.c_int, [_P, _IP]),
     ("lm_layout_eval_device", C.c_int, [_P, _P, C.c_int, _I64, _P]),
     ("lm_plan_destroy", None, [_P]),
+    ("lm_plan_exchange", C.c_int,
+     [_P, _P, C.c_int, C.c_int, C.c_int, C.POINTER(_P)]),
+    ("lm_exchange_describe", C.c_int, [_P, C.c_char_p, C.c_size_t]),
+    ("lm_exchange_sizes", C.c_int, [_P, _I64P, _I64P, _I64P, _I64P]),
+    ("lm_exchange_pack", C.c_int, [_P, C.c_int, _P, _I64, _P, _I64, _P]),
+    ("lm_exchange_unpack", C.c_int, [_P, C.c_int, _P, _I64, _P, _I64, _P]),
+    ("lm_exchange_destroy", None, [_P]),
     ("lm_tv_plan_create", C.c_int,
      [_P, _P, _P, _P, _P, C.c_int, C.c_int, C.c_int, C.POINTER(_P)]),
     ("lm_tv_plan_describe", C.c_int, [_P, C.c_char_p, C.c_size_t]),
@@ -417,6 +424,91 @@ class TVPlan:
         buf = C.create_string_buffer(8192)
         _check(lib().lm_tv_plan_args(self._h, buf, 8192), "lm_tv_plan_args")
         return buf.raw
+
+
+class Exchange:
+    """Rank `rank` of a relayout whose source and destination are both
+    sharded over `world` ranks (see lm_plan_exchange)."""
+
+    __slots__ = ("_h", "elem_bytes", "world")
+
+    def __init__(self, src: Layout, dst: Layout, elem_bytes: int, rank: int,
+                 world: int):
+        out = C.c_void_p()
+        _check(lib().lm_plan_exchange(src.handle, dst.handle, int(elem_bytes),
+                                      int(rank), int(world), C.byref(out)),
+               "lm_plan_exchange")
+        self._h = out
+        self.elem_bytes = int(elem_bytes)
+        self.world = int(world)
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h and _lib is not None:
+            _lib.lm_exchange_destroy(h)
+            self._h = None
+
+    def describe(self) -> dict:
+        cap = 4096
+        while True:
+            buf = C.create_string_buffer(cap)
+            rc = lib().lm_exchange_describe(self._h, buf, cap)
+            if rc == -11:
+                cap *= 4
+                continue
+            _check(rc, "lm_exchange_describe")
+            return json.loads(buf.value.decode())
+
+    def sizes(self) -> dict:
+        sl, dl = C.c_int64(), C.c_int64()
+        sc = (C.c_int64 * self.world)()
+        rc = (C.c_int64 * self.world)()
+        _check(lib().lm_exchange_sizes(self._h, C.byref(sl), C.byref(dl), sc,
+                                       rc), "lm_exchange_sizes")
+        return {"src_local": sl.value, "dst_local": dl.value,
+                "send": list(sc), "recv": list(rc)}
+
+    def pack(self, peer: int, src_local, send, stream=None) -> None:
+        sp, scap = _dev_buffer(src_local, self.elem_bytes)
+        dp, dcap = _dev_buffer(send, self.elem_bytes)
+        _check(lib().lm_exchange_pack(self._h, int(peer), C.c_void_p(sp),
+                                      scap, C.c_void_p(dp), dcap,
+                                      _stream_handle(stream)),
+               "lm_exchange_pack")
+
+    def unpack(self, peer: int, recv, dst_local, stream=None) -> None:
+        sp, scap = _dev_buffer(recv, self.elem_bytes)
+        dp, dcap = _dev_buffer(dst_local, self.elem_bytes)
+        _check(lib().lm_exchange_unpack(self._h, int(peer), C.c_void_p(sp),
+                                        scap, C.c_void_p(dp), dcap,
+                                        _stream_handle(stream)),
+               "lm_exchange_unpack")
+
+
+def exchange_copy(ex: Exchange, src_local, dst_local, group=None) -> None:
+    """Pack every peer's box, exchange the buffers with one
+    torch.distributed all_to_all_single, unpack: the sharded relayout of
+    rank ex's shards (CUDA uint8 tensors)."""
+    import torch
+    import torch.distributed as dist
+    sz = ex.sizes()
+    eb = ex.elem_bytes
+    send = torch.empty(sum(sz["send"]) * eb, dtype=torch.uint8,
+                       device=src_local.device)
+    recv = torch.empty(sum(sz["recv"]) * eb, dtype=torch.uint8,
+                       device=dst_local.device)
+    off = 0
+    for q, n in enumerate(sz["send"]):
+        if n:
+            ex.pack(q, src_local, send[off:off + n * eb])
+        off += n * eb
+    dist.all_to_all_single(recv, send, [n * eb for n in sz["recv"]],
+                           [n * eb for n in sz["send"]], group=group)
+    off = 0
+    for p, n in enumerate(sz["recv"]):
+        if n:
+            ex.unpack(p, recv[off:off + n * eb], dst_local)
+        off += n * eb
 
 
 def _stream_handle(stream) -> C.c_void_p:

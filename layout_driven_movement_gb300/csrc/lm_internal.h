@@ -309,6 +309,10 @@ namespace lm {
 // Shared-memory wavefronts of one warp access (lm_plan.cpp): addr in bytes,
 // `bytes` per lane.
 int64_t warp_wavefronts(const int64_t* addr, const bool* valid, int bytes);
+// Common refinement of two layouts' leaves into coalesced joint modes
+// (lm_plan.cpp); false when the extents do not nest.
+bool joint_modes(const lm_layout& src, const lm_layout& dst,
+                 std::vector<JMode>& out);
 int launch_tv(const lm_tv_plan& plan, const char* src, char* dst,
               void* stream);  // lm_tv.cu
 

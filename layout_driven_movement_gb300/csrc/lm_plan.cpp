@@ -355,6 +355,14 @@ int64_t warp_wavefronts(const int64_t* addr, const bool* valid, int bytes) {
   return wavefronts(addr, valid, 32, bytes);
 }
 
+bool joint_modes(const lm_layout& src, const lm_layout& dst,
+                 std::vector<JMode>& out) {
+  out.clear();
+  if (!refine(src.leaves, dst.leaves, out)) return false;
+  out = coalesce_joint(out);
+  return true;
+}
+
 namespace {
 
 struct StagedChoice {

@@ -1,0 +1,191 @@
+"""Sharded relayouts with one all-to-all exchange (CPU).
+
+lm_plan_exchange gives each rank the boxes it sends and receives.  Here
+every rank cuts its shard of the source out of a seeded global source,
+packs each outgoing box by the plan's description (numpy, the boxes'
+modes and bases), exchanges the buffers with a real torch.distributed
+all_to_all_single over gloo, unpacks them into its destination shard, and
+checks the shard against the oracle's copy of the whole tensor: every
+slot the rank owns holds the oracle's value, every other slot of its
+buffer is untouched.  The device pack/unpack kernels are the layout copies
+of the other tests; tests/test_gpu_exchange.py runs them for all ranks on
+one GPU.
+"""
+
+import socket
+
+import numpy as np
+import pytest
+
+from oracle import layout_oracle as lo
+from workloads import WORKLOADS, seeded_bytes
+
+lm = pytest.importorskip("layout_driven_movement_gb300")
+
+FILL = 0xA5
+
+CASES = [
+    # row-sharded fp32 transpose: rows in, transposed rows out
+    ("transpose_f32", ("layout", (96, 80), (80, 1)),
+     ("layout", (96, 80), (1, 96)), 4),
+    # NHWC -> NCHW sharded by N on both sides: no traffic between ranks
+    ("nhwc_nchw_f16", ("layout", (6, 16, 5, 7), (560, 1, 112, 16)),
+     ("layout", (6, 16, 5, 7), (560, 35, 7, 1)), 2),
+    # batched padded TV gather, batch sharded on both sides
+    ("tv_gather_f64", ("concat", WORKLOADS["C4"].src[1], ("layout", 37, 72)),
+     ("layout", (((4, 8), 2), 37), (((1, 4), 32), 64)), 8),
+    # 2-head interleave: heads in, positions out
+    ("interleave_f16", ("layout", (2, 600), (600, 1)),
+     ("layout", (2, 600), (1, 2)), 2),
+    # a 3-D permutation whose slowest modes differ on the two sides
+    ("permute_u8", ("layout", (12, 10, 9), (90, 9, 1)),
+     ("layout", (12, 10, 9), (1, 108, 12)), 1),
+]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from layout_driven_movement_gb300 import _build
+    _build.build()
+    lm.lib()
+
+
+def box_offsets(box, side):
+    """Offsets of a box's elements (colex over its modes) on one side."""
+    n = int(np.prod([m[0] for m in box])) if box else 1
+    i = np.arange(n)
+    off = np.zeros(n, dtype=np.int64)
+    for e, s, d in box:
+        off += (i % e) * (d if side == "d" else s)
+        i //= e
+    return off
+
+
+def owned_dst(desc, rank):
+    """Global destination offsets rank owns: its range of the out mode."""
+    ms = [list(m) for m in desc["modes"]]
+    k = desc["out_mode"]
+    e = ms[k][0]
+    lo_, hi = e * rank // desc["world"], e * (rank + 1) // desc["world"]
+    ms[k][0] = hi - lo_
+    return lo_ * ms[k][2] + box_offsets(ms, "d")
+
+
+def global_problem(src, dst, eb):
+    S, D = lm.build_layout(src), lm.build_layout(dst)
+    inp = seeded_bytes("bytes", "uint8", S.cosize * eb, 17)
+    want = np.full(D.cosize * eb, FILL, np.uint8)
+    lo.copy(lo.build(src), lo.build(dst), inp, want, eb)
+    return S, D, inp, want
+
+
+def pack(desc, src_local, peer, eb):
+    b = desc["send"][peer]
+    if b["count"] == 0:
+        return np.zeros(0, np.uint8)
+    idx = b["base"] + box_offsets(b["box"], "s")
+    return src_local.reshape(-1, eb)[idx].reshape(-1)
+
+
+def unpack(desc, buf, dst_local, peer, eb):
+    b = desc["recv"][peer]
+    if b["count"] == 0:
+        return
+    idx = b["base"] + box_offsets(b["box"], "d")
+    dst_local.reshape(-1, eb)[idx] = buf.reshape(-1, eb)
+
+
+def check_rank(desc, dst_local, want, eb, rank):
+    own = owned_dst(desc, rank) - desc["dst_origin"]
+    got = dst_local.reshape(-1, eb)
+    exp = want.reshape(-1, eb)[own + desc["dst_origin"]]
+    assert (got[own] == exp).all()
+    mask = np.ones(len(got), bool)
+    mask[own] = False
+    assert (got[mask] == FILL).all()
+
+
+@pytest.mark.parametrize("world", [1, 2, 3])
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_boxes_partition_and_move_everything(case, world):
+    """All ranks in one process: the send and receive descriptions agree,
+    every logical index moves exactly once, the shards come out right."""
+    _, src, dst, eb = case
+    S, D, inp, want = global_problem(src, dst, eb)
+    descs = [lm.Exchange(S, D, eb, r, world).describe() for r in range(world)]
+    total = sum(b["count"] for d in descs for b in d["send"])
+    assert total == S.size
+    for p in range(world):
+        for q in range(world):
+            assert descs[p]["send"][q]["count"] == descs[q]["recv"][p]["count"]
+            assert descs[p]["send"][q]["box"] == descs[q]["recv"][p]["box"]
+    src_local = [inp[d["src_origin"] * eb:(d["src_origin"] + d["src_local"]) * eb]
+                 for d in descs]
+    sent = [[pack(descs[p], src_local[p], q, eb) for q in range(world)]
+            for p in range(world)]
+    for q in range(world):
+        dl = np.full(descs[q]["dst_local"] * eb, FILL, np.uint8)
+        for p in range(world):
+            unpack(descs[q], sent[p][q], dl, p, eb)
+        check_rank(descs[q], dl, want, eb, q)
+
+
+def test_exchange_rejects():
+    S = lm.Layout.parse("(4,8):(8,1)")
+    D = lm.Layout.parse("(4,8):(1,4)")
+    for args, code in [((S, D, 3, 0, 2), -1), ((S, D, 4, 2, 2), -1),
+                       ((S, D, 4, 0, 9), -1),   # no mode with 9 coordinates
+                       ((S, lm.Layout.parse("(4,8):(1,4)").swizzle(1, 0, 2),
+                         4, 0, 2), -3)]:
+        with pytest.raises(lm.LayoutMoveError) as e:
+            lm.Exchange(*args)
+        assert e.value.status == code
+
+
+def _rank_main(rank, world, port, q):
+    import torch
+    import torch.distributed as dist
+    try:
+        dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}",
+                                rank=rank, world_size=world)
+        lm.lib()
+        for _, src, dst, eb in CASES:
+            S, D, inp, want = global_problem(src, dst, eb)
+            desc = lm.Exchange(S, D, eb, rank, world).describe()
+            o, n = desc["src_origin"], desc["src_local"]
+            src_local = inp[o * eb:(o + n) * eb]
+            send = np.concatenate([pack(desc, src_local, p, eb)
+                                   for p in range(world)])
+            sc = [b["count"] * eb for b in desc["send"]]
+            rc = [b["count"] * eb for b in desc["recv"]]
+            recv = torch.empty(sum(rc), dtype=torch.uint8)
+            dist.all_to_all_single(recv, torch.from_numpy(send), rc, sc)
+            dl = np.full(desc["dst_local"] * eb, FILL, np.uint8)
+            off = 0
+            for p in range(world):
+                unpack(desc, recv[off:off + rc[p]].numpy(), dl, p, eb)
+                off += rc[p]
+            check_rank(desc, dl, want, eb, rank)
+        dist.barrier()
+        dist.destroy_process_group()
+        q.put((rank, "ok"))
+    except Exception as exc:  # reported to the parent
+        q.put((rank, repr(exc)))
+
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_ranks_exchange_over_gloo(world):
+    import torch.multiprocessing as mp
+    with socket.socket() as sock:
+        sock.bind(("127.0.0.1", 0))
+        port = sock.getsockname()[1]
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_rank_main, args=(r, world, port, q))
+             for r in range(world)]
+    for p in procs:
+        p.start()
+    results = dict(q.get(timeout=300) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+    assert results == {r: "ok" for r in range(world)}, results

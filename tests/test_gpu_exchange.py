@@ -1,0 +1,74 @@
+"""GPU parity of the sharded relayout's pack and unpack (lm_exchange_*).
+
+All ranks of an exchange run one after another on one device: each packs
+its boxes from its source shard with the library's copy kernels, the
+"all-to-all" is a device-to-device copy of each box buffer to its
+receiver (no collective, no rank waits on another), and each rank unpacks
+what it received into its destination shard.  Every shard is compared
+byte for byte with the oracle's copy of the whole tensor.
+"""
+
+import pytest
+
+from test_exchange_gloo import CASES, FILL, check_rank, global_problem
+from workloads import WORKLOADS
+
+torch = pytest.importorskip("torch")
+lm = pytest.importorskip("layout_driven_movement_gb300")
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from layout_driven_movement_gb300 import _build
+    _build.build()
+    lm.lib()
+
+
+def run_exchange(src, dst, eb, world):
+    S, D, inp, want = global_problem(src, dst, eb)
+    xs = [lm.Exchange(S, D, eb, r, world) for r in range(world)]
+    descs = [x.describe() for x in xs]
+    g_src = torch.from_numpy(inp).cuda()
+    sends = []
+    for r, (x, d) in enumerate(zip(xs, descs)):
+        o, n = d["src_origin"], d["src_local"]
+        local = g_src[o * eb:(o + n) * eb].clone()
+        bufs = []
+        for q in range(world):
+            c = d["send"][q]["count"]
+            b = torch.full((c * eb,), 0x5C, dtype=torch.uint8, device="cuda")
+            if c:
+                x.pack(q, local, b)
+            bufs.append(b)
+        sends.append(bufs)
+    for q, (x, d) in enumerate(zip(xs, descs)):
+        dl = torch.full((d["dst_local"] * eb,), FILL, dtype=torch.uint8,
+                        device="cuda")
+        for p in range(world):
+            recv = sends[p][q].clone()   # the exchange, on one device
+            if recv.numel():
+                x.unpack(p, recv, dl)
+        torch.cuda.synchronize()
+        check_rank(d, dl.cpu().numpy(), want, eb, q)
+
+
+@pytest.mark.parametrize("world", [2, 3])
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_exchange_on_one_device(case, world):
+    _, src, dst, eb = case
+    run_exchange(src, dst, eb, world)
+
+
+def test_exchange_row_sharded_transpose_large():
+    """The 4096x4096 fp32 transpose, rows sharded four ways on both sides:
+    each rank's boxes are 1024x1024 transposes through the STAGED path."""
+    w = WORKLOADS["C2"]
+    # rows of a row-major source in, rows of the row-major result out
+    src = ("layout", (4096, 4096), (4096, 1))
+    dst = ("layout", (4096, 4096), (1, 4096))
+    x = lm.Exchange(lm.build_layout(src), lm.build_layout(dst), 4, 0, 4)
+    counts = {b["count"] for b in x.describe()["send"]}
+    assert counts == {1024 * 1024}
+    run_exchange(src, dst, w.elem_bytes, 4)
