@@ -323,6 +323,22 @@ int lm_layout_copy(const lm_plan* plan, const void* src_dev,
                    int64_t src_capacity_elems, void* dst_dev,
                    int64_t dst_capacity_elems, void* cuda_stream);
 
+/* The same copy for buffers in host memory, through caller-provided device
+ * staging buffers (src_dev / dst_dev, of src_capacity_elems /
+ * dst_capacity_elems elements): enqueues on cuda_stream the upload of the
+ * whole host source (src_capacity_elems elements), the copy of
+ * lm_layout_copy between the staging buffers, and the download of the
+ * destination's [0, cosize) into dst_host.  When the destination layout
+ * does not cover every slot below its cosize, the host destination is
+ * uploaded first, so slots outside the image come back unchanged.  Host
+ * buffers should be page-locked for the transfers to be asynchronous.
+ * Allocates nothing.  Errors: as lm_layout_copy (the staging buffers are
+ * the device buffers it checks), LM_E_CUDA for a failed transfer. */
+int lm_layout_copy_host(const lm_plan* plan, const void* src_host,
+                        int64_t src_capacity_elems, void* dst_host,
+                        int64_t dst_capacity_elems, void* src_dev,
+                        void* dst_dev, void* cuda_stream);
+
 /* Number of kernel launches lm_layout_copy makes for this plan. */
 int lm_plan_launches(const lm_plan* plan, int* launches);
 

@@ -18,6 +18,7 @@ from typing import Iterable, Sequence
 
 __all__ = [
     "LayoutMoveError", "Layout", "Plan", "lib", "layout_copy",
+    "layout_copy_host",
     "layout_eval_device", "build_layout", "device_status", "STATUS",
     "TVPlan", "tv_copy", "stripmined_tune", "Exchange", "exchange_copy",
 ]
@@ -76,6 +77,7 @@ SIGNATURES = [
     ("lm_plan_extent", C.c_int, [_P, _I64P, _I64P, _I64P]),
     ("lm_layout_copy", C.c_int, [_P, _P, _I64, _P, _I64, _P]),
     ("lm_plan_launches", C.c_int, [_P, _IP]),
+    ("lm_layout_copy_host", C.c_int, [_P, _P, _I64, _P, _I64, _P, _P, _P]),
     ("lm_layout_eval_device", C.c_int, [_P, _P, C.c_int, _I64, _P]),
     ("lm_plan_destroy", None, [_P]),
     ("lm_plan_exchange", C.c_int,
@@ -564,6 +566,28 @@ def tv_copy(plan: TVPlan, src, dst, stream=None) -> None:
     _check(lib().lm_tv_copy(plan.handle, C.c_void_p(sp), scap,
                             C.c_void_p(dp), dcap, _stream_handle(stream)),
            "lm_tv_copy")
+
+
+def layout_copy_host(plan: Plan, src_host, dst_host, src_dev, dst_dev,
+                     stream=None) -> None:
+    """Enqueue upload, copy and download for host tensors (pinned for
+    asynchrony) through the device staging tensors src_dev / dst_dev, which
+    must be at least as large as the host tensors."""
+    for t in (src_host, dst_host):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("host buffers must be contiguous CPU tensors")
+    sp, scap = _dev_buffer(src_dev, plan.elem_bytes)
+    dp, dcap = _dev_buffer(dst_dev, plan.elem_bytes)
+    hs = src_host.numel() * src_host.element_size() // plan.elem_bytes
+    hd = dst_host.numel() * dst_host.element_size() // plan.elem_bytes
+    if scap < hs or dcap < hd:
+        raise ValueError("staging buffers smaller than the host buffers")
+    _check(lib().lm_layout_copy_host(plan.handle,
+                                     C.c_void_p(src_host.data_ptr()), hs,
+                                     C.c_void_p(dst_host.data_ptr()), hd,
+                                     C.c_void_p(sp), C.c_void_p(dp),
+                                     _stream_handle(stream)),
+           "lm_layout_copy_host")
 
 
 def layout_copy_ptr(plan: Plan, src_ptr: int, src_cap: int, dst_ptr: int,

@@ -569,9 +569,7 @@ __device__ __forceinline__ uint32_t xword(const uint32_t (&in)[R][4], int W) {
 // both contiguous.
 // ---------------------------------------------------------------------------
 
-constexpr int kZipUnroll = 2;
-
-template <int EB, int R>
+template <int EB, int R, int U>
 __global__ void __launch_bounds__(256)
     lm_zip_kernel(const __grid_constant__ VecArgs a,
                   const char* __restrict__ src, char* __restrict__ dst) {
@@ -579,11 +577,11 @@ __global__ void __launch_bounds__(256)
   pdl_wait();
   const uint64_t nthreads = uint64_t(gridDim.x) * blockDim.x;
   for (uint64_t q0 = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-       q0 < a.n_vec; q0 += kZipUnroll * nthreads) {
-    uint32_t in[kZipUnroll][R][4];
-    int64_t doff[kZipUnroll];
+       q0 < a.n_vec; q0 += U * nthreads) {
+    uint32_t in[U][R][4];
+    int64_t doff[U];
 #pragma unroll
-    for (int u = 0; u < kZipUnroll; ++u) {
+    for (int u = 0; u < U; ++u) {
       const uint64_t q64 = q0 + u * nthreads;
       doff[u] = -1;
       if (q64 < a.n_vec) {
@@ -611,7 +609,7 @@ __global__ void __launch_bounds__(256)
       }
     }
 #pragma unroll
-    for (int u = 0; u < kZipUnroll; ++u) {
+    for (int u = 0; u < U; ++u) {
       if (doff[u] < 0) continue;
 #pragma unroll
       for (int j = 0; j < R; ++j)
@@ -1106,16 +1104,31 @@ int launch_vec_tiled(const VecArgs& v, const char* src, char* dst,
   return check_launch();
 }
 
+// Blocks in flight per vector of each thread: LM_ZIP_UNROLL (1 or 2).
+int zip_unroll() {
+  static const int u = [] {
+    const char* e = std::getenv("LM_ZIP_UNROLL");
+    return e && e[0] == '2' ? 2 : 1;
+  }();
+  return u;
+}
+
+template <int EB, int R, int U>
+int launch_zip_u(const VecArgs& v, const char* src, char* dst,
+                 cudaStream_t st) {
+  const DeviceInfo di = device_info();
+  const uint64_t want = (uint64_t(v.n_vec) + 256 * U - 1) / (256 * U);
+  const uint64_t cap = uint64_t(di.sms) * 8 * uint64_t(waves_vec());
+  const unsigned grid = unsigned(std::max<uint64_t>(1, std::min(want, cap)));
+  launch_k(lm_zip_kernel<EB, R, U>, grid, 256, 0, st, v, src, dst);
+  return check_launch();
+}
+
 template <int EB, int R>
 int launch_zip_t(const VecArgs& v, const char* src, char* dst,
                  cudaStream_t st) {
-  const DeviceInfo di = device_info();
-  const uint64_t want = (uint64_t(v.n_vec) + 256 * kZipUnroll - 1) /
-                        (256 * kZipUnroll);
-  const uint64_t cap = uint64_t(di.sms) * 8 * uint64_t(waves_vec());
-  const unsigned grid = unsigned(std::max<uint64_t>(1, std::min(want, cap)));
-  launch_k(lm_zip_kernel<EB, R>, grid, 256, 0, st, v, src, dst);
-  return check_launch();
+  return zip_unroll() == 2 ? launch_zip_u<EB, R, 2>(v, src, dst, st)
+                           : launch_zip_u<EB, R, 1>(v, src, dst, st);
 }
 
 int launch_zip(const VecArgs& v, int eb, const char* src, char* dst,
@@ -1350,6 +1363,48 @@ int lm_layout_copy(const lm_plan* plan, const void* src_dev,
                                       cap_bytes, static_cast<char*>(dst_dev),
                                       cuda_stream);
       if (rc != LM_OK) return rc;
+    }
+    return LM_OK;
+  } catch (const lm::Error& e) {
+    return e.status;
+  } catch (...) {
+    return LM_E_INVALID;
+  }
+}
+
+int lm_layout_copy_host(const lm_plan* plan, const void* src_host,
+                        int64_t src_capacity_elems, void* dst_host,
+                        int64_t dst_capacity_elems, void* src_dev,
+                        void* dst_dev, void* cuda_stream) {
+  try {
+    if (!plan) return LM_E_INVALID;
+    if (plan->size == 0) return LM_OK;
+    if (!src_host || !dst_host || !src_dev || !dst_dev) return LM_E_INVALID;
+    if (src_capacity_elems < plan->src_cosize ||
+        dst_capacity_elems < plan->dst_cosize)
+      return LM_E_CAPACITY;
+    const int64_t eb = plan->eb;
+    cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+    const size_t in_bytes = size_t(lm::mul_chk(src_capacity_elems, eb));
+    const size_t out_bytes = size_t(lm::mul_chk(plan->dst_cosize, eb));
+    cudaError_t e =
+        cudaMemcpyAsync(src_dev, src_host, in_bytes, cudaMemcpyHostToDevice, st);
+    // a destination with slots outside its image round-trips them
+    if (e == cudaSuccess && plan->size < plan->dst_cosize)
+      e = cudaMemcpyAsync(dst_dev, dst_host, out_bytes, cudaMemcpyHostToDevice,
+                          st);
+    if (e != cudaSuccess) {
+      lm::set_cuda_error(int(e));
+      return LM_E_CUDA;
+    }
+    const int rc = lm_layout_copy(plan, src_dev, src_capacity_elems, dst_dev,
+                                  dst_capacity_elems, cuda_stream);
+    if (rc != LM_OK) return rc;
+    e = cudaMemcpyAsync(dst_host, dst_dev, out_bytes, cudaMemcpyDeviceToHost,
+                        st);
+    if (e != cudaSuccess) {
+      lm::set_cuda_error(int(e));
+      return LM_E_CUDA;
     }
     return LM_OK;
   } catch (const lm::Error& e) {

@@ -406,3 +406,26 @@ def test_shards_compose_the_full_copy(world):
             lm.layout_copy(lm.Plan(S, D, eb, rank=r, world=world), src, dst)
         torch.cuda.synchronize()
         assert np.array_equal(dst.cpu().numpy(), want), name
+
+
+@pytest.mark.parametrize("name", ["transpose_ragged_f32", "gap_dst_untouched",
+                                  "head_interleave_f16", "padded_tv_gather_f64"])
+def test_copy_host_buffers_round_trip(name):
+    """lm_layout_copy_host: upload, copy and download on a side stream from
+    and into pinned host tensors; destination slots outside the image (the
+    gap case) come back with the host's own bytes."""
+    _, s, d, eb = {c[0]: c for c in SMALL}[name]
+    S, D = lm.build_layout(s), lm.build_layout(d)
+    plan = lm.Plan(S, D, eb)
+    inp = seeded_bytes("bytes", "uint8", S.cosize * eb, 31)
+    host_dst = np.full(D.cosize * eb, 0x3C, dtype=np.uint8)
+    want = host_dst.copy()
+    lo.copy(lo.build(s), lo.build(d), inp, want, eb)
+    hs = torch.from_numpy(inp).pin_memory()
+    hd = torch.from_numpy(host_dst).pin_memory()
+    sd = torch.full((S.cosize * eb,), 0x11, dtype=torch.uint8, device="cuda")
+    dd = torch.full((D.cosize * eb,), 0x22, dtype=torch.uint8, device="cuda")
+    st = torch.cuda.Stream()
+    lm.layout_copy_host(plan, hs, hd, sd, dd, st)
+    st.synchronize()
+    assert np.array_equal(hd.numpy(), want)
