@@ -1110,7 +1110,11 @@ static void plan_box(lm_plan& P, std::vector<JMode> ms, int64_t s_base,
     int k = 0;
     for (size_t j = 1; j < ms.size(); ++j)
       if (ms[j].e > ms[size_t(k)].e) k = int(j);
-    split(k, ms[size_t(k)].e / 2);
+    // halve the longest mode at a multiple of 64 coordinates, so both
+    // halves start on 16-byte boundaries whenever the whole did
+    int64_t at = ms[size_t(k)].e / 2;
+    if (ms[size_t(k)].e >= 256) at = at / 64 * 64;
+    split(k, at);
     return;
   }
   Piece pc;

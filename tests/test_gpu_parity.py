@@ -429,3 +429,27 @@ def test_copy_host_buffers_round_trip(name):
     lm.layout_copy_host(plan, hs, hd, sd, dd, st)
     st.synchronize()
     assert np.array_equal(hd.numpy(), want)
+
+
+def test_copy_beyond_2_to_32_elements_sampled():
+    """The 70000x70000 byte transpose (4.9e9 elements, 64-bit offsets,
+    several pieces), checked at 300000 seeded logical indices computed one
+    by one by the oracle, plus a guard band past the destination."""
+    S = lm.Layout.parse("(70000,70000):(1,70000)")
+    D = lm.Layout.parse("(70000,70000):(70000,1)")
+    plan = lm.Plan(S, D, 1)
+    n = 70000 * 70000
+    inp = seeded_bytes("bytes", "uint8", n, 77)
+    src = torch.from_numpy(inp).cuda()
+    raw = torch.full((n + GUARD,), GUARD_FILL, dtype=torch.uint8, device="cuda")
+    lm.layout_copy(plan, src, raw[:n])
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(5)
+    i = np.concatenate([rng.integers(0, n, 300000), [0, n - 1, 2 ** 31,
+                                                     2 ** 32 + 7]])
+    OS, OD = lo.parse("(70000,70000):(1,70000)"), lo.parse(
+        "(70000,70000):(70000,1)")
+    so, do = OS.at(i), OD.at(i)
+    got = raw[torch.from_numpy(do).cuda()].cpu().numpy()
+    assert (got == inp[so]).all()
+    assert (raw[n:].cpu().numpy() == GUARD_FILL).all()

@@ -562,3 +562,20 @@ def test_local_partition_rejects():
         with pytest.raises(lm.LayoutMoveError) as e:
             tile.local_partition(lm.Layout.parse(thr_t), t)
         assert e.value.status == code, thr_t
+
+
+def test_plans_beyond_2_to_31_elements_split_aligned():
+    """A 70000x70000 byte transpose (4.9e9 elements): the plan splits into
+    pieces under 2^31 elements each, at multiples of 64 coordinates, so
+    every piece keeps the shared-memory path; together they cover the copy."""
+    S = lm.Layout.parse("(70000,70000):(1,70000)")
+    D = lm.Layout.parse("(70000,70000):(70000,1)")
+    d = lm.Plan(S, D, 1).describe()
+    total = 0
+    for p in d["pieces"]:
+        n = int(np.prod([m[0] for m in p["modes"]]))
+        assert n < 2 ** 31
+        assert p["path"] == "STAGED", p
+        assert p["s_base"] % 16 == 0 and p["d_base"] % 16 == 0
+        total += n
+    assert total == 70000 * 70000
