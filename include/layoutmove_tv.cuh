@@ -26,6 +26,8 @@
 //
 // Pass the arguments as `const __grid_constant__ lm_tv_args` so the value
 // tables are read from the parameter bank rather than copied per thread.
+// Needs C++17 (nvcc -std=c++17) and cp.async (sm_80 or later; the library
+// builds it for sm_103a).
 #ifndef LAYOUTMOVE_TV_CUH
 #define LAYOUTMOVE_TV_CUH
 

@@ -290,3 +290,57 @@ def test_replayed_gpu_cases_match_oracle(case):
     got = np.full(D.cosize * eb, 0xA5, np.uint8)
     replay(args_of(plan), inp, got, S.cosize, D.cosize)
     assert (got == want).all()
+
+
+def _random_tv_case(rng):
+    eb = int(rng.choice([1, 2, 4, 8]))
+    n0, n1 = int(rng.choice([8, 16, 32])), int(rng.choice([8, 16, 32]))
+    g0, g1 = int(rng.integers(1, 4)), int(rng.integers(1, 4))
+    R, Cc = n0 * g0, n1 * g1
+
+    def matrix(order):
+        return f"({R},{Cc}):(1,{R})" if order else f"({R},{Cc}):({Cc},1)"
+
+    src_t, dst_t = matrix(rng.integers(2)), matrix(rng.integers(2))
+    pad = int(rng.choice([0, 0, 1, 4]))
+    if rng.integers(2):
+        smem_t = f"({n0},{n1}):(1,{n0 + pad})"
+    else:
+        smem_t = f"({n0},{n1}):({n1 + pad},1)"
+    swz = None
+    if pad == 0 and rng.integers(2):
+        b = int(rng.integers(1, 4))
+        swz = (b, int(rng.integers(0, 3)), int(rng.integers(b, 6)))
+    threads = int(rng.choice([32, 64, 128]))
+    t0 = int(rng.choice([1, 2, 4, 8, 16, 32]))
+    t0 = min(t0, threads)
+    t1 = threads // t0
+    tl = f"({t0},{t1}):(1,{t0})" if rng.integers(2) else f"({t0},{t1}):({t1},1)"
+    t0s = int(rng.choice([1, 2, 4, 8, 16, 32]))
+    t0s = min(t0s, threads)
+    ts = f"({t0s},{threads // t0s}):(1,{t0s})"
+    return (src_t, dst_t, (n0, n1), smem_t, swz, tl, ts, eb)
+
+
+def test_random_tv_plans_replay_exactly():
+    """Random tiles, shared layouts (padded, swizzled), thread layouts and
+    element sizes: every case the planner accepts replays to the oracle's
+    copy with every address in bounds; rejections carry a status."""
+    rng = np.random.default_rng(2024)
+    planned = 0
+    for _ in range(40):
+        case = _random_tv_case(rng)
+        try:
+            plan, S, D, OS, OD, _ = build_case(*case)
+        except lm.LayoutMoveError as e:
+            assert e.status in (-1, -3), (case, e.status)
+            continue
+        eb = case[-1]
+        inp = seeded_bytes("bytes", "uint8", S.cosize * eb, 3)
+        want = np.full(D.cosize * eb, 0xA5, np.uint8)
+        lo.copy(OS, OD, inp, want, eb)
+        got = np.full(D.cosize * eb, 0xA5, np.uint8)
+        replay(args_of(plan), inp, got, S.cosize, D.cosize)
+        assert (got == want).all(), case
+        planned += 1
+    assert planned >= 12
