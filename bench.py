@@ -305,6 +305,7 @@ def run_native(args) -> dict | None:
         return None
 
     tv = measure_tv(suite, args, torch, peak) if not args.quick else {}
+    xch = measure_exchange(suite, args, torch, peak) if not args.quick else {}
     e2e = measure_e2e(suite, args, torch) if not args.quick else None
     cpu = cpu_baseline(suite) if world == 1 and not args.quick else None
     clocks = clk.summary()
@@ -327,6 +328,7 @@ def run_native(args) -> dict | None:
                          " steps with CUDA events around every copy",
             "per_config": per_cfg,
             "tv_copy": tv,
+            "exchange": xch,
         },
         "clocks": clocks,
         "roofline": roofline,
@@ -433,6 +435,70 @@ def measure_tv(suite, args, torch, peak) -> dict:
             "median_us": round(ms * 1e3, 2), "gbs": round(gbs, 1),
             "frac_of_peak": round(gbs / peak, 4)}
     return out
+
+
+def measure_exchange(suite, args, torch, peak, world=4) -> dict:
+    """The sharded relayout's device work on one GPU: the 4096x4096 fp32
+    transpose with rows sharded over `world` ranks on both sides.  Every
+    rank's packs and unpacks run back to back on this device (the
+    all-to-all between them is a collective on several GPUs and is not
+    timed here); reported as the algorithmic bytes of the whole copy, twice
+    (pack and unpack each read and write every element once), over the
+    time of all of them."""
+    it = next((i for i in suite.items if i["name"] == "C2"), None)
+    if it is None:
+        return {}
+    lm = suite.lm
+    eb = it["w"].elem_bytes
+    src = lm.Layout.parse("(4096,4096):(4096,1)")
+    dst = lm.Layout.parse("(4096,4096):(1,4096)")
+    xs = [lm.Exchange(src, dst, eb, r, world) for r in range(world)]
+    sizes = [x.sizes() for x in xs]
+    total = 4096 * 4096 * eb
+    buf_in = it["src"][:total]
+    buf_out = it["dst"][:total]
+    send = torch.empty(total, dtype=torch.uint8, device=buf_in.device)
+    soff = []       # byte offset of box (p, q) in the packed buffer
+    off = 0
+    for p in range(world):
+        row = []
+        for q in range(world):
+            row.append(off)
+            off += sizes[p]["send"][q] * eb
+        soff.append(row)
+    dsc = [x.describe() for x in xs]
+
+    def one():
+        for p, x in enumerate(xs):
+            o, n = dsc[p]["src_origin"] * eb, dsc[p]["src_local"] * eb
+            for q in range(world):
+                c = sizes[p]["send"][q] * eb
+                x.pack(q, buf_in[o:o + n], send[soff[p][q]:soff[p][q] + c])
+        for q, x in enumerate(xs):
+            o, n = dsc[q]["dst_origin"] * eb, dsc[q]["dst_local"] * eb
+            for p in range(world):
+                c = sizes[p]["send"][q] * eb
+                x.unpack(p, send[soff[p][q]:soff[p][q] + c], buf_out[o:o + n])
+
+    for _ in range(3):
+        one()
+    rounds = min(args.steps, 200)
+    e0, e1 = (torch.cuda.Event(enable_timing=True),
+              torch.cuda.Event(enable_timing=True))
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(rounds):
+        one()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / rounds
+    gbs = 2 * 2 * total / (ms * 1e-3) / 1e9
+    return {"workload": f"4096x4096 fp32 transpose, rows sharded over {world} "
+                        "ranks on both sides, all ranks' packs and unpacks on "
+                        "this GPU (the all-to-all itself not timed)",
+            "copies_per_round": 2 * world * world,
+            "us_per_round": round(ms * 1e3, 2), "gbs": round(gbs, 1),
+            "frac_of_peak": round(gbs / peak, 4)}
 
 
 def measure_e2e(suite, args, torch) -> dict:
