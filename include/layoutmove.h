@@ -405,6 +405,20 @@ int lm_exchange_unpack(const lm_exchange* x, int peer, const void* recv,
                        int64_t recv_capacity_elems, void* dst_local,
                        int64_t dst_capacity_elems, void* cuda_stream);
 
+/* All of this rank's packs, into one buffer holding the boxes for peers
+ * 0..world-1 one after another (each box compact, as lm_exchange_pack
+ * writes it; the send counts give the offsets), and all of its unpacks from
+ * one buffer laid out the same way by sender.  When both the in and the out
+ * mode split evenly over the ranks (every box the same shape) and differ,
+ * each is a single layout copy ("one_copy_per_side" in the description);
+ * otherwise one copy per peer.  Errors: as lm_exchange_pack/unpack. */
+int lm_exchange_pack_all(const lm_exchange* x, const void* src_local,
+                         int64_t src_capacity_elems, void* send,
+                         int64_t send_capacity_elems, void* cuda_stream);
+int lm_exchange_unpack_all(const lm_exchange* x, const void* recv,
+                           int64_t recv_capacity_elems, void* dst_local,
+                           int64_t dst_capacity_elems, void* cuda_stream);
+
 void lm_exchange_destroy(lm_exchange* x);
 
 /* ---------------------------------------------------------------------------

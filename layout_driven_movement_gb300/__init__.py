@@ -21,6 +21,7 @@ __all__ = [
     "layout_copy_host",
     "layout_eval_device", "build_layout", "device_status", "STATUS",
     "TVPlan", "tv_copy", "stripmined_tune", "Exchange", "exchange_copy",
+    "exchange_pack_all", "exchange_unpack_all",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -86,6 +87,8 @@ SIGNATURES = [
     ("lm_exchange_sizes", C.c_int, [_P, _I64P, _I64P, _I64P, _I64P]),
     ("lm_exchange_pack", C.c_int, [_P, C.c_int, _P, _I64, _P, _I64, _P]),
     ("lm_exchange_unpack", C.c_int, [_P, C.c_int, _P, _I64, _P, _I64, _P]),
+    ("lm_exchange_pack_all", C.c_int, [_P, _P, _I64, _P, _I64, _P]),
+    ("lm_exchange_unpack_all", C.c_int, [_P, _P, _I64, _P, _I64, _P]),
     ("lm_exchange_destroy", None, [_P]),
     ("lm_tv_plan_create", C.c_int,
      [_P, _P, _P, _P, _P, C.c_int, C.c_int, C.c_int, C.POINTER(_P)]),
@@ -487,6 +490,25 @@ class Exchange:
                "lm_exchange_unpack")
 
 
+def _exchange_all(fn, ex, a, b, stream, what):
+    ap, acap = _dev_buffer(a, ex.elem_bytes)
+    bp, bcap = _dev_buffer(b, ex.elem_bytes)
+    _check(fn(ex._h, C.c_void_p(ap), acap, C.c_void_p(bp), bcap,
+              _stream_handle(stream)), what)
+
+
+def exchange_pack_all(ex: Exchange, src_local, send, stream=None) -> None:
+    """Every peer's box into one buffer, peer after peer."""
+    _exchange_all(lib().lm_exchange_pack_all, ex, src_local, send, stream,
+                  "lm_exchange_pack_all")
+
+
+def exchange_unpack_all(ex: Exchange, recv, dst_local, stream=None) -> None:
+    """Every sender's box from one buffer, sender after sender."""
+    _exchange_all(lib().lm_exchange_unpack_all, ex, recv, dst_local, stream,
+                  "lm_exchange_unpack_all")
+
+
 def exchange_copy(ex: Exchange, src_local, dst_local, group=None) -> None:
     """Pack every peer's box, exchange the buffers with one
     torch.distributed all_to_all_single, unpack: the sharded relayout of
@@ -499,18 +521,10 @@ def exchange_copy(ex: Exchange, src_local, dst_local, group=None) -> None:
                        device=src_local.device)
     recv = torch.empty(sum(sz["recv"]) * eb, dtype=torch.uint8,
                        device=dst_local.device)
-    off = 0
-    for q, n in enumerate(sz["send"]):
-        if n:
-            ex.pack(q, src_local, send[off:off + n * eb])
-        off += n * eb
+    exchange_pack_all(ex, src_local, send)
     dist.all_to_all_single(recv, send, [n * eb for n in sz["recv"]],
                            [n * eb for n in sz["send"]], group=group)
-    off = 0
-    for p, n in enumerate(sz["recv"]):
-        if n:
-            ex.unpack(p, recv[off:off + n * eb], dst_local)
-        off += n * eb
+    exchange_unpack_all(ex, recv, dst_local)
 
 
 def _stream_handle(stream) -> C.c_void_p:

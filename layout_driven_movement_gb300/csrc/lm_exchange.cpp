@@ -36,10 +36,16 @@ struct lm_exchange {
   int64_t src_local = 0, dst_local = 0;  // elements of the shard buffers
   int64_t src_origin = 0, dst_origin = 0;  // global offsets of their starts
   std::vector<PeerCopy> send, recv;
+  // when both modes split evenly, every box has the same shape and the
+  // packs (unpacks) of all peers form one layout copy each
+  lm_plan* pack_all = nullptr;
+  lm_plan* unpack_all = nullptr;
   std::string describe;
   ~lm_exchange() {
     for (PeerCopy& p : send) lm_plan_destroy(p.plan);
     for (PeerCopy& p : recv) lm_plan_destroy(p.plan);
+    lm_plan_destroy(pack_all);
+    lm_plan_destroy(unpack_all);
   }
 };
 
@@ -72,6 +78,47 @@ lm_plan* box_plan(const std::vector<JMode>& box, bool side_is_dst, int eb) {
                              : lm_plan_copy(&S, &C, eb, &p);
   if (rc != LM_OK) fail(rc);
   return p;
+}
+
+// The packs of all peers as one copy: the shard's box with the out mode
+// cut into (box extent, peer), the packed buffer peer-major with each box
+// compact.  The unpacks likewise, the in mode cut into (box extent, peer).
+// Only when every box has the same shape (both modes split evenly) and the
+// two modes differ.
+void plan_all(lm_exchange& X) {
+  const std::vector<JMode>& ms = X.modes;
+  const int ki = X.in_mode, ko = X.out_mode, w = X.world;
+  if (ki == ko || ms[size_t(ki)].e % w || ms[size_t(ko)].e % w) return;
+  std::vector<int64_t> x;
+  for (const JMode& m : ms) x.push_back(m.e);
+  x[size_t(ki)] /= w;
+  x[size_t(ko)] /= w;
+  std::vector<std::pair<int64_t, int64_t>> shard_s, shard_d, packed;
+  int64_t cw = 1;
+  for (size_t j = 0; j < ms.size(); ++j) {
+    shard_s.push_back({x[j], ms[j].s});
+    shard_d.push_back({x[j], ms[j].d});
+    packed.push_back({x[j], cw});
+    cw = mul_chk(cw, x[j]);
+  }
+  // pack: peer q steps along the out mode in the source
+  std::vector<std::pair<int64_t, int64_t>> ps = shard_s, pd = packed;
+  ps.push_back({w, mul_chk(x[size_t(ko)], ms[size_t(ko)].s)});
+  pd.push_back({w, cw});
+  // unpack: peer p steps along the in mode in the destination
+  std::vector<std::pair<int64_t, int64_t>> us = packed, ud = shard_d;
+  us.push_back({w, cw});
+  ud.push_back({w, mul_chk(x[size_t(ki)], ms[size_t(ki)].d)});
+  const lm_layout PS = leaves_layout(ps), PD = leaves_layout(pd);
+  const lm_layout US = leaves_layout(us), UD = leaves_layout(ud);
+  lm_plan *a = nullptr, *b = nullptr;
+  if (lm_plan_copy(&PS, &PD, X.eb, &a) != LM_OK) return;
+  if (lm_plan_copy(&US, &UD, X.eb, &b) != LM_OK) {
+    lm_plan_destroy(a);
+    return;
+  }
+  X.pack_all = a;
+  X.unpack_all = b;
 }
 
 // The joint mode with at least `world` coordinates and the largest stride
@@ -198,6 +245,8 @@ lm_exchange* plan_exchange(const lm_layout& src, const lm_layout& dst, int eb,
     }
     os << ']';
   }
+  plan_all(*X);
+  os << ",\"one_copy_per_side\":" << (X->pack_all ? "true" : "false");
   os << '}';
   X->describe = os.str();
   return X.release();
@@ -268,6 +317,50 @@ int lm_exchange_unpack(const lm_exchange* x, int peer, const void* recv,
   char* d = static_cast<char*>(dst_local) + pc.base * x->eb;
   return lm_layout_copy(pc.plan, recv, recv_capacity_elems, d,
                         dst_capacity_elems - pc.base, cuda_stream);
+}
+
+int lm_exchange_pack_all(const lm_exchange* x, const void* src_local,
+                         int64_t src_capacity_elems, void* send,
+                         int64_t send_capacity_elems, void* cuda_stream) {
+  if (!x) return LM_E_INVALID;
+  if (!x->pack_all) {
+    int64_t off = 0;
+    for (int q = 0; q < x->world; ++q) {
+      const int64_t n = x->send[size_t(q)].count;
+      if (n && off + n > send_capacity_elems) return LM_E_CAPACITY;
+      const int rc = lm_exchange_pack(
+          x, q, src_local, src_capacity_elems,
+          n ? static_cast<char*>(send) + off * x->eb : send, n, cuda_stream);
+      if (rc != LM_OK) return rc;
+      off += n;
+    }
+    return LM_OK;
+  }
+  if (src_capacity_elems < x->src_local) return LM_E_CAPACITY;
+  return lm_layout_copy(x->pack_all, src_local, src_capacity_elems, send,
+                        send_capacity_elems, cuda_stream);
+}
+
+int lm_exchange_unpack_all(const lm_exchange* x, const void* recv,
+                           int64_t recv_capacity_elems, void* dst_local,
+                           int64_t dst_capacity_elems, void* cuda_stream) {
+  if (!x) return LM_E_INVALID;
+  if (!x->unpack_all) {
+    int64_t off = 0;
+    for (int p = 0; p < x->world; ++p) {
+      const int64_t n = x->recv[size_t(p)].count;
+      if (n && off + n > recv_capacity_elems) return LM_E_CAPACITY;
+      const int rc = lm_exchange_unpack(
+          x, p, n ? static_cast<const char*>(recv) + off * x->eb : recv, n,
+          dst_local, dst_capacity_elems, cuda_stream);
+      if (rc != LM_OK) return rc;
+      off += n;
+    }
+    return LM_OK;
+  }
+  if (dst_capacity_elems < x->dst_local) return LM_E_CAPACITY;
+  return lm_layout_copy(x->unpack_all, recv, recv_capacity_elems, dst_local,
+                        dst_capacity_elems, cuda_stream);
 }
 
 void lm_exchange_destroy(lm_exchange* x) { delete x; }

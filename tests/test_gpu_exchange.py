@@ -72,3 +72,49 @@ def test_exchange_row_sharded_transpose_large():
     counts = {b["count"] for b in x.describe()["send"]}
     assert counts == {1024 * 1024}
     run_exchange(src, dst, w.elem_bytes, 4)
+
+
+@pytest.mark.parametrize("world", [2, 3, 4])
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_pack_all_and_unpack_all(case, world):
+    """One buffer per rank for all peers: pack_all writes exactly the
+    per-peer packs one after another (one copy when the boxes are equal),
+    and unpack_all of the exchanged buffers gives the oracle's shards."""
+    _, src, dst, eb = case
+    S, D, inp, want = global_problem(src, dst, eb)
+    try:
+        xs = [lm.Exchange(S, D, eb, r, world) for r in range(world)]
+    except lm.LayoutMoveError as e:      # no mode with `world` coordinates
+        assert e.status == -1
+        return
+    descs = [x.describe() for x in xs]
+    sizes = [x.sizes() for x in xs]
+    g_src = torch.from_numpy(inp).cuda()
+    packed = []
+    for r, (x, d) in enumerate(zip(xs, descs)):
+        o, n = d["src_origin"], d["src_local"]
+        local = g_src[o * eb:(o + n) * eb].clone()
+        total = sum(sizes[r]["send"]) * eb
+        buf = torch.full((total,), 0x5C, dtype=torch.uint8, device="cuda")
+        lm.exchange_pack_all(x, local, buf)
+        ref = torch.full((total,), 0x5C, dtype=torch.uint8, device="cuda")
+        off = 0
+        for q in range(world):
+            c = sizes[r]["send"][q] * eb
+            if c:
+                x.pack(q, local, ref[off:off + c])
+            off += c
+        torch.cuda.synchronize()
+        assert torch.equal(buf, ref)
+        packed.append(buf)
+    for q, (x, d) in enumerate(zip(xs, descs)):
+        parts, off = [], []
+        for p in range(world):
+            start = sum(sizes[p]["send"][:q]) * eb
+            parts.append(packed[p][start:start + sizes[p]["send"][q] * eb])
+        recv = torch.cat(parts)
+        dl = torch.full((d["dst_local"] * eb,), FILL, dtype=torch.uint8,
+                        device="cuda")
+        lm.exchange_unpack_all(x, recv, dl)
+        torch.cuda.synchronize()
+        check_rank(d, dl.cpu().numpy(), want, eb, q)
