@@ -180,6 +180,71 @@ __device__ __forceinline__ void store_tile(const lm_tv_args& a, const Bases& b,
   }
 }
 
+// ---------------------------------------------------------------------------
+// The same phases with every tile-invariant offset computed once per thread
+// (for phases of at most MAXV values per thread): the shared offsets
+// swizzled, and the global in-tile offsets swizzled when the side's swizzle
+// commutes with the tile base.  Per value a tile then costs one add.
+// ---------------------------------------------------------------------------
+
+template <int MAXV>
+struct Offsets {
+  int32_t load_g[MAXV], load_s[MAXV];    // global (in-tile), shared
+  int32_t store_s[MAXV], store_g[MAXV];  // shared, global (in-tile)
+};
+
+template <int MAXV>
+__device__ __forceinline__ void thread_offsets(const lm_tv_args& a,
+                                               const Bases& b,
+                                               Offsets<MAXV>& o) {
+#pragma unroll
+  for (int v = 0; v < MAXV; ++v) {
+    o.load_g[v] = o.load_s[v] = o.store_s[v] = o.store_g[v] = 0;
+    if (v < a.load.n_val) {
+      const int64_t g = int64_t(b.load_from) + a.load.from_val[v];
+      o.load_g[v] = int32_t(a.src_swz_tile ? swizzle(g, a.src_swz) : g);
+      o.load_s[v] = swizzle32(b.load_to + a.load.to_val[v], a.smem_swz);
+    }
+    if (v < a.store.n_val) {
+      o.store_s[v] = swizzle32(b.store_from + a.store.from_val[v], a.smem_swz);
+      const int64_t g = int64_t(b.store_to) + a.store.to_val[v];
+      o.store_g[v] = int32_t(a.dst_swz_tile ? swizzle(g, a.dst_swz) : g);
+    }
+  }
+}
+
+template <int VB, int MAXV>
+__device__ __forceinline__ void load_tile(const lm_tv_args& a,
+                                          const Offsets<MAXV>& o,
+                                          const char* src, char* smem,
+                                          int64_t src_tile_base, int t) {
+  if (t >= a.load.n_thr) return;
+#pragma unroll
+  for (int v = 0; v < MAXV; ++v) {
+    if (v >= a.load.n_val) break;
+    int64_t go = src_tile_base + o.load_g[v];
+    if (!a.src_swz_tile) go = swizzle(go, a.src_swz);
+    copy_to_shared<VB>(smem + o.load_s[v], src + go);
+  }
+}
+
+template <int VB, int MAXV>
+__device__ __forceinline__ void store_tile(const lm_tv_args& a,
+                                           const Offsets<MAXV>& o,
+                                           const char* smem, char* dst,
+                                           int64_t dst_tile_base, int t) {
+  typedef typename Word<VB>::T T;
+  if (t >= a.store.n_thr) return;
+#pragma unroll
+  for (int v = 0; v < MAXV; ++v) {
+    if (v >= a.store.n_val) break;
+    int64_t go = dst_tile_base + o.store_g[v];
+    if (!a.dst_swz_tile) go = swizzle(go, a.dst_swz);
+    *reinterpret_cast<T*>(dst + go) =
+        *reinterpret_cast<const T*>(smem + o.store_s[v]);
+  }
+}
+
 }  // namespace lm_tv
 
 #endif  // LAYOUTMOVE_TV_CUH

@@ -66,6 +66,12 @@ typedef struct lm_tv_args {
   int32_t dst_swz[3];
   int32_t grid_fast;      /* n_tiles < 2^32 and every grid_ext < 2^31: tile
                              coordinates by grid_div in 32 bits             */
+  int32_t src_swz_tile;   /* 1: src_swz commutes with adding a tile base (no
+                             swizzle, or every grid stride a multiple of
+                             2^(B+M+S) bytes), so it may be applied to the
+                             in-tile offset alone                           */
+  int32_t dst_swz_tile;   /* the same for dst_swz                           */
+  int32_t offsets32;      /* 1: every in-tile byte offset fits 31 bits      */
   lm_tv_phase load;       /* source (global) -> shared tile                 */
   lm_tv_phase store;      /* shared tile -> destination (global)            */
 } lm_tv_args;

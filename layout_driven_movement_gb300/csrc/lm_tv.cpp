@@ -360,6 +360,22 @@ lm_tv_plan plan_tv(const lm_layout& src, const lm_layout& smem,
   set_swz(A.src_swz, bytes_swz(src.swz, eb));
   set_swz(A.smem_swz, bytes_swz(smem.swz, eb));
   set_swz(A.dst_swz, bytes_swz(dst.swz, eb));
+  // a swizzle reads bits [M+S, M+S+B) and writes [M, M+B): a tile base that
+  // is a multiple of 2^(B+M+S) leaves both alone
+  auto commutes = [&](const int32_t* z, bool dst_side) {
+    if (z[0] == 0) return 1;
+    const int64_t blk = int64_t(1) << (z[0] + z[1] + z[2]);
+    for (int k = 0; k < A.n_grid; ++k)
+      if ((dst_side ? A.grid_dst[k] : A.grid_src[k]) % blk) return 0;
+    return 1;
+  };
+  A.src_swz_tile = commutes(A.src_swz, false);
+  A.dst_swz_tile = commutes(A.dst_swz, true);
+  auto fits31 = [&](const std::vector<int64_t>& off) {
+    for (int64_t o : off)
+      if (o < 0 || o * eb >= (int64_t(1) << 31)) return false;
+    return true;
+  };
 
   Side S, M, D;
   S.off = tile_offsets(tsrc);
@@ -371,6 +387,7 @@ lm_tv_plan plan_tv(const lm_layout& src, const lm_layout& smem,
   D.swz = dst.swz;
   for (const JMode& m : g2) D.grid_strides.push_back(m.d);
 
+  A.offsets32 = fits31(S.off) && fits31(D.off) ? 1 : 0;
   int gl = 0, gsd = 0;
   int rc = plan_phase(S, M, n, thr_load, eb, vec_load, A.load, &gl);
   if (rc != LM_OK) fail(rc);

@@ -58,7 +58,71 @@ __global__ void __launch_bounds__(1024)
   }
 }
 
+// The same loop with every tile-invariant offset in registers (phases of
+// at most MAXV values per thread, in-tile offsets within 31 bits, blocks
+// of at most 512 threads).
+template <int VL, int VS, int MAXV>
+__global__ void __launch_bounds__(512)
+    lm_tv_cached_kernel(const __grid_constant__ lm_tv_args a,
+                        const char* __restrict__ src, char* __restrict__ dst,
+                        int two) {
+  extern __shared__ __align__(16) char tile_smem[];
+  const int t = int(threadIdx.x);
+  const int64_t step = gridDim.x;
+  int64_t tile = blockIdx.x;
+  if (tile >= a.n_tiles) return;  // whole block
+  lm_tv::Offsets<MAXV> o;
+  lm_tv::thread_offsets<MAXV>(a, lm_tv::thread_bases(a, t), o);
+  int64_t sb, db;
+  lm_tv::tile_bases(a, tile, &sb, &db);
+  if (two) {
+    lm_tv::load_tile<VL, MAXV>(a, o, src, tile_smem, sb, t);
+    lm_tv::commit_copies();
+  }
+  for (int i = 0; tile < a.n_tiles; ++i, tile += step) {
+    char* cur = tile_smem + (two ? (i & 1) * a.smem_bytes : 0);
+    const int64_t next = tile + step;
+    int64_t nsb = 0, ndb = 0;
+    if (next < a.n_tiles) lm_tv::tile_bases(a, next, &nsb, &ndb);
+    if (two) {
+      if (next < a.n_tiles)
+        lm_tv::load_tile<VL, MAXV>(
+            a, o, src, tile_smem + ((i + 1) & 1) * a.smem_bytes, nsb, t);
+      lm_tv::commit_copies();
+      lm_tv::wait_copies_but<1>();
+    } else {
+      lm_tv::load_tile<VL, MAXV>(a, o, src, cur, sb, t);
+      lm_tv::wait_copies();
+    }
+    __syncthreads();
+    lm_tv::store_tile<VS, MAXV>(a, o, cur, dst, db, t);
+    __syncthreads();
+    sb = nsb;
+    db = ndb;
+  }
+}
+
 typedef void (*TvKernel)(const lm_tv_args, const char*, char*, int);
+
+template <int VL, int MAXV>
+TvKernel pick_cached_store(int vs) {
+  switch (vs) {
+    case 4: return lm_tv_cached_kernel<VL, 4, MAXV>;
+    case 8: return lm_tv_cached_kernel<VL, 8, MAXV>;
+    case 16: return lm_tv_cached_kernel<VL, 16, MAXV>;
+  }
+  return nullptr;
+}
+
+template <int MAXV>
+TvKernel pick_cached(int vl, int vs) {
+  switch (vl) {
+    case 4: return pick_cached_store<4, MAXV>(vs);
+    case 8: return pick_cached_store<8, MAXV>(vs);
+    case 16: return pick_cached_store<16, MAXV>(vs);
+  }
+  return nullptr;
+}
 
 template <int VL>
 TvKernel pick_store(int vs) {
@@ -94,7 +158,12 @@ int launch_tv(const lm_tv_plan& plan, const char* src, char* dst,
               void* stream) {
   const lm_tv_args& a = plan.args;
   if (a.n_tiles == 0) return LM_OK;
-  TvKernel k = pick(a.load.vec_bytes, a.store.vec_bytes);
+  const int most = a.load.n_val > a.store.n_val ? a.load.n_val : a.store.n_val;
+  TvKernel k = nullptr;
+  const bool cached = a.offsets32 && a.block_threads <= 512;
+  if (cached && most <= 4)
+    k = pick_cached<4>(a.load.vec_bytes, a.store.vec_bytes);
+  if (!k) k = pick(a.load.vec_bytes, a.store.vec_bytes);
   if (!k) return LM_E_INVALID;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

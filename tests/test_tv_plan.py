@@ -48,6 +48,8 @@ class Args(C.Structure):
                 ("grid_div", FastDiv * MAXG),
                 ("src_swz", C.c_int32 * 3), ("smem_swz", C.c_int32 * 3),
                 ("dst_swz", C.c_int32 * 3), ("grid_fast", C.c_int32),
+                ("src_swz_tile", C.c_int32), ("dst_swz_tile", C.c_int32),
+                ("offsets32", C.c_int32),
                 ("load", Phase), ("store", Phase)]
 
 
@@ -107,6 +109,10 @@ def replay(a, src_bytes, dst_bytes, src_cos, dst_cos):
                 if load:
                     g = swz((sb + bf + phase.from_val[v]).astype(np.int64),
                             a.src_swz)
+                    if a.src_swz_tile:   # the swizzle commutes with the base
+                        assert (g == sb + swz(
+                            (bf + phase.from_val[v]).astype(np.int64),
+                            a.src_swz)).all()
                     s = swz((bt + phase.to_val[v]).astype(np.int64),
                             a.smem_swz)
                     cos = src_cos
@@ -115,6 +121,10 @@ def replay(a, src_bytes, dst_bytes, src_cos, dst_cos):
                             a.smem_swz)
                     g = swz((db + bt + phase.to_val[v]).astype(np.int64),
                             a.dst_swz)
+                    if a.dst_swz_tile:
+                        assert (g == db + swz(
+                            (bt + phase.to_val[v]).astype(np.int64),
+                            a.dst_swz)).all()
                     cos = dst_cos
                 # byte offsets
                 assert (g >= 0).all() and ((g + vb) <= cos * eb).all()

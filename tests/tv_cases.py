@@ -54,6 +54,15 @@ CASES = [
      ("layout", (((4, 8), 16), 12), (((128, 1), 8), 512)),
      "(8,16):(1,8)", "((4,8),4):((1,4),32)", 4,
      {"load.vec_bytes": 16, "store.vec_bytes": 4}),
+    # a destination swizzle reaching above the tile bases: applied to the
+    # whole offset per value, not folded into the in-tile offsets
+    ("tiles_wide_swizzle_bf16",
+     zd((512, 384), (384, 1), (64, 64)),
+     ("swizzle", 3, 3, 6, ("layout", (64, 64), (64, 1))),
+     ("swizzle", 2, 3, 13,
+      ("layout", ((64, 64), (8, 6)), ((64, 1), (24576, 4096)))),
+     "(32,8):(8,1)", "(32,8):(8,1)", 2,
+     {"load.vec_bytes": 16, "store.vec_bytes": 16}),
     # the layouts bench.py times on the 4096x4096 fp32 transpose, smaller
     ("bench_transpose_scalar_xor5",
      zd((320, 192), (1, 320), (64, 64)),
