@@ -15,7 +15,10 @@
 //       __syncthreads();
 //     }
 //
-// where VL / VS are a.load.vec_bytes / a.store.vec_bytes.  Thread t moves
+// where VL / VS are a.load.vec_bytes / a.store.vec_bytes.  When both phases
+// have at most MAXV values per thread and a.offsets32 is set, the overloads
+// taking an Offsets<MAXV> (filled once by thread_offsets) keep every
+// tile-invariant offset in registers instead.  Thread t moves
 // its local_partition of the grouped tile ("CUTLASS Layout可视化" §5.3):
 // value v of the load phase goes from src + Swz_src(src_base + base_from(t)
 // + from_val[v]) to smem + Swz_smem(base_to(t) + to_val[v]), all in bytes.

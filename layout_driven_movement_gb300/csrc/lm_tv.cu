@@ -6,6 +6,8 @@
 
 #include <cuda_runtime.h>
 
+#include <cstdlib>
+
 #include <map>
 #include <mutex>
 #include <utility>
@@ -60,68 +62,86 @@ __global__ void __launch_bounds__(1024)
 
 // The same loop with every tile-invariant offset in registers (phases of
 // at most MAXV values per thread, in-tile offsets within 31 bits, blocks
-// of at most 512 threads).
-template <int VL, int VS, int MAXV>
+// of at most 512 threads) and NS shared tiles: the loads of a block's next
+// NS-1 tiles are in flight while it stores the current one.  Every
+// iteration commits one group of copies (possibly empty), so waiting until
+// at most NS-1 groups are pending means the current tile has landed.
+template <int VL, int VS, int MAXV, int NS>
 __global__ void __launch_bounds__(512)
     lm_tv_cached_kernel(const __grid_constant__ lm_tv_args a,
                         const char* __restrict__ src, char* __restrict__ dst,
-                        int two) {
+                        int /*unused*/) {
   extern __shared__ __align__(16) char tile_smem[];
   const int t = int(threadIdx.x);
   const int64_t step = gridDim.x;
-  int64_t tile = blockIdx.x;
-  if (tile >= a.n_tiles) return;  // whole block
+  const int64_t first = blockIdx.x;
+  if (first >= a.n_tiles) return;  // whole block
   lm_tv::Offsets<MAXV> o;
   lm_tv::thread_offsets<MAXV>(a, lm_tv::thread_bases(a, t), o);
   int64_t sb, db;
-  lm_tv::tile_bases(a, tile, &sb, &db);
-  if (two) {
-    lm_tv::load_tile<VL, MAXV>(a, o, src, tile_smem, sb, t);
+#pragma unroll
+  for (int k = 0; k < NS - 1; ++k) {
+    const int64_t tile = first + k * step;
+    if (tile < a.n_tiles) {
+      lm_tv::tile_bases(a, tile, &sb, &db);
+      lm_tv::load_tile<VL, MAXV>(a, o, src, tile_smem + k * a.smem_bytes, sb,
+                                 t);
+    }
     lm_tv::commit_copies();
   }
-  for (int i = 0; tile < a.n_tiles; ++i, tile += step) {
-    char* cur = tile_smem + (two ? (i & 1) * a.smem_bytes : 0);
-    const int64_t next = tile + step;
-    int64_t nsb = 0, ndb = 0;
-    if (next < a.n_tiles) lm_tv::tile_bases(a, next, &nsb, &ndb);
-    if (two) {
-      if (next < a.n_tiles)
-        lm_tv::load_tile<VL, MAXV>(
-            a, o, src, tile_smem + ((i + 1) & 1) * a.smem_bytes, nsb, t);
-      lm_tv::commit_copies();
-      lm_tv::wait_copies_but<1>();
-    } else {
-      lm_tv::load_tile<VL, MAXV>(a, o, src, cur, sb, t);
-      lm_tv::wait_copies();
+  int slot = 0;  // the shared tile of the current tile
+  for (int64_t tile = first; tile < a.n_tiles; tile += step) {
+    const int64_t ahead = tile + (NS - 1) * step;
+    const int ahead_slot = slot == 0 ? NS - 1 : slot - 1;
+    if (ahead < a.n_tiles) {
+      // the slot was last read before the barrier ending the previous
+      // iteration
+      lm_tv::tile_bases(a, ahead, &sb, &db);
+      lm_tv::load_tile<VL, MAXV>(a, o, src,
+                                 tile_smem + ahead_slot * a.smem_bytes, sb, t);
     }
+    lm_tv::commit_copies();
+    lm_tv::wait_copies_but<NS - 1>();
     __syncthreads();
-    lm_tv::store_tile<VS, MAXV>(a, o, cur, dst, db, t);
+    lm_tv::tile_bases(a, tile, &sb, &db);
+    lm_tv::store_tile<VS, MAXV>(a, o, tile_smem + slot * a.smem_bytes, dst,
+                                db, t);
     __syncthreads();
-    sb = nsb;
-    db = ndb;
+    slot = slot + 1 == NS ? 0 : slot + 1;
   }
 }
 
 typedef void (*TvKernel)(const lm_tv_args, const char*, char*, int);
 
-template <int VL, int MAXV>
+template <int VL, int MAXV, int NS>
 TvKernel pick_cached_store(int vs) {
   switch (vs) {
-    case 4: return lm_tv_cached_kernel<VL, 4, MAXV>;
-    case 8: return lm_tv_cached_kernel<VL, 8, MAXV>;
-    case 16: return lm_tv_cached_kernel<VL, 16, MAXV>;
+    case 4: return lm_tv_cached_kernel<VL, 4, MAXV, NS>;
+    case 8: return lm_tv_cached_kernel<VL, 8, MAXV, NS>;
+    case 16: return lm_tv_cached_kernel<VL, 16, MAXV, NS>;
   }
   return nullptr;
 }
 
-template <int MAXV>
+template <int MAXV, int NS>
 TvKernel pick_cached(int vl, int vs) {
   switch (vl) {
-    case 4: return pick_cached_store<4, MAXV>(vs);
-    case 8: return pick_cached_store<8, MAXV>(vs);
-    case 16: return pick_cached_store<16, MAXV>(vs);
+    case 4: return pick_cached_store<4, MAXV, NS>(vs);
+    case 8: return pick_cached_store<8, MAXV, NS>(vs);
+    case 16: return pick_cached_store<16, MAXV, NS>(vs);
   }
   return nullptr;
+}
+
+// Shared tiles per block for the cached kernel: LM_TV_STAGES (2..4,
+// default 4), fewer when they do not fit.
+int tv_stages() {
+  static const int n = [] {
+    const char* e = std::getenv("LM_TV_STAGES");
+    const int v = e ? std::atoi(e) : 4;
+    return v < 2 ? 2 : (v > 4 ? 4 : v);
+  }();
+  return n;
 }
 
 template <int VL>
@@ -160,17 +180,27 @@ int launch_tv(const lm_tv_plan& plan, const char* src, char* dst,
   if (a.n_tiles == 0) return LM_OK;
   const int most = a.load.n_val > a.store.n_val ? a.load.n_val : a.store.n_val;
   TvKernel k = nullptr;
-  const bool cached = a.offsets32 && a.block_threads <= 512;
-  if (cached && most <= 4)
-    k = pick_cached<4>(a.load.vec_bytes, a.store.vec_bytes);
-  if (!k) k = pick(a.load.vec_bytes, a.store.vec_bytes);
+  int smem = 0, two = 0;
+  if (a.offsets32 && a.block_threads <= 512 && most <= 4) {
+    int ns = tv_stages();
+    while (ns > 2 && int64_t(ns) * a.smem_bytes > 232448) --ns;
+    if (2 * int64_t(a.smem_bytes) <= 232448) {
+      k = ns == 4   ? pick_cached<4, 4>(a.load.vec_bytes, a.store.vec_bytes)
+          : ns == 3 ? pick_cached<4, 3>(a.load.vec_bytes, a.store.vec_bytes)
+                    : pick_cached<4, 2>(a.load.vec_bytes, a.store.vec_bytes);
+      smem = ns * a.smem_bytes;
+    }
+  }
+  if (!k) {
+    k = pick(a.load.vec_bytes, a.store.vec_bytes);
+    // two shared tiles when they fit beside each other
+    two = 2 * int64_t(a.smem_bytes) <= 232448 && a.n_tiles > 1 ? 1 : 0;
+    smem = a.smem_bytes * (two ? 2 : 1);
+  }
   if (!k) return LM_E_INVALID;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail_cuda(e);
-  // two shared tiles when they fit beside each other
-  int two = 2 * int64_t(a.smem_bytes) <= 232448 && a.n_tiles > 1 ? 1 : 0;
-  const int smem = a.smem_bytes * (two ? 2 : 1);
   if (smem > 49152) {
     static std::mutex mu;
     static std::map<std::pair<int, const void*>, int> done;
