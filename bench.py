@@ -599,6 +599,8 @@ class OracleWindows:
         self.bufs = bufs
         self.exprs = {n: (lo.build(WORKLOADS[n].src), lo.build(WORKLOADS[n].dst))
                       for n in names}
+        for _, out in bufs.values():   # map every page before timing
+            out.fill(0)
 
     def run(self, frac: float, shift: int = 0):
         nbytes, elems = 0.0, 0
@@ -615,11 +617,20 @@ class OracleWindows:
             elems += n
         return time.perf_counter() - t0, nbytes, elems
 
-    def calibrate(self, seconds: float) -> float:
-        """Fraction of every workload that takes about `seconds`."""
-        probe = 2.0 ** -12
-        t, _, _ = self.run(probe)
-        return min(1.0, probe * seconds / max(t, 1e-4))
+    def calibrate(self, seconds: float, least: float = 2.0 ** -20) -> float:
+        """Fraction of every workload that takes about `seconds` (at least
+        `least`): two probe windows give the fixed cost and the cost per
+        fraction."""
+        p1, p2 = 2.0 ** -11, 2.0 ** -7
+        t1, _, _ = self.run(p1)
+        t2, _, _ = self.run(p2)
+        per = max((t2 - t1) / (p2 - p1), 1e-6)
+        fixed = max(t1 - per * p1, 0.0)
+        f = min(1.0, max(least, (seconds - fixed) / per))
+        # large windows cost more per element than the probes (fresh
+        # temporaries): one run at the estimate corrects it
+        t, _, _ = self.run(f)
+        return min(1.0, max(least, f * seconds / max(t, 1e-4)))
 
 
 def cpu_baseline(suite) -> dict:
@@ -627,7 +638,7 @@ def cpu_baseline(suite) -> dict:
                          np.zeros(it["dst"].numel(), dtype=np.uint8))
             for it in suite.items}
     ow = OracleWindows(BENCH_SUITE, bufs)
-    frac = ow.calibrate(12.0)
+    frac = ow.calibrate(12.0, least=2.0 ** -7)
     secs, nbytes, elems = ow.run(frac)
     return {"value": round(nbytes / secs / 1e9, 3), "unit": UNIT, "cores": 1,
             "kind": "oracle",
