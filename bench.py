@@ -301,12 +301,25 @@ def run_native(args) -> dict | None:
                 "kernel": dom_kernel + " (" + dom_name + ")",
                 "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                 if peak_kind == "measured" else "fallback 6.8 TB/s"}
+    # end to end: every rank at once, the slowest rank's time
+    e2e = None
+    if not args.quick:
+        if world > 1:
+            dist.barrier()
+        e2e = measure_e2e(suite, args, torch)
+        if world > 1:
+            t = torch.tensor([e2e["ms"]], dtype=torch.float64)
+            gathered = [torch.zeros_like(t) for _ in range(world)]
+            dist.all_gather(gathered, t)
+            e2e["ms"] = max(float(g[0]) for g in gathered)
+        e2e["value"] = round(suite.bytes_per_step * e2e["steps"] * world /
+                             (e2e["ms"] * 1e-3) / 1e9, 1)
+        del e2e["ms"]
     if rank != 0:
         return None
 
     tv = measure_tv(suite, args, torch, peak) if not args.quick else {}
     xch = measure_exchange(suite, args, torch, peak) if not args.quick else {}
-    e2e = measure_e2e(suite, args, torch) if not args.quick else None
     cpu = cpu_baseline(suite) if world == 1 and not args.quick else None
     clocks = clk.summary()
     line = {
@@ -577,8 +590,7 @@ def measure_e2e(suite, args, torch) -> dict:
     end.record(main)
     torch.cuda.synchronize()
     ms = start.elapsed_time(end)
-    val = suite.bytes_per_step * steps / (ms * 1e-3) / 1e9
-    return {"value": round(val, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+    return {"ms": ms, "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps,
             "path": "layout_copy_host per workload, one stream each"}
 
