@@ -7,10 +7,11 @@ through the C ABI:
   C3  bf16 8192x8192 -> 64x64 tiles, Swizzle<3,4,3> inside (VEC 16 B)
   C4  fp64 2^20 padded 8x8 tiles gathered into TV order    (STAGED)
   C5a fp16 NHWC (64,56,56,256) -> NCHW                     (STAGED)
-  C5b fp16 (2,16384,128) head-major -> stride-2 interleave (STAGED)
+  C5b fp16 (2,16384,128) head-major -> stride-2 interleave (ZIP)
 
-value = algorithmic bytes (read + written, SURVEY 8(d) per workload) over
-the summed CUDA-event time of the copies, on the launching stream.  The five
+value = algorithmic bytes (every element read and written once; C4's
+source also counts its pad slots, which share DRAM sectors with the data)
+over the CUDA-event time of the steps, on the launching stream.  The five
 buffer pairs (1.87 GB per step) are each reused only after > 1.6 GB of other
 traffic, larger than the 126 MiB L2, so no explicit flush is done.
 
@@ -42,7 +43,8 @@ from workloads import BENCH_SUITE, WORKLOADS, seeded_bytes  # noqa: E402
 METRIC = ("layout_copy GB/s (read+write) and % of GB300 HBM peak; "
           "bit-exact vs CPU oracle")
 UNIT = "GB/s"
-# algorithmic bytes per copy (read + written), SURVEY 8(d)
+# algorithmic bytes per copy (read + written; C4 reads 72 source slots per
+# 64-element tile)
 ALGO_BYTES = {"C2": 134_217_728, "C3": 268_435_456, "C4": 1_140_850_688,
               "C5a": 205_520_896, "C5b": 16_777_216}
 DOMINANT = "C4"          # largest share of the step: lm_bulk_kernel<8>
