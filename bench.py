@@ -545,26 +545,42 @@ def measure_exchange(suite, args, torch, peak, world=4) -> dict:
             "frac_of_peak": round(gbs / peak, 4)}
 
 
-def measure_e2e(suite, args, torch) -> dict:
+def measure_e2e(suite, args, torch, shards=4) -> dict:
     """The same metric through the public API with host buffers: every step
-    runs layout_copy_host for each workload -- upload of its source from
-    pinned host memory, the copy, download of its destination into pinned
-    host memory -- each workload on its own stream, so one workload's
-    upload overlaps another's download on the two directions of the host
-    link."""
+    runs layout_copy_host -- upload of the source from pinned host memory,
+    the copy, download of the destination into pinned host memory -- for
+    every workload, each on its own stream so uploads and downloads share
+    the two directions of the host link.  A workload whose shards
+    (Plan(..., rank, world)) own disjoint source and destination ranges runs
+    as `shards` shards, each moving only its ranges, so its transfers spread
+    over several copy engines."""
     steps = max(2, min(args.steps, 5))
-    hs = [torch.from_numpy(it["host"]).pin_memory() for it in suite.items]
-    hd = [torch.empty(it["dst"].numel(), dtype=torch.uint8).pin_memory()
-          for it in suite.items]
-    h2d = sum(h.numel() for h in hs)
-    d2h = sum(h.numel() for h in hd)
     lm = suite.lm
+    jobs, h2d, d2h, sharded = [], 0, 0, []
+    for it in suite.items:
+        hs = torch.from_numpy(it["host"]).pin_memory()
+        hd = torch.empty(it["dst"].numel(), dtype=torch.uint8).pin_memory()
+        eb = it["w"].elem_bytes
+        plans = [lm.Plan(it["S"], it["D"], eb, rank=r, world=shards)
+                 for r in range(shards)]
+        descs = [p.describe() for p in plans]
+        src_moved = sum(d["src_range"][1] - d["src_range"][0] for d in descs)
+        if not all(d["dst_own"] for d in descs) or src_moved > it["S"].cosize:
+            plans, descs = [it["plan"]], [it["plan"].describe()]
+        else:
+            sharded.append(it["name"])
+        for p, d in zip(plans, descs):
+            jobs.append((p, hs, hd, it["src"], it["dst"]))
+            whole = len(plans) == 1
+            h2d += hs.numel() if whole else (d["src_range"][1] -
+                                             d["src_range"][0]) * eb
+            d2h += (d["dst_range"][1] - d["dst_range"][0]) * eb
     main = torch.cuda.current_stream()
-    streams = [torch.cuda.Stream() for _ in suite.items]
+    streams = [torch.cuda.Stream() for _ in jobs]
 
     def one():
-        for it, a, b, st in zip(suite.items, hs, hd, streams):
-            lm.layout_copy_host(it["plan"], a, b, it["src"], it["dst"], st)
+        for (p, hs, hd, sdev, ddev), st in zip(jobs, streams):
+            lm.layout_copy_host(p, hs, hd, sdev, ddev, st)
 
     def fork():
         ev = torch.cuda.Event()
@@ -594,7 +610,9 @@ def measure_e2e(suite, args, torch) -> dict:
     ms = start.elapsed_time(end)
     return {"ms": ms, "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps,
-            "path": "layout_copy_host per workload, one stream each"}
+            "path": f"layout_copy_host, {len(jobs)} plans on their own "
+                    f"streams ({', '.join(sharded) or 'none'} as {shards} "
+                    "shards each)"}
 
 
 # --------------------------------------------------------------------------

@@ -300,7 +300,11 @@ int lm_plan_copy(const lm_layout* src, const lm_layout* dst, int elem_bytes,
 int lm_plan_copy_shard(const lm_layout* src, const lm_layout* dst,
                        int elem_bytes, int rank, int world, lm_plan** out);
 
-/* One-line JSON description: pieces, path, modes, vector width, tile. */
+/* One-line JSON description: pieces, path, modes, vector width, tile; the
+ * element ranges of src and dst the copy can reach ("src_range",
+ * "dst_range": [0, cosize) for a whole copy, the shard's own for a shard)
+ * and whether no other shard writes inside the destination range
+ * ("dst_own"). */
 int lm_plan_describe(const lm_plan* plan, char* buf, size_t cap);
 
 /* Elements of src and dst that the plan reads and writes (sizes of their
@@ -330,10 +334,15 @@ int lm_layout_copy(const lm_plan* plan, const void* src_dev,
  * lm_layout_copy between the staging buffers, and the download of the
  * destination's [0, cosize) into dst_host.  When the destination layout
  * does not cover every slot below its cosize, the host destination is
- * uploaded first, so slots outside the image come back unchanged.  Host
- * buffers should be page-locked for the transfers to be asynchronous.
- * Allocates nothing.  Errors: as lm_layout_copy (the staging buffers are
- * the device buffers it checks), LM_E_CUDA for a failed transfer. */
+ * uploaded first, so slots outside the image come back unchanged.  A shard
+ * (lm_plan_copy_shard) moves only the ranges its pieces reach
+ * ("src_range" / "dst_range" of its description), so the shards of one
+ * copy may run on separate streams over the same host and staging buffers
+ * -- provided each owns its destination range ("dst_own"); a shard that
+ * does not is refused with LM_E_INVALID.  Host buffers should be
+ * page-locked for the transfers to be asynchronous.  Allocates nothing.
+ * Errors: as lm_layout_copy (the staging buffers are the device buffers it
+ * checks), LM_E_INVALID, LM_E_CUDA for a failed transfer. */
 int lm_layout_copy_host(const lm_plan* plan, const void* src_host,
                         int64_t src_capacity_elems, void* dst_host,
                         int64_t dst_capacity_elems, void* src_dev,

@@ -295,6 +295,10 @@ struct lm_plan {
   lm::Swz s_swz, d_swz;  // elements
   bool joint = true;
   std::vector<lm::Piece> pieces;
+  // element ranges the copy can touch, [lo, hi): [0, cosize) unless the
+  // plan is a shard (lm_plan_copy_shard) of a joint pair
+  int64_t src_lo = 0, src_hi = 0, dst_lo = 0, dst_hi = 0;
+  bool dst_own = true;  // no other shard writes inside [dst_lo, dst_hi)
   std::string describe;
 };
 

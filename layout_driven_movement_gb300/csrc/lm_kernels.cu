@@ -1383,16 +1383,29 @@ int lm_layout_copy_host(const lm_plan* plan, const void* src_host,
     if (src_capacity_elems < plan->src_cosize ||
         dst_capacity_elems < plan->dst_cosize)
       return LM_E_CAPACITY;
+    // a shard whose destination range holds other shards' elements cannot
+    // download it without racing them
+    if (!plan->dst_own) return LM_E_INVALID;
     const int64_t eb = plan->eb;
     cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
-    const size_t in_bytes = size_t(lm::mul_chk(src_capacity_elems, eb));
-    const size_t out_bytes = size_t(lm::mul_chk(plan->dst_cosize, eb));
-    cudaError_t e =
-        cudaMemcpyAsync(src_dev, src_host, in_bytes, cudaMemcpyHostToDevice, st);
+    // a whole plan moves [0, capacity) up and [0, cosize) down; a shard
+    // only the ranges its pieces reach
+    const bool whole = plan->src_lo == 0 && plan->src_hi == plan->src_cosize;
+    const int64_t in_lo = whole ? 0 : plan->src_lo;
+    const int64_t in_hi = whole ? src_capacity_elems : plan->src_hi;
+    const int64_t out_lo = plan->dst_lo, out_hi = plan->dst_hi;
+    const size_t in_bytes = size_t(lm::mul_chk(in_hi - in_lo, eb));
+    const size_t out_bytes = size_t(lm::mul_chk(out_hi - out_lo, eb));
+    char* sd = static_cast<char*>(src_dev) + in_lo * eb;
+    const char* sh = static_cast<const char*>(src_host) + in_lo * eb;
+    char* dd = static_cast<char*>(dst_dev) + out_lo * eb;
+    char* dh = static_cast<char*>(dst_host) + out_lo * eb;
+    cudaError_t e = cudaSuccess;
+    if (in_bytes)
+      e = cudaMemcpyAsync(sd, sh, in_bytes, cudaMemcpyHostToDevice, st);
     // a destination with slots outside its image round-trips them
-    if (e == cudaSuccess && plan->size < plan->dst_cosize)
-      e = cudaMemcpyAsync(dst_dev, dst_host, out_bytes, cudaMemcpyHostToDevice,
-                          st);
+    if (e == cudaSuccess && out_bytes && plan->size < plan->dst_cosize)
+      e = cudaMemcpyAsync(dd, dh, out_bytes, cudaMemcpyHostToDevice, st);
     if (e != cudaSuccess) {
       lm::set_cuda_error(int(e));
       return LM_E_CUDA;
@@ -1400,8 +1413,8 @@ int lm_layout_copy_host(const lm_plan* plan, const void* src_host,
     const int rc = lm_layout_copy(plan, src_dev, src_capacity_elems, dst_dev,
                                   dst_capacity_elems, cuda_stream);
     if (rc != LM_OK) return rc;
-    e = cudaMemcpyAsync(dst_host, dst_dev, out_bytes, cudaMemcpyDeviceToHost,
-                        st);
+    if (out_bytes)
+      e = cudaMemcpyAsync(dh, dd, out_bytes, cudaMemcpyDeviceToHost, st);
     if (e != cudaSuccess) {
       lm::set_cuda_error(int(e));
       return LM_E_CUDA;

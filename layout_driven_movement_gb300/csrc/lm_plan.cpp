@@ -1142,7 +1142,11 @@ static void plan_box(lm_plan& P, std::vector<JMode> ms, int64_t s_base,
 static std::string describe(const lm_plan& P) {
   std::ostringstream os;
   os << "{\"size\":" << P.size << ",\"elem_bytes\":" << P.eb
-     << ",\"joint\":" << (P.joint ? "true" : "false") << ",\"pieces\":[";
+     << ",\"joint\":" << (P.joint ? "true" : "false")
+     << ",\"src_range\":[" << P.src_lo << ',' << P.src_hi
+     << "],\"dst_range\":[" << P.dst_lo << ',' << P.dst_hi
+     << "],\"dst_own\":" << (P.dst_own ? "true" : "false")
+     << ",\"pieces\":[";
   for (size_t i = 0; i < P.pieces.size(); ++i) {
     const Piece& pc = P.pieces[i];
     if (i) os << ',';
@@ -1359,6 +1363,7 @@ static int plan_copy_impl(const lm_layout* src, const lm_layout* dst,
     P->d_swz = dst->swz;
     // byte offsets must fit int64
     mul_chk(std::max(P->src_cosize, P->dst_cosize), elem_bytes);
+    bool dst_own = false;
     if (P->size > 0) {
       if (!affine_injective(dst->leaves)) fail(LM_E_NOT_INJECTIVE);
       std::vector<JMode> jm;
@@ -1382,6 +1387,19 @@ static int plan_copy_impl(const lm_layout* src, const lm_layout* dst,
           const int64_t lo = e * rank / world, hi = e * (rank + 1) / world;
           s_base = mul_chk(lo, jm[k].s);
           d_base = mul_chk(lo, jm[k].d);
+          // the shard owns [lo*D, hi*D) of the destination when every
+          // other mode fits inside one step D of the split mode and the
+          // boundaries fall on whole 16-byte chunks and swizzle blocks
+          int64_t span = 1;
+          for (size_t j = 0; j < jm.size(); ++j)
+            if (j != k) span = add_chk(span, mul_chk(jm[j].e - 1, jm[j].d));
+          int64_t blk = std::max<int64_t>(1, 16 / elem_bytes);
+          if (P->d_swz.on())
+            blk = std::max(blk, int64_t(1) << (P->d_swz.b + P->d_swz.m +
+                                               P->d_swz.s));
+          const int64_t D = jm[k].d;
+          dst_own = span <= D && mul_chk(lo, D) % blk == 0 &&
+                    (hi == e || mul_chk(hi, D) % blk == 0);
           jm[k].e = hi - lo;
         }
         plan_box(*P, jm, s_base, d_base, 0);
@@ -1400,6 +1418,43 @@ static int plan_copy_impl(const lm_layout* src, const lm_layout* dst,
           if (uint64_t(hi) >= (uint64_t(1) << 31)) pc.gen.wide = 1;
           P->pieces.push_back(std::move(pc));
         }
+      }
+    }
+    P->src_lo = P->dst_lo = 0;
+    P->src_hi = P->src_cosize;
+    P->dst_hi = P->dst_cosize;
+    P->dst_own = world == 1 || dst_own;
+    if (P->joint && world > 1) {
+      // the offsets the pieces reach, widened to whole swizzle blocks and
+      // to 16-byte chunks (the loads move whole chunks)
+      int64_t slo = P->src_cosize, shi = 0, dlo = P->dst_cosize, dhi = 0;
+      for (const Piece& pc : P->pieces) {
+        int64_t sa = pc.s_base, sb = pc.s_base, da = pc.d_base, db = pc.d_base;
+        for (const JMode& m : pc.modes) {
+          sb = add_chk(sb, mul_chk(m.e - 1, m.s));
+          db = add_chk(db, mul_chk(m.e - 1, m.d));
+        }
+        slo = std::min(slo, sa);
+        shi = std::max(shi, sb + 1);
+        dlo = std::min(dlo, da);
+        dhi = std::max(dhi, db + 1);
+      }
+      auto widen = [&](int64_t& lo, int64_t& hi, const Swz& z, int64_t cos) {
+        int64_t blk = std::max<int64_t>(1, 16 / elem_bytes);
+        if (z.on()) blk = std::max(blk, int64_t(1) << (z.b + z.m + z.s));
+        lo = lo / blk * blk;
+        hi = std::min(cos, (hi + blk - 1) / blk * blk);
+        if (lo >= hi) lo = hi = 0;
+      };
+      if (!P->pieces.empty()) {
+        widen(slo, shi, P->s_swz, P->src_cosize);
+        widen(dlo, dhi, P->d_swz, P->dst_cosize);
+        P->src_lo = slo;
+        P->src_hi = shi;
+        P->dst_lo = dlo;
+        P->dst_hi = dhi;
+      } else {
+        P->src_hi = P->dst_hi = 0;
       }
     }
     P->describe = describe(*P);

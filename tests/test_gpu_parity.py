@@ -453,3 +453,36 @@ def test_copy_beyond_2_to_32_elements_sampled():
     got = raw[torch.from_numpy(do).cuda()].cpu().numpy()
     assert (got == inp[so]).all()
     assert (raw[n:].cpu().numpy() == GUARD_FILL).all()
+
+
+def test_copy_host_buffers_by_shards_on_streams():
+    """Shards of one copy (lm_plan_copy_shard), each through
+    lm_layout_copy_host on its own stream over shared host and device
+    buffers: each moves only its own ranges and together they give the
+    oracle's result.  A shard whose destination range is not its own is
+    refused."""
+    _, s, d, eb = {c[0]: c for c in SMALL}["padded_tv_gather_f64"]
+    S, D = lm.build_layout(s), lm.build_layout(d)
+    inp = seeded_bytes("bytes", "uint8", S.cosize * eb, 41)
+    want = np.full(D.cosize * eb, 0x3C, dtype=np.uint8)
+    lo.copy(lo.build(s), lo.build(d), inp, want, eb)
+    hs = torch.from_numpy(inp).pin_memory()
+    hd = torch.from_numpy(np.full(D.cosize * eb, 0x3C, np.uint8)).pin_memory()
+    sd = torch.full((S.cosize * eb,), 0x11, dtype=torch.uint8, device="cuda")
+    dd = torch.full((D.cosize * eb,), 0x22, dtype=torch.uint8, device="cuda")
+    plans = [lm.Plan(S, D, eb, rank=r, world=3) for r in range(3)]
+    assert all(p.describe()["dst_own"] for p in plans)
+    streams = [torch.cuda.Stream() for _ in plans]
+    for p, st in zip(plans, streams):
+        lm.layout_copy_host(p, hs, hd, sd, dd, st)
+    torch.cuda.synchronize()
+    assert np.array_equal(hd.numpy(), want)
+    A = lm.Layout.parse("(4,100):(100,1)")
+    shared = lm.Plan(A, A, 4, rank=1, world=8)
+    assert not shared.describe()["dst_own"]
+    with pytest.raises(lm.LayoutMoveError) as e:
+        lm.layout_copy_host(shared, torch.zeros(400).pin_memory(),
+                            torch.zeros(400).pin_memory(),
+                            torch.zeros(400, device="cuda"),
+                            torch.zeros(400, device="cuda"))
+    assert e.value.status == -1

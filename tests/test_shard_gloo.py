@@ -139,3 +139,31 @@ def test_two_ranks_over_gloo():
     for p in procs:
         p.join(timeout=60)
     assert results == {0: "ok", 1: "ok"}, results
+
+
+def test_shard_ranges_and_ownership():
+    """A shard's described source and destination ranges hold every offset
+    its pieces reach; where the shards own their destination ranges, those
+    ranges are disjoint and tile [0, cosize)."""
+    from workloads import WORKLOADS as W
+    for name in ["C2", "C3", "C4", "C5a", "C5b"]:
+        w = W[name]
+        S, D = lm.build_layout(w.src), lm.build_layout(w.dst)
+        descs = [lm.Plan(S, D, w.elem_bytes, rank=r, world=4).describe()
+                 for r in range(4)]
+        for r, d in enumerate(descs):
+            pairs = shard_pairs(w.src, w.dst, w.elem_bytes, r, 4) \
+                if name == "C2" else None
+            if pairs is not None and len(pairs):
+                assert d["src_range"][0] <= pairs[:, 0].min()
+                assert pairs[:, 0].max() < d["src_range"][1]
+                assert d["dst_range"][0] <= pairs[:, 1].min()
+                assert pairs[:, 1].max() < d["dst_range"][1]
+        if all(d["dst_own"] for d in descs):
+            rng = sorted(tuple(d["dst_range"]) for d in descs)
+            assert rng[0][0] == 0 and rng[-1][1] == D.cosize
+            for a, b in zip(rng, rng[1:]):
+                assert a[1] == b[0]
+    whole = lm.Plan(lm.Layout.parse("(8,8):(1,8)"),
+                    lm.Layout.parse("(8,8):(8,1)"), 4).describe()
+    assert whole["src_range"] == [0, 64] and whole["dst_own"]
