@@ -308,7 +308,7 @@ def run_native(args) -> dict | None:
     if not args.quick:
         if world > 1:
             dist.barrier()
-        e2e = measure_e2e(suite, args, torch)
+        e2e = measure_e2e(suite, args, torch, shards=args.e2e_shards)
         if world > 1:
             t = torch.tensor([e2e["ms"]], dtype=torch.float64)
             gathered = [torch.zeros_like(t) for _ in range(world)]
@@ -733,6 +733,8 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workloads", default="",
                     help="comma-separated subset of the suite (profiling)")
+    ap.add_argument("--e2e-shards", type=int, default=4,
+                    help="shards per workload in the end-to-end figure")
     ap.add_argument("--quick", action="store_true",
                     help="skip the clock sampler, e2e and CPU legs (profiling)")
     args = ap.parse_args()
