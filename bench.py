@@ -320,6 +320,7 @@ def run_native(args) -> dict | None:
     if rank != 0:
         return None
 
+    ceiling = measure_d2d(suite, torch) if not args.quick else None
     tv = measure_tv(suite, args, torch, peak) if not args.quick else {}
     xch = measure_exchange(suite, args, torch, peak) if not args.quick else {}
     cpu = cpu_baseline(suite) if world == 1 and not args.quick else None
@@ -342,6 +343,7 @@ def run_native(args) -> dict | None:
             "breakdown": "per_config: a second pass of " + str(k2) +
                          " steps with CUDA events around every copy",
             "per_config": per_cfg,
+            "d2d_copy_ceiling_gbs": ceiling,
             "tv_copy": tv,
             "exchange": xch,
         },
@@ -400,6 +402,29 @@ def measured_traffic(kernel: str):
         return rec["dram_bytes_per_launch"]
     except Exception:
         return None
+
+
+def measure_d2d(suite, torch) -> float:
+    """The practical ceiling on this GPU now: a plain device-to-device copy
+    (cudaMemcpyAsync through torch) moving the suite's bytes per step --
+    half of them read, half written -- timed like the suite, median of 30."""
+    n = suite.bytes_per_step // 2
+    a = torch.empty(n, dtype=torch.uint8, device=suite.items[0]["src"].device)
+    b = torch.empty_like(a)
+    for _ in range(3):
+        b.copy_(a)
+    times = []
+    for _ in range(30):
+        e0, e1 = (torch.cuda.Event(enable_timing=True),
+                  torch.cuda.Event(enable_timing=True))
+        e0.record()
+        b.copy_(a)
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    ms = statistics.median(times)
+    del a, b
+    return round(2 * n / (ms * 1e-3) / 1e9, 1)
 
 
 def measure_tv(suite, args, torch, peak) -> dict:
