@@ -271,6 +271,7 @@ def run_native(args) -> dict | None:
     value = suite.bytes_per_step * args.steps * world / (total_ms * 1e-3) / 1e9
 
     peak, peak_kind = peaks()
+    iso = isolated_times(suite, torch) if not args.quick else {}
     per_cfg = {}
     for it in suite.items:
         ms = statistics.median(per[it["name"]])
@@ -290,6 +291,12 @@ def run_native(args) -> dict | None:
                 minus=("bank_read_wavefronts", "bank_read_wavefronts_ideal")),
             "bytes": it["bytes"], "median_us": round(ms * 1e3, 2),
             "gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4)}
+        if it["name"] in iso:
+            ims = iso[it["name"]]
+            igbs = it["bytes"] / (ims * 1e-3) / 1e9
+            per_cfg[it["name"]].update({
+                "isolated_us": round(ims * 1e3, 2),
+                "isolated_frac_of_peak": round(igbs / peak, 4)})
     dom_name = DOMINANT if DOMINANT in per else suite.items[0]["name"]
     dom_item = next(it for it in suite.items if it["name"] == dom_name)
     dom_kernel = kernel_name(dom_item["plan"], dom_item["w"].elem_bytes)
@@ -402,6 +409,31 @@ def measured_traffic(kernel: str):
         return rec["dram_bytes_per_launch"]
     except Exception:
         return None
+
+
+def isolated_times(suite, torch, runs=20) -> dict:
+    """Each copy alone: L2 flushed (a 512 MiB write) before every run, the
+    copy timed by events around it, median over `runs` (ms) -- the kernel
+    without its neighbours' write-backs and launch overlap."""
+    dev = suite.items[0]["src"].device
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    lm = suite.lm
+    out = {}
+    for it in suite.items:
+        times = []
+        for r in range(runs + 3):
+            flush.fill_(r & 255)
+            e0, e1 = (torch.cuda.Event(enable_timing=True),
+                      torch.cuda.Event(enable_timing=True))
+            e0.record()
+            lm.layout_copy(it["plan"], it["src"], it["dst"])
+            e1.record()
+            torch.cuda.synchronize()
+            if r >= 3:
+                times.append(e0.elapsed_time(e1))
+        out[it["name"]] = statistics.median(times)
+    del flush
+    return out
 
 
 def measure_d2d(suite, torch) -> float:
