@@ -412,17 +412,19 @@ def measured_traffic(kernel: str):
 
 
 def isolated_times(suite, torch, runs=20) -> dict:
-    """Each copy alone: L2 flushed (a 512 MiB write) before every run, the
-    copy timed by events around it, median over `runs` (ms) -- the kernel
-    without its neighbours' write-backs and launch overlap."""
+    """Each copy alone: L2 flushed before every run by reading a 512 MiB
+    buffer (which writes back the previous copy's dirty lines and leaves
+    only clean ones), the copy timed by events around it, median over
+    `runs` (ms) -- the kernel without its neighbours' write-backs and launch
+    overlap."""
     dev = suite.items[0]["src"].device
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    flush = torch.ones(512 << 20, dtype=torch.uint8, device=dev)
     lm = suite.lm
     out = {}
     for it in suite.items:
         times = []
         for r in range(runs + 3):
-            flush.fill_(r & 255)
+            flush.max()
             e0, e1 = (torch.cuda.Event(enable_timing=True),
                       torch.cuda.Event(enable_timing=True))
             e0.record()
