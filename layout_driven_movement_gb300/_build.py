@@ -1,9 +1,10 @@
 """Compile the layoutmove shared library in place.
 
-Three translation units -- the host layout algebra and the planner (plain
-C++17, compiled with g++) and the kernels (CUDA, compiled with nvcc for
-sm_103a only) -- are built in parallel into ``_build/`` and linked into
-``liblayoutmove.so`` next to this file.  The CUDA runtime is linked
+Every translation unit under ``csrc/`` -- the host layout algebra, the
+copy, tile-copy and exchange planners (plain C++17, compiled with g++) and
+the kernels (CUDA, compiled with nvcc for sm_103a only) -- is built in
+parallel into ``_build/`` and linked into ``liblayoutmove.so`` next to this
+file.  The CUDA runtime is linked
 statically, so the library loads without any other CUDA shared object.
 """
 
