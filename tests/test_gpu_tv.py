@@ -185,3 +185,34 @@ def test_consumer_kernel_built_apart_uses_the_building_block(tmp_path):
     assert rc == 0
     torch.cuda.synchronize()
     assert np.array_equal(dst.cpu().numpy(), want)
+
+
+def test_random_tv_cases_on_device():
+    """The randomized cases of the host replay (random tiles, padded and
+    swizzled shared layouts, thread layouts, element sizes), run on the
+    device and compared byte for byte with the oracle."""
+    import test_tv_plan as hp
+    rng = np.random.default_rng(2024)
+    ran = 0
+    for _ in range(40):
+        case = hp._random_tv_case(rng)
+        src_t, dst_t, tile, smem_t, swz, tl, ts, eb = case
+        smem = ("layout",) + _parse_pair(smem_t)
+        if swz:
+            smem = ("swizzle",) + tuple(swz) + (smem,)
+        src = ("zipped_divide", ("layout",) + _parse_pair(src_t), tile)
+        dst = ("zipped_divide", ("layout",) + _parse_pair(dst_t), tile)
+        try:
+            run_tv(src, smem, dst, tl, ts, eb, seed=ran)
+        except lm.LayoutMoveError as e:
+            assert e.status in (-1, -3)
+            continue
+        ran += 1
+    assert ran >= 12
+
+
+def _parse_pair(text):
+    """'(a,b):(c,d)' -> ((a, b), (c, d))"""
+    sh, st = text.split(":")
+    return (tuple(int(v) for v in sh.strip("()").split(",")),
+            tuple(int(v) for v in st.strip("()").split(",")))
