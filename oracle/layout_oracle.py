@@ -471,9 +471,10 @@ def stripmined_offset(thread_id, k_row: int, pitch: int, strips: int):
 # ---------------------------------------------------------------------------
 
 def thread_coordinate(thr: Layout, thr_idx: int) -> list[int]:
-    """The per-mode coordinate (a 1-D index into each top mode of thr) that
-    the thread layout maps to thread number thr_idx, found by trying every
-    coordinate.  thr must reach thr_idx exactly once."""
+    """§5.3: the thread layout maps a coordinate to a thread number; this
+    is the per-mode coordinate (a 1-D index into each top mode of thr) that
+    it maps to thread number thr_idx, found by trying every coordinate.
+    thr must reach thr_idx exactly once."""
     hits = np.nonzero(thr.at(np.arange(thr.size)) == thr_idx)[0]
     if len(hits) != 1:
         raise ValueError("the thread layout must reach the thread once")
