@@ -328,6 +328,7 @@ def run_native(args) -> dict | None:
         return None
 
     ceiling = measure_d2d(suite, torch) if not args.quick else None
+    other = measure_eval_and_generic(suite, torch, peak) if not args.quick else {}
     tv = measure_tv(suite, args, torch, peak) if not args.quick else {}
     xch = measure_exchange(suite, args, torch, peak) if not args.quick else {}
     cpu = cpu_baseline(suite) if world == 1 and not args.quick else None
@@ -351,6 +352,7 @@ def run_native(args) -> dict | None:
                          " steps with CUDA events around every copy",
             "per_config": per_cfg,
             "d2d_copy_ceiling_gbs": ceiling,
+            "other_kernels": other,
             "tv_copy": tv,
             "exchange": xch,
         },
@@ -435,6 +437,61 @@ def isolated_times(suite, torch, runs=20) -> dict:
                 times.append(e0.elapsed_time(e1))
         out[it["name"]] = statistics.median(times)
     del flush
+    return out
+
+
+def _timed(torch, fn, runs=20, flush=None):
+    """Median event time (ms) of fn, L2 flushed by a read before each run."""
+    times = []
+    for r in range(runs + 3):
+        if flush is not None:
+            flush.max()
+        e0, e1 = (torch.cuda.Event(enable_timing=True),
+                  torch.cuda.Event(enable_timing=True))
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        if r >= 3:
+            times.append(e0.elapsed_time(e1))
+    return statistics.median(times)
+
+
+def measure_eval_and_generic(suite, torch, peak) -> dict:
+    """The two kernels the suite does not time.  layout_eval: the offset
+    table of the padded TV source layout (75.5 M entries, int64: 604 MB
+    written).  GENERIC: a 6000x7000 fp32 relayout whose two layouts have no
+    common refinement (6000 and 7000 do not nest), so it runs one element
+    per thread with a full decomposition on each side."""
+    lm = suite.lm
+    dev = suite.items[0]["src"].device
+    flush = torch.ones(512 << 20, dtype=torch.uint8, device=dev)
+    out = {}
+    it = next((i for i in suite.items if i["name"] == "C4"), None)
+    if it is not None:
+        L = it["S"]
+        table = torch.empty(L.size, dtype=torch.int64, device=dev)
+        ms = _timed(torch, lambda: lm.layout_eval_device(L, table),
+                    flush=flush)
+        gbs = L.size * 8 / (ms * 1e-3) / 1e9
+        out["layout_eval"] = {
+            "workload": "offset table of the padded TV source layout, "
+                        f"{L.size} int64 entries", "median_us": round(ms * 1e3, 2),
+            "gbs_written": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4)}
+        del table
+    S = lm.Layout.parse("(6000,7000):(7000,1)")
+    D = lm.Layout.parse("(7000,6000):(1,7000)")
+    plan = lm.Plan(S, D, 4)
+    a = torch.empty(S.cosize * 4, dtype=torch.uint8, device=dev)
+    b = torch.empty(D.cosize * 4, dtype=torch.uint8, device=dev)
+    ms = _timed(torch, lambda: lm.layout_copy(plan, a, b), flush=flush)
+    gbs = 2 * S.size * 4 / (ms * 1e-3) / 1e9
+    out["generic"] = {
+        "workload": "6000x7000 fp32 between layouts with no common "
+                    "refinement", "path": plan.describe()["pieces"][0]["path"],
+        "median_us": round(ms * 1e3, 2), "gbs": round(gbs, 1),
+        "frac_of_peak": round(gbs / peak, 4)}
+    del a, b, flush
     return out
 
 

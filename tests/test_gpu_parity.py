@@ -486,3 +486,28 @@ def test_copy_host_buffers_by_shards_on_streams():
                             torch.zeros(400, device="cuda"),
                             torch.zeros(400, device="cuda"))
     assert e.value.status == -1
+
+
+def test_generic_without_common_refinement_full_size_sampled():
+    """The 6000x7000 fp32 pair bench.py times on the GENERIC path (no
+    common refinement: 6000 and 7000 do not nest), checked at 200000
+    seeded logical indices computed one by one by the oracle, plus the
+    guard band."""
+    src_t, dst_t = "(6000,7000):(7000,1)", "(7000,6000):(1,7000)"
+    S, D = lm.Layout.parse(src_t), lm.Layout.parse(dst_t)
+    plan = lm.Plan(S, D, 4)
+    assert [p["path"] for p in plan.describe()["pieces"]] == ["GENERIC"]
+    n = S.size
+    inp = seeded_bytes("bytes", "uint8", S.cosize * 4, 13)
+    src = torch.from_numpy(inp).cuda()
+    raw = torch.full((D.cosize * 4 + GUARD,), GUARD_FILL, dtype=torch.uint8,
+                     device="cuda")
+    lm.layout_copy(plan, src, raw[:D.cosize * 4])
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(8)
+    i = np.concatenate([rng.integers(0, n, 200000), [0, n - 1]])
+    so, do = lo.parse(src_t).at(i), lo.parse(dst_t).at(i)
+    got = raw[:D.cosize * 4].view(torch.int32)[torch.from_numpy(do).cuda()]
+    want = inp.view(np.int32)[so]
+    assert (got.cpu().numpy() == want).all()
+    assert (raw[D.cosize * 4:].cpu().numpy() == GUARD_FILL).all()
