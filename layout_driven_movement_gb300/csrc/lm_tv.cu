@@ -62,72 +62,50 @@ __global__ void __launch_bounds__(1024)
 
 // The same loop with every tile-invariant offset in registers (phases of
 // at most MAXV values per thread, in-tile offsets within 31 bits, blocks
-// of at most 512 threads), moving TP consecutive tiles per step between
-// two barriers, with NS steps of shared tiles: the loads of a block's next
-// NS-1 steps are in flight while it stores the current one.  Every
+// of at most 512 threads), with NS shared tiles: the loads of a block's
+// next NS-1 tiles are in flight while it stores the current one.  Every
 // iteration commits one group of copies (possibly empty), so waiting until
-// at most NS-1 groups are pending means the current step has landed.
-template <int VL, int VS, int MAXV, int NS, int TP>
+// at most NS-1 groups are pending means the current tile has landed.
+template <int VL, int VS, int MAXV, int NS>
 __global__ void __launch_bounds__(512)
     lm_tv_cached_kernel(const __grid_constant__ lm_tv_args a,
                         const char* __restrict__ src, char* __restrict__ dst,
                         int /*unused*/) {
   extern __shared__ __align__(16) char tile_smem[];
   const int t = int(threadIdx.x);
-  const int64_t n_steps = (a.n_tiles + TP - 1) / TP;
   const int64_t stride = gridDim.x;
   const int64_t first = blockIdx.x;
-  if (first >= n_steps) return;  // whole block
+  if (first >= a.n_tiles) return;  // whole block
   lm_tv::Offsets<MAXV> o;
   lm_tv::thread_offsets<MAXV>(a, lm_tv::thread_bases(a, t), o);
+  int64_t sb, db;
 #pragma unroll
   for (int k = 0; k < NS - 1; ++k) {
-    const int64_t step = first + k * stride;
-    if (step < n_steps) {
-#pragma unroll
-      for (int j = 0; j < TP; ++j) {
-        const int64_t tile = step * TP + j;
-        if (tile < a.n_tiles) {
-          int64_t sb, db;
-          lm_tv::tile_bases(a, tile, &sb, &db);
-          lm_tv::load_tile<VL, MAXV>(
-              a, o, src, tile_smem + (k * TP + j) * a.smem_bytes, sb, t);
-        }
-      }
+    const int64_t tile = first + k * stride;
+    if (tile < a.n_tiles) {
+      lm_tv::tile_bases(a, tile, &sb, &db);
+      lm_tv::load_tile<VL, MAXV>(a, o, src, tile_smem + k * a.smem_bytes, sb,
+                                 t);
     }
     lm_tv::commit_copies();
   }
-  int slot = 0;  // the shared tiles of the current step
-  for (int64_t step = first; step < n_steps; step += stride) {
-    const int64_t ahead = step + (NS - 1) * stride;
+  int slot = 0;  // the shared tile of the current tile
+  for (int64_t tile = first; tile < a.n_tiles; tile += stride) {
+    const int64_t ahead = tile + (NS - 1) * stride;
     // the ahead slot was last read before the barrier ending the previous
     // iteration
     const int aslot = slot == 0 ? NS - 1 : slot - 1;
-    if (ahead < n_steps) {
-#pragma unroll
-      for (int j = 0; j < TP; ++j) {
-        const int64_t tile = ahead * TP + j;
-        if (tile < a.n_tiles) {
-          int64_t sb, db;
-          lm_tv::tile_bases(a, tile, &sb, &db);
-          lm_tv::load_tile<VL, MAXV>(
-              a, o, src, tile_smem + (aslot * TP + j) * a.smem_bytes, sb, t);
-        }
-      }
+    if (ahead < a.n_tiles) {
+      lm_tv::tile_bases(a, ahead, &sb, &db);
+      lm_tv::load_tile<VL, MAXV>(a, o, src, tile_smem + aslot * a.smem_bytes,
+                                 sb, t);
     }
     lm_tv::commit_copies();
     lm_tv::wait_copies_but<NS - 1>();
     __syncthreads();
-#pragma unroll
-    for (int j = 0; j < TP; ++j) {
-      const int64_t tile = step * TP + j;
-      if (tile < a.n_tiles) {
-        int64_t sb, db;
-        lm_tv::tile_bases(a, tile, &sb, &db);
-        lm_tv::store_tile<VS, MAXV>(
-            a, o, tile_smem + (slot * TP + j) * a.smem_bytes, dst, db, t);
-      }
-    }
+    lm_tv::tile_bases(a, tile, &sb, &db);
+    lm_tv::store_tile<VS, MAXV>(a, o, tile_smem + slot * a.smem_bytes, dst,
+                                db, t);
     __syncthreads();
     slot = slot + 1 == NS ? 0 : slot + 1;
   }
@@ -135,35 +113,25 @@ __global__ void __launch_bounds__(512)
 
 typedef void (*TvKernel)(const lm_tv_args, const char*, char*, int);
 
-template <int VL, int TP>
+template <int VL>
 TvKernel pick_cached_store(int vs) {
   switch (vs) {
-    case 4: return lm_tv_cached_kernel<VL, 4, 4, 2, TP>;
-    case 8: return lm_tv_cached_kernel<VL, 8, 4, 2, TP>;
-    case 16: return lm_tv_cached_kernel<VL, 16, 4, 2, TP>;
+    case 4: return lm_tv_cached_kernel<VL, 4, 4, 2>;
+    case 8: return lm_tv_cached_kernel<VL, 8, 4, 2>;
+    case 16: return lm_tv_cached_kernel<VL, 16, 4, 2>;
   }
   return nullptr;
 }
 
-template <int TP>
+// Two shared tiles per block: three and four measured 4% and 8% slower on
+// the 8192^2 bf16 tiling, and so did moving two tiles between barriers.
 TvKernel pick_cached(int vl, int vs) {
   switch (vl) {
-    case 4: return pick_cached_store<4, TP>(vs);
-    case 8: return pick_cached_store<8, TP>(vs);
-    case 16: return pick_cached_store<16, TP>(vs);
+    case 4: return pick_cached_store<4>(vs);
+    case 8: return pick_cached_store<8>(vs);
+    case 16: return pick_cached_store<16>(vs);
   }
   return nullptr;
-}
-
-// Tiles moved per step between two barriers by the cached kernel:
-// LM_TV_TILES (1 or 2, default 1: two measured 4% slower on the 8192^2 bf16
-// tiling), 1 when two steps of two do not fit.
-int tv_tiles() {
-  static const int n = [] {
-    const char* e = std::getenv("LM_TV_TILES");
-    return e && e[0] == '2' ? 2 : 1;
-  }();
-  return n;
 }
 
 template <int VL>
@@ -203,16 +171,10 @@ int launch_tv(const lm_tv_plan& plan, const char* src, char* dst,
   const int most = a.load.n_val > a.store.n_val ? a.load.n_val : a.store.n_val;
   TvKernel k = nullptr;
   int smem = 0, two = 0;
-  int64_t units = a.n_tiles;  // grid-stride units of the chosen kernel
-  if (a.offsets32 && a.block_threads <= 512 && most <= 4) {
-    int tp = tv_tiles();
-    if (tp == 2 && 4 * int64_t(a.smem_bytes) > 232448) tp = 1;
-    if (2 * int64_t(tp) * a.smem_bytes <= 232448) {
-      k = tp == 2 ? pick_cached<2>(a.load.vec_bytes, a.store.vec_bytes)
-                  : pick_cached<1>(a.load.vec_bytes, a.store.vec_bytes);
-      smem = 2 * tp * a.smem_bytes;
-      units = (a.n_tiles + tp - 1) / tp;
-    }
+  if (a.offsets32 && a.block_threads <= 512 && most <= 4 &&
+      2 * int64_t(a.smem_bytes) <= 232448) {
+    k = pick_cached(a.load.vec_bytes, a.store.vec_bytes);
+    smem = 2 * a.smem_bytes;
   }
   if (!k) {
     k = pick(a.load.vec_bytes, a.store.vec_bytes);
@@ -246,7 +208,8 @@ int launch_tv(const lm_tv_plan& plan, const char* src, char* dst,
   if (e != cudaSuccess) return fail_cuda(e);
   if (per_sm < 1) return LM_E_INVALID;  // the block cannot be resident
   const int64_t resident = int64_t(sms) * per_sm;
-  const unsigned grid = unsigned(units < resident ? units : resident);
+  const unsigned grid =
+      unsigned(a.n_tiles < resident ? a.n_tiles : resident);
   k<<<grid, unsigned(a.block_threads), size_t(smem),
       static_cast<cudaStream_t>(stream)>>>(a, src, dst, two);
   e = cudaGetLastError();
