@@ -6,8 +6,6 @@
 
 #include <cuda_runtime.h>
 
-#include <cstdlib>
-
 #include <map>
 #include <mutex>
 #include <utility>
