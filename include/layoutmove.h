@@ -97,6 +97,17 @@ int lm_layout_to_string(const lm_layout* layout, char* buf, size_t cap);
  * the affine part; with a swizzle, rounded up to a multiple of 2^(M+B), the
  * smallest bound that holds every swizzled offset whatever the layout.  A
  * buffer of cosize elements holds every offset. */
+/* print_layout ("CUTLASS Layout可视化" §3.1, §4.1): a rank-2 layout as a
+ * grid, one line per mode-0 coordinate (row), one column per mode-1
+ * coordinate, each entry the offset (swizzle applied) right-aligned to a
+ * common width.  With bank_elem_bytes > 0 each entry is instead the shared-
+ * memory bank of the element, (offset * bank_elem_bytes / 4) mod 32: the
+ * "take every offset mod 32" check of §6.4, printed.  Buffer rules as
+ * lm_layout_to_string.  Errors: LM_E_INVALID (NULL, rank != 2, more than
+ * 2^16 entries, bank_elem_bytes outside 0..16), LM_E_BUFFER. */
+int lm_layout_print_grid(const lm_layout* layout, int bank_elem_bytes,
+                         char* buf, size_t cap);
+
 int lm_layout_size(const lm_layout* layout, int64_t* size);
 int lm_layout_cosize(const lm_layout* layout, int64_t* cosize);
 

@@ -45,6 +45,7 @@ SIGNATURES = [
      [C.c_int, _I64P, _I64P, C.c_int, _IP, C.POINTER(_P)]),
     ("lm_layout_parse", C.c_int, [C.c_char_p, C.POINTER(_P)]),
     ("lm_layout_to_string", C.c_int, [_P, C.c_char_p, C.c_size_t]),
+    ("lm_layout_print_grid", C.c_int, [_P, C.c_int, C.c_char_p, C.c_size_t]),
     ("lm_layout_size", C.c_int, [_P, _I64P]),
     ("lm_layout_cosize", C.c_int, [_P, _I64P]),
     ("lm_layout_rank", C.c_int, [_P, _IP, _IP]),
@@ -214,6 +215,20 @@ class Layout:
             return buf.value.decode()
 
     __repr__ = __str__
+
+    def print_grid(self, bank_elem_bytes: int = 0) -> str:
+        """print_layout's grid of a rank-2 layout (rows = mode 0); with
+        bank_elem_bytes > 0, the shared-memory bank of every entry."""
+        cap = 1 << 16
+        while True:
+            buf = C.create_string_buffer(cap)
+            rc = lib().lm_layout_print_grid(self._h, int(bank_elem_bytes), buf,
+                                            cap)
+            if rc == -11:
+                cap *= 4
+                continue
+            _check(rc, "lm_layout_print_grid")
+            return buf.value.decode()
 
     @property
     def size(self) -> int:

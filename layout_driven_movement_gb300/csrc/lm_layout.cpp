@@ -837,6 +837,46 @@ int lm_layout_to_string(const lm_layout* layout, char* buf, size_t cap) {
   });
 }
 
+int lm_layout_print_grid(const lm_layout* layout, int bank_elem_bytes,
+                         char* buf, size_t cap) {
+  return guard([&] {
+    if (!layout || (!buf && cap)) fail(LM_E_INVALID);
+    if (bank_elem_bytes < 0 || bank_elem_bytes > 16) fail(LM_E_INVALID);
+    const std::vector<lm::Node> modes = lm::top_modes(*layout);
+    if (modes.size() != 2) fail(LM_E_INVALID);
+    const std::vector<lm::Leaf> l0 = lm::flatten(modes[0]),
+                                l1 = lm::flatten(modes[1]);
+    int64_t rows = 1, cols = 1;
+    for (const lm::Leaf& l : l0) rows = lm::mul_chk(rows, l.e);
+    for (const lm::Leaf& l : l1) cols = lm::mul_chk(cols, l.e);
+    if (lm::mul_chk(rows, cols) > (int64_t(1) << 16)) fail(LM_E_INVALID);
+    std::vector<int64_t> v(size_t(rows * cols));
+    size_t width = 1;
+    for (int64_t r = 0; r < rows; ++r)
+      for (int64_t c = 0; c < cols; ++c) {
+        int64_t o = layout->swz.apply(lm::eval_affine(l0, r) +
+                                      lm::eval_affine(l1, c));
+        if (bank_elem_bytes) o = (o * bank_elem_bytes / 4) % 32;
+        v[size_t(r * cols + c)] = o;
+        width = std::max(width, std::to_string(o).size());
+      }
+    std::string s;
+    for (int64_t r = 0; r < rows; ++r) {
+      for (int64_t c = 0; c < cols; ++c) {
+        const std::string t = std::to_string(v[size_t(r * cols + c)]);
+        if (c) s += ' ';
+        s += std::string(width - t.size(), ' ') + t;
+      }
+      s += '\n';
+    }
+    if (cap == 0) fail(LM_E_BUFFER);
+    const size_t n = std::min(s.size(), cap - 1);
+    std::memcpy(buf, s.data(), n);
+    buf[n] = '\0';
+    if (s.size() + 1 > cap) fail(LM_E_BUFFER);
+  });
+}
+
 int lm_layout_size(const lm_layout* layout, int64_t* size) {
   return guard([&] {
     if (!layout || !size) fail(LM_E_INVALID);

@@ -579,3 +579,37 @@ def test_plans_beyond_2_to_31_elements_split_aligned():
         assert p["s_base"] % 16 == 0 and p["d_base"] % 16 == 0
         total += n
     assert total == 70000 * 70000
+
+
+def _grid_ints(text):
+    return [[int(v) for v in line.split()] for line in text.splitlines()]
+
+
+def test_print_grid_matches_oracle_and_page_grids():
+    """lm_layout_print_grid gives the oracle's print_layout grid (row =
+    mode-0 coordinate) for the page's 4x2 grids, the swizzled 8x8 tile,
+    nested and random rank-2 layouts; its bank view is every offset times
+    the element size over 4, mod 32."""
+    texts = ["(4,2):(2,1)", "(4,2):(1,4)", "((4,2),(2,4)):((2,16),(1,8))",
+             "(8,8):(8,1)", "(16,12):(1,16)"]
+    rng = np.random.default_rng(11)
+    for _ in range(20):
+        e0, e1 = int(rng.integers(1, 9)), int(rng.integers(1, 9))
+        d0, d1 = int(rng.integers(0, 40)), int(rng.integers(0, 40))
+        texts.append(f"({e0},{e1}):({d0},{d1})")
+    for t in texts:
+        L, O = lm.Layout.parse(t), lo.parse(t)
+        want = lo.print_grid(O)
+        assert _grid_ints(L.print_grid()) == want, t
+        for eb in (2, 4, 8):
+            banks = [[(v * eb // 4) % 32 for v in row] for row in want]
+            assert _grid_ints(L.print_grid(eb)) == banks, (t, eb)
+    sw = lm.Layout.parse("(8,8):(8,1)").swizzle(3, 0, 3)
+    osw = lo.Swizzled(3, 0, 3, lo.parse("(8,8):(8,1)"))
+    assert _grid_ints(sw.print_grid()) == lo.print_grid(osw)
+    assert _grid_ints(sw.print_grid())[1] == [9, 8, 11, 10, 13, 12, 15, 14]
+    lines = lm.Layout.parse("(4,2):(2,1)").print_grid().splitlines()
+    assert lines == ["0 1", "2 3", "4 5", "6 7"]
+    for bad in ["8:1", "(2,2,2):(1,2,4)"]:
+        with pytest.raises(lm.LayoutMoveError):
+            lm.Layout.parse(bad).print_grid()
