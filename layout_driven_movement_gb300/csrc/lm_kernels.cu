@@ -145,34 +145,29 @@ __global__ void __launch_bounds__(256)
 }
 
 // The same table in 16-byte stores: when the first leaf's extent is a
-// multiple of G * R (R = 16 / sizeof(OUT)), each thread decomposes one
-// index in G * R and steps the first leaf for the others, storing G
-// consecutive 16-byte groups.
-template <typename OUT, int G>
+// multiple of R = 16 / sizeof(OUT), each thread decomposes one index in R
+// and steps the first leaf for the other R - 1 entries.
+template <typename OUT>
 __global__ void __launch_bounds__(256)
     lm_eval_vec_kernel(const __grid_constant__ EvalArgs a,
                        OUT* __restrict__ table) {
   constexpr int R = 16 / int(sizeof(OUT));
   pdl_trigger();
   pdl_wait();
-  const uint64_t nq = a.n / (R * G);
+  const uint64_t nq = a.n / R;
   const uint64_t stride = uint64_t(gridDim.x) * blockDim.x;
   for (uint64_t q = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x; q < nq;
        q += stride) {
-    const uint64_t i = q * (R * G);
+    const uint64_t i = q * R;
     const int64_t off =
         a.wide ? side_offset64(i, a.nl, a.ext64, a.str)
                : side_offset32(uint32_t(i), a.nl, a.ext, a.div, a.str);
+    OUT v[R];
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      OUT v[R];
-#pragma unroll
-      for (int u = 0; u < R; ++u)
-        v[u] = OUT(swz_apply(a.swz, off + (g * R + u) * a.str[0]));
-      uint4 w;
-      memcpy(&w, v, 16);
-      __stcs(reinterpret_cast<uint4*>(table) + q * G + g, w);
-    }
+    for (int u = 0; u < R; ++u) v[u] = OUT(swz_apply(a.swz, off + u * a.str[0]));
+    uint4 w;
+    memcpy(&w, v, 16);
+    __stcs(reinterpret_cast<uint4*>(table) + q, w);
   }
 }
 
@@ -1359,25 +1354,15 @@ int launch_eval(const lm_layout& L, void* table, int offset_bytes,
   const int R = 16 / offset_bytes;
   if (a.nl > 0 && c[0].e % R == 0 &&
       reinterpret_cast<uintptr_t>(table) % 16 == 0) {
-    // groups per thread: up to 4 16-byte groups along the first leaf
-    const int G = c[0].e % (4 * R) == 0 ? 4 : c[0].e % (2 * R) == 0 ? 2 : 1;
-    const uint64_t wantv = (a.n / (R * G) + 255) / 256;
+    const uint64_t wantv = (a.n / R + 255) / 256;
     const unsigned gridv = unsigned(std::max<uint64_t>(
         1, std::min<uint64_t>(wantv, uint64_t(di.sms) * 16)));
-    auto go = [&](auto* kern, auto* tab) {
-      launch_k(kern, gridv, 256, 0, st, a, tab);
-    };
-    int32_t* t32 = static_cast<int32_t*>(table);
-    int64_t* t64 = static_cast<int64_t*>(table);
-    if (offset_bytes == 4) {
-      if (G == 4) go(lm_eval_vec_kernel<int32_t, 4>, t32);
-      else if (G == 2) go(lm_eval_vec_kernel<int32_t, 2>, t32);
-      else go(lm_eval_vec_kernel<int32_t, 1>, t32);
-    } else {
-      if (G == 4) go(lm_eval_vec_kernel<int64_t, 4>, t64);
-      else if (G == 2) go(lm_eval_vec_kernel<int64_t, 2>, t64);
-      else go(lm_eval_vec_kernel<int64_t, 1>, t64);
-    }
+    if (offset_bytes == 4)
+      launch_k(lm_eval_vec_kernel<int32_t>, gridv, 256, 0, st, a,
+               static_cast<int32_t*>(table));
+    else
+      launch_k(lm_eval_vec_kernel<int64_t>, gridv, 256, 0, st, a,
+               static_cast<int64_t*>(table));
     return check_launch();
   }
   if (offset_bytes == 4)
