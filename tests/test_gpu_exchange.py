@@ -118,3 +118,32 @@ def test_pack_all_and_unpack_all(case, world):
         lm.exchange_unpack_all(x, recv, dl)
         torch.cuda.synchronize()
         check_rank(d, dl.cpu().numpy(), want, eb, q)
+
+
+def test_exchange_copy_single_rank_nccl():
+    """exchange_copy end to end -- pack_all, torch.distributed's
+    all_to_all_single, unpack_all -- in a one-rank NCCL group on this GPU
+    (the whole copy is the rank's own box)."""
+    import os
+    import socket
+    import torch.distributed as dist
+    if not dist.is_nccl_available():
+        pytest.skip("NCCL not available")
+    with socket.socket() as sock:
+        sock.bind(("127.0.0.1", 0))
+        port = sock.getsockname()[1]
+    dist.init_process_group("nccl", init_method=f"tcp://127.0.0.1:{port}",
+                            rank=0, world_size=1)
+    try:
+        _, src, dst, eb = CASES[0]
+        S, D, inp, want = global_problem(src, dst, eb)
+        x = lm.Exchange(S, D, eb, 0, 1)
+        d = x.describe()
+        local = torch.from_numpy(inp).cuda()[:d["src_local"] * eb].clone()
+        out = torch.full((d["dst_local"] * eb,), FILL, dtype=torch.uint8,
+                         device="cuda")
+        lm.exchange_copy(x, local, out)
+        torch.cuda.synchronize()
+        check_rank(d, out.cpu().numpy(), want, eb, 0)
+    finally:
+        dist.destroy_process_group()
