@@ -520,7 +520,7 @@ def measure_d2d(suite, torch) -> float:
 
 def measure_tv(suite, args, torch, peak) -> dict:
     """Time lm_tv_copy on the suite's full-size buffers (TV_CONFIGS), the
-    copies of one round back to back with events around each."""
+    copies of one pass back to back with events around each."""
     lm = suite.lm
     items = {it["name"]: it for it in suite.items}
     runs = []
@@ -536,15 +536,15 @@ def measure_tv(suite, args, torch, peak) -> dict:
         runs.append((key, it, plan))
     if not runs:
         return {}
-    rounds = min(args.steps, 300)
+    passes = min(args.steps, 300)
     for _ in range(3):
         for _, it, plan in runs:
             lm.tv_copy(plan, it["src"], it["dst"])
     ev = [[(torch.cuda.Event(enable_timing=True),
             torch.cuda.Event(enable_timing=True)) for _ in runs]
-          for _ in range(rounds)]
+          for _ in range(passes)]
     torch.cuda.synchronize()
-    for r in range(rounds):
+    for r in range(passes):
         for k, (_, it, plan) in enumerate(runs):
             ev[r][k][0].record()
             lm.tv_copy(plan, it["src"], it["dst"])
@@ -553,7 +553,7 @@ def measure_tv(suite, args, torch, peak) -> dict:
     out = {}
     for k, (key, it, plan) in enumerate(runs):
         ms = statistics.median(ev[r][k][0].elapsed_time(ev[r][k][1])
-                               for r in range(rounds))
+                               for r in range(passes))
         gbs = it["bytes"] / (ms * 1e-3) / 1e9
         d = plan.describe()
         out[key] = {
@@ -623,7 +623,7 @@ def measure_exchange(suite, args, torch, peak, world=4) -> dict:
     for _ in range(3):
         one()
     torch.cuda.synchronize()
-    # 32 small launches per round: replay them as one CUDA graph so the
+    # small launches per pass: replay them as one CUDA graph so the
     # host's launch rate does not set the time
     run, how = one, "eager launches"
     try:
@@ -633,31 +633,31 @@ def measure_exchange(suite, args, torch, peak, world=4) -> dict:
         with torch.cuda.graph(graph, stream=side):
             one()
         torch.cuda.synchronize()
-        run, how = graph.replay, "one CUDA graph per round"
+        run, how = graph.replay, "one CUDA graph per pass"
     except Exception as exc:  # capture unsupported: time eager launches
         how = f"eager launches (graph capture failed: {type(exc).__name__})"
         torch.cuda.synchronize()
-    rounds = min(args.steps, 200)
+    passes = min(args.steps, 200)
     for _ in range(3):
         run()
     e0, e1 = (torch.cuda.Event(enable_timing=True),
               torch.cuda.Event(enable_timing=True))
     torch.cuda.synchronize()
     e0.record()
-    for _ in range(rounds):
+    for _ in range(passes):
         run()
     e1.record()
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / rounds
+    ms = e0.elapsed_time(e1) / passes
     # pack, stand-in exchange and unpack each read and write every element
     gbs = 3 * 2 * total / (ms * 1e-3) / 1e9
     return {"workload": f"4096x4096 fp32 transpose, rows sharded over {world} "
                         "ranks on both sides, all ranks' packs and unpacks on "
                         "this GPU; the all-to-all stands in as device copies "
                         "of the boxes, timed too",
-            "layout_copies_per_round": 2 * world, "one_copy_per_side": one_copy,
+            "layout_copies_per_pass": 2 * world, "one_copy_per_side": one_copy,
             "launch": how,
-            "us_per_round": round(ms * 1e3, 2), "gbs": round(gbs, 1),
+            "us_per_pass": round(ms * 1e3, 2), "gbs": round(gbs, 1),
             "frac_of_peak": round(gbs / peak, 4)}
 
 
