@@ -167,3 +167,43 @@ def test_shard_ranges_and_ownership():
     whole = lm.Plan(lm.Layout.parse("(8,8):(1,8)"),
                     lm.Layout.parse("(8,8):(8,1)"), 4).describe()
     assert whole["src_range"] == [0, 64] and whole["dst_own"]
+
+
+def test_random_shard_ranges_hold_their_pairs():
+    """Random compact permutations split over 2-5 ranks: each shard's
+    described source and destination ranges contain every offset it
+    touches, and shards that own their destination ranges have disjoint
+    ones."""
+    rng = np.random.default_rng(17)
+    for _ in range(50):
+        n = int(rng.integers(2, 4))
+        shape = tuple(int(rng.integers(2, 9)) for _ in range(n))
+
+        def compact(order):
+            st, w = [0] * n, 1
+            for k in order:
+                st[k] = w
+                w *= shape[k]
+            return tuple(st)
+
+        src = ("layout", shape, compact(rng.permutation(n)))
+        dst = ("layout", shape, compact(rng.permutation(n)))
+        eb = int(rng.choice([1, 2, 4, 8]))
+        world = int(rng.integers(2, 6))
+        parts, owned = [], []
+        for r in range(world):
+            d = lm.Plan(lm.build_layout(src), lm.build_layout(dst), eb,
+                        rank=r, world=world).describe()
+            pr = shard_pairs(src, dst, eb, r, world)
+            parts.append(pr)
+            if len(pr):
+                assert d["src_range"][0] <= pr[:, 0].min()
+                assert pr[:, 0].max() < d["src_range"][1]
+                assert d["dst_range"][0] <= pr[:, 1].min()
+                assert pr[:, 1].max() < d["dst_range"][1]
+            if d["dst_own"]:
+                owned.append(tuple(d["dst_range"]))
+        check_partition(parts, src, dst)
+        owned.sort()
+        for a, b in zip(owned, owned[1:]):
+            assert a[1] <= b[0], owned
