@@ -385,7 +385,10 @@ void lm_plan_destroy(lm_plan* plan);
  * the largest source stride ("in" mode) and produces the destination
  * elements of range r of the mode with the largest destination stride
  * ("out" mode); ranges are balanced (coordinates e*r/world up to
- * e*(r+1)/world), and both modes need at least `world` coordinates.  The
+ * e*(r+1)/world), and both modes need at least `world` coordinates: when
+ * the largest-stride mode of either side is shorter, the call fails with
+ * LM_E_INVALID rather than shard a faster mode (whose ranges would overlap
+ * in memory).  The
  * local shard buffers hold the global layouts' offsets from the shard's
  * first to its last, rebased to 0 (src_local / dst_local elements; for the
  * row-sharded transpose of a row-major matrix, the rows themselves).  Rank
@@ -395,8 +398,9 @@ void lm_plan_destroy(lm_plan* plan);
  * do not shard: this is the copy of "CUTE布局代数" §5.1 (make_copy of a
  * layout pair) split over ranks, and only the placement of the shards
  * needs the exchange, every logical index being independent.
- * Errors: LM_E_INVALID (NULL, elem_bytes, rank/world, an empty copy, no
- * joint mode with `world` coordinates), LM_E_INCOMPATIBLE (sizes differ or
+ * Errors: LM_E_INVALID (NULL, elem_bytes, rank/world, an empty copy, a
+ * largest-stride mode with fewer than `world` coordinates on either side),
+ * LM_E_INCOMPATIBLE (sizes differ or
  * no common refinement), LM_E_NOT_REPRESENTABLE (a swizzled side),
  * LM_E_NOT_INJECTIVE. */
 int lm_plan_exchange(const lm_layout* src, const lm_layout* dst,

@@ -121,16 +121,18 @@ void plan_all(lm_exchange& X) {
   X.unpack_all = b;
 }
 
-// The joint mode with at least `world` coordinates and the largest stride
-// on one side.
+// The joint mode with the largest stride on one side, or -1 when that mode
+// has fewer than `world` coordinates: the shards are ranges of exactly that
+// mode, so a shorter one cannot be split over every rank, and falling back
+// to a faster mode would give shard ranges that overlap in memory.
 int slowest_mode(const std::vector<JMode>& ms, int world, bool dst_side) {
   int k = -1;
   for (int j = 0; j < int(ms.size()); ++j) {
-    if (ms[size_t(j)].e < world) continue;
     const int64_t sj = dst_side ? ms[size_t(j)].d : ms[size_t(j)].s;
     const int64_t sk = k < 0 ? -1 : (dst_side ? ms[size_t(k)].d : ms[size_t(k)].s);
     if (k < 0 || sj > sk) k = j;
   }
+  if (k >= 0 && ms[size_t(k)].e < world) return -1;
   return k;
 }
 

@@ -33,21 +33,22 @@ int main(void) {
   if (check(lm_layout_to_string(z, buf, sizeof buf), "print z")) return 1;
   printf("zipped_divide %s\n", buf);
   lm_layout *s = NULL, *d = NULL;
-  lm_layout_parse("(4096,4096):(1,4096)", &s);
-  lm_layout_parse("(4096,4096):(4096,1)", &d);
+  if (check(lm_layout_parse("(4096,4096):(1,4096)", &s), "parse s")) return 1;
+  if (check(lm_layout_parse("(4096,4096):(4096,1)", &d), "parse d")) return 1;
   if (check(lm_plan_copy(s, d, 4, &plan), "plan")) return 1;
   if (check(lm_plan_describe(plan, buf, sizeof buf), "describe")) return 1;
   printf("plan_path %s\n", strstr(buf, "\"path\":\"STAGED\"") ? "STAGED" : "?");
   lm_layout* col = NULL;
-  lm_layout_parse("32:8", &col);
+  if (check(lm_layout_parse("32:8", &col), "parse col")) return 1;
   if (check(lm_smem_wavefronts(col, 4, 4, &v, &w), "banks")) return 1;
   printf("banks %lld %lld\n", (long long)v, (long long)w);
   lm_layout *tile = NULL, *thr = NULL;
-  lm_layout_parse("(8,8):(8,1)", &tile);
-  lm_layout_parse("(4,2):(1,4)", &thr);
+  if (check(lm_layout_parse("(8,8):(8,1)", &tile), "parse tile")) return 1;
+  if (check(lm_layout_parse("(4,2):(1,4)", &thr), "parse thr")) return 1;
   if (check(lm_layout_local_partition(tile, thr, 5, &part, &base), "part"))
     return 1;
-  lm_layout_to_string(part, buf, sizeof buf);
+  if (check(lm_layout_to_string(part, buf, sizeof buf), "print part"))
+    return 1;
   printf("local_partition %s %lld\n", buf, (long long)base);
   lm_layout_destroy(r);
   r = NULL;

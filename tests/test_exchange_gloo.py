@@ -42,6 +42,21 @@ CASES = [
      ("layout", (12, 10, 9), (1, 108, 12)), 1),
 ]
 
+# Cases whose largest-stride mode on one side is short: the most ranks that
+# mode can be split over (more are refused with LM_E_INVALID).
+MAX_WORLD = {"interleave_f16": 2}
+
+
+def refused(name, S, D, eb, world):
+    """True (after checking the refusal) when `world` ranks exceed what the
+    case's slowest mode allows."""
+    if world <= MAX_WORLD.get(name, world):
+        return False
+    with pytest.raises(lm.LayoutMoveError) as e:
+        lm.Exchange(S, D, eb, 0, world)
+    assert e.value.status == -1
+    return True
+
 
 @pytest.fixture(scope="module", autouse=True)
 def built():
@@ -110,9 +125,12 @@ def check_rank(desc, dst_local, want, eb, rank):
 def test_boxes_partition_and_move_everything(case, world):
     """All ranks in one process: the send and receive descriptions agree,
     every logical index moves exactly once, the shards come out right."""
-    _, src, dst, eb = case
+    name, src, dst, eb = case
     S, D, inp, want = global_problem(src, dst, eb)
+    if refused(name, S, D, eb, world):
+        return
     descs = [lm.Exchange(S, D, eb, r, world).describe() for r in range(world)]
+    _assert_disjoint_shards(descs)
     total = sum(b["count"] for d in descs for b in d["send"])
     assert total == S.size
     for p in range(world):
@@ -149,7 +167,9 @@ def _rank_main(rank, world, port, q):
         dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}",
                                 rank=rank, world_size=world)
         lm.lib()
-        for _, src, dst, eb in CASES:
+        for name, src, dst, eb in CASES:
+            if world > MAX_WORLD.get(name, world):
+                continue            # refused; checked in one process
             S, D, inp, want = global_problem(src, dst, eb)
             desc = lm.Exchange(S, D, eb, rank, world).describe()
             o, n = desc["src_origin"], desc["src_local"]
@@ -225,6 +245,7 @@ def test_random_exchanges_move_everything():
             assert e.status == -1      # no mode with `world` coordinates
             continue
         assert sum(b["count"] for d in descs for b in d["send"]) == S.size
+        _assert_disjoint_shards(descs)
         src_local = [inp[d["src_origin"] * eb:
                          (d["src_origin"] + d["src_local"]) * eb]
                      for d in descs]
@@ -237,3 +258,40 @@ def test_random_exchanges_move_everything():
             check_rank(descs[q], dl, want, eb, q)
         done += 1
     assert done >= 30
+
+
+def _assert_disjoint_shards(descs):
+    """The ranks' source shards, and their destination shards, are
+    disjoint ranges of the global buffers."""
+    for org, n in (("src_origin", "src_local"), ("dst_origin", "dst_local")):
+        spans = sorted((d[org], d[org] + d[n]) for d in descs)
+        for (a0, a1), (b0, b1) in zip(spans, spans[1:]):
+            assert a1 <= b0, (org, spans)
+
+
+@pytest.mark.parametrize("world", [3, 4, 8])
+def test_short_slowest_mode_is_rejected(world):
+    """The 2-head interleave sharded over more ranks than heads: the source's
+    largest-stride mode (heads, 2 coordinates) cannot be split `world` ways,
+    and sharding a faster mode instead would give overlapping source shards,
+    so the plan is refused."""
+    S = lm.Layout.parse("(2,1024):(1024,1)")
+    D = lm.Layout.parse("(2,1024):(1,2)")
+    for r in range(world):
+        with pytest.raises(lm.LayoutMoveError) as ei:
+            lm.Exchange(S, D, 2, r, world)
+        assert ei.value.status == -1
+    # two ranks split the heads, and the shards are disjoint
+    descs = [lm.Exchange(S, D, 2, r, 2).describe() for r in range(2)]
+    _assert_disjoint_shards(descs)
+    assert sum(d["src_local"] for d in descs) == 2048
+
+
+def test_short_destination_mode_is_rejected():
+    """The same on the destination side: the interleave's reverse, whose
+    destination's largest-stride mode has 2 coordinates."""
+    S = lm.Layout.parse("(2,1024):(1,2)")
+    D = lm.Layout.parse("(2,1024):(1024,1)")
+    with pytest.raises(lm.LayoutMoveError) as ei:
+        lm.Exchange(S, D, 2, 0, 4)
+    assert ei.value.status == -1

@@ -10,7 +10,8 @@ byte for byte with the oracle's copy of the whole tensor.
 
 import pytest
 
-from test_exchange_gloo import CASES, FILL, check_rank, global_problem
+from test_exchange_gloo import (CASES, FILL, check_rank, global_problem,
+                                refused)
 from workloads import WORKLOADS
 
 torch = pytest.importorskip("torch")
@@ -26,8 +27,10 @@ def built():
     lm.lib()
 
 
-def run_exchange(src, dst, eb, world):
+def run_exchange(src, dst, eb, world, name=""):
     S, D, inp, want = global_problem(src, dst, eb)
+    if refused(name, S, D, eb, world):
+        return
     xs = [lm.Exchange(S, D, eb, r, world) for r in range(world)]
     descs = [x.describe() for x in xs]
     g_src = torch.from_numpy(inp).cuda()
@@ -57,8 +60,8 @@ def run_exchange(src, dst, eb, world):
 @pytest.mark.parametrize("world", [2, 3])
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
 def test_exchange_on_one_device(case, world):
-    _, src, dst, eb = case
-    run_exchange(src, dst, eb, world)
+    name, src, dst, eb = case
+    run_exchange(src, dst, eb, world, name)
 
 
 def test_exchange_row_sharded_transpose_large():
