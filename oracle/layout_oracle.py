@@ -16,8 +16,8 @@ fusion, no reordering):
   "CUTE布局代数：GPU张量计算的内存优化革命" §2.1);
 * a 1-D logical index is split into leaf coordinates first-leaf-fastest
   ("colex"); the pages never state the order, this is the reading the
-  stripmined thread-map formula and the column-major example force (see
-  ``stripmined_offset`` and the tests);
+  stripmined thread-map formula and the column-major example force (the
+  tests check the generic evaluator against both);
 * a 2-D coordinate (row, col) of a rank-2 layout addresses mode 0 with row
   and mode 1 with col ("CUTLASS Layout可视化" §3.3);
 * Swizzle<B,M,S> XORs the B offset bits starting at bit M+S into the B bits
@@ -31,9 +31,10 @@ fusion, no reordering):
   which the two inverses agree ("CUTE布局代数" §2.3);
 * the copy is out[dst(i)] = in[src(i)] for every logical index i, moving raw
   element bytes ("CUTE布局代数" §5.1, make_copy(gmem_layout, smem_layout));
-* the thread maps are the pitch-linear map and the stripmined get_offset map
-  of the PitchLinearStripminedThreadMap article (hotelren.com/news/5252042,
-  §1.2 and §2.2);
+* the thread maps are the pitch-linear map and the stripmined map of the
+  PitchLinearStripminedThreadMap article (hotelren.com/news/5252042, §1.2
+  and §2.2), the latter evaluated as the layout
+  (Pitch, Strips, groups):(1, kRow, Pitch*Strips*kRow);
 * a thread's part of a tile under local_partition is one element of every
   thread-layout-shaped block, at the thread's coordinate in the block
   ("CUTLASS Layout可视化" §5.3);
@@ -454,16 +455,18 @@ def pitch_linear_offset(thread_id, k_row: int, pitch: int):
 
 
 def stripmined_offset(thread_id, k_row: int, pitch: int, strips: int):
-    """§2.2 get_offset: the thread id splits into a position inside the
-    Pitch (fast), a strip number inside Strips, and the number of whole
-    Pitch x Strips groups before it; the offset is the position, plus the
-    strip times kRow, plus the group count times Pitch*Strips*kRow."""
+    """§2.2's stripmined map, read as a layout: a thread id is a logical
+    index into the three modes (Pitch, Strips, groups) -- a position inside
+    the Pitch, a strip inside Strips, and the whole Pitch x Strips groups
+    before it -- whose strides are 1 element, one kRow row per strip, and
+    Pitch*Strips rows of kRow per group.  The offset is that layout
+    evaluated by the generic colex evaluator (``Layout.at``), with as many
+    groups as the largest thread id needs."""
     t = _as_index(thread_id)
-    in_pitch = t % pitch
-    above = t // pitch
-    strip = above % strips
-    group = above // strips
-    return in_pitch + strip * k_row + group * (pitch * strips * k_row)
+    per_group = pitch * strips
+    groups = int(t.max()) // per_group + 1 if t.size else 1
+    L = Layout((pitch, strips, groups), (1, k_row, per_group * k_row))
+    return L.at(t)
 
 
 # ---------------------------------------------------------------------------

@@ -108,18 +108,32 @@ def test_stripmined_host_program_listing_values():
     assert off[63] == 567 and off[8] == 16 and off[24] == 48
 
 
+def _get_offset_by_hand(t, k_row, pitch, strips):
+    """The article's §2.2 get_offset, worked as its three named parts: the
+    position inside the Pitch, the strip inside Strips, the group of
+    Pitch x Strips threads; each part times its step."""
+    pos, strip, group = t % pitch, (t // pitch) % strips, t // (pitch * strips)
+    return pos + strip * k_row + group * (pitch * strips * k_row)
+
+
 def pin_stripmined_is_colex_layout():
-    """R1: get_offset equals the layout (Pitch, Strips, G):(1, kRow,
-    Pitch*Strips*kRow) evaluated first-leaf-fastest.  The formula is the
-    page's; the evaluator is the generic one, so this pins colex order."""
+    """R1: the page's get_offset arithmetic equals the oracle's generic
+    evaluator on the layout (Pitch, Strips, G):(1, kRow, Pitch*Strips*kRow)
+    only if that evaluator splits an index first-leaf-fastest, so this pins
+    colex order (the oracle's stripmined map is that layout; the page's
+    arithmetic lives only here)."""
     for pitch, strips, k_row in itertools.product((1, 2, 3, 8), (1, 2, 4, 5),
                                                   (1, 7, 16)):
         groups = 6
         L = lo.Layout((pitch, strips, groups),
                       (1, k_row, pitch * strips * k_row))
         t = np.arange(L.size)
-        assert (L.at(t) == lo.stripmined_offset(t, k_row, pitch,
-                                                strips)).all()
+        want = _get_offset_by_hand(t, k_row, pitch, strips)
+        assert (L.at(t) == want).all()
+        assert (lo.stripmined_offset(t, k_row, pitch, strips) == want).all()
+        # one thread at a time sizes the groups from that thread alone
+        assert lo.stripmined_offset(int(t[-1]), k_row, pitch,
+                                    strips) == want[-1]
 
 
 def test_stripmined_is_colex_layout():
