@@ -90,8 +90,11 @@ def dist_env():
 # --------------------------------------------------------------------------
 
 class ClockSampler:
-    """nvidia-smi samples (every 100 ms) of the GPU under test; only samples
-    stamped inside the timed window count."""
+    """nvidia-smi samples (every 50 ms) of the GPU under test; only samples
+    stamped inside the sampled window count.  The window is the suite
+    running without a break for SOAK_S seconds before and after the timed
+    steps, which sit inside it (the timed steps alone last milliseconds,
+    shorter than the sampling interval)."""
 
     FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,"
               "clocks_event_reasons.active,"
@@ -115,7 +118,7 @@ class ClockSampler:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}",
                  f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE,
+                 "-lms", "50"], stdout=subprocess.PIPE,
                 stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -229,14 +232,18 @@ def run_native(args) -> dict | None:
     n = len(suite.items)
     ev0, ev1 = (torch.cuda.Event(enable_timing=True),
                 torch.cuda.Event(enable_timing=True))
+    # steps of uninterrupted load around the timed steps, so the clock
+    # sampler sees the GPU in the state the timed steps run in
+    soak = 0 if args.quick else soak_steps(suite, torch)
     with ClockSampler(gpu_smi_id(local) if not args.quick else "") as clk:
         if not args.quick:
-            time.sleep(1.0)         # let the sampler start
+            time.sleep(0.5)         # let the sampler start
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
         t_start = time.time()
-        t0 = time.perf_counter()
+        for _ in range(soak):
+            suite.step()
         # the headline region: K steps back to back, events only at its ends,
         # so consecutive copies overlap launch and tail (programmatic
         # dependent launch keeps their stream order)
@@ -244,12 +251,14 @@ def run_native(args) -> dict | None:
         for _ in range(args.steps):
             suite.step()
         ev1.record()
+        for _ in range(soak):
+            suite.step()
         torch.cuda.synchronize()
-        wall = time.perf_counter() - t0
         clk.window = (t_start, time.time())
         if world > 1:
             dist.barrier()
     total_ms = ev0.elapsed_time(ev1)
+    wall = total_ms * 1e-3
     # per-copy breakdown: a second timed pass with events around every copy
     k2 = min(args.steps, 1000)
     events = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)]
@@ -269,6 +278,11 @@ def run_native(args) -> dict | None:
         total_ms = max(float(g[0]) for g in gathered)
         wall = max(float(g[1]) for g in gathered)
     value = suite.bytes_per_step * args.steps * world / (total_ms * 1e-3) / 1e9
+    # the bulk-copy kernels bound their waits on the device; a wait that gave
+    # up would leave part of a destination unwritten, so no number stands
+    if lm.device_status() != 0:
+        raise RuntimeError("a copy kernel gave up a bounded wait "
+                           "(LM_E_TIMEOUT): the run is invalid")
 
     peak, peak_kind = peaks()
     iso = isolated_times(suite, torch) if not args.quick else {}
@@ -333,6 +347,11 @@ def run_native(args) -> dict | None:
     xch = measure_exchange(suite, args, torch, peak) if not args.quick else {}
     cpu = cpu_baseline(suite) if world == 1 and not args.quick else None
     clocks = clk.summary()
+    if soak:
+        clocks["window"] = (f"the suite without a break: {soak} steps "
+                            "before and after the timed steps, which lie "
+                            "inside the sampled window")
+        clocks["window_s"] = round(clk.window[1] - clk.window[0], 3)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -363,6 +382,23 @@ def run_native(args) -> dict | None:
         "gpu_launches": suite.launches_per_step * args.steps,
     }
     return line
+
+
+SOAK_S = 0.6
+
+
+def soak_steps(suite, torch) -> int:
+    """Steps that keep the GPU busy for about SOAK_S seconds (from the time
+    of a few steps)."""
+    e0, e1 = (torch.cuda.Event(enable_timing=True),
+              torch.cuda.Event(enable_timing=True))
+    e0.record()
+    for _ in range(10):
+        suite.step()
+    e1.record()
+    torch.cuda.synchronize()
+    per = max(e0.elapsed_time(e1) / 10, 1e-3)
+    return int(SOAK_S * 1e3 / per) + 1
 
 
 def staged_sum(pieces, key, ideal_key, minus=None):
@@ -661,7 +697,168 @@ def measure_exchange(suite, args, torch, peak, world=4) -> dict:
             "frac_of_peak": round(gbs / peak, 4)}
 
 
-def measure_e2e(suite, args, torch, shards=4) -> dict:
+# --------------------------------------------------------------------------
+# host topology: which NUMA node the GPU hangs off, where pinned memory goes
+# --------------------------------------------------------------------------
+
+def _cpulist(text: str) -> list[int]:
+    cpus = []
+    for part in text.strip().split(","):
+        if not part:
+            continue
+        if "-" in part:
+            a, b = part.split("-")
+            cpus.extend(range(int(a), int(b) + 1))
+        else:
+            cpus.append(int(part))
+    return cpus
+
+
+def _ranges(cpus) -> str:
+    cpus = sorted(set(cpus))
+    out, k = [], 0
+    while k < len(cpus):
+        j = k
+        while j + 1 < len(cpus) and cpus[j + 1] == cpus[j] + 1:
+            j += 1
+        out.append(str(cpus[k]) if j == k else f"{cpus[k]}-{cpus[j]}")
+        k = j + 1
+    return ",".join(out)
+
+
+def _read(path: str) -> str | None:
+    try:
+        with open(path) as fh:
+            return fh.read().strip()
+    except OSError:
+        return None
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True,
+                             timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.startswith("Model name:"):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    info = _read("/proc/cpuinfo") or ""
+    fields = {}
+    for ln in info.splitlines():
+        if ":" in ln:
+            k, v = ln.split(":", 1)
+            fields.setdefault(k.strip(), v.strip())
+    if "model name" in fields:
+        return fields["model name"]
+    return (f"CPU implementer {fields.get('CPU implementer', '?')} part "
+            f"{fields.get('CPU part', '?')}")
+
+
+def host_topology(local: int) -> dict:
+    """The GPU's PCI address and NUMA node, that node's CPUs, and this
+    process's CPU affinity."""
+    import torch
+    props = torch.cuda.get_device_properties(local)
+    bdf = None
+    bus = getattr(props, "pci_bus_id", None)
+    if bus is not None:
+        bdf = (f"{getattr(props, 'pci_domain_id', 0) or 0:04x}:{bus:02x}:"
+               f"{getattr(props, 'pci_device_id', 0) or 0:02x}.0")
+    else:
+        try:
+            out = subprocess.run(
+                ["nvidia-smi", f"--id={gpu_smi_id(local)}",
+                 "--query-gpu=pci.bus_id", "--format=csv,noheader"],
+                capture_output=True, text=True, timeout=20).stdout.strip()
+            dom, rest = out.lower().split(":", 1)
+            bdf = f"{int(dom, 16):04x}:{rest}"
+        except Exception:
+            bdf = None
+    node = -1
+    if bdf:
+        txt = _read(f"/sys/bus/pci/devices/{bdf}/numa_node")
+        node = int(txt) if txt not in (None, "") else -1
+    node_cpus = []
+    if node >= 0:
+        node_cpus = _cpulist(_read(
+            f"/sys/devices/system/node/node{node}/cpulist") or "")
+    aff = sorted(os.sched_getaffinity(0))
+    return {"gpu_pci": bdf, "gpu_numa_node": node,
+            "gpu_node_cpus": _ranges(node_cpus),
+            "process_affinity": _ranges(aff), "nproc": len(aff),
+            "cpu_model": cpu_model()}
+
+
+def _set_mempolicy(node: int | None) -> bool:
+    """Prefer `node` for this thread's page allocations (None: back to the
+    default policy), by the set_mempolicy system call."""
+    import ctypes
+    import platform
+    nr = {"x86_64": 238, "aarch64": 237}.get(platform.machine())
+    if nr is None:
+        return False
+    libc = ctypes.CDLL(None, use_errno=True)
+    if node is None:
+        rc = libc.syscall(ctypes.c_long(nr), ctypes.c_int(0), None,
+                          ctypes.c_ulong(0))
+    else:
+        mask = (ctypes.c_ulong * 2)()
+        mask[node // 64] = 1 << (node % 64)
+        rc = libc.syscall(ctypes.c_long(nr), ctypes.c_int(1), mask,
+                          ctypes.c_ulong(129))      # MPOL_PREFERRED
+    return rc == 0
+
+
+def pinned_near_gpu(topo: dict, local: int, items) -> tuple[list, str]:
+    """Pinned host tensors of the given sizes (and contents: an array or
+    None), allocated and first written by a thread bound to the CPUs of the
+    GPU's NUMA node with that node preferred for its pages."""
+    import threading
+    import torch
+    res = {}
+
+    def work():
+        try:
+            how = []
+            node = topo["gpu_numa_node"]
+            if node >= 0:
+                want = set(_cpulist(topo["gpu_node_cpus"]))
+                cpus = want & set(os.sched_getaffinity(0))
+                if cpus:
+                    os.sched_setaffinity(0, cpus)
+                    how.append(f"allocated by a thread bound to CPUs "
+                               f"{_ranges(cpus)} of node {node}")
+                else:
+                    how.append(f"no CPU of node {node} in this process's "
+                               "affinity")
+                if _set_mempolicy(node):
+                    how.append(f"pages preferred on node {node}")
+            else:
+                how.append("GPU NUMA node unknown: default placement")
+            torch.cuda.set_device(local)
+            out = []
+            for n, content in items:
+                t = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+                if content is not None:
+                    t.numpy()[:] = content
+                out.append(t)
+            if node >= 0:
+                _set_mempolicy(None)
+            res["t"], res["how"] = out, "; ".join(how)
+        except Exception as exc:       # reported by the caller
+            res["err"] = exc
+
+    th = threading.Thread(target=work)
+    th.start()
+    th.join()
+    if "err" in res:
+        raise res["err"]
+    return res["t"], res["how"]
+
+
+def measure_e2e(suite, args, torch, shards=4, topo=None) -> dict:
     """The same metric through the public API with host buffers: every step
     runs layout_copy_host -- upload of the source from pinned host memory,
     the copy, download of the destination into pinned host memory -- for
@@ -669,13 +866,23 @@ def measure_e2e(suite, args, torch, shards=4) -> dict:
     the two directions of the host link.  A workload whose shards
     (Plan(..., rank, world)) own disjoint source and destination ranges runs
     as `shards` shards, each moving only its ranges, so its transfers spread
-    over several copy engines."""
-    steps = max(2, min(args.steps, 5))
+    over several copy engines.
+
+    In the same run, the same uploads and downloads without the copies give
+    the link's ceilings for these byte counts: uploads alone, downloads
+    alone, and both at once (the end-to-end figure's own bound).  Pinned
+    buffers are allocated near the GPU (pinned_near_gpu)."""
+    steps = max(20, min(args.steps, 40))
     lm = suite.lm
-    jobs, h2d, d2h, sharded = [], 0, 0, []
-    for it in suite.items:
-        hs = torch.from_numpy(it["host"]).pin_memory()
-        hd = torch.empty(it["dst"].numel(), dtype=torch.uint8).pin_memory()
+    local = suite.items[0]["src"].device.index or 0
+    topo = topo or host_topology(local)
+    pinned, how = pinned_near_gpu(
+        topo, local, [x for it in suite.items
+                      for x in ((it["host"].size, it["host"]),
+                                (it["dst"].numel(), None))])
+    jobs, h2d, d2h, sharded, moves = [], 0, 0, [], []
+    for k, it in enumerate(suite.items):
+        hs, hd = pinned[2 * k], pinned[2 * k + 1]
         eb = it["w"].elem_bytes
         plans = [lm.Plan(it["S"], it["D"], eb, rank=r, world=shards)
                  for r in range(shards)]
@@ -685,50 +892,87 @@ def measure_e2e(suite, args, torch, shards=4) -> dict:
             plans, descs = [it["plan"]], [it["plan"].describe()]
         else:
             sharded.append(it["name"])
+        whole = len(plans) == 1
         for p, d in zip(plans, descs):
             jobs.append((p, hs, hd, it["src"], it["dst"]))
-            whole = len(plans) == 1
-            h2d += hs.numel() if whole else (d["src_range"][1] -
-                                             d["src_range"][0]) * eb
-            d2h += (d["dst_range"][1] - d["dst_range"][0]) * eb
+            up = ((0, hs.numel()) if whole else
+                  (d["src_range"][0] * eb, d["src_range"][1] * eb))
+            down = (d["dst_range"][0] * eb, d["dst_range"][1] * eb)
+            moves.append((hs, hd, it["src"], it["dst"], up, down))
+            h2d += up[1] - up[0]
+            d2h += down[1] - down[0]
     main = torch.cuda.current_stream()
     streams = [torch.cuda.Stream() for _ in jobs]
 
-    def one():
+    def copies():
         for (p, hs, hd, sdev, ddev), st in zip(jobs, streams):
             lm.layout_copy_host(p, hs, hd, sdev, ddev, st)
 
-    def fork():
-        ev = torch.cuda.Event()
-        ev.record(main)
-        for st in streams:
-            st.wait_event(ev)
+    def transfers(up: bool, down: bool):
+        def run():
+            for (hs, hd, sdev, ddev, (u0, u1), (d0, d1)), st in zip(moves,
+                                                                   streams):
+                with torch.cuda.stream(st):
+                    if up:
+                        sdev[u0:u1].copy_(hs[u0:u1], non_blocking=True)
+                    if down:
+                        hd[d0:d1].copy_(ddev[d0:d1], non_blocking=True)
+        return run
 
-    def join():
-        for st in streams:
+    def timed(fn) -> float:
+        """ms per step of fn over `steps` steps, streams forked from and
+        joined to the current stream around them."""
+        def fork():
             ev = torch.cuda.Event()
-            ev.record(st)
-            main.wait_event(ev)
+            ev.record(main)
+            for st in streams:
+                st.wait_event(ev)
 
-    fork()
-    one()
-    join()
-    torch.cuda.synchronize()
-    start, end = (torch.cuda.Event(enable_timing=True),
-                  torch.cuda.Event(enable_timing=True))
-    start.record(main)
-    fork()
-    for _ in range(steps):
-        one()
-    join()
-    end.record(main)
-    torch.cuda.synchronize()
-    ms = start.elapsed_time(end)
-    return {"ms": ms, "unit": UNIT, "h2d_bytes_per_step": h2d,
+        def join():
+            for st in streams:
+                ev = torch.cuda.Event()
+                ev.record(st)
+                main.wait_event(ev)
+
+        fork()
+        fn()
+        join()
+        torch.cuda.synchronize()
+        start, end = (torch.cuda.Event(enable_timing=True),
+                      torch.cuda.Event(enable_timing=True))
+        start.record(main)
+        fork()
+        for _ in range(steps):
+            fn()
+        join()
+        end.record(main)
+        torch.cuda.synchronize()
+        return start.elapsed_time(end) / steps
+
+    ms = timed(copies)
+    if lm.device_status() != 0:
+        raise RuntimeError("a copy kernel gave up a bounded wait "
+                           "(LM_E_TIMEOUT): the end-to-end run is invalid")
+    up_ms = timed(transfers(True, False))
+    down_ms = timed(transfers(False, True))
+    both_ms = timed(transfers(True, True))
+    gb = 1e9
+    return {"ms": ms * steps, "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps,
             "path": f"layout_copy_host, {len(jobs)} plans on their own "
                     f"streams ({', '.join(sharded) or 'none'} as {shards} "
-                    "shards each)"}
+                    "shards each)",
+            "h2d_ceiling_gbs": round(h2d / (up_ms * 1e-3) / gb, 1),
+            "d2h_ceiling_gbs": round(d2h / (down_ms * 1e-3) / gb, 1),
+            "duplex_ceiling_gbs": round((h2d + d2h) / (both_ms * 1e-3) / gb,
+                                        1),
+            "transfers_only_value": round(
+                suite.bytes_per_step / (both_ms * 1e-3) / gb, 1),
+            "ceilings": "the same uploads and downloads on the same streams "
+                        "without the copies, this run: uploads alone, "
+                        "downloads alone, both at once; transfers_only_value "
+                        "is the metric for the last (the bound of value)",
+            "pinned": how, "topology": topo}
 
 
 # --------------------------------------------------------------------------
@@ -738,7 +982,10 @@ def measure_e2e(suite, args, torch, shards=4) -> dict:
 class OracleWindows:
     """The CPU oracle's copy over windows of each workload's logical
     indices (the same fraction of every workload, so a sample mirrors the
-    suite's mix).  Buffers are full-size host arrays."""
+    suite's mix).  Buffers are full-size host arrays.  With threads > 1 each
+    window is split into that many contiguous index ranges, copied by one
+    thread each (numpy releases the interpreter lock inside the oracle's
+    array operations, so the threads run on separate cores)."""
 
     def __init__(self, names, bufs):
         from oracle import layout_oracle as lo
@@ -750,8 +997,10 @@ class OracleWindows:
         for _, out in bufs.values():   # map every page before timing
             out.fill(0)
 
-    def run(self, frac: float, shift: int = 0):
+    def run(self, frac: float, shift: int = 0, threads: int = 1):
+        from concurrent.futures import ThreadPoolExecutor
         nbytes, elems = 0.0, 0
+        pool = ThreadPoolExecutor(threads) if threads > 1 else None
         t0 = time.perf_counter()
         for name in self.names:
             S, D = self.exprs[name]
@@ -759,46 +1008,76 @@ class OracleWindows:
             inp, out = self.bufs[name]
             n = max(1, min(S.size, int(S.size * frac)))
             start = (shift * n) % max(1, S.size - n + 1)
-            idx = np.arange(start, start + n, dtype=np.int64)
-            self.lo.copy(S, D, inp, out, eb, indices=idx)
+
+            def part(k, S=S, D=D, eb=eb, inp=inp, out=out, n=n, start=start):
+                a = start + n * k // threads
+                b = start + n * (k + 1) // threads
+                if b > a:
+                    idx = np.arange(a, b, dtype=np.int64)
+                    self.lo.copy(S, D, inp, out, eb, indices=idx)
+
+            if pool is None:
+                part(0)
+            else:
+                list(pool.map(part, range(threads)))
             nbytes += ALGO_BYTES[name] * n / S.size
             elems += n
-        return time.perf_counter() - t0, nbytes, elems
+        dt = time.perf_counter() - t0
+        if pool is not None:
+            pool.shutdown()
+        return dt, nbytes, elems
 
-    def calibrate(self, seconds: float, least: float = 2.0 ** -20) -> float:
+    def calibrate(self, seconds: float, least: float = 2.0 ** -20,
+                  threads: int = 1) -> float:
         """Fraction of every workload that takes about `seconds` (at least
         `least`): two probe windows give the fixed cost and the cost per
         fraction."""
         p1, p2 = 2.0 ** -11, 2.0 ** -7
-        t1, _, _ = self.run(p1)
-        t2, _, _ = self.run(p2)
+        t1, _, _ = self.run(p1, threads=threads)
+        t2, _, _ = self.run(p2, threads=threads)
         per = max((t2 - t1) / (p2 - p1), 1e-6)
         fixed = max(t1 - per * p1, 0.0)
         f = min(1.0, max(least, (seconds - fixed) / per))
         # large windows cost more per element than the probes (fresh
         # temporaries): one run at the estimate corrects it
-        t, _, _ = self.run(f)
+        t, _, _ = self.run(f, threads=threads)
         return min(1.0, max(least, f * seconds / max(t, 1e-4)))
 
 
+def host_cores() -> int:
+    return len(os.sched_getaffinity(0))
+
+
 def cpu_baseline(suite) -> dict:
+    """The oracle as it stands, on this host: one core, then every core of
+    the process's affinity (the same loop over contiguous index ranges, one
+    thread each), each on a window of about 8 s of work."""
     bufs = {it["name"]: (it["host"],
                          np.zeros(it["dst"].numel(), dtype=np.uint8))
             for it in suite.items}
     ow = OracleWindows(BENCH_SUITE, bufs)
-    frac = ow.calibrate(12.0, least=2.0 ** -7)
-    secs, nbytes, elems = ow.run(frac)
-    return {"value": round(nbytes / secs / 1e9, 3), "unit": UNIT, "cores": 1,
-            "kind": "oracle",
+    legs = {}
+    ncores = host_cores()
+    for key, threads in (("cores_1", 1), ("cores_all", ncores)):
+        frac = ow.calibrate(8.0, least=2.0 ** -7, threads=threads)
+        secs, nbytes, elems = ow.run(frac, threads=threads)
+        legs[key] = {
+            "value": round(nbytes / secs / 1e9, 3), "threads": threads,
             "sample": f"numpy oracle copy of {frac:.4f} of every workload's "
-                      f"logical indices (one contiguous window each), "
-                      f"{elems} elements in {secs:.1f} s, single thread"}
+                      f"logical indices (one contiguous window each, split "
+                      f"into {threads} ranges), {elems} elements in "
+                      f"{secs:.1f} s"}
+    return {"value": legs["cores_all"]["value"], "unit": UNIT,
+            "cores": ncores, "kind": "oracle",
+            "sample": legs["cores_all"]["sample"],
+            "cores_1": legs["cores_1"], "cores_all": legs["cores_all"],
+            "nproc": ncores, "cpu_model": cpu_model()}
 
 
 def run_reference(args) -> dict | None:
-    """The reference arm: the CPU oracle as it stands, on this host's cores,
-    each step a window of every workload sized so the whole run takes about
-    a minute."""
+    """The reference arm: the CPU oracle as it stands, on every host core of
+    this process (contiguous index ranges, one thread each), each step a
+    window of every workload sized so the whole run takes about a minute."""
     world, rank, _ = dist_env()
     if rank != 0:
         return None
@@ -810,13 +1089,14 @@ def run_reference(args) -> dict | None:
         bufs[name] = (seeded_bytes(w.values, w.dtype, lo.cosize(S), w.seed),
                       np.zeros(lo.cosize(D) * w.elem_bytes, dtype=np.uint8))
     ow = OracleWindows(BENCH_SUITE, bufs)
+    threads = host_cores()
     per_step = 60.0 / (args.steps + args.warmup)
-    frac = ow.calibrate(per_step)
+    frac = ow.calibrate(per_step, threads=threads)
     for k in range(args.warmup):
-        ow.run(frac, shift=k)
+        ow.run(frac, shift=k, threads=threads)
     secs, nbytes, elems = 0.0, 0.0, 0
     for k in range(args.steps):
-        t, b, e = ow.run(frac, shift=args.warmup + k)
+        t, b, e = ow.run(frac, shift=args.warmup + k, threads=threads)
         secs += t
         nbytes += b
         elems += e
@@ -831,10 +1111,13 @@ def run_reference(args) -> dict | None:
         "config": {"workload": "relayout suite C2+C3+C4+C5a+C5b, one "
                                "layout_copy each per step",
                    "sample_fraction_per_step": frac},
-        "cpu_baseline": {"value": round(gbs, 4), "unit": UNIT, "cores": 1,
-                         "kind": "oracle",
+        "cpu_baseline": {"value": round(gbs, 4), "unit": UNIT,
+                         "cores": threads, "kind": "oracle",
                          "sample": f"{frac:.2e} of every workload per step, "
-                                   f"{elems} logical indices in {secs:.1f} s"},
+                                   f"{elems} logical indices in {secs:.1f} s, "
+                                   f"{threads} threads over contiguous index "
+                                   "ranges",
+                         "nproc": threads, "cpu_model": cpu_model()},
         "e2e": {"value": round(gbs, 4), "unit": UNIT,
                 "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }

@@ -333,7 +333,11 @@ int lm_plan_extent(const lm_plan* plan, int64_t* size, int64_t* src_cosize,
  * alignment and the pointers lack it, the same plan runs with narrower
  * accesses.  Destination slots outside dst's image are not written.  The
  * call returns after enqueueing; it synchronises nothing.  A launch failure
- * returns LM_E_CUDA (lm_last_cuda_error has the cudaError_t). */
+ * returns LM_E_CUDA (lm_last_cuda_error has the cudaError_t).  For plans
+ * whose description shows a STAGED piece with "bulk" set, LM_OK is
+ * provisional: those kernels bound their waits on the device, and a wait
+ * that gives up is reported only by lm_device_status, which a caller that
+ * needs the result must check after the stream has reached the copy. */
 int lm_layout_copy(const lm_plan* plan, const void* src_dev,
                    int64_t src_capacity_elems, void* dst_dev,
                    int64_t dst_capacity_elems, void* cuda_stream);
@@ -507,10 +511,16 @@ int lm_last_cuda_error(void);
  * then report in *status whether a kernel of this library on the current
  * device gave up a bounded wait since the last reset: LM_OK, or
  * LM_E_TIMEOUT (the bulk-copy STAGED kernels bound every mbarrier wait at
- * about a second; a block that gives up records it here, drains its own
- * copies and exits, leaving its part of the destination unwritten).  The
- * record is per device, shared by every stream and sticky; reset != 0
- * clears it after reading.  Errors: LM_E_INVALID (NULL status), LM_E_CUDA. */
+ * about a second; a block that gives up records it here, waits -- again
+ * bounded, about four seconds per stage -- for its own copies still in
+ * flight, and exits, leaving its part of the destination unwritten).  If
+ * even that drain runs out (copies from global memory that do not complete
+ * in seconds mean the memory system has failed), the block has exited with
+ * bulk copies still writing into shared memory it no longer owns, which can
+ * corrupt a later block on that SM: after LM_E_TIMEOUT treat every result
+ * on the device since the last reset as suspect.  The record is per device,
+ * shared by every stream and sticky; reset != 0 clears it after reading.
+ * Errors: LM_E_INVALID (NULL status), LM_E_CUDA. */
 int lm_device_status(void* cuda_stream, int reset, int* status);
 
 /* Self-test of the bounded device wait (no counterpart on the source

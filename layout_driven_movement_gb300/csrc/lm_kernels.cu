@@ -796,13 +796,20 @@ __global__ void __launch_bounds__(256)
 // tile loop.
 //
 // Every wait is bounded (kWaitCycles of clock64, about a second): a wait
-// that gives up sets bit 0 of g_lm_device_status, the producer then waits,
-// again bounded, for the copies it still has in flight, and the block
-// returns.  The host reads the word with lm_device_status.
+// that gives up sets bit 0 of g_lm_device_status, and the producer then
+// waits for the copies it still has in flight (kDrainCycles per stage) so
+// that the block leaves no bulk copy writing into shared memory it no longer
+// owns.  The drain is bounded too: copies from global memory complete unless
+// the memory system itself has failed, so a drain that still runs out sets
+// bit 1 -- the block has exited with copies in flight, which may overwrite
+// the shared memory of a block that runs on that SM later -- and the host
+// must then treat the device's results as suspect.  The host reads the word
+// with lm_device_status.
 // ---------------------------------------------------------------------------
 
 __device__ unsigned int g_lm_device_status = 0;
 constexpr long long kWaitCycles = 2000000000LL;
+constexpr long long kDrainCycles = 4 * kWaitCycles;
 constexpr int kBulkSegsPerLane = 4;  // up to 128 segments per tile
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -833,17 +840,19 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 // Bounded wait for the phase with the given parity to complete.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          long long limit = kWaitCycles) {
   if (mbar_try(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try(bar, parity))
-    if (clock64() - t0 > kWaitCycles) return false;
+    if (clock64() - t0 > limit) return false;
   return true;
 }
 // The same, agreed by the whole warp (every lane waits, so every lane has
 // acquired the phase; the warp proceeds only if all lanes saw it complete).
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
-  return __all_sync(0xffffffffu, mbar_wait(bar, parity));
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity,
+                                          long long limit = kWaitCycles) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, limit));
 }
 
 __device__ __forceinline__ void bulk_g2s(uint32_t dst_smem, const void* src,
@@ -957,9 +966,12 @@ __global__ void __launch_bounds__(256)
   }
   if (!ok) {
     if (lane == 0) atomicOr(&g_lm_device_status, 1u);
-    if (warp == 0)  // drain this block's copies still in flight
-      for (uint32_t j = i; j < issued; ++j)
-        warp_wait(full(j % NS), (j / NS) & 1);
+    if (warp == 0) {  // drain this block's copies still in flight
+      bool drained = true;
+      for (uint32_t j = i; j < issued && drained; ++j)
+        drained = warp_wait(full(j % NS), (j / NS) & 1, kDrainCycles);
+      if (!drained && lane == 0) atomicOr(&g_lm_device_status, 2u);
+    }
   }
 }
 

@@ -54,6 +54,7 @@ def run_exchange(src, dst, eb, world, name=""):
             if recv.numel():
                 x.unpack(p, recv, dl)
         torch.cuda.synchronize()
+        assert lm.device_status() == 0
         check_rank(d, dl.cpu().numpy(), want, eb, q)
 
 
@@ -120,6 +121,7 @@ def test_pack_all_and_unpack_all(case, world):
                         device="cuda")
         lm.exchange_unpack_all(x, recv, dl)
         torch.cuda.synchronize()
+        assert lm.device_status() == 0
         check_rank(d, dl.cpu().numpy(), want, eb, q)
 
 
@@ -147,6 +149,7 @@ def test_exchange_copy_single_rank_nccl():
                          device="cuda")
         lm.exchange_copy(x, local, out)
         torch.cuda.synchronize()
+        assert lm.device_status() == 0
         check_rank(d, out.cpu().numpy(), want, eb, 0)
     finally:
         dist.destroy_process_group()

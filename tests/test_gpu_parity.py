@@ -81,6 +81,8 @@ def run_case(src_spec, dst_spec, eb, values="bytes", dtype="uint8", seed=7,
                                d_view.data_ptr(), n_dst_cap, stream)
         stream.synchronize()
     torch.cuda.synchronize()
+    # a bulk-path LM_OK holds only once no bounded wait gave up
+    assert lm.device_status() == 0
     got = d_view.cpu().numpy()
     bad = np.nonzero(got != want)[0]
     assert bad.size == 0, (
