@@ -660,6 +660,10 @@ def build_layout(spec) -> Layout:
         return build_layout(spec[1]).compose(build_layout(spec[2]))
     if kind == "zipped_divide":
         return build_layout(spec[1]).zipped_divide(list(spec[2]))
+    if kind == "blocked_product":
+        return build_layout(spec[1]).blocked_product(build_layout(spec[2]))
+    if kind == "logical_product":
+        return build_layout(spec[1]).logical_product(build_layout(spec[2]))
     if kind == "concat":
         parts: Iterable = [build_layout(s) for s in spec[1:]]
         it = iter(parts)

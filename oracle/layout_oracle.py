@@ -633,7 +633,8 @@ def build(spec):
 
     ("layout", shape, stride) | ("swizzle", B, M, S, spec) |
     ("compose", outer, inner) | ("zipped_divide", spec, tiler) |
-    ("concat", spec, spec, ...)"""
+    ("concat", spec, spec, ...) | ("blocked_product", tile, grid) |
+    ("logical_product", tile, grid); the products take plain layouts"""
     kind = spec[0]
     if kind == "layout":
         return Layout(spec[1], spec[2])
@@ -645,4 +646,8 @@ def build(spec):
         return ZippedDivide(build(spec[1]), spec[2])
     if kind == "concat":
         return Concat(*[build(s) for s in spec[1:]])
+    if kind == "blocked_product":
+        return BlockedProduct(build(spec[1]), build(spec[2]))
+    if kind == "logical_product":
+        return LogicalProduct(build(spec[1]), build(spec[2]))
     raise ValueError(f"unknown layout description {kind!r}")

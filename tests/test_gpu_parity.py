@@ -14,6 +14,7 @@ import pytest
 
 from oracle import layout_oracle as lo
 from workloads import EVAL_C1, WORKLOADS, seeded_bytes
+from product_cases import PRODUCT_CASES
 
 torch = pytest.importorskip("torch")
 lm = pytest.importorskip("layout_driven_movement_gb300")
@@ -288,6 +289,22 @@ def test_layout_eval_c1_blocked_page_values():
     # (r=1, c=0) -> 2 and (r=3, c=1)? read as the leaf coordinate (3,0,1,0):
     # colex index 3 + 4*0 + 8*1 = 11 -> 6 + 1 = 7
     assert t[1] == 2 and t[3 + 8] == 7
+
+
+# --------------------------------------------------------------------------
+# layouts built by the products ("CUTE布局代数" §4.1), copied on the device
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("case", PRODUCT_CASES, ids=[c[0] for c in PRODUCT_CASES])
+def test_product_built_layouts(case):
+    """Copies whose source or destination the library builds with
+    blocked_product / logical_product, compared in full with the oracle's
+    products (BlockedProduct, LogicalProduct) through its copy."""
+    name, s, d, eb, built, paths = case
+    side = s if s[0].endswith("product") else d
+    assert str(lm.build_layout(side)) == built
+    run_case(s, d, eb, seed=900 + sum(map(ord, name)) % 97,
+             expect_paths=paths)
 
 
 # --------------------------------------------------------------------------

@@ -613,3 +613,18 @@ def test_print_grid_matches_oracle_and_page_grids():
     for bad in ["8:1", "(2,2,2):(1,2,4)"]:
         with pytest.raises(lm.LayoutMoveError):
             lm.Layout.parse(bad).print_grid()
+
+
+def test_product_built_copy_layouts_match_oracle():
+    """The product-built layouts of the GPU product cases: the library's
+    closed forms, and their offsets at seeded sample indices equal to the
+    oracle's products."""
+    from product_cases import PRODUCT_CASES
+    rng = np.random.default_rng(31)
+    for name, s, d, eb, built, _ in PRODUCT_CASES:
+        spec = s if s[0].endswith("product") else d
+        L, OL = lm.build_layout(spec), lo.build(spec)
+        assert str(L) == built, name
+        assert L.size == OL.size and L.cosize == lo.cosize(OL), name
+        idx = np.concatenate([[0, L.size - 1], rng.integers(0, L.size, 2000)])
+        assert [L(int(i)) for i in idx] == OL.at(idx).tolist(), name
