@@ -66,6 +66,9 @@ TV_CONFIGS = {
     # the same with 16-byte loads; the store phase then conflicts 4 ways
     "C2v": ("Sw<3,2,6> o (64,64):(1,64)", "(16,16):(1,16)", "(8,32):(32,1)",
             (64, 64)),
+    # the conflict-free tile with the planner's tuned stripmined thread
+    # layouts (no thread layout given)
+    "C2t": ("Sw<5,0,6> o (64,64):(1,64)", None, None, (64, 64)),
 }
 FALLBACK_HBM_GBS = 6800.0
 
@@ -567,8 +570,10 @@ def measure_tv(suite, args, torch, peak) -> dict:
         S, D = it["S"], it["D"]
         if tiler:
             S, D = S.zipped_divide(list(tiler)), D.zipped_divide(list(tiler))
-        plan = lm.TVPlan(S, lm.Layout.parse(smem), D, lm.Layout.parse(tl),
-                         lm.Layout.parse(ts), it["w"].elem_bytes)
+        plan = lm.TVPlan(S, lm.Layout.parse(smem), D,
+                         lm.Layout.parse(tl) if tl else None,
+                         lm.Layout.parse(ts) if ts else None,
+                         it["w"].elem_bytes)
         runs.append((key, it, plan))
     if not runs:
         return {}
@@ -593,8 +598,9 @@ def measure_tv(suite, args, torch, peak) -> dict:
         gbs = it["bytes"] / (ms * 1e-3) / 1e9
         d = plan.describe()
         out[key] = {
-            "smem": TV_CONFIGS[key][0], "thr_load": TV_CONFIGS[key][1],
-            "thr_store": TV_CONFIGS[key][2],
+            "smem": TV_CONFIGS[key][0], "thr_load": d["load"]["thr"],
+            "thr_store": d["store"]["thr"],
+            "tuned": [d["load"]["tuned"], d["store"]["tuned"]],
             "vec_bytes": [d["load"]["vec_bytes"], d["store"]["vec_bytes"]],
             "smem_wavefronts_per_tile": [
                 [d["load"]["smem_wavefronts"], d["load"]["smem_wavefronts_ideal"]],

@@ -468,10 +468,21 @@ void lm_exchange_destroy(lm_exchange* x);
  * 16, 8, ..., elem_bytes that works) along one tile mode: that many
  * consecutive coordinates must be contiguous and aligned on both of its
  * sides; the thread layout then partitions the tile with that mode counted
- * in vectors, at most 128 vectors per thread.  lm_tv_plan_describe gives
- * the choices and the shared-memory wavefronts the bank model of
- * lm_smem_wavefronts predicts per tile for each phase.
- * Errors: LM_E_INVALID (NULL, elem_bytes, limits above, empty tile),
+ * in vectors, at most 128 vectors per thread.  A NULL thread layout asks
+ * for the tuned one: the stripmined map of the PitchLinearStripminedThreadMap
+ * article (§2.2) with Pitch and Strips chosen as lm_stripmined_tune chooses
+ * them (§4.1-§4.2: fewest 128-byte global segments per warp, then fewest
+ * shared-memory wavefronts), where the phase's global side gives the row
+ * (its unit-stride tile mode, else mode 0; the other mode counts rows) and
+ * the search keeps to maps whose one Pitch x Strips group holds every
+ * thread with Pitch and Strips dividing the tile, the ones a thread layout
+ * can express: (Pitch, Strips):(1, Pitch) along (row, rows), up to 256
+ * threads, on tiles of rank 1 or 2.  lm_tv_plan_describe gives the
+ * choices (the thread layouts, and Pitch, Strips and segments when tuned)
+ * and the shared-memory wavefronts the bank model of lm_smem_wavefronts
+ * predicts per tile for each phase.
+ * Errors: LM_E_INVALID (NULL src/smem/dst/out, elem_bytes, limits above,
+ * empty tile, a NULL thread layout for a tile of rank above 2),
  * LM_E_INCOMPATIBLE (sizes or tile modes differ, grids do not refine),
  * LM_E_NOT_INJECTIVE (smem or dst), LM_E_NOT_REPRESENTABLE (no vector
  * width fits, a thread extent does not divide its mode, or the offsets are

@@ -412,11 +412,16 @@ class TVPlan:
     __slots__ = ("_h", "elem_bytes")
 
     def __init__(self, src: Layout, smem: Layout, dst: Layout,
-                 thr_load: Layout, thr_store: Layout, elem_bytes: int,
-                 vec_load_bytes: int = 0, vec_store_bytes: int = 0):
+                 thr_load: Layout | None, thr_store: Layout | None,
+                 elem_bytes: int, vec_load_bytes: int = 0,
+                 vec_store_bytes: int = 0):
+        """thr_load / thr_store None: the library's tuned stripmined thread
+        layout for that phase (see lm_tv_plan_create)."""
         out = C.c_void_p()
+        tl = thr_load.handle if thr_load is not None else None
+        ts = thr_store.handle if thr_store is not None else None
         _check(lib().lm_tv_plan_create(src.handle, smem.handle, dst.handle,
-                                       thr_load.handle, thr_store.handle,
+                                       tl, ts,
                                        int(elem_bytes), int(vec_load_bytes),
                                        int(vec_store_bytes), C.byref(out)),
                "lm_tv_plan_create")

@@ -319,6 +319,13 @@ bool joint_modes(const lm_layout& src, const lm_layout& dst,
                  std::vector<JMode>& out);
 int launch_tv(const lm_tv_plan& plan, const char* src, char* dst,
               void* stream);  // lm_tv.cu
+// The Pitch/Strips search of lm_stripmined_tune (lm_plan.cpp); with
+// `partition` only one-group maps that tile the tile.
+int stripmined_search(int64_t threads, int64_t k_row, int64_t rows,
+                      int64_t ld, int elem_bytes, int vec_elems,
+                      const lm_layout* smem, bool partition, int64_t* pitch,
+                      int64_t* strips, int64_t* segments,
+                      int64_t* wavefronts);
 
 // implemented in lm_kernels.cu
 int launch_piece(const lm_plan& plan, const Piece& pc, const char* src,

@@ -1198,6 +1198,99 @@ static std::string describe(const lm_plan& P) {
 
 using lm::fail;
 
+namespace lm {
+
+// The search behind lm_stripmined_tune.  With `partition`, only maps whose
+// one Pitch x Strips group holds every thread (P*S == threads) and whose P
+// and S divide the tile's vectors per row and rows are candidates: those
+// are the pitch-linear thread layouts (P, S):(1, P) that tile the tile, the
+// form a local_partition thread layout can take.
+int stripmined_search(int64_t threads, int64_t k_row, int64_t rows,
+                      int64_t ld, int elem_bytes, int vec_elems,
+                      const lm_layout* smem, bool partition, int64_t* pitch,
+                      int64_t* strips, int64_t* segments,
+                      int64_t* wavefronts) {
+  if (threads < 1 || threads > 1024 || k_row < 1 || rows < 1 || ld < k_row ||
+      vec_elems < 1 || k_row % vec_elems)
+    return LM_E_INVALID;
+  const int64_t vb = int64_t(elem_bytes) * vec_elems;
+  if (elem_bytes < 1 || vb > 16 || (vb & (vb - 1)) ||
+      (elem_bytes & (elem_bytes - 1)))
+    return LM_E_INVALID;
+  if (smem) {
+    const std::vector<Node> m = top_modes(*smem);
+    if (m.size() != 2) return LM_E_INVALID;
+    int64_t s0 = 1, s1 = 1;
+    for (const Leaf& l : flatten(m[0])) s0 *= l.e;
+    for (const Leaf& l : flatten(m[1])) s1 *= l.e;
+    if (s0 != rows || s1 != k_row) return LM_E_INVALID;
+  }
+  try {
+    const int64_t R = k_row / vec_elems;  // vectors per row
+    int64_t best_p = 0, best_s = 0, best_seg = -1, best_wf = -1;
+    std::vector<int64_t> gaddr(32), saddr(32);
+    bool valid[32];
+    for (int64_t P = 1; P <= R && P <= threads; P *= 2)
+      for (int64_t S = 1; S <= rows && P * S <= threads; S *= 2) {
+        if (partition && (P * S != threads || R % P || rows % S)) continue;
+        int64_t seg = 0, wf = 0;
+        bool fits = true;
+        for (int64_t w0 = 0; w0 < threads && fits; w0 += 32) {
+          int64_t segs[32];
+          int ns = 0;
+          for (int l = 0; l < 32; ++l) {
+            const int64_t t = w0 + l;
+            valid[l] = t < threads;
+            gaddr[size_t(l)] = saddr[size_t(l)] = 0;
+            if (!valid[l]) continue;
+            const int64_t d = t / P;
+            const int64_t row = d % S + (d / S) * P * S;
+            const int64_t col = (t % P) * vec_elems;
+            if (row >= rows) {
+              fits = false;
+              break;
+            }
+            const int64_t g = mul_chk(row * ld + col, elem_bytes) / 128;
+            bool seen = false;
+            for (int q = 0; q < ns; ++q) seen = seen || segs[q] == g;
+            if (!seen) segs[ns++] = g;
+            const int64_t o =
+                smem ? smem->swz.apply(eval_affine(smem->leaves,
+                                                   row + rows * col))
+                     : row * k_row + col;
+            saddr[size_t(l)] = mul_chk(o, elem_bytes);
+            if (saddr[size_t(l)] % vb) return LM_E_INVALID;
+          }
+          if (!fits) break;
+          seg += ns;
+          wf += warp_wavefronts(saddr.data(), valid, int(vb));
+        }
+        if (!fits) continue;
+        const bool better =
+            best_seg < 0 || seg < best_seg ||
+            (seg == best_seg &&
+             (wf < best_wf || (wf == best_wf && (P > best_p ||
+                                                 (P == best_p && S > best_s)))));
+        if (better) {
+          best_p = P;
+          best_s = S;
+          best_seg = seg;
+          best_wf = wf;
+        }
+      }
+    if (best_seg < 0) return LM_E_NOT_REPRESENTABLE;
+    *pitch = best_p;
+    *strips = best_s;
+    *segments = best_seg;
+    *wavefronts = best_wf;
+    return LM_OK;
+  } catch (const Error& e) {
+    return e.status;
+  }
+}
+
+}  // namespace lm
+
 extern "C" {
 
 // Shared-memory wavefronts of the accesses `access` describes: access i
@@ -1258,82 +1351,9 @@ int lm_stripmined_tune(int64_t threads, int64_t k_row, int64_t rows,
                        const lm_layout* smem, int64_t* pitch, int64_t* strips,
                        int64_t* segments, int64_t* wavefronts) {
   if (!pitch || !strips || !segments || !wavefronts) return LM_E_INVALID;
-  if (threads < 1 || threads > 1024 || k_row < 1 || rows < 1 || ld < k_row ||
-      vec_elems < 1 || k_row % vec_elems)
-    return LM_E_INVALID;
-  const int64_t vb = int64_t(elem_bytes) * vec_elems;
-  if (elem_bytes < 1 || vb > 16 || (vb & (vb - 1)) ||
-      (elem_bytes & (elem_bytes - 1)))
-    return LM_E_INVALID;
-  if (smem) {
-    const std::vector<lm::Node> m = lm::top_modes(*smem);
-    if (m.size() != 2) return LM_E_INVALID;
-    int64_t s0 = 1, s1 = 1;
-    for (const lm::Leaf& l : lm::flatten(m[0])) s0 *= l.e;
-    for (const lm::Leaf& l : lm::flatten(m[1])) s1 *= l.e;
-    if (s0 != rows || s1 != k_row) return LM_E_INVALID;
-  }
-  try {
-    const int64_t R = k_row / vec_elems;  // vectors per row
-    int64_t best_p = 0, best_s = 0, best_seg = -1, best_wf = -1;
-    std::vector<int64_t> gaddr(32), saddr(32);
-    bool valid[32];
-    for (int64_t P = 1; P <= R && P <= threads; P *= 2)
-      for (int64_t S = 1; S <= rows && P * S <= threads; S *= 2) {
-        int64_t seg = 0, wf = 0;
-        bool fits = true;
-        for (int64_t w0 = 0; w0 < threads && fits; w0 += 32) {
-          int64_t segs[32];
-          int ns = 0;
-          for (int l = 0; l < 32; ++l) {
-            const int64_t t = w0 + l;
-            valid[l] = t < threads;
-            gaddr[size_t(l)] = saddr[size_t(l)] = 0;
-            if (!valid[l]) continue;
-            const int64_t d = t / P;
-            const int64_t row = d % S + (d / S) * P * S;
-            const int64_t col = (t % P) * vec_elems;
-            if (row >= rows) {
-              fits = false;
-              break;
-            }
-            const int64_t g = lm::mul_chk(row * ld + col, elem_bytes) / 128;
-            bool seen = false;
-            for (int q = 0; q < ns; ++q) seen = seen || segs[q] == g;
-            if (!seen) segs[ns++] = g;
-            const int64_t o =
-                smem ? smem->swz.apply(lm::eval_affine(smem->leaves,
-                                                       row + rows * col))
-                     : row * k_row + col;
-            saddr[size_t(l)] = lm::mul_chk(o, elem_bytes);
-            if (saddr[size_t(l)] % vb) return LM_E_INVALID;
-          }
-          if (!fits) break;
-          seg += ns;
-          wf += lm::warp_wavefronts(saddr.data(), valid, int(vb));
-        }
-        if (!fits) continue;
-        const bool better =
-            best_seg < 0 || seg < best_seg ||
-            (seg == best_seg &&
-             (wf < best_wf || (wf == best_wf && (P > best_p ||
-                                                 (P == best_p && S > best_s)))));
-        if (better) {
-          best_p = P;
-          best_s = S;
-          best_seg = seg;
-          best_wf = wf;
-        }
-      }
-    if (best_seg < 0) return LM_E_NOT_REPRESENTABLE;
-    *pitch = best_p;
-    *strips = best_s;
-    *segments = best_seg;
-    *wavefronts = best_wf;
-    return LM_OK;
-  } catch (const lm::Error& e) {
-    return e.status;
-  }
+  return lm::stripmined_search(threads, k_row, rows, ld, elem_bytes,
+                               vec_elems, smem, false, pitch, strips,
+                               segments, wavefronts);
 }
 
 }  // extern "C"

@@ -102,7 +102,7 @@ bool vector_ok(const Side& s, const std::vector<int64_t>& n, int g,
 // Returns LM_OK or the status of the first check that failed.
 int plan_phase(const Side& from, const Side& to, const std::vector<int64_t>& n,
                const lm_layout& thr, int eb, int vec_bytes_req,
-               lm_tv_phase& P, int* g_out) {
+               lm_tv_phase& P, int* g_out, int want_g = -1) {
   if (thr.swz.on() || !compact_bijection(thr.leaves)) return LM_E_INVALID;
   if (thr.size < 1 || thr.size > 1024) return LM_E_INVALID;
   const std::vector<Node> tm = top_modes(thr);
@@ -124,6 +124,7 @@ int plan_phase(const Side& from, const Side& to, const std::vector<int64_t>& n,
   int g = -1;
   int64_t v = 1;
   for (auto [cg, cv] : cands) {
+    if (want_g >= 0 && cg != want_g) continue;
     bool fits = true;
     for (int k = 0; k < r; ++k) {
       const int64_t units = k == cg ? n[size_t(k)] / cv : n[size_t(k)];
@@ -233,6 +234,93 @@ int plan_phase(const Side& from, const Side& to, const std::vector<int64_t>& n,
   return LM_OK;
 }
 
+// A phase's thread layout when the caller gives none: the stripmined map of
+// the PitchLinearStripminedThreadMap article (§2.2), Pitch and Strips chosen
+// by the same search as lm_stripmined_tune (§4.1-§4.2: coalesced global
+// segments first, then shared-memory wavefronts under the bank model).  The
+// phase's global side fixes the row: its unit-stride tile mode a (mode 0 if
+// none) holds the vectors of a row, the other mode b counts rows, ld apart
+// in global memory.  A thread layout must tile a contiguous block
+// (local_partition), which the stripmined map does when one Pitch x Strips
+// group holds every thread, so only those candidates are searched: the
+// thread layout is (P, S):(1, P) over (a, b), P threads along a row and S
+// rows.  Up to 256 threads; fewer when the tile has fewer vectors or no
+// candidate divides it.  Tiles of rank 1 or 2 only.
+struct TunedThreads {
+  lm_layout thr;
+  int mode = 0;        // a, the vector mode
+  int64_t vec = 1;     // elements per vector
+  int64_t pitch = 0, strips = 0, segments = 0, wavefronts = 0;
+};
+
+TunedThreads default_threads(const Side& global, const Side& shared,
+                             const std::vector<int64_t>& n,
+                             const lm_layout& smem, int eb, int vec_bytes_req) {
+  const int r = int(n.size());
+  if (r < 1 || r > 2) fail(LM_E_INVALID);
+  TunedThreads T;
+  // the global side's unit-stride mode
+  int a = 0;
+  int64_t before = 1;
+  for (int k = 0; k < r; ++k) {
+    if (n[size_t(k)] > 1 &&
+        global.off[size_t(before)] - global.off[0] == 1) {
+      a = k;
+      break;
+    }
+    before *= n[size_t(k)];
+  }
+  const int b = r == 2 ? 1 - a : -1;
+  const int64_t k_row = n[size_t(a)];
+  const int64_t rows = b >= 0 ? n[size_t(b)] : 1;
+  int64_t ld = k_row;
+  if (b >= 0) {
+    const int64_t wb = b == 0 ? 1 : n[0];
+    ld = std::max(k_row, global.off[size_t(wb)] - global.off[0]);
+  }
+  // the widest vector along a that both sides take
+  const int64_t vmax = std::max<int64_t>(1, 16 / eb);
+  int64_t v = 0;
+  for (int64_t c = vmax; c >= 1; c /= 2) {
+    if (vec_bytes_req > 0 && c * eb != vec_bytes_req) continue;
+    if (k_row % c == 0 && vector_ok(global, n, a, c) &&
+        vector_ok(shared, n, a, c)) {
+      v = c;
+      break;
+    }
+  }
+  if (v == 0) fail(LM_E_NOT_REPRESENTABLE);
+  // the shared layout seen as (rows, k_row)
+  lm_layout view;
+  const std::vector<Node> sm = top_modes(smem);
+  if (r == 1)
+    view.root = Node::make_tuple({Node::make_leaf(1, 0), sm[0]});
+  else
+    view.root = Node::make_tuple({sm[size_t(b)], sm[size_t(a)]});
+  view.swz = smem.swz;
+  finalize(view);
+  int64_t units = (k_row / v) * rows, threads = 1;
+  while (threads * 2 <= std::min<int64_t>(256, units)) threads *= 2;
+  int rc = LM_E_NOT_REPRESENTABLE;
+  for (; threads >= 1 && rc != LM_OK; threads /= 2)
+    rc = stripmined_search(threads, k_row, rows, ld, eb, int(v), &view, true,
+                           &T.pitch, &T.strips, &T.segments, &T.wavefronts);
+  if (rc != LM_OK) fail(rc);
+  // (P, S):(1, P) over (a, b), written in the tile's mode order
+  if (r == 1)
+    T.thr.root = Node::make_leaf(T.pitch, 1);
+  else if (a == 0)
+    T.thr.root = Node::make_tuple(
+        {Node::make_leaf(T.pitch, 1), Node::make_leaf(T.strips, T.pitch)});
+  else
+    T.thr.root = Node::make_tuple(
+        {Node::make_leaf(T.strips, T.pitch), Node::make_leaf(T.pitch, 1)});
+  finalize(T.thr);
+  T.mode = a;
+  T.vec = v;
+  return T;
+}
+
 // Simulated shared-memory wavefronts of one tile for one phase's shared
 // side (`from` when reading the tile, `to` when writing it).
 int64_t phase_wavefronts(const lm_tv_phase& P, const Swz& z,
@@ -287,8 +375,8 @@ void set_swz(int32_t* out, const Swz& z) {
 }
 
 lm_tv_plan plan_tv(const lm_layout& src, const lm_layout& smem,
-                   const lm_layout& dst, const lm_layout& thr_load,
-                   const lm_layout& thr_store, int eb, int vec_load,
+                   const lm_layout& dst, const lm_layout* thr_load,
+                   const lm_layout* thr_store, int eb, int vec_load,
                    int vec_store) {
   if (eb != 1 && eb != 2 && eb != 4 && eb != 8 && eb != 16)
     fail(LM_E_INVALID);
@@ -389,9 +477,17 @@ lm_tv_plan plan_tv(const lm_layout& src, const lm_layout& smem,
 
   A.offsets32 = fits31(S.off) && fits31(D.off) ? 1 : 0;
   int gl = 0, gsd = 0;
-  int rc = plan_phase(S, M, n, thr_load, eb, vec_load, A.load, &gl);
+  // phases without a thread layout from the caller get the tuned one
+  TunedThreads tl, ts;
+  if (!thr_load) tl = default_threads(S, M, n, smem, eb, vec_load);
+  if (!thr_store) ts = default_threads(D, M, n, smem, eb, vec_store);
+  int rc = thr_load ? plan_phase(S, M, n, *thr_load, eb, vec_load, A.load, &gl)
+                    : plan_phase(S, M, n, tl.thr, eb, int(tl.vec * eb),
+                                 A.load, &gl, tl.mode);
   if (rc != LM_OK) fail(rc);
-  rc = plan_phase(M, D, n, thr_store, eb, vec_store, A.store, &gsd);
+  rc = thr_store ? plan_phase(M, D, n, *thr_store, eb, vec_store, A.store, &gsd)
+                 : plan_phase(M, D, n, ts.thr, eb, int(ts.vec * eb), A.store,
+                              &gsd, ts.mode);
   if (rc != LM_OK) fail(rc);
   A.block_threads =
       int32_t((std::max(A.load.n_thr, A.store.n_thr) + 31) / 32 * 32);
@@ -402,6 +498,16 @@ lm_tv_plan plan_tv(const lm_layout& src, const lm_layout& smem,
   const Swz zb = bytes_swz(smem.swz, eb);
   const int64_t wl = phase_wavefronts(A.load, zb, true, &wl_ideal);
   const int64_t ws = phase_wavefronts(A.store, zb, false, &ws_ideal);
+  auto tuned = [](const lm_layout* given, const TunedThreads& t) {
+    std::ostringstream o;
+    o << ",\"thr\":\"" << to_string(given ? *given : t.thr) << "\"";
+    if (given)
+      o << ",\"tuned\":false";
+    else
+      o << ",\"tuned\":true,\"pitch\":" << t.pitch << ",\"strips\":"
+        << t.strips << ",\"segments\":" << t.segments;
+    return o.str();
+  };
   std::ostringstream os;
   os << "{\"path\":\"TV\",\"n_tiles\":" << A.n_tiles
      << ",\"tile_elems\":" << tile_size << ",\"smem_bytes\":" << A.smem_bytes
@@ -409,11 +515,12 @@ lm_tv_plan plan_tv(const lm_layout& src, const lm_layout& smem,
      << A.load.n_thr << ",\"values\":" << A.load.n_val
      << ",\"vec_bytes\":" << A.load.vec_bytes << ",\"vec_mode\":" << gl
      << ",\"smem_wavefronts\":" << wl << ",\"smem_wavefronts_ideal\":"
-     << wl_ideal << "},\"store\":{\"threads\":" << A.store.n_thr
+     << wl_ideal << tuned(thr_load, tl)
+     << "},\"store\":{\"threads\":" << A.store.n_thr
      << ",\"values\":" << A.store.n_val << ",\"vec_bytes\":"
      << A.store.vec_bytes << ",\"vec_mode\":" << gsd
      << ",\"smem_wavefronts\":" << ws << ",\"smem_wavefronts_ideal\":"
-     << ws_ideal << "}}";
+     << ws_ideal << tuned(thr_store, ts) << "}}";
   P.describe = os.str();
   return P;
 }
@@ -429,11 +536,10 @@ int lm_tv_plan_create(const lm_layout* src, const lm_layout* smem,
                       int vec_load_bytes, int vec_store_bytes,
                       lm_tv_plan** out) {
   if (out) *out = nullptr;
-  if (!src || !smem || !dst || !thr_load || !thr_store || !out)
-    return LM_E_INVALID;
+  if (!src || !smem || !dst || !out) return LM_E_INVALID;
   try {
-    *out = new lm_tv_plan(lm::plan_tv(*src, *smem, *dst, *thr_load,
-                                      *thr_store, elem_bytes, vec_load_bytes,
+    *out = new lm_tv_plan(lm::plan_tv(*src, *smem, *dst, thr_load, thr_store,
+                                      elem_bytes, vec_load_bytes,
                                       vec_store_bytes));
     return LM_OK;
   } catch (const lm::Error& e) {

@@ -44,7 +44,9 @@ def run_tv(src_spec, smem_spec, dst_spec, thr_l, thr_s, eb, vl=0, vs=0,
            seed=11, expect=None):
     S, D = lm.build_layout(src_spec), lm.build_layout(dst_spec)
     M = lm.build_layout(smem_spec)
-    plan = lm.TVPlan(S, M, D, lm.Layout.parse(thr_l), lm.Layout.parse(thr_s),
+    plan = lm.TVPlan(S, M, D,
+                     lm.Layout.parse(thr_l) if thr_l is not None else None,
+                     lm.Layout.parse(thr_s) if thr_s is not None else None,
                      eb, vl, vs)
     desc = plan.describe()
     if expect:
@@ -74,6 +76,34 @@ def run_tv(src_spec, smem_spec, dst_spec, thr_l, thr_s, eb, vl=0, vs=0,
 def test_tv_copy_matches_oracle(case):
     _, src, smem, dst, tl, ts, eb, expect = case
     run_tv(src, smem, dst, tl, ts, eb, expect=expect)
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_tv_copy_tuned_thread_layouts(case):
+    """The same cases with no thread layouts: each phase runs the stripmined
+    map whose Pitch and Strips the planner tuned (segments, then bank
+    wavefronts); the result is the oracle's copy."""
+    name, src, smem, dst, _, _, eb, _ = case
+    if name == "nested_tile_modes":      # no tuned layout for nested modes
+        return
+    desc = run_tv(src, smem, dst, None, None, eb, seed=13)
+    assert desc["load"]["tuned"] and desc["store"]["tuned"]
+
+
+def test_tv_full_size_tuned_transpose_f32():
+    """The 4096x4096 fp32 transpose in 64x64 tiles through the conflict-free
+    5-bit-XOR shared tile, thread layouts tuned: the tune gives Pitch 64
+    (one 256-byte column of the tile per 64 threads) in both phases and
+    the bank model no conflicts; compared in full with the oracle."""
+    w = WORKLOADS["C2"]
+    src = ("zipped_divide", w.src, (64, 64))
+    dst = ("zipped_divide", w.dst, (64, 64))
+    smem = ("swizzle", 5, 0, 6, ("layout", (64, 64), (1, 64)))
+    desc = run_tv(src, smem, dst, None, None, 4, seed=6,
+                  expect={"load.pitch": 64, "store.pitch": 64,
+                          "load.smem_wavefronts": 128,
+                          "store.smem_wavefronts": 128})
+    assert desc["n_tiles"] == 64 * 64
 
 
 def test_tv_forced_vector_widths():

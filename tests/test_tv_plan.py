@@ -354,3 +354,118 @@ def test_random_tv_plans_replay_exactly():
         assert (got == want).all(), case
         planned += 1
     assert planned >= 12
+
+
+# --------------------------------------------------------------------------
+# tuned thread layouts (no thread layout from the caller)
+# --------------------------------------------------------------------------
+
+def _tile_sizes(spec):
+    """Sizes of the tile modes (mode 0's own modes) of a layout expression
+    of the oracle."""
+    L = lo.build(spec)
+    base = L.inner if isinstance(L, lo.Swizzled) else L
+    if isinstance(base, lo.ZippedDivide):
+        return [int(t) for t in base.tiler]
+    t = base.modes()[0]
+    return [m.size for m in t.modes()] if not isinstance(t.shape, int) else [t.size]
+
+
+def _tuned_by_oracle(glob_spec, smem_spec, n, eb, vec, threads):
+    """The one-group search the planner documents, recomputed from the
+    oracle: the phase's global side gives the row (its unit-stride tile mode
+    a, else mode 0; ld = the other mode's step), Pitch x Strips == threads
+    with both dividing the tile, cost = (128-byte global segments per warp,
+    shared wavefronts of the same accesses, larger Pitch, larger Strips)."""
+    G, M = lo.build(glob_spec), lo.build(smem_spec)
+    r = len(n)
+    weight = [1, n[0]]
+    a = 0
+    for k in range(r):
+        if n[k] > 1 and int(G.at(weight[k])) - int(G.at(0)) == 1:
+            a = k
+            break
+    b = 1 - a if r == 2 else None
+    k_row, rows = n[a], (n[b] if b is not None else 1)
+    ld = k_row if b is None else max(k_row, int(G.at(weight[b])) - int(G.at(0)))
+    R = k_row // vec
+    best = None
+    P = 1
+    while P <= R and P <= threads:
+        S = threads // P
+        if P * S == threads and R % P == 0 and rows % S == 0:
+            t = np.arange(threads)
+            row, col = t // P, (t % P) * vec
+            g = (row * ld + col) * eb // 128
+            if b is None:
+                idx = col
+            elif a == 0:
+                idx = col + n[0] * row
+            else:
+                idx = row + n[0] * col
+            s_off = M.at(idx)
+            seg = wf = 0
+            for w0 in range(0, threads, 32):
+                seg += len(set(g[w0:w0 + 32].tolist()))
+                wf += lo.smem_wavefronts(s_off[w0:w0 + 32] * eb, vec * eb)[0]
+            key = (seg, wf, -P, -S)
+            if best is None or key < best[0]:
+                best = (key, P, S, seg)
+        P *= 2
+    return best[1], best[2], best[3]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_tuned_thread_layouts(case):
+    """With no thread layouts the planner tunes both phases: the plan replays
+    to the oracle's copy with every address in bounds, and each phase's
+    Pitch and Strips are the best one-group stripmined map by the oracle's
+    own recomputation of the documented cost.  Tiles with nested modes may
+    have no tuned layout (LM_E_NOT_REPRESENTABLE)."""
+    name, src, smem, dst, _, _, eb, _ = case
+    S, D = lm.build_layout(src), lm.build_layout(dst)
+    try:
+        plan = lm.TVPlan(S, lm.build_layout(smem), D, None, None, eb)
+    except lm.LayoutMoveError as e:
+        assert name == "nested_tile_modes" and e.status == -3
+        return
+    d = plan.describe()
+    n = _tile_sizes(src)
+    for phase, glob in (("load", src), ("store", dst)):
+        p = d[phase]
+        assert p["tuned"] is True
+        vec = p["vec_bytes"] // eb
+        pitch, strips, seg = _tuned_by_oracle(glob, smem, n, eb, vec,
+                                              p["threads"])
+        assert (p["pitch"], p["strips"], p["segments"]) == (pitch, strips,
+                                                            seg), (phase, p)
+        a = p["vec_mode"]
+        want_thr = (f"({pitch},{strips}):(1,{pitch})" if a == 0
+                    else f"({strips},{pitch}):({pitch},1)")
+        if len(n) == 1:
+            want_thr = f"{pitch}:1"
+        assert p["thr"] == want_thr, (phase, p)
+    inp = seeded_bytes("bytes", "uint8", S.cosize * eb, 19)
+    want = np.full(D.cosize * eb, 0xA5, np.uint8)
+    lo.copy(lo.build(src), lo.build(dst), inp, want, eb)
+    got = np.full(D.cosize * eb, 0xA5, np.uint8)
+    replay(args_of(plan), inp, got, S.cosize, D.cosize)
+    assert (got == want).all()
+
+
+def test_tuned_thread_layout_mixes_with_a_given_one():
+    """One phase given, the other tuned; a tile of rank 3 cannot be tuned."""
+    _, src, smem, dst, tl, _, eb, _ = CASES[0]
+    S, D, M = lm.build_layout(src), lm.build_layout(dst), lm.build_layout(smem)
+    d = lm.TVPlan(S, M, D, lm.Layout.parse(tl), None, eb).describe()
+    assert d["load"]["tuned"] is False and d["load"]["thr"] == tl
+    assert d["store"]["tuned"] is True
+    S3 = lm.Layout.parse("((4,4,4),8):((1,4,16),64)")
+    D3 = lm.Layout.parse("((4,4,4),8):((16,4,1),64)")
+    M3 = lm.Layout.parse("(4,4,4):(1,4,16)")
+    T3 = lm.Layout.parse("(4,4,4):(1,4,16)")
+    lm.TVPlan(S3, M3, D3, T3, T3, 4)          # plans with given layouts
+    for tl, ts in ((None, T3), (T3, None)):
+        with pytest.raises(lm.LayoutMoveError) as e:
+            lm.TVPlan(S3, M3, D3, tl, ts, 4)
+        assert e.value.status == -1
