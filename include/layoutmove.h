@@ -363,6 +363,38 @@ int lm_layout_copy_host(const lm_plan* plan, const void* src_host,
                         int64_t dst_capacity_elems, void* src_dev,
                         void* dst_dev, void* cuda_stream);
 
+/* Bytes of the fixed device staging area of lm_layout_copy_host_static
+ * (32 MiB). */
+#define LM_HOST_COPY_STATIC_BYTES (32u * 1024u * 1024u)
+
+/* lm_layout_copy_host for callers that cannot allocate device memory: the
+ * same upload, copy and download, staged through a fixed area inside the
+ * library instead of caller-provided device buffers.  The source pages have
+ * no counterpart; this is a convenience of the ABI.  It is for code that
+ * has no way to obtain device memory: a library embedded in a program whose
+ * memory manager owns the device's memory, or a path that cannot afford
+ * cudaMalloc/cudaFree (cudaFree waits for the whole device).  The call
+ * allocates nothing.
+ *
+ * The area is a __device__ array of LM_HOST_COPY_STATIC_BYTES that every
+ * GPU which loads the library holds until the process exits.  The source
+ * is staged at its start, the destination at the next 256-byte boundary
+ * after src_capacity_elems * elem_bytes; a copy whose two parts do not fit
+ * is refused with LM_E_CAPACITY before anything is enqueued.  The first
+ * call on a device, with that device current, looks up the area's device
+ * address (cudaGetSymbolAddress); make that first call before any stream
+ * capture.  Every call on a device shares the one area, which keeps the
+ * last call's bytes: calls whose work overlaps on the GPU (other streams,
+ * other host threads) race and must be ordered by the caller.  No part of
+ * the area needs to start cleared: every destination byte that comes back
+ * is written by the copy or, when the destination layout leaves slots of
+ * [0, cosize) uncovered, uploaded from dst_host first.  Arguments, host
+ * buffer rules, shard rules and other errors are those of
+ * lm_layout_copy_host. */
+int lm_layout_copy_host_static(const lm_plan* plan, const void* src_host,
+                               int64_t src_capacity_elems, void* dst_host,
+                               int64_t dst_capacity_elems, void* cuda_stream);
+
 /* Number of kernel launches lm_layout_copy makes for this plan. */
 int lm_plan_launches(const lm_plan* plan, int* launches);
 

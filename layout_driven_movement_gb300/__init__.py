@@ -18,7 +18,7 @@ from typing import Iterable, Sequence
 
 __all__ = [
     "LayoutMoveError", "Layout", "Plan", "lib", "layout_copy",
-    "layout_copy_host",
+    "layout_copy_host", "layout_copy_host_static", "HOST_COPY_STATIC_BYTES",
     "layout_eval_device", "build_layout", "device_status", "STATUS",
     "TVPlan", "tv_copy", "stripmined_tune", "Exchange", "exchange_copy",
     "exchange_pack_all", "exchange_unpack_all",
@@ -80,6 +80,7 @@ SIGNATURES = [
     ("lm_layout_copy", C.c_int, [_P, _P, _I64, _P, _I64, _P]),
     ("lm_plan_launches", C.c_int, [_P, _IP]),
     ("lm_layout_copy_host", C.c_int, [_P, _P, _I64, _P, _I64, _P, _P, _P]),
+    ("lm_layout_copy_host_static", C.c_int, [_P, _P, _I64, _P, _I64, _P]),
     ("lm_layout_eval_device", C.c_int, [_P, _P, C.c_int, _I64, _P]),
     ("lm_plan_destroy", None, [_P]),
     ("lm_plan_exchange", C.c_int,
@@ -622,6 +623,32 @@ def layout_copy_host(plan: Plan, src_host, dst_host, src_dev, dst_dev,
                                      C.c_void_p(sp), C.c_void_p(dp),
                                      _stream_handle(stream)),
            "lm_layout_copy_host")
+
+
+# Size of the fixed device staging area of layout_copy_host_static (the
+# header's LM_HOST_COPY_STATIC_BYTES).
+HOST_COPY_STATIC_BYTES = 32 * 1024 * 1024
+
+
+def layout_copy_host_static(plan: Plan, src_host, dst_host,
+                            stream=None) -> None:
+    """layout_copy_host without device staging buffers from the caller: for
+    code that cannot allocate device memory (a program whose memory manager
+    owns the device's memory, or a path that cannot afford cudaMalloc or
+    cudaFree).  The library stages through its own fixed area of
+    HOST_COPY_STATIC_BYTES on each device; larger copies are refused
+    (LM_E_CAPACITY).  Calls share that area, so calls that overlap on the
+    GPU race.  Nothing is allocated here either: the host tensors are
+    passed by pointer."""
+    for t in (src_host, dst_host):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("host buffers must be contiguous CPU tensors")
+    hs = src_host.numel() * src_host.element_size() // plan.elem_bytes
+    hd = dst_host.numel() * dst_host.element_size() // plan.elem_bytes
+    _check(lib().lm_layout_copy_host_static(
+        plan.handle, C.c_void_p(src_host.data_ptr()), hs,
+        C.c_void_p(dst_host.data_ptr()), hd, _stream_handle(stream)),
+        "lm_layout_copy_host_static")
 
 
 def layout_copy_ptr(plan: Plan, src_ptr: int, src_cap: int, dst_ptr: int,
