@@ -425,7 +425,8 @@ def kernel_name(plan, eb: int) -> str:
         store = (f"XposeStore<{eb}, {pc['rows']}>" if pc["store"] == "transpose"
                  else f"GatherStore<{eb}>")
         if pc["bulk"]:
-            return f"lm_bulk_kernel<{eb}, {store}, {pc['stages']}>"
+            tma = "true" if pc.get("tma") else "false"
+            return f"lm_bulk_kernel<{eb}, {store}, {pc['stages']}, {tma}>"
         return f"lm_staged_kernel<{eb}, {store}, {pc['stages']}>"
     if pc["path"] == "VEC":
         return f"lm_vec_tiled_kernel<{pc['vec_bytes']}, 4>"

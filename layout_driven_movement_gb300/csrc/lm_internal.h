@@ -251,6 +251,20 @@ struct StagedArgs {
   int32_t bulk_stages = 3;
   uint32_t n_seg = 0, seg_bytes = 0;
   int64_t src_reach = 0;
+  // tensor-map form (tma == 1, with bulk == 1; transposes): the piece's
+  // source is a tensor of t_rank dimensions -- dim 0 the unit-stride mode,
+  // dim 1 the tile's other mode, then the rest -- loaded one box of t_box
+  // elements per tile by a single cp.async.bulk.tensor; grid mode k
+  // advances dim g_tdim[k] by g_tstep[k] elements per coordinate.  The box
+  // lands densely (rows of t_box[0] elements), which is the image the
+  // store side reads.
+  int32_t tma = 0;
+  int32_t t_rank = 0;
+  uint64_t t_dim[5];                    // extents, elements
+  uint64_t t_stride[5];                 // bytes (t_stride[0] unused)
+  uint32_t t_box[5];
+  int32_t g_tdim[kMaxModes];
+  uint32_t g_tstep[kMaxModes];
 };
 
 struct EvalArgs {

@@ -19,6 +19,7 @@
 //
 // No tensor cores: the work is pure data movement.
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -864,17 +865,75 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst_smem, const void* src,
       : "memory");
 }
 
-template <int EB, class Store, int NS>
+// One box of a tiled tensor map into shared memory (the tensor-memory-
+// accelerator copy), completing on an mbarrier; c[] are the box's first
+// element coordinates, dim 0 first.
+__device__ __forceinline__ void tma_g2s(uint32_t dst_smem, const CUtensorMap* m,
+                                        int rank, int32_t c0, int32_t c1,
+                                        int32_t c2, int32_t c3, int32_t c4,
+                                        uint32_t bar) {
+  const uint64_t map = reinterpret_cast<uint64_t>(m);
+  const int32_t c[5] = {c0, c1, c2, c3, c4};
+  switch (rank) {
+    case 2:
+      asm volatile(
+          "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::"
+          "complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n" ::"r"(dst_smem),
+          "l"(map), "r"(c[0]), "r"(c[1]), "r"(bar)
+          : "memory");
+      break;
+    case 3:
+      asm volatile(
+          "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::"
+          "complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];\n" ::"r"(
+              dst_smem),
+          "l"(map), "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(bar)
+          : "memory");
+      break;
+    case 4:
+      asm volatile(
+          "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::"
+          "complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];\n" ::"r"(
+              dst_smem),
+          "l"(map), "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3]), "r"(bar)
+          : "memory");
+      break;
+    default:
+      asm volatile(
+          "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::"
+          "complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, %6}], [%7];\n" ::"r"(
+              dst_smem),
+          "l"(map), "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3]), "r"(c[4]),
+          "r"(bar)
+          : "memory");
+      break;
+  }
+}
+
+// Bytes of dynamic shared memory a bulk-form block asks for: mbarriers
+// (128 bytes), the stages, and 128 bytes of slack to align them.
+inline int bulk_smem_bytes(const StagedArgs& a, int ns) {
+  return int(256 + ns * a.stage_bytes);
+}
+
+// The bulk-copy STAGED kernel.  TMA == false: one cp.async.bulk per source
+// segment; TMA == true: one tensor-map box per tile (tmap describes the
+// piece's source, StagedArgs::tma).
+template <int EB, class Store, int NS, bool TMA>
 __global__ void __launch_bounds__(256)
     lm_bulk_kernel(const __grid_constant__ StagedArgs a,
+                   const __grid_constant__ CUtensorMap tmap,
                    const char* __restrict__ src, char* __restrict__ dst) {
   extern __shared__ __align__(128) unsigned char smem[];
   const uint32_t tid = threadIdx.x, nt = blockDim.x;
   const uint32_t warp = tid >> 5, lane = tid & 31, n_warps = nt >> 5;
-  const uint32_t bars = uint32_t(__cvta_generic_to_shared(smem));
+  // mbarriers and stages from the first 128-byte boundary (tensor copies
+  // need 128-byte aligned destinations; the launch adds the slack)
+  const uint32_t base = uint32_t(__cvta_generic_to_shared(smem));
+  const uint32_t bars = (base + 127u) & ~127u;
   auto full = [&](uint32_t s) { return bars + 8u * s; };
   auto empty = [&](uint32_t s) { return bars + 8u * (NS + s); };
-  unsigned char* stages = smem + 128;
+  unsigned char* stages = smem + (bars - base) + 128;
   const uint32_t stage0 = bars + 128;
 
   Store st;
@@ -929,16 +988,40 @@ __global__ void __launch_bounds__(256)
     const uint32_t s = i % NS;
     if (i >= uint32_t(NS) && !warp_wait(empty(s), ((i / NS) - 1) & 1))
       return false;
-    int64_t sb, db;
-    tile_base(a, blockIdx.x + i * G, sb, db);
-    if (lane == 0) mbar_arrive_expect_tx(full(s), tile_bytes);
-    __syncwarp();
-    const char* base = src + a.s_base + sb;
     const uint32_t sdst = stage0 + s * a.stage_bytes;
+    if constexpr (TMA) {
+      if (lane == 0) {
+        // the tile's box origin: grid coordinates times the box steps
+        int32_t c0 = 0, c1 = 0, c2 = 0, c3 = 0, c4 = 0;
+        uint32_t t = blockIdx.x + i * G;
 #pragma unroll
-    for (int k = 0; k < kBulkSegsPerLane; ++k)
-      if (seg_src[k] >= 0)
-        bulk_g2s(sdst + seg_sm[k], base + seg_src[k], a.seg_bytes, full(s));
+        for (int k = 0; k < kMaxModes; ++k) {
+          if (k >= a.ng) break;
+          const uint32_t q = fdiv(t, a.g_div[k]);
+          const int32_t v = int32_t((t - q * a.g_ext[k]) * a.g_tstep[k]);
+          const int32_t d = a.g_tdim[k];
+          c0 += d == 0 ? v : 0;
+          c1 += d == 1 ? v : 0;
+          c2 += d == 2 ? v : 0;
+          c3 += d == 3 ? v : 0;
+          c4 += d == 4 ? v : 0;
+          t = q;
+        }
+        mbar_arrive_expect_tx(full(s), tile_bytes);
+        tma_g2s(sdst, &tmap, a.t_rank, c0, c1, c2, c3, c4, full(s));
+      }
+      __syncwarp();
+    } else {
+      int64_t sb, db;
+      tile_base(a, blockIdx.x + i * G, sb, db);
+      if (lane == 0) mbar_arrive_expect_tx(full(s), tile_bytes);
+      __syncwarp();
+      const char* base = src + a.s_base + sb;
+#pragma unroll
+      for (int k = 0; k < kBulkSegsPerLane; ++k)
+        if (seg_src[k] >= 0)
+          bulk_g2s(sdst + seg_sm[k], base + seg_src[k], a.seg_bytes, full(s));
+    }
     return true;
   };
 
@@ -1240,34 +1323,95 @@ bool allow_smem(K kern, int bytes) {
   return true;
 }
 
-template <int EB, class Store, int NS>
+// cuTensorMapEncodeTiled from the driver, found once through the runtime
+// (the library links no driver library of its own).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType,
+                                   cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                         cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+// The tensor map of a piece's source (StagedArgs::tma) at `src`.
+bool encode_source_map(const StagedArgs& a, int eb, const char* src,
+                       CUtensorMap* m) {
+  const EncodeTiledFn fn = encode_tiled();
+  if (!fn) return false;
+  const CUtensorMapDataType dt =
+      eb == 1   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+      : eb == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16
+      : eb == 4 ? CU_TENSOR_MAP_DATA_TYPE_UINT32
+                : CU_TENSOR_MAP_DATA_TYPE_UINT64;
+  cuuint64_t dims[5], strides[4];
+  cuuint32_t box[5], es[5];
+  for (int k = 0; k < a.t_rank; ++k) {
+    dims[k] = a.t_dim[k];
+    box[k] = a.t_box[k];
+    es[k] = 1;
+    if (k > 0) strides[k - 1] = a.t_stride[k];
+  }
+  return fn(m, dt, cuuint32_t(a.t_rank),
+            const_cast<char*>(src) + a.s_base, dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int EB, class Store, int NS, bool TMA>
 int launch_bulk_ns(const StagedArgs& a, const char* src, char* dst,
                    cudaStream_t st) {
-  const int smem = int(128 + NS * a.stage_bytes);
-  if (!allow_smem(lm_bulk_kernel<EB, Store, NS>, smem)) return LM_E_CUDA;
+  const int smem = bulk_smem_bytes(a, NS);
+  auto kern = lm_bulk_kernel<EB, Store, NS, TMA>;
+  if (!allow_smem(kern, smem)) return LM_E_CUDA;
+  CUtensorMap m;
+  std::memset(&m, 0, sizeof(m));
+  if constexpr (TMA) {
+    if (!encode_source_map(a, EB, src, &m)) {
+      set_cuda_error(0);
+      return LM_E_CUDA;
+    }
+  }
   const DeviceInfo di = device_info();
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-          &per_sm, lm_bulk_kernel<EB, Store, NS>, a.threads, size_t(smem)) !=
-          cudaSuccess ||
+          &per_sm, kern, a.threads, size_t(smem)) != cudaSuccess ||
       per_sm < 1)
     per_sm = 1;
   const unsigned grid = unsigned(
       staged_grid(a.n_tiles, uint64_t(di.sms) * uint64_t(per_sm)));
-  launch_k(lm_bulk_kernel<EB, Store, NS>, grid, unsigned(a.threads),
-           size_t(smem), st, a, src, dst);
+  launch_k(kern, grid, unsigned(a.threads), size_t(smem), st, a, m, src, dst);
   return check_launch();
+}
+
+template <int EB, class Store, bool TMA>
+int launch_bulk_t(const StagedArgs& a, const char* src, char* dst,
+                  cudaStream_t st) {
+  switch (a.bulk_stages) {
+    case 2: return launch_bulk_ns<EB, Store, 2, TMA>(a, src, dst, st);
+    case 4: return launch_bulk_ns<EB, Store, 4, TMA>(a, src, dst, st);
+    default: return launch_bulk_ns<EB, Store, 3, TMA>(a, src, dst, st);
+  }
 }
 
 template <int EB, class Store>
 int launch_staged_t(const StagedArgs& a, const char* src, int64_t src_cap,
                     char* dst, cudaStream_t st) {
   if (a.bulk && src_cap >= a.src_reach) {
-    switch (a.bulk_stages) {
-      case 2: return launch_bulk_ns<EB, Store, 2>(a, src, dst, st);
-      case 4: return launch_bulk_ns<EB, Store, 4>(a, src, dst, st);
-      default: return launch_bulk_ns<EB, Store, 3>(a, src, dst, st);
-    }
+    if (a.tma && encode_tiled())
+      return launch_bulk_t<EB, Store, true>(a, src, dst, st);
+    return launch_bulk_t<EB, Store, false>(a, src, dst, st);
   }
   if (a.stages == 3 && 3 * a.stage_bytes <= 49152)
     return launch_staged_ns<EB, Store, 3>(a, src, src_cap, dst, st);

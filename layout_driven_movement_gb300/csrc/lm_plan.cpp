@@ -172,6 +172,20 @@ int bulk_stages() {
   static int v = std::clamp(env_int("LM_BULK_STAGES", 2), 2, 4);
   return v;
 }
+// Tensor-map (TMA) tile loads for STAGED transposes (LM_TMA=1 turns them
+// on) and their pipeline depth (LM_TMA_STAGES, 2..4).  Off by default:
+// measured on GB300, one box per tile (64 rows of 256 bytes) took 29.3 us
+// for the 4096x4096 fp32 transpose and 41.6 us for NHWC->NCHW against
+// 23.2 and 33.4 us for the per-thread cp.async loads, whatever the depth,
+// tiles per block or micro-tile order.
+bool tma_enabled() {
+  static bool v = env_int("LM_TMA", 0) != 0;
+  return v;
+}
+int tma_stages() {
+  static int v = std::clamp(env_int("LM_TMA_STAGES", 3), 2, 4);
+  return v;
+}
 // Bulk copies pay off for long rows: the bf16/fp32 transposes' 128-256 byte
 // rows ran faster with per-thread cp.async (measured on GB300), the 9 KiB
 // segments of the padded TV gather faster with one bulk copy.
@@ -281,7 +295,8 @@ bool smem_search_enabled() {
 template <class ReadAddr>
 SmemLayout search_smem(int threads, int64_t n_seg, int64_t seg_bytes,
                        int64_t n_reads, int per, int width,
-                       const ReadAddr& read_addr, bool allow_swizzle = true) {
+                       const ReadAddr& read_addr, bool allow_swizzle = true,
+                       bool allow_pad = true) {
   SmemLayout best;
   const int64_t cps = seg_bytes / 16;
   const int64_t n_l = n_seg * cps;
@@ -289,7 +304,7 @@ SmemLayout search_smem(int threads, int64_t n_seg, int64_t seg_bytes,
   const int64_t spt = (n_reads + threads - 1) / threads;
   const bool search = smem_search_enabled();
   const std::vector<int64_t> pads =
-      n_seg > 1 && search
+      n_seg > 1 && search && allow_pad
           ? std::vector<int64_t>{0, 16, 32, 48, 64, 80, 96, 112}
           : std::vector<int64_t>{0};
   std::vector<Swz> zs{Swz{}};
@@ -565,34 +580,65 @@ static StagedChoice plan_transpose(const std::vector<JMode>& ms,
   auto al = [&](int64_t elems) { return (elems * eb) % 16 == 0; };
   if (!al(s_base) || !al(d_base) || !al(mb.s)) return ch;
   if (R == V && !al(ma.d)) return ch;
-  std::vector<JMode> grid;
+  // the tensor dimension of each joint mode for tensor-map loads: a, b,
+  // then the rest in order
+  std::vector<int> tdim(size_t(n), 0);
+  {
+    int next = 2;
+    for (int k = 0; k < n; ++k)
+      tdim[size_t(k)] = k == a ? 0 : (k == b ? 1 : next++);
+  }
+  struct GridMode {
+    JMode m;
+    int tdim;
+    int64_t tstep;
+  };
+  std::vector<GridMode> gm;
   for (int k = 0; k < n; ++k) {
     const JMode& m = ms[size_t(k)];
     const int64_t t = k == a ? Ta : (k == b ? Tb : 1);
     if (t == m.e) continue;
-    grid.push_back({m.e / t, m.s * t, m.d * t});
+    gm.push_back({{m.e / t, m.s * t, m.d * t}, tdim[size_t(k)], t});
     if (!al(m.s * t) || !al(m.d * t)) return ch;
   }
-  if (grid.size() > size_t(kMaxModes)) return ch;
-  std::sort(grid.begin(), grid.end(), mode_before);
+  if (gm.size() > size_t(kMaxModes)) return ch;
+  std::sort(gm.begin(), gm.end(), [](const GridMode& x, const GridMode& y) {
+    return mode_before(x.m, y.m);
+  });
+  std::vector<JMode> grid;
+  for (const GridMode& g : gm) grid.push_back(g.m);
   if (prod_e(grid) >= (int64_t(1) << 32)) return ch;
   const int64_t s_reach = add_chk(mul_chk(mul_chk(Tb - 1, mb.s), eb), seg_bytes);
   const int64_t d_reach = add_chk(mul_chk(mul_chk(Ta - 1, ma.d), eb), Tb * eb);
   if (s_reach >= (int64_t(1) << 31) || d_reach >= (int64_t(1) << 31))
     return ch;
 
-  const bool bulk = bulk_enabled() && !ssb.on() && Tb <= 128 &&
-                    seg_bytes >= kBulkMinSegment;
+  // tensor-map loads: one box per tile, for sources whose modes a tensor
+  // map can describe (at most 5, byte strides multiples of 16 below 2^40,
+  // boxes of at most 256 per dimension)
+  bool tma = tma_enabled() && !ssb.on() && n <= 5 && Ta <= 256 && Tb <= 256;
+  for (int k = 0; k < n && tma; ++k) {
+    const JMode& m = ms[size_t(k)];
+    if (m.e >= (int64_t(1) << 31)) tma = false;
+    if (k != a && (!al(m.s) || m.s * eb >= (int64_t(1) << 40) || m.s <= 0))
+      tma = false;
+  }
+  const bool bulk = tma || (bulk_enabled() && !ssb.on() && Tb <= 128 &&
+                            seg_bytes >= kBulkMinSegment);
   // without a swizzle (bulk copies write rows linearly) run the micro-tile
   // index along a first: 8 lanes then read 8 consecutive chunks of a row
-  const bool acfast = bulk && n_ac >= 8;
+  // (LM_TMA_ACFAST=0 keeps the b-first order on tensor-map tiles: stores
+  // coalesced, shared reads conflicting)
+  const bool acfast =
+      bulk && n_ac >= 8 && !(tma && env_int("LM_TMA_ACFAST", 1) == 0);
   auto read_addr = [&](int64_t j, int r, int64_t pitch) {
     const int64_t bc = acfast ? j / n_ac : j % n_bc;
     const int64_t ac = acfast ? j % n_ac : j / n_bc;
     return (bc * R + r) * pitch + ac * 16;
   };
+  // a tensor-map box lands densely: rows at their own length, no pad
   const SmemLayout best = search_smem(int(threads), Tb, seg_bytes, n_micro,
-                                      int(R), 16, read_addr, !bulk);
+                                      int(R), 16, read_addr, !bulk, !tma);
   if (best.cost < 0) return ch;
 
   StagedArgs& A = pc.st;
@@ -631,6 +677,23 @@ static StagedChoice plan_transpose(const std::vector<JMode>& ms,
     A.n_seg = uint32_t(Tb);
     A.seg_bytes = uint32_t(seg_bytes);
     A.src_reach = src_reach(A);
+  }
+  if (tma) {
+    A.tma = 1;
+    A.bulk_stages = tma_stages();
+    // tensor copies land on 128-byte boundaries: every stage starts on one
+    A.stage_bytes = (A.stage_bytes + 127u) & ~127u;
+    A.t_rank = int32_t(n);
+    for (int k = 0; k < n; ++k) {
+      const int d = tdim[size_t(k)];
+      A.t_dim[d] = uint64_t(ms[size_t(k)].e);
+      A.t_stride[d] = uint64_t(mul_chk(ms[size_t(k)].s, eb));
+      A.t_box[d] = uint32_t(k == a ? Ta : (k == b ? Tb : 1));
+    }
+    for (size_t k = 0; k < gm.size(); ++k) {
+      A.g_tdim[k] = int32_t(gm[k].tdim);
+      A.g_tstep[k] = uint32_t(gm[k].tstep);
+    }
   }
   pc.path = PATH_STAGED;
   pc.xr = int(R);
@@ -1180,7 +1243,8 @@ static std::string describe(const lm_plan& P) {
          << "\",\"rows\":" << A.xr << ",\"threads\":" << A.threads
          << ",\"stages\":" << (A.bulk ? A.bulk_stages : A.stages)
          << ",\"bulk\":"
-         << (A.bulk ? "true" : "false")
+         << (A.bulk ? "true" : "false") << ",\"tma\":"
+         << (A.tma ? "true" : "false")
          << ",\"stage_bytes\":" << A.stage_bytes << ",\"smem_swizzle\":["
          << A.m_swz.b << ',' << A.m_swz.m << ',' << A.m_swz.s << ']'
          << ",\"bank_wavefronts\":" << pc.bank_cost

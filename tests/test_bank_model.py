@@ -66,6 +66,34 @@ def test_search_makes_transposes_conflict_free():
         assert p["bank_wavefronts"] == p["bank_wavefronts_ideal"], name
 
 
+def test_tensor_map_images_read_conflict_free():
+    """With tensor-map loads (LM_TMA=1) the tile lands densely (no pad, no
+    swizzle); the micro-tiles then run along the row, 8 lanes reading 8
+    consecutive chunks, which the model finds conflict-free."""
+    code = (
+        "import json, layout_driven_movement_gb300 as lm\n"
+        "from workloads import WORKLOADS, ELEM_BYTES\n"
+        "out = {}\n"
+        "for n in ['C2', 'C5a']:\n"
+        "    w = WORKLOADS[n]\n"
+        "    d = lm.Plan(lm.build_layout(w.src), lm.build_layout(w.dst),\n"
+        "                ELEM_BYTES[w.dtype]).describe()\n"
+        "    out[n] = [p for p in d['pieces'] if p['path'] == 'STAGED'][0]\n"
+        "print(json.dumps(out))\n")
+    env = dict(os.environ, LM_TMA="1", PYTHONPATH=ROOT)
+    r = subprocess.run([sys.executable, "-c", code], env=env, cwd=ROOT,
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    got = json.loads(r.stdout.strip().splitlines()[-1])
+    for name, p in got.items():
+        assert p["tma"] and p["bulk"] and p["smem_swizzle"] == [0, 0, 0], name
+        assert p["bank_read_wavefronts"] == p["bank_read_wavefronts_ideal"]
+    # by default the transposes keep the per-thread cp.async loads
+    for name in ["C2", "C5a"]:
+        p = staged_piece(name)
+        assert not p["tma"] and not p["bulk"], name
+
+
 def test_gather_of_tv_tiles_is_two_way():
     p = staged_piece("C4")
     assert p["store"] == "gather" and p["bulk"]
@@ -83,7 +111,7 @@ def test_plain_image_predicts_eightfold_transpose_conflicts():
         "                ELEM_BYTES[w.dtype]).describe()\n"
         "    out[n] = [p for p in d['pieces'] if p['path'] == 'STAGED'][0]\n"
         "print(json.dumps(out))\n")
-    env = dict(os.environ, LM_SMEM_SEARCH="0", PYTHONPATH=ROOT)
+    env = dict(os.environ, LM_SMEM_SEARCH="0", LM_TMA="0", PYTHONPATH=ROOT)
     r = subprocess.run([sys.executable, "-c", code], env=env, cwd=ROOT,
                        capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stderr

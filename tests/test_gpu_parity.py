@@ -331,11 +331,16 @@ VARIANT_CASES = ["transpose_ragged_f32", "transpose_1000x1000_f16",
 
 
 def test_bulk_path_is_planned_for_long_segments():
-    for name, bulk in (("C2", False), ("C4", True), ("C5a", False)):
+    """C4's 9 KiB segments load by one bulk copy each; the transposes (C2,
+    C5a) keep per-thread cp.async loads (tensor-map boxes only with
+    LM_TMA=1)."""
+    for name, bulk, tma in (("C2", False, False), ("C4", True, False),
+                            ("C5a", False, False)):
         w = WORKLOADS[name]
         d = lm.Plan(lm.build_layout(w.src), lm.build_layout(w.dst),
                     w.elem_bytes).describe()
-        assert all(p["bulk"] == bulk for p in d["pieces"]), (name, d)
+        assert all(p["bulk"] == bulk and p["tma"] == tma
+                   for p in d["pieces"]), (name, d)
 
 
 def test_short_interleaves_plan_the_register_path():
@@ -364,11 +369,16 @@ def test_short_interleaves_plan_the_register_path():
 
 @pytest.mark.parametrize("env", [{"LM_BULK": "0"},
                                  {"LM_BULK": "0", "LM_STAGES": "3"},
-                                 {"LM_BULK_STAGES": "2"},
-                                 {"LM_BULK_STAGES": "4", "LM_VEC_UNROLL": "8"},
+                                 {"LM_TMA": "1"},
+                                 {"LM_TMA": "1", "LM_TMA_ACFAST": "0"},
+                                 {"LM_BULK_STAGES": "2", "LM_TMA": "1",
+                                  "LM_TMA_STAGES": "2"},
+                                 {"LM_BULK_STAGES": "4", "LM_TMA": "1",
+                                  "LM_TMA_STAGES": "4", "LM_VEC_UNROLL": "8"},
                                  {"LM_ZIP": "0"}])
 def test_pipeline_variants_parity(env):
-    """The cp.async load path (LM_BULK=0, 2 or 3 stages) and other bulk
+    """The cp.async load path (LM_BULK=0, 2 or 3 stages), tensor-map tile
+    loads for transposes (LM_TMA=1, both micro-tile orders) and other
     pipeline depths, in a fresh process since the knobs are read once."""
     import os
     import subprocess
@@ -388,6 +398,31 @@ def test_pipeline_variants_parity(env):
                            env.get("LM_BULK", "1")))
     r = subprocess.run([sys.executable, "-c", code], capture_output=True,
                        text=True, env={**os.environ, **env}, timeout=600)
+    assert r.returncode == 0 and "ok" in r.stdout, r.stdout + r.stderr
+
+
+def test_tensor_map_transposes_full_size():
+    """The opt-in tensor-map loads (LM_TMA=1) on the full-size fp32
+    transpose and NHWC->NCHW, compared in full with the oracle, in a fresh
+    process since the knob is read once."""
+    import os
+    import subprocess
+    import sys
+    here = os.path.dirname(os.path.abspath(__file__))
+    code = (
+        "import sys; sys.path[:0] = [%r, %r]\n"
+        "import test_gpu_parity as t\n"
+        "from workloads import WORKLOADS\n"
+        "t.lm.lib()\n"
+        "for n in ('C2', 'C5a'):\n"
+        "    w = WORKLOADS[n]\n"
+        "    p = t.run_case(w.src, w.dst, w.elem_bytes, values=w.values,\n"
+        "                   dtype=w.dtype, seed=w.seed, src_round16=True)\n"
+        "    assert all(pc['tma'] for pc in p.describe()['pieces']), n\n"
+        "print('ok')\n" % (here, os.path.dirname(here)))
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True,
+                       text=True, env={**os.environ, "LM_TMA": "1"},
+                       timeout=900)
     assert r.returncode == 0 and "ok" in r.stdout, r.stdout + r.stderr
 
 
