@@ -498,11 +498,12 @@ def _timed(torch, fn, runs=20, flush=None):
 
 
 def measure_eval_and_generic(suite, torch, peak) -> dict:
-    """The two kernels the suite does not time.  layout_eval: the offset
-    table of the padded TV source layout (75.5 M entries, int64: 604 MB
-    written).  GENERIC: a 6000x7000 fp32 relayout whose two layouts have no
-    common refinement (6000 and 7000 do not nest), so it runs one element
-    per thread with a full decomposition on each side."""
+    """The kernels the suite does not time.  layout_eval: the offset table
+    of the padded TV source layout (67 M entries, int64: 537 MB written),
+    beside a write-only fill of the same bytes (the write ceiling).
+    GENERIC: a 6000x7000 fp32 relayout whose two layouts have no common
+    refinement, one element per thread with a full decomposition on each
+    side; and the 6000x7000 pair that refines once a side is coalesced."""
     lm = suite.lm
     dev = suite.items[0]["src"].device
     flush = torch.ones(512 << 20, dtype=torch.uint8, device=dev)
@@ -514,24 +515,43 @@ def measure_eval_and_generic(suite, torch, peak) -> dict:
         ms = _timed(torch, lambda: lm.layout_eval_device(L, table),
                     flush=flush)
         gbs = L.size * 8 / (ms * 1e-3) / 1e9
+        fill_ms = _timed(torch, lambda: table.fill_(7), flush=flush)
+        fill_gbs = L.size * 8 / (fill_ms * 1e-3) / 1e9
         out["layout_eval"] = {
             "workload": "offset table of the padded TV source layout, "
                         f"{L.size} int64 entries", "median_us": round(ms * 1e3, 2),
-            "gbs_written": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4)}
+            "gbs_written": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+            "fill_ceiling_gbs": round(fill_gbs, 1),
+            "frac_of_fill": round(gbs / fill_gbs, 4)}
         del table
     S = lm.Layout.parse("(6000,7000):(7000,1)")
-    D = lm.Layout.parse("(7000,6000):(1,7000)")
-    plan = lm.Plan(S, D, 4)
-    a = torch.empty(S.cosize * 4, dtype=torch.uint8, device=dev)
-    b = torch.empty(D.cosize * 4, dtype=torch.uint8, device=dev)
-    ms = _timed(torch, lambda: lm.layout_copy(plan, a, b), flush=flush)
-    gbs = 2 * S.size * 4 / (ms * 1e-3) / 1e9
-    out["generic"] = {
-        "workload": "6000x7000 fp32 between layouts with no common "
-                    "refinement", "path": plan.describe()["pieces"][0]["path"],
-        "median_us": round(ms * 1e3, 2), "gbs": round(gbs, 1),
-        "frac_of_peak": round(gbs / peak, 4)}
-    del a, b, flush
+    pairs = {
+        # 6000 and 7000 do not nest and the padded destination does not
+        # coalesce: no common refinement, one element per thread
+        "generic": ("(7000,6000):(1,7001)",
+                    "6000x7000 fp32 into a padded (7000,6000):(1,7001) "
+                    "destination: no common refinement"),
+        # the same matrix against (7000,6000):(1,7000), the single run
+        # 42000000:1, refines into a transpose
+        "coalesced_transpose": ("(7000,6000):(1,7000)",
+                                "6000x7000 fp32 against (7000,6000):(1,7000)"
+                                ", refined once the destination is seen "
+                                "as one run: a transpose"),
+    }
+    for key, (d_txt, what) in pairs.items():
+        D = lm.Layout.parse(d_txt)
+        plan = lm.Plan(S, D, 4)
+        a = torch.empty(S.cosize * 4, dtype=torch.uint8, device=dev)
+        b = torch.empty(D.cosize * 4, dtype=torch.uint8, device=dev)
+        ms = _timed(torch, lambda: lm.layout_copy(plan, a, b), flush=flush)
+        gbs = 2 * S.size * 4 / (ms * 1e-3) / 1e9
+        out[key] = {
+            "workload": what,
+            "path": "+".join(p["path"] for p in plan.describe()["pieces"]),
+            "median_us": round(ms * 1e3, 2), "gbs": round(gbs, 1),
+            "frac_of_peak": round(gbs / peak, 4)}
+        del a, b
+    del flush
     return out
 
 

@@ -276,6 +276,19 @@ struct EvalArgs {
   int64_t ext64[kMaxLeaves];
   int64_t str[kMaxLeaves];              // elements
   Swz swz;                              // elements
+  // tiled form: tiles of tile_elems consecutive indices, whose offsets are
+  // inner(r) + outer(tile) -- the inner leaves (n_in) cover the first
+  // leaves and part of one (tile_elems = their product), the outer leaves
+  // (n_out) number the tiles
+  int32_t n_in = 0, n_out = 0;
+  uint32_t tile_elems = 0;
+  uint64_t n_tiles = 0;
+  uint32_t in_ext[kMaxLeaves];
+  FastDiv in_div[kMaxLeaves];
+  int64_t in_str[kMaxLeaves];
+  uint32_t out_ext[kMaxLeaves];
+  FastDiv out_div[kMaxLeaves];
+  int64_t out_str[kMaxLeaves];
 };
 
 // ---------------------------------------------------------------------------
@@ -347,4 +360,5 @@ int launch_piece(const lm_plan& plan, const Piece& pc, const char* src,
 int launch_eval(const lm_layout& L, void* table, int offset_bytes,
                 void* stream);
 void set_cuda_error(int e);
+unsigned int* device_status_word();  // device address, current device
 }  // namespace lm

@@ -30,6 +30,7 @@
 #include <mutex>
 
 #include "lm_internal.h"
+#include "lm_mbar.cuh"
 
 namespace lm {
 
@@ -169,6 +170,61 @@ __global__ void __launch_bounds__(256)
     uint4 w;
     memcpy(&w, v, 16);
     __stcs(reinterpret_cast<uint4*>(table) + q, w);
+  }
+}
+
+// The table tile by tile: a tile is tile_elems consecutive indices whose
+// offsets split into a part inside the tile (the first leaves) and the
+// tile's base (the rest).  Each thread computes the in-tile offsets of its U
+// vectors once; per tile it adds the base, one decomposition of the tile
+// number, and writes 16-byte vectors (a warp writes 512 contiguous bytes).
+template <typename OUT, int U>
+__global__ void __launch_bounds__(256)
+    lm_eval_tiled_kernel(const __grid_constant__ EvalArgs a,
+                         OUT* __restrict__ table) {
+  constexpr int R = 16 / int(sizeof(OUT));
+  const uint32_t tid = threadIdx.x, nt = blockDim.x;
+  const uint32_t n_vec = a.tile_elems / R;
+  int64_t off[U][R];
+#pragma unroll
+  for (int u = 0; u < U; ++u)
+#pragma unroll
+    for (int e = 0; e < R; ++e) {
+      uint32_t r = (tid + uint32_t(u) * nt) * R + uint32_t(e);
+      int64_t o = 0;
+#pragma unroll
+      for (int k = 0; k < kMaxLeaves; ++k) {
+        if (k >= a.n_in) break;
+        const uint32_t q = fdiv(r, a.in_div[k]);
+        o += int64_t(r - q * a.in_ext[k]) * a.in_str[k];
+        r = q;
+      }
+      off[u][e] = o;
+    }
+  pdl_trigger();
+  pdl_wait();
+  for (uint64_t tile = blockIdx.x; tile < a.n_tiles; tile += gridDim.x) {
+    int64_t base = 0;
+    uint32_t q = uint32_t(tile);
+#pragma unroll
+    for (int k = 0; k < kMaxLeaves; ++k) {
+      if (k >= a.n_out) break;
+      const uint32_t qn = fdiv(q, a.out_div[k]);
+      base += int64_t(q - qn * a.out_ext[k]) * a.out_str[k];
+      q = qn;
+    }
+    uint4* out = reinterpret_cast<uint4*>(table + tile * a.tile_elems);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const uint32_t j = tid + uint32_t(u) * nt;
+      if (j >= n_vec) break;
+      OUT v[R];
+#pragma unroll
+      for (int e = 0; e < R; ++e) v[e] = OUT(swz_apply(a.swz, base + off[u][e]));
+      uint4 w;
+      memcpy(&w, v, 16);
+      __stcs(out + j, w);
+    }
   }
 }
 
@@ -809,52 +865,8 @@ __global__ void __launch_bounds__(256)
 // ---------------------------------------------------------------------------
 
 __device__ unsigned int g_lm_device_status = 0;
-constexpr long long kWaitCycles = 2000000000LL;
-constexpr long long kDrainCycles = 4 * kWaitCycles;
 constexpr int kBulkSegsPerLane = 4;  // up to 128 segments per tile
 
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar),
-               "r"(count)
-               : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar,
-                                                      uint32_t bytes) {
-  asm volatile(
-      "mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar),
-      "r"(bytes)
-      : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar)
-               : "memory");
-}
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n"
-      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait for the phase with the given parity to complete.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
-                                          long long limit = kWaitCycles) {
-  if (mbar_try(bar, parity)) return true;
-  const long long t0 = clock64();
-  while (!mbar_try(bar, parity))
-    if (clock64() - t0 > limit) return false;
-  return true;
-}
-// The same, agreed by the whole warp (every lane waits, so every lane has
-// acquired the phase; the warp proceeds only if all lanes saw it complete).
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity,
-                                          long long limit = kWaitCycles) {
-  return __all_sync(0xffffffffu, mbar_wait(bar, parity, limit));
-}
 
 __device__ __forceinline__ void bulk_g2s(uint32_t dst_smem, const void* src,
                                          uint32_t bytes, uint32_t bar) {
@@ -1077,6 +1089,24 @@ __global__ void lm_selftest_wait_kernel(int arrive) {
 // ---------------------------------------------------------------------------
 // host side: launches
 // ---------------------------------------------------------------------------
+
+// Device address of g_lm_device_status on the current device (looked up
+// once per device), for kernels of other files that record timeouts.
+unsigned int* device_status_word() {
+  static std::mutex mu;
+  static unsigned int* addr[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+    return nullptr;
+  std::lock_guard<std::mutex> g(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_lm_device_status) != cudaSuccess)
+      return nullptr;
+    addr[dev] = static_cast<unsigned int*>(p);
+  }
+  return addr[dev];
+}
 
 struct DeviceInfo {
   int sms = 0;
@@ -1486,6 +1516,60 @@ int launch_piece(const lm_plan& P, const Piece& pc, const char* src,
   return launch_generic(pc.gen, src, dst, st);
 }
 
+// Tiles for lm_eval_tiled_kernel: the largest tile of at most 2048 * R
+// consecutive indices (at least 64 * R) that is the product of the first
+// leaves and a divisor of the next, a multiple of R, with fewer than 2^32
+// tiles and in-tile offsets in 32-bit index arithmetic.  False when none.
+bool eval_tiles(const std::vector<Leaf>& c, int R, EvalArgs& a) {
+  if (a.nl == 0 || a.n % uint64_t(R)) return false;
+  const int64_t tmax = 2048 * int64_t(R), tmin = 64 * int64_t(R);
+  int64_t best = 0;
+  int best_k = -1;
+  int64_t best_f = 1, before = 1;
+  for (int k = 0; k < int(c.size()) && before <= tmax; ++k) {
+    for (int64_t f = 1; f <= c[size_t(k)].e && before * f <= tmax; ++f) {
+      if (c[size_t(k)].e % f) continue;
+      const int64_t t = before * f;
+      if (t % R == 0 && t > best) {
+        best = t;
+        best_k = k;
+        best_f = f;
+      }
+    }
+    before *= c[size_t(k)].e;
+  }
+  if (best < tmin || uint64_t(best) > a.n) return false;
+  const uint64_t tiles = a.n / uint64_t(best);
+  if (tiles >= (uint64_t(1) << 32)) return false;
+  int n_in = 0, n_out = 0;
+  for (int k = 0; k < int(c.size()); ++k) {
+    const Leaf& l = c[size_t(k)];
+    if (k < best_k || (k == best_k && best_f == l.e)) {
+      a.in_ext[n_in] = uint32_t(l.e);
+      a.in_str[n_in++] = l.d;
+    } else if (k == best_k) {
+      if (best_f > 1) {
+        a.in_ext[n_in] = uint32_t(best_f);
+        a.in_str[n_in++] = l.d;
+      }
+      a.out_ext[n_out] = uint32_t(l.e / best_f);
+      a.out_str[n_out++] = mul_chk(l.d, best_f);
+    } else {
+      if (l.e >= (int64_t(1) << 32)) return false;
+      a.out_ext[n_out] = uint32_t(l.e);
+      a.out_str[n_out++] = l.d;
+    }
+    if (n_in > kMaxLeaves || n_out > kMaxLeaves) return false;
+  }
+  for (int k = 0; k < n_in; ++k) a.in_div[k] = make_fastdiv(a.in_ext[k]);
+  for (int k = 0; k < n_out; ++k) a.out_div[k] = make_fastdiv(a.out_ext[k]);
+  a.n_in = n_in;
+  a.n_out = n_out;
+  a.tile_elems = uint32_t(best);
+  a.n_tiles = tiles;
+  return true;
+}
+
 int launch_eval(const lm_layout& L, void* table, int offset_bytes,
                 void* stream) {
   EvalArgs a;
@@ -1508,6 +1592,29 @@ int launch_eval(const lm_layout& L, void* table, int offset_bytes,
   const unsigned grid = unsigned(
       std::max<uint64_t>(1, std::min<uint64_t>(want, uint64_t(di.sms) * 16)));
   const int R = 16 / offset_bytes;
+  if (reinterpret_cast<uintptr_t>(table) % 16 == 0 && eval_tiles(c, R, a)) {
+    const uint64_t per_block = 8;   // tiles per block: blocks turn over often
+    const unsigned gridt = unsigned(std::max<uint64_t>(
+        1, std::min<uint64_t>((a.n_tiles + per_block - 1) / per_block,
+                              uint64_t(di.sms) * 64)));
+    const uint32_t vecs = a.tile_elems / uint32_t(R);
+    if (offset_bytes == 4) {
+      if (vecs <= 4 * 256)
+        launch_k(lm_eval_tiled_kernel<int32_t, 4>, gridt, 256, 0, st, a,
+                 static_cast<int32_t*>(table));
+      else
+        launch_k(lm_eval_tiled_kernel<int32_t, 8>, gridt, 256, 0, st, a,
+                 static_cast<int32_t*>(table));
+    } else {
+      if (vecs <= 4 * 256)
+        launch_k(lm_eval_tiled_kernel<int64_t, 4>, gridt, 256, 0, st, a,
+                 static_cast<int64_t*>(table));
+      else
+        launch_k(lm_eval_tiled_kernel<int64_t, 8>, gridt, 256, 0, st, a,
+                 static_cast<int64_t*>(table));
+    }
+    return check_launch();
+  }
   if (a.nl > 0 && c[0].e % R == 0 &&
       reinterpret_cast<uintptr_t>(table) % 16 == 0) {
     const uint64_t wantv = (a.n / R + 255) / 256;

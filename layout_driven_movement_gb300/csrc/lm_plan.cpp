@@ -370,10 +370,23 @@ int64_t warp_wavefronts(const int64_t* addr, const bool* valid, int bytes) {
   return wavefronts(addr, valid, 32, bytes);
 }
 
+// A common refinement of the two sides' leaves, trying each side's leaves
+// as given and coalesced: coalescing keeps a side's offset function (it
+// only merges leaves that continue each other), but removes boundaries the
+// other side does not share -- (6000,7000):(7000,1) against
+// (7000,6000):(1,7000) refines only once the second side is seen as the
+// single run 42000000:1.
+bool refine_sides(const std::vector<Leaf>& s, const std::vector<Leaf>& d,
+                  std::vector<JMode>& out) {
+  if (refine(s, d, out)) return true;
+  const std::vector<Leaf> cs = coalesce_leaves(s), cd = coalesce_leaves(d);
+  return refine(cs, d, out) || refine(s, cd, out) || refine(cs, cd, out);
+}
+
 bool joint_modes(const lm_layout& src, const lm_layout& dst,
                  std::vector<JMode>& out) {
   out.clear();
-  if (!refine(src.leaves, dst.leaves, out)) return false;
+  if (!refine_sides(src.leaves, dst.leaves, out)) return false;
   out = coalesce_joint(out);
   return true;
 }
@@ -1451,7 +1464,7 @@ static int plan_copy_impl(const lm_layout* src, const lm_layout* dst,
     if (P->size > 0) {
       if (!affine_injective(dst->leaves)) fail(LM_E_NOT_INJECTIVE);
       std::vector<JMode> jm;
-      if (refine(src->leaves, dst->leaves, jm)) {
+      if (refine_sides(src->leaves, dst->leaves, jm)) {
         P->joint = true;
         jm = coalesce_joint(jm);
         int64_t s_base = 0, d_base = 0;

@@ -10,8 +10,11 @@
 #include <mutex>
 #include <utility>
 
+#include <cstdlib>
+
 #include "layoutmove_tv.cuh"
 #include "lm_internal.h"
+#include "lm_mbar.cuh"
 
 namespace lm {
 namespace {
@@ -109,7 +112,122 @@ __global__ void __launch_bounds__(512)
   }
 }
 
+// The cached loop without block-wide barriers: NS shared tiles, each with
+// a "full" mbarrier that every loading thread's cp.async copies of the
+// tile arrive on when they land (cp.async.mbarrier.arrive.noinc) and an
+// "empty" mbarrier every storing thread arrives on once it has read the
+// tile.  A thread loads tile i + NS - 1 after the storers released its
+// stage, then waits for tile i to be full and stores its share; warps run
+// ahead of each other up to the pipeline depth.  Every wait is bounded: a
+// thread that gives up records it in the device status word, waits for its
+// own copies (a hardware wait) and leaves.  Load phases of 4-, 8- and
+// 16-byte vectors only (all of them cp.async).
+template <int VL, int VS, int MAXV, int NS>
+__global__ void __launch_bounds__(512)
+    lm_tv_mbar_kernel(const __grid_constant__ lm_tv_args a,
+                      const char* __restrict__ src, char* __restrict__ dst,
+                      unsigned int* status) {
+  extern __shared__ __align__(128) char smem_raw[];
+  const uint32_t bars = uint32_t(__cvta_generic_to_shared(smem_raw));
+  auto full = [&](int s) { return bars + 8u * uint32_t(s); };
+  auto empty = [&](int s) { return bars + 8u * uint32_t(NS + s); };
+  char* tiles = smem_raw + 128;
+  const int t = int(threadIdx.x);
+  const bool loader = t < a.load.n_thr, storer = t < a.store.n_thr;
+  if (t == 0) {
+#pragma unroll
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(full(s), uint32_t(a.load.n_thr));
+      mbar_init(empty(s), uint32_t(a.store.n_thr));
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  __syncthreads();
+  const int64_t first = blockIdx.x, stride = gridDim.x;
+  if (first >= a.n_tiles) return;  // whole block
+  const int64_t n_local = (a.n_tiles - first + stride - 1) / stride;
+  lm_tv::Offsets<MAXV> o;
+  lm_tv::thread_offsets<MAXV>(a, lm_tv::thread_bases(a, t), o);
+  bool ok = true;
+  // tile number i of this block into stage i % NS
+  auto issue = [&](int64_t i) -> bool {
+    const int s = int(i % NS);
+    if (i >= NS && !mbar_wait(empty(s), uint32_t((i / NS) - 1) & 1u))
+      return false;
+    int64_t sb, db;
+    lm_tv::tile_bases(a, first + i * stride, &sb, &db);
+    lm_tv::load_tile<VL, MAXV>(a, o, src, tiles + s * a.smem_bytes, sb, t);
+    cp_async_arrive_noinc(full(s));
+    return true;
+  };
+  if (loader)
+    for (int64_t i = 0; i < NS - 1 && i < n_local && ok; ++i) ok = issue(i);
+  for (int64_t i = 0; i < n_local && ok; ++i) {
+    if (loader && i + NS - 1 < n_local) ok = issue(i + NS - 1);
+    if (!ok) break;
+    if (storer) {
+      const int s = int(i % NS);
+      if (!mbar_wait(full(s), uint32_t(i / NS) & 1u)) {
+        ok = false;
+        break;
+      }
+      int64_t sb, db;
+      lm_tv::tile_bases(a, first + i * stride, &sb, &db);
+      lm_tv::store_tile<VS, MAXV>(a, o, tiles + s * a.smem_bytes, dst, db, t);
+      mbar_arrive(empty(s));
+    }
+  }
+  if (!ok && status) atomicOr(status, 1u);
+  lm_tv::wait_copies();  // no copy of this thread outlives it
+}
+
 typedef void (*TvKernel)(const lm_tv_args, const char*, char*, int);
+typedef void (*TvMbarKernel)(const lm_tv_args, const char*, char*,
+                             unsigned int*);
+
+template <int VL, int NS>
+TvMbarKernel pick_mbar_store(int vs) {
+  switch (vs) {
+    case 4: return lm_tv_mbar_kernel<VL, 4, 4, NS>;
+    case 8: return lm_tv_mbar_kernel<VL, 8, 4, NS>;
+    case 16: return lm_tv_mbar_kernel<VL, 16, 4, NS>;
+  }
+  return nullptr;
+}
+
+template <int NS>
+TvMbarKernel pick_mbar_ns(int vl, int vs) {
+  switch (vl) {
+    case 4: return pick_mbar_store<4, NS>(vs);
+    case 8: return pick_mbar_store<8, NS>(vs);
+    case 16: return pick_mbar_store<16, NS>(vs);
+  }
+  return nullptr;
+}
+
+// The mbarrier pipeline (LM_TV_MBAR=1; the barrier-paced kernels by
+// default) and its depth (LM_TV_STAGES, 2..4).  Measured on GB300 it ran
+// the bench's tile copies as fast as the barrier-paced kernels, no faster
+// (54.8 against 53.6 us for the 8192^2 bf16 tiling, 29.0 against 29.1 us for
+// the fp32 transpose with 16-byte loads), at any depth.
+int tv_mbar_stages() {
+  static const int v = [] {
+    const char* e = std::getenv("LM_TV_MBAR");
+    if (!e || e[0] != '1') return 0;
+    const char* d = std::getenv("LM_TV_STAGES");
+    const int n = d ? std::atoi(d) : 3;
+    return n < 2 ? 2 : (n > 4 ? 4 : n);
+  }();
+  return v;
+}
+
+TvMbarKernel pick_mbar(int vl, int vs, int ns) {
+  switch (ns) {
+    case 2: return pick_mbar_ns<2>(vl, vs);
+    case 4: return pick_mbar_ns<4>(vl, vs);
+    default: return pick_mbar_ns<3>(vl, vs);
+  }
+}
 
 template <int VL>
 TvKernel pick_cached_store(int vs) {
@@ -160,6 +278,49 @@ int fail_cuda(cudaError_t e) {
   return LM_E_CUDA;
 }
 
+// Dynamic shared memory above 48 KiB needs an opt-in per device and kernel.
+cudaError_t allow_tv_smem(const void* k, int dev, int smem) {
+  if (smem <= 49152) return cudaSuccess;
+  static std::mutex mu;
+  static std::map<std::pair<int, const void*>, int> done;
+  std::lock_guard<std::mutex> g(mu);
+  const auto key = std::make_pair(dev, k);
+  auto it = done.find(key);
+  if (it == done.end() || it->second < smem) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    done[key] = smem;
+  }
+  return cudaSuccess;
+}
+
+// One block per resident slot at most, grid-stride over the tiles.
+int launch_mbar(TvMbarKernel k, const lm_tv_args& a, const char* src,
+                char* dst, void* stream, int smem, unsigned int* status) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e);
+  e = allow_tv_smem(reinterpret_cast<const void*>(k), dev, smem);
+  if (e != cudaSuccess) return fail_cuda(e);
+  int sms = 0, per_sm = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return fail_cuda(e);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k,
+                                                    a.block_threads,
+                                                    size_t(smem));
+  if (e != cudaSuccess) return fail_cuda(e);
+  if (per_sm < 1) return LM_E_INVALID;  // the block cannot be resident
+  const int64_t resident = int64_t(sms) * per_sm;
+  const unsigned grid =
+      unsigned(a.n_tiles < resident ? a.n_tiles : resident);
+  k<<<grid, unsigned(a.block_threads), size_t(smem),
+      static_cast<cudaStream_t>(stream)>>>(a, src, dst, status);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return fail_cuda(e);
+  return LM_OK;
+}
+
 }  // namespace
 
 int launch_tv(const lm_tv_plan& plan, const char* src, char* dst,
@@ -167,6 +328,16 @@ int launch_tv(const lm_tv_plan& plan, const char* src, char* dst,
   const lm_tv_args& a = plan.args;
   if (a.n_tiles == 0) return LM_OK;
   const int most = a.load.n_val > a.store.n_val ? a.load.n_val : a.store.n_val;
+  const int ns = tv_mbar_stages();
+  if (ns && a.offsets32 && a.block_threads <= 512 && most <= 4 &&
+      128 + ns * int64_t(a.smem_bytes) <= 232448 && a.smem_bytes % 16 == 0) {
+    const TvMbarKernel mk =
+        pick_mbar(a.load.vec_bytes, a.store.vec_bytes, ns);
+    unsigned int* status = device_status_word();
+    if (mk && status)
+      return launch_mbar(mk, a, src, dst, stream, 128 + ns * a.smem_bytes,
+                         status);
+  }
   TvKernel k = nullptr;
   int smem = 0, two = 0;
   if (a.offsets32 && a.block_threads <= 512 && most <= 4 &&

@@ -155,8 +155,17 @@ SMALL = [
      ("layout", (512, 33), (33, 1)), 4),
     ("swizzled_src", ("swizzle", 2, 4, 4, ("layout", (128, 96), (96, 1))),
      ("layout", (128, 96), (1, 128)), 2),
-    ("non_refinable_generic", ("layout", (6, 5), (1, 6)),
-     ("layout", (5, 6), (6, 1)), 4),
+    # 6 and 5 do not nest, and the padded strides keep both sides from
+    # coalescing into one run: no common refinement, GENERIC
+    ("non_refinable_generic", ("layout", (6, 5), (1, 7)),
+     ("layout", (5, 6), (7, 1)), 4),
+    # the same shapes refine once a side is seen as one run: the row-major
+    # 600x700 matrix against the destination (700,600):(1,700) = 420000:1
+    # is a transpose
+    ("coalesced_refinement_f32", ("layout", (600, 700), (700, 1)),
+     ("layout", (700, 600), (1, 700)), 4),
+    ("coalesced_refinement_small_u8", ("layout", (6, 5), (5, 1)),
+     ("layout", (5, 6), (1, 5)), 1),
     ("transpose_tall_f32", ("layout", (2048, 96), (1, 2048)),
      ("layout", (2048, 96), (96, 1)), 4),
     ("vec_untiled_prime", ("layout", (8, 2053), (1, 8)),
@@ -261,6 +270,10 @@ def test_src_capacity_exactly_cosize_staged_tail():
 @pytest.mark.parametrize("spec", [
     EVAL_C1, WORKLOADS["C1"].dst, WORKLOADS["C3"].dst, WORKLOADS["C4"].src,
     ("layout", (7, 11, 13), (1, 1000, 7)),
+    # tiles that cut a leaf: 6 x 500 of (6,1000,...), 15 x 256 of 2^22
+    ("layout", (6, 1000, 7), (7000, 7, 1)),
+    ("layout", (3, 5, 1 << 22), (5, 1, 15)),
+    ("swizzle", 2, 3, 6, ("layout", (12, 64, 40), (64, 1, 768))),
 ])
 @pytest.mark.parametrize("width", [4, 8])
 def test_layout_eval_device(spec, width):

@@ -106,6 +106,34 @@ def test_tv_full_size_tuned_transpose_f32():
     assert desc["n_tiles"] == 64 * 64
 
 
+def test_tv_mbarrier_pipeline_parity():
+    """The mbarrier-paced kernel (LM_TV_MBAR=1, 2 to 4 shared tiles) on every
+    case with given and tuned thread layouts and on the full-size bf16
+    tiling, in fresh processes since the knobs are read once."""
+    import os
+    import subprocess
+    import sys
+    here = os.path.dirname(os.path.abspath(__file__))
+    code = (
+        "import sys; sys.path[:0] = [%r, %r]\n"
+        "import test_gpu_tv as t\n"
+        "t.lm.lib()\n"
+        "for c in t.CASES:\n"
+        "    name, src, smem, dst, tl, ts, eb, expect = c\n"
+        "    t.run_tv(src, smem, dst, tl, ts, eb, expect=expect)\n"
+        "    if name != 'nested_tile_modes':\n"
+        "        t.run_tv(src, smem, dst, None, None, eb, seed=13)\n"
+        "t.test_tv_full_size_tiles_swizzled_bf16()\n"
+        "assert t.lm.device_status() == 0\n"
+        "print('ok')\n" % (here, os.path.dirname(here)))
+    for stages in ("2", "3", "4"):
+        r = subprocess.run([sys.executable, "-c", code], capture_output=True,
+                           text=True, timeout=900,
+                           env={**os.environ, "LM_TV_MBAR": "1",
+                                "LM_TV_STAGES": stages})
+        assert r.returncode == 0 and "ok" in r.stdout, r.stdout + r.stderr
+
+
 def test_tv_forced_vector_widths():
     src = zd((128, 96), (1, 128), (32, 32))
     dst = zd((128, 96), (96, 1), (32, 32))

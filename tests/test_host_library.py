@@ -502,10 +502,14 @@ def test_plan_errors():
 
 
 def test_plan_non_refinable_pair_is_generic_and_empty_plan():
-    s = lm.Layout.parse("(2,3):(1,2)")
+    s = lm.Layout.parse("(2,3):(1,3)")
     d = lm.Layout.parse("(3,2):(2,1)")
     desc = lm.Plan(s, d, 4).describe()
     assert not desc["joint"] and desc["pieces"][0]["path"] == "GENERIC"
+    # (2,3):(1,2) is the single run 6:1, which refines against (3,2)
+    desc = lm.Plan(lm.Layout.parse("(2,3):(1,2)"), d, 4).describe()
+    assert desc["joint"] and desc["pieces"][0]["modes"] == [[3, 1, 2],
+                                                            [2, 3, 1]]
     e = lm.Plan(lm.Layout.parse("(0,4):(1,0)"), lm.Layout.parse("(0,4):(4,1)"), 4)
     assert e.describe()["pieces"] == [] and e.launches == 0
 
@@ -628,3 +632,36 @@ def test_product_built_copy_layouts_match_oracle():
         assert L.size == OL.size and L.cosize == lo.cosize(OL), name
         idx = np.concatenate([[0, L.size - 1], rng.integers(0, L.size, 2000)])
         assert [L(int(i)) for i in idx] == OL.at(idx).tolist(), name
+
+
+def test_refinement_of_coalesced_sides():
+    """Pairs whose raw leaves do not nest but whose coalesced leaves do are
+    planned on the joint paths: the 6000x7000 fp32 matrix against the
+    destination (7000,6000):(1,7000) (one run of 42,000,000) is a
+    transpose; with a padded destination there is no refinement."""
+    S = lm.Layout.parse("(6000,7000):(7000,1)")
+    d = lm.Plan(S, lm.Layout.parse("(7000,6000):(1,7000)"), 4).describe()
+    assert d["joint"] and [p["path"] for p in d["pieces"]] == ["STAGED"]
+    assert d["pieces"][0]["modes"] == [[6000, 7000, 1], [7000, 1, 6000]]
+    d = lm.Plan(S, lm.Layout.parse("(7000,6000):(1,7001)"), 4).describe()
+    assert not d["joint"] and d["pieces"][0]["path"] == "GENERIC"
+    # every accepted joint plan still maps each logical index like the two
+    # layouts do (sampled against the oracle)
+    rng = np.random.default_rng(77)
+    for s_txt, d_txt in [("(6,5):(5,1)", "(5,6):(1,5)"),
+                         ("(4,9,2):(18,2,1)", "(12,6):(1,12)"),
+                         ("(10,21):(1,10)", "(6,35):(35,1)")]:
+        plan = lm.Plan(lm.Layout.parse(s_txt), lm.Layout.parse(d_txt), 2)
+        desc = plan.describe()
+        assert desc["joint"], (s_txt, d_txt)
+        OS, OD = lo.parse(s_txt), lo.parse(d_txt)
+        i = np.arange(OS.size)
+        ms = desc["pieces"][0]["modes"]
+        so = np.zeros_like(i)
+        do = np.zeros_like(i)
+        rem = i.copy()
+        for e, st, dt in ms:
+            so += (rem % e) * st
+            do += (rem % e) * dt
+            rem //= e
+        assert (so == OS.at(i)).all() and (do == OD.at(i)).all()
