@@ -555,15 +555,21 @@ def test_copy_host_buffers_by_shards_on_streams():
     assert e.value.status == -1
 
 
-def test_generic_without_common_refinement_full_size_sampled():
-    """The 6000x7000 fp32 pair bench.py times on the GENERIC path (no
-    common refinement: 6000 and 7000 do not nest), checked at 200000
-    seeded logical indices computed one by one by the oracle, plus the
-    guard band."""
-    src_t, dst_t = "(6000,7000):(7000,1)", "(7000,6000):(1,7000)"
+@pytest.mark.parametrize("dst_t,path", [
+    # no common refinement: 6000 and 7000 do not nest and the padded
+    # destination does not coalesce (GENERIC)
+    ("(7000,6000):(1,7001)", "GENERIC"),
+    # the destination is the single run 42000000:1: a transpose (STAGED)
+    ("(7000,6000):(1,7000)", "STAGED"),
+])
+def test_generic_without_common_refinement_full_size_sampled(dst_t, path):
+    """The 6000x7000 fp32 pairs bench.py times, checked at 200000 seeded
+    logical indices computed one by one by the oracle, plus the guard
+    band."""
+    src_t = "(6000,7000):(7000,1)"
     S, D = lm.Layout.parse(src_t), lm.Layout.parse(dst_t)
     plan = lm.Plan(S, D, 4)
-    assert [p["path"] for p in plan.describe()["pieces"]] == ["GENERIC"]
+    assert [p["path"] for p in plan.describe()["pieces"]] == [path]
     n = S.size
     inp = seeded_bytes("bytes", "uint8", S.cosize * 4, 13)
     src = torch.from_numpy(inp).cuda()
