@@ -425,7 +425,8 @@ def kernel_name(plan, eb: int) -> str:
         store = (f"XposeStore<{eb}, {pc['rows']}>" if pc["store"] == "transpose"
                  else f"GatherStore<{eb}>")
         if pc["bulk"]:
-            tma = "true" if pc.get("tma") else "false"
+            # ncu prints the bool template argument as 0 / 1
+            tma = 1 if pc.get("tma") else 0
             return f"lm_bulk_kernel<{eb}, {store}, {pc['stages']}, {tma}>"
         return f"lm_staged_kernel<{eb}, {store}, {pc['stages']}>"
     if pc["path"] == "VEC":
