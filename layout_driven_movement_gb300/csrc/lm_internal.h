@@ -234,6 +234,13 @@ struct StagedArgs {
                                         //    first (conflict-free rows
                                         //    without a swizzle)
   uint32_t x_pitch = 0;                 // smem bytes between rows
+  int32_t x_blocks = 0;                 // 1: micro-tiles in warp blocks of
+                                        //    8 along b x 4 along a (each
+                                        //    quarter-warp 8 bank groups of a
+                                        //    128-byte-swizzled image)
+  uint32_t x_region = 0;                // smem bytes per 128-byte column
+                                        //    region of the tile (0: rows of
+                                        //    the whole tile width)
   int64_t x_da = 0;                     // dst bytes per 16-byte chunk of a
   int64_t x_db = 0;                     // dst bytes per R rows of b
   int64_t x_vstep = 0;                  // dst bytes between output vectors
@@ -259,6 +266,10 @@ struct StagedArgs {
   // lands densely (rows of t_box[0] elements), which is the image the
   // store side reads.
   int32_t tma = 0;
+  int32_t t_swz128 = 0;                 // boxes of 128-byte rows, swizzled
+                                        // (t_regions of them per tile, one
+                                        // per x_region of the stage)
+  uint32_t t_regions = 1;
   int32_t t_rank = 0;
   uint64_t t_dim[5];                    // extents, elements
   uint64_t t_stride[5];                 // bytes (t_stride[0] unused)

@@ -723,7 +723,19 @@ struct XposeStore {
       for (int r = 0; r < R; ++r) sm[k][r] = 0;
       if (j < a.n_micro) {
         uint32_t ac, bc;
-        if (a.x_acfast) {
+        if (a.x_blocks) {
+          // warp blocks of 8 micro-tiles along b by 4 along a; each
+          // quarter-warp covers 8 bank groups of the swizzled image
+          const uint32_t w = j >> 5, l = j & 31, nwb = a.n_bc >> 3;
+          const uint32_t wa = w / nwb, wb = w - wa * nwb;
+          if constexpr (R == 4) {
+            bc = 8u * wb + 2u * (l >> 3) + (l & 1u);
+            ac = 4u * wa + ((l >> 1) & 3u);
+          } else {
+            bc = 8u * wb + 4u * ((l >> 3) & 1u) + (l & 3u);
+            ac = 4u * wa + 2u * (l >> 4) + ((l >> 2) & 1u);
+          }
+        } else if (a.x_acfast) {
           bc = fdiv(j, a.ac_div);
           ac = j - bc * a.n_ac;
         } else {
@@ -731,7 +743,11 @@ struct XposeStore {
           bc = j - ac * a.n_bc;
         }
         dst[k] = int32_t(int64_t(ac) * a.x_da + int64_t(bc) * a.x_db);
-        const uint32_t lin = bc * uint32_t(R) * a.x_pitch + ac * 16u;
+        // chunk ac of the row: in its 128-byte column region when the tile
+        // is stored as such regions
+        const uint32_t col = a.x_region ? (ac >> 3) * a.x_region + (ac & 7u) * 16u
+                                        : ac * 16u;
+        const uint32_t lin = bc * uint32_t(R) * a.x_pitch + col;
 #pragma unroll
         for (int r = 0; r < R; ++r)
           sm[k][r] = swz_apply32(a.m_swz, lin + uint32_t(r) * a.x_pitch);
@@ -923,9 +939,10 @@ __device__ __forceinline__ void tma_g2s(uint32_t dst_smem, const CUtensorMap* m,
 }
 
 // Bytes of dynamic shared memory a bulk-form block asks for: mbarriers
-// (128 bytes), the stages, and 128 bytes of slack to align them.
+// (128 bytes), the stages, and slack to align them (128 bytes, or 1024 for
+// tensor-map stages).
 inline int bulk_smem_bytes(const StagedArgs& a, int ns) {
-  return int(256 + ns * a.stage_bytes);
+  return int((a.tma ? 128 + 1024 : 256) + ns * a.stage_bytes);
 }
 
 // The bulk-copy STAGED kernel.  TMA == false: one cp.async.bulk per source
@@ -939,14 +956,16 @@ __global__ void __launch_bounds__(256)
   extern __shared__ __align__(128) unsigned char smem[];
   const uint32_t tid = threadIdx.x, nt = blockDim.x;
   const uint32_t warp = tid >> 5, lane = tid & 31, n_warps = nt >> 5;
-  // mbarriers and stages from the first 128-byte boundary (tensor copies
-  // need 128-byte aligned destinations; the launch adds the slack)
+  // mbarriers from the first 128-byte boundary, stages from the next
+  // 1024-byte one (swizzled tensor copies need 1024-byte aligned
+  // destinations, plain ones 128; the launch adds the slack)
   const uint32_t base = uint32_t(__cvta_generic_to_shared(smem));
   const uint32_t bars = (base + 127u) & ~127u;
   auto full = [&](uint32_t s) { return bars + 8u * s; };
   auto empty = [&](uint32_t s) { return bars + 8u * (NS + s); };
-  unsigned char* stages = smem + (bars - base) + 128;
-  const uint32_t stage0 = bars + 128;
+  const uint32_t stage0 =
+      TMA ? ((bars + 128u + 1023u) & ~1023u) : bars + 128u;
+  unsigned char* stages = smem + (stage0 - base);
 
   Store st;
   st.init(a, tid, nt);
@@ -1020,7 +1039,10 @@ __global__ void __launch_bounds__(256)
           t = q;
         }
         mbar_arrive_expect_tx(full(s), tile_bytes);
-        tma_g2s(sdst, &tmap, a.t_rank, c0, c1, c2, c3, c4, full(s));
+        // one box per 128-byte column region (one box when unswizzled)
+        for (uint32_t g = 0; g < a.t_regions; ++g)
+          tma_g2s(sdst + g * a.x_region, &tmap, a.t_rank,
+                  c0 + int32_t(g * a.t_box[0]), c1, c2, c3, c4, full(s));
       }
       __syncwarp();
     } else {
@@ -1394,7 +1416,8 @@ bool encode_source_map(const StagedArgs& a, int eb, const char* src,
   }
   return fn(m, dt, cuuint32_t(a.t_rank),
             const_cast<char*>(src) + a.s_base, dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_INTERLEAVE_NONE,
+            a.t_swz128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

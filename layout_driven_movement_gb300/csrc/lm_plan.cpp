@@ -174,10 +174,12 @@ int bulk_stages() {
 }
 // Tensor-map (TMA) tile loads for STAGED transposes (LM_TMA=1 turns them
 // on) and their pipeline depth (LM_TMA_STAGES, 2..4).  Off by default:
-// measured on GB300, one box per tile (64 rows of 256 bytes) took 29.3 us
-// for the 4096x4096 fp32 transpose and 41.6 us for NHWC->NCHW against
-// 23.2 and 33.4 us for the per-thread cp.async loads, whatever the depth,
-// tiles per block or micro-tile order.
+// measured on GB300, one dense box per tile (64 rows of 256 bytes) took
+// 29.3 us for the 4096x4096 fp32 transpose and 41.6 us for NHWC->NCHW
+// against 23.2 and 33.4 us for the per-thread cp.async loads, whatever the
+// depth, tiles per block or micro-tile order (ncu: the L1 pipeline 78%
+// busy with scattered stores or conflicting shared reads); with 128-byte
+// swizzled boxes and warp-block micro-tiles the fp32 transpose took 25.2 us.
 bool tma_enabled() {
   static bool v = env_int("LM_TMA", 0) != 0;
   return v;
@@ -642,9 +644,36 @@ static StagedChoice plan_transpose(const std::vector<JMode>& ms,
   // index along a first: 8 lanes then read 8 consecutive chunks of a row
   // (LM_TMA_ACFAST=0 keeps the b-first order on tensor-map tiles: stores
   // coalesced, shared reads conflicting)
-  const bool acfast =
-      bulk && n_ac >= 8 && !(tma && env_int("LM_TMA_ACFAST", 1) == 0);
+  // Tensor-map boxes of 128-byte rows with the hardware's 128-byte swizzle
+  // (16-byte chunk c of row y at chunk c ^ (y % 8), the tile's width in
+  // column regions of Tb rows each): with micro-tiles in warp blocks of 8
+  // along b by 4 along a, each quarter-warp reads 8 distinct bank groups and
+  // each store instruction writes whole 128-byte lines.  4- and 8-byte
+  // elements (R = 4 or 2).
+  const bool tma_swz = tma && R == V && (R == 4 || R == 2) &&
+                       seg_bytes % 128 == 0 && Tb % 8 == 0 && n_bc % 8 == 0 &&
+                       n_ac % 4 == 0 && env_int("LM_TMA_SWIZZLE", 1) != 0;
+  const bool acfast = !tma_swz && bulk && n_ac >= 8 &&
+                      !(tma && env_int("LM_TMA_ACFAST", 1) == 0);
+  const int64_t region = Tb * 128;
+  auto block_coords = [&](int64_t j, int64_t* ac, int64_t* bc) {
+    const int64_t w = j >> 5, l = j & 31, nwb = n_bc / 8;
+    if (R == 4) {
+      *bc = 8 * (w % nwb) + 2 * (l >> 3) + (l & 1);
+      *ac = 4 * (w / nwb) + ((l >> 1) & 3);
+    } else {
+      *bc = 8 * (w % nwb) + 4 * ((l >> 3) & 1) + (l & 3);
+      *ac = 4 * (w / nwb) + 2 * (l >> 4) + ((l >> 2) & 1);
+    }
+  };
+  const Swz swz128{3, 4, 3};
   auto read_addr = [&](int64_t j, int r, int64_t pitch) {
+    if (tma_swz) {
+      int64_t ac, bc;
+      block_coords(j, &ac, &bc);
+      const int64_t lin = (ac >> 3) * region + (ac & 7) * 16 + (bc * R + r) * 128;
+      return swz128.apply(lin);
+    }
     const int64_t bc = acfast ? j / n_ac : j % n_bc;
     const int64_t ac = acfast ? j % n_ac : j / n_bc;
     return (bc * R + r) * pitch + ac * 16;
@@ -694,8 +723,9 @@ static StagedChoice plan_transpose(const std::vector<JMode>& ms,
   if (tma) {
     A.tma = 1;
     A.bulk_stages = tma_stages();
-    // tensor copies land on 128-byte boundaries: every stage starts on one
-    A.stage_bytes = (A.stage_bytes + 127u) & ~127u;
+    // tensor copies land on 128-byte boundaries (swizzled ones on 1024):
+    // every stage starts on one
+    A.stage_bytes = (A.stage_bytes + 1023u) & ~1023u;
     A.t_rank = int32_t(n);
     for (int k = 0; k < n; ++k) {
       const int d = tdim[size_t(k)];
@@ -706,6 +736,15 @@ static StagedChoice plan_transpose(const std::vector<JMode>& ms,
     for (size_t k = 0; k < gm.size(); ++k) {
       A.g_tdim[k] = int32_t(gm[k].tdim);
       A.g_tstep[k] = uint32_t(gm[k].tstep);
+    }
+    if (tma_swz) {
+      A.t_swz128 = 1;
+      A.t_regions = uint32_t(seg_bytes / 128);
+      A.t_box[0] = uint32_t(128 / eb);
+      A.x_blocks = 1;
+      A.x_region = uint32_t(region);
+      A.x_pitch = 128;
+      A.m_swz = swz128;
     }
   }
   pc.path = PATH_STAGED;
@@ -1257,7 +1296,8 @@ static std::string describe(const lm_plan& P) {
          << ",\"stages\":" << (A.bulk ? A.bulk_stages : A.stages)
          << ",\"bulk\":"
          << (A.bulk ? "true" : "false") << ",\"tma\":"
-         << (A.tma ? "true" : "false")
+         << (A.tma ? "true" : "false") << ",\"tma_swizzle\":"
+         << (A.t_swz128 ? "true" : "false")
          << ",\"stage_bytes\":" << A.stage_bytes << ",\"smem_swizzle\":["
          << A.m_swz.b << ',' << A.m_swz.m << ',' << A.m_swz.s << ']'
          << ",\"bank_wavefronts\":" << pc.bank_cost

@@ -383,7 +383,9 @@ def test_short_interleaves_plan_the_register_path():
 @pytest.mark.parametrize("env", [{"LM_BULK": "0"},
                                  {"LM_BULK": "0", "LM_STAGES": "3"},
                                  {"LM_TMA": "1"},
-                                 {"LM_TMA": "1", "LM_TMA_ACFAST": "0"},
+                                 {"LM_TMA": "1", "LM_TMA_SWIZZLE": "0"},
+                                 {"LM_TMA": "1", "LM_TMA_SWIZZLE": "0",
+                                  "LM_TMA_ACFAST": "0"},
                                  {"LM_BULK_STAGES": "2", "LM_TMA": "1",
                                   "LM_TMA_STAGES": "2"},
                                  {"LM_BULK_STAGES": "4", "LM_TMA": "1",
