@@ -278,6 +278,44 @@ struct StagedArgs {
   uint32_t g_tstep[kMaxModes];
 };
 
+// Tiled copy of a pair without a common refinement (PATH_GTILE).  One side
+// ("inner") runs with unit stride along the logical index; the other
+// ("outer") has its unit-stride leaf at logical weight W, so with
+// i = u + W*v (u < W) the outer side's offset is lo(u) + hi(v) -- its
+// leaves before that leaf over u, the rest over v -- and contiguous along
+// v, while the inner side's offset (its full decomposition of i) is
+// contiguous along u.  Tiles of kGtU x kGtV (u, v) are staged through
+// shared memory: read along the source's contiguous direction, written
+// along the destination's.  32-bit logical indices.
+constexpr int kGtU = 32, kGtV = 64;
+constexpr int kGtLeaves = 4;            // leaves per part at most
+struct GTileArgs {
+  uint64_t n = 0;
+  uint32_t W = 1;                       // u extent
+  uint32_t nv = 0;                      // v extent, n / W
+  uint32_t n_ut = 0, n_vt = 0;          // tiles along u and v
+  FastDiv ut_div;                       // division by n_ut
+  int32_t outer_src = 1;                // 1: the source is the outer side
+  int32_t n_lo = 0, n_hi = 0, n_in = 0;
+  uint32_t lo_ext[kMaxLeaves];
+  FastDiv lo_div[kMaxLeaves];
+  int64_t lo_str[kMaxLeaves];           // bytes
+  uint32_t hi_ext[kMaxLeaves];
+  FastDiv hi_div[kMaxLeaves];
+  int64_t hi_str[kMaxLeaves];           // bytes
+  uint32_t in_ext[kMaxLeaves];
+  FastDiv in_div[kMaxLeaves];
+  int64_t in_str[kMaxLeaves];           // bytes
+  // the steps a thread takes between its elements, as digits in each part's
+  // mixed radix: u by 4 over the lo leaves, the index by 8 * W over the
+  // inner leaves
+  uint32_t lo_step[kMaxLeaves];
+  uint32_t in_step[kMaxLeaves];
+  int64_t s_base = 0, d_base = 0;       // bytes
+  Swz s_swz, d_swz;                     // bytes
+  int32_t narrow = 0;                   // every byte offset below 2^31
+};
+
 struct EvalArgs {
   uint64_t n = 0;
   int32_t nl = 0;
@@ -305,7 +343,13 @@ struct EvalArgs {
 // ---------------------------------------------------------------------------
 // The lowered plan.
 // ---------------------------------------------------------------------------
-enum Path : int { PATH_GENERIC = 0, PATH_VEC = 1, PATH_STAGED = 2, PATH_ZIP = 3 };
+enum Path : int {
+  PATH_GENERIC = 0,
+  PATH_VEC = 1,
+  PATH_STAGED = 2,
+  PATH_ZIP = 3,
+  PATH_GTILE = 4
+};
 
 struct JMode {
   int64_t e, s, d;  // extent, src stride, dst stride (elements)
@@ -319,6 +363,7 @@ struct Piece {
   int64_t tile_elems = 0;          // STAGED: elements per tile
   int xr = 0;                      // STAGED transpose: rows per micro-tile
   GenericArgs gen;                 // always filled (fallback)
+  GTileArgs gt;                    // PATH_GTILE
   VecArgs vec;
   StagedArgs st;
   int64_t bank_cost = 0, bank_ideal = 0;  // STAGED: simulated smem wavefronts

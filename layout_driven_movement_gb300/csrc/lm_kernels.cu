@@ -88,6 +88,29 @@ __device__ __forceinline__ void st_stream(T* p, const T& v) {
   __stcs(p, v);
 }
 
+// cp.async: 16-byte copies from global to shared memory (with a source
+// size, the rest zero-filled), groups and waits.
+__device__ __forceinline__ void cp_async16(uint32_t smem_addr, const void* g,
+                                           int src_bytes) {
+  asm volatile(
+      "cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_addr),
+      "l"(g), "r"(src_bytes)
+      : "memory");
+}
+__device__ __forceinline__ void cp_async16_full(uint32_t smem_addr,
+                                                const void* g) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_addr),
+               "l"(g)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
 __device__ __forceinline__ int64_t swz_apply(const Swz& z, int64_t o) {
   return z.b > 0 ? (o ^ ((o >> z.s) & (((int64_t(1) << z.b) - 1) << z.m))) : o;
 }
@@ -259,6 +282,208 @@ __global__ void __launch_bounds__(256)
 }
 
 // ---------------------------------------------------------------------------
+// GTILE copy: a pair without a common refinement, tile by tile through
+// shared memory (GTileArgs)
+// ---------------------------------------------------------------------------
+
+// offset (bytes) of a 32-bit index over n leaves
+__device__ __forceinline__ int64_t leaves_offset(uint32_t q, int n,
+                                                 const uint32_t* ext,
+                                                 const FastDiv* div,
+                                                 const int64_t* str) {
+  int64_t off = 0;
+#pragma unroll
+  for (int k = 0; k < kMaxLeaves; ++k) {
+    if (k >= n) break;
+    const uint32_t qn = fdiv(q, div[k]);
+    off += int64_t(q - qn * ext[k]) * str[k];
+    q = qn;
+  }
+  return off;
+}
+
+// A position in the mixed radix of up to NL leaves, with its byte
+// offset: set once by division, then advanced by a constant step given as
+// digits (add with carries), so a thread's next element costs a few adds.
+template <int NL, typename OFF>
+struct Digits {
+  uint32_t c[NL];
+  OFF off;
+
+  __device__ __forceinline__ void set(uint32_t q, int n, const uint32_t* ext,
+                                      const FastDiv* div, const int64_t* str) {
+    off = 0;
+#pragma unroll
+    for (int k = 0; k < NL; ++k) {
+      c[k] = 0;
+      if (k < n) {
+        const uint32_t qn = fdiv(q, div[k]);
+        c[k] = q - qn * ext[k];
+        off += OFF(c[k]) * OFF(str[k]);
+        q = qn;
+      }
+    }
+  }
+  // the last leaf may run past its extent: the step never leaves the
+  // caller's range, so no carry out of it is ever needed
+  __device__ __forceinline__ void step(int n, const uint32_t* ext,
+                                       const uint32_t* d, const int64_t* str) {
+    uint32_t carry = 0;
+#pragma unroll
+    for (int k = 0; k < NL; ++k) {
+      if (k < n) {
+        uint32_t x = c[k] + d[k] + carry;
+        carry = (k + 1 < n && x >= ext[k]) ? 1u : 0u;
+        x -= carry ? ext[k] : 0u;
+        off += (OFF(x) - OFF(c[k])) * OFF(str[k]);
+        c[k] = x;
+      }
+    }
+  }
+};
+
+// One element from global into shared memory: cp.async for 4, 8 and 16
+// bytes (asynchronous: the caller commits and waits), a plain load and
+// store otherwise.
+template <int EB>
+__device__ __forceinline__ void elem_to_shared(void* s, const char* g) {
+  if constexpr (EB >= 4) {
+    const uint32_t a = uint32_t(__cvta_generic_to_shared(s));
+    if constexpr (EB == 16)
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(a),
+                   "l"(g)
+                   : "memory");
+    else
+      asm volatile("cp.async.ca.shared.global [%0], [%1], %2;\n" ::"r"(a),
+                   "l"(g), "n"(EB)
+                   : "memory");
+  } else {
+    using T = typename VecT<EB>::T;
+    *reinterpret_cast<T*>(s) = *reinterpret_cast<const T*>(g);
+  }
+}
+
+// OUTER_SRC: the source is the outer side -- it is read along v (lanes
+// over v, its offset lo(u) + hi(v)) and the destination, the inner side,
+// written along u (lanes over u, its offset from the full index).  The
+// other way round otherwise.  Two shared tiles of kGtU x (kGtV + 1)
+// elements (the pad keeps the lanes that walk along u in distinct banks):
+// a block's next tile loads (cp.async) while it stores the current one.
+template <int EB, bool OUTER_SRC, int NL, typename OFF>
+__global__ void __launch_bounds__(256)
+    lm_gtile_kernel(const __grid_constant__ GTileArgs a,
+                    const char* __restrict__ src, char* __restrict__ dst) {
+  using T = typename VecT<EB>::T;
+  extern __shared__ __align__(16) unsigned char gt_smem[];
+  typedef T Tile[kGtU][kGtV + 1];
+  Tile* tiles = reinterpret_cast<Tile*>(gt_smem);
+  pdl_trigger();
+  pdl_wait();
+  const uint32_t t = threadIdx.x;
+  const uint32_t n_tiles = a.n_ut * a.n_vt;
+  // lanes over v: 4 rows of u per pass; lanes over u: 8 columns of v
+  const uint32_t vl_v = t % kGtV, ul_v = t / kGtV;
+  const uint32_t ul_u = t % kGtU, vl_u = t / kGtU;
+  // swizzles only where a side has one (a uniform test, not per element)
+  const bool sswz = a.s_swz.b > 0, dswz = a.d_swz.b > 0;
+  auto sw_s = [&](OFF o) {
+    return sswz ? OFF(swz_apply(a.s_swz, int64_t(o))) : o;
+  };
+  auto sw_d = [&](OFF o) {
+    return dswz ? OFF(swz_apply(a.d_swz, int64_t(o))) : o;
+  };
+  auto origin = [&](uint32_t ti, uint32_t* u0, uint32_t* v0) {
+    const uint32_t vt = fdiv(ti, a.ut_div);
+    *u0 = (ti - vt * a.n_ut) * kGtU;
+    *v0 = vt * kGtV;
+  };
+  auto load = [&](uint32_t ti, Tile& tl) {
+    uint32_t u0, v0;
+    origin(ti, &u0, &v0);
+    if constexpr (OUTER_SRC) {  // the outer source along v
+      const uint32_t v = v0 + vl_v;
+      if (v >= a.nv) return;
+      const OFF base = OFF(
+          a.s_base + leaves_offset(v, a.n_hi, a.hi_ext, a.hi_div, a.hi_str));
+      Digits<NL, OFF> lo;
+      lo.set(u0 + ul_v, a.n_lo, a.lo_ext, a.lo_div, a.lo_str);
+#pragma unroll
+      for (int p = 0; p < kGtU / 4; ++p) {
+        const uint32_t ul = ul_v + 4u * uint32_t(p);
+        if (u0 + ul >= a.W) break;
+        if (p) lo.step(a.n_lo, a.lo_ext, a.lo_step, a.lo_str);
+        elem_to_shared<EB>(&tl[ul][vl_v],
+                           src + sw_s(base + lo.off));
+      }
+    } else {  // the inner source along u
+      const uint32_t u = u0 + ul_u;
+      if (u >= a.W) return;
+      Digits<NL, OFF> in;
+      in.set(u + a.W * (v0 + vl_u), a.n_in, a.in_ext, a.in_div, a.in_str);
+#pragma unroll
+      for (int p = 0; p < kGtV / 8; ++p) {
+        const uint32_t vl = vl_u + 8u * uint32_t(p);
+        if (v0 + vl >= a.nv) break;
+        if (p) in.step(a.n_in, a.in_ext, a.in_step, a.in_str);
+        elem_to_shared<EB>(&tl[ul_u][vl],
+                           src + sw_s(OFF(a.s_base) + in.off));
+      }
+    }
+  };
+  auto store = [&](uint32_t ti, const Tile& tl) {
+    uint32_t u0, v0;
+    origin(ti, &u0, &v0);
+    if constexpr (OUTER_SRC) {  // the inner destination along u
+      const uint32_t u = u0 + ul_u;
+      if (u >= a.W) return;
+      Digits<NL, OFF> in;
+      in.set(u + a.W * (v0 + vl_u), a.n_in, a.in_ext, a.in_div, a.in_str);
+#pragma unroll
+      for (int p = 0; p < kGtV / 8; ++p) {
+        const uint32_t vl = vl_u + 8u * uint32_t(p);
+        if (v0 + vl >= a.nv) break;
+        if (p) in.step(a.n_in, a.in_ext, a.in_step, a.in_str);
+        *reinterpret_cast<T*>(dst + sw_d(OFF(a.d_base) + in.off)) =
+            tl[ul_u][vl];
+      }
+    } else {  // the outer destination along v
+      const uint32_t v = v0 + vl_v;
+      if (v >= a.nv) return;
+      const OFF base = OFF(
+          a.d_base + leaves_offset(v, a.n_hi, a.hi_ext, a.hi_div, a.hi_str));
+      Digits<NL, OFF> lo;
+      lo.set(u0 + ul_v, a.n_lo, a.lo_ext, a.lo_div, a.lo_str);
+#pragma unroll
+      for (int p = 0; p < kGtU / 4; ++p) {
+        const uint32_t ul = ul_v + 4u * uint32_t(p);
+        if (u0 + ul >= a.W) break;
+        if (p) lo.step(a.n_lo, a.lo_ext, a.lo_step, a.lo_str);
+        *reinterpret_cast<T*>(dst + sw_d(base + lo.off)) =
+            tl[ul][vl_v];
+      }
+    }
+  };
+  uint32_t ti = blockIdx.x;
+  if (ti >= n_tiles) return;
+  load(ti, tiles[0]);
+  cp_async_commit();
+  for (int buf = 0;; buf ^= 1) {
+    const uint32_t next = ti + gridDim.x;
+    // the other tile was last read before the barrier ending the previous
+    // iteration
+    if (next < n_tiles) load(next, tiles[buf ^ 1]);
+    cp_async_commit();
+    cp_async_wait<1>();  // this tile's copies have landed
+    __syncthreads();
+    store(ti, tiles[buf]);
+    __syncthreads();
+    if (next >= n_tiles) break;
+    ti = next;
+  }
+  cp_async_wait<0>();
+}
+
+// ---------------------------------------------------------------------------
 // VEC copy: 16-byte (or narrower) vectors along the shared run
 // ---------------------------------------------------------------------------
 
@@ -414,27 +639,6 @@ __global__ void __launch_bounds__(256)
 //                 tiles that are a 2-D transpose.
 // ---------------------------------------------------------------------------
 
-
-__device__ __forceinline__ void cp_async16(uint32_t smem_addr, const void* g,
-                                           int src_bytes) {
-  asm volatile(
-      "cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_addr),
-      "l"(g), "r"(src_bytes)
-      : "memory");
-}
-__device__ __forceinline__ void cp_async16_full(uint32_t smem_addr,
-                                                const void* g) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_addr),
-               "l"(g)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;\n" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
-}
 
 __device__ __forceinline__ uint4 lds128(const unsigned char* p) {
   return *reinterpret_cast<const uint4*>(p);
@@ -1519,6 +1723,57 @@ int launch_staged(const StagedArgs& a, int eb, const char* src, int64_t cap,
   }
 }
 
+template <int EB, bool OUTER_SRC, int NL, typename OFF>
+int launch_gtile_t(const GTileArgs& g, const char* src, char* dst,
+                   cudaStream_t st) {
+  auto kern = lm_gtile_kernel<EB, OUTER_SRC, NL, OFF>;
+  const int smem = 2 * kGtU * (kGtV + 1) * EB;
+  if (!allow_smem(kern, smem)) return LM_E_CUDA;
+  const DeviceInfo di = device_info();
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256,
+                                                    size_t(smem)) !=
+          cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  // about two tiles per block, as for STAGED tiles
+  const uint64_t tiles = uint64_t(g.n_ut) * g.n_vt;
+  const unsigned grid = unsigned(std::max<uint64_t>(
+      1, std::min<uint64_t>((tiles + 1) / 2,
+                            uint64_t(di.sms) * uint64_t(per_sm) * 64)));
+  launch_k(kern, grid, 256, size_t(smem), st, g, src, dst);
+  return check_launch();
+}
+
+// kernels unrolled for 2 leaves per part with 32-bit offsets (the common
+// case), else for 4 leaves with 64-bit offsets
+template <int EB, int NL, typename OFF>
+int launch_gtile_n(const GTileArgs& g, const char* src, char* dst,
+                   cudaStream_t st) {
+  return g.outer_src ? launch_gtile_t<EB, true, NL, OFF>(g, src, dst, st)
+                     : launch_gtile_t<EB, false, NL, OFF>(g, src, dst, st);
+}
+
+template <int EB>
+int launch_gtile_e(const GTileArgs& g, const char* src, char* dst,
+                   cudaStream_t st) {
+  if (g.narrow && g.n_lo <= 2 && g.n_in <= 2)
+    return launch_gtile_n<EB, 2, int32_t>(g, src, dst, st);
+  return launch_gtile_n<EB, kGtLeaves, int64_t>(g, src, dst, st);
+}
+
+int launch_gtile(const GTileArgs& g, int eb, const char* src, char* dst,
+                 cudaStream_t st) {
+  switch (eb) {
+    case 1: return launch_gtile_e<1>(g, src, dst, st);
+    case 2: return launch_gtile_e<2>(g, src, dst, st);
+    case 4: return launch_gtile_e<4>(g, src, dst, st);
+    case 8: return launch_gtile_e<8>(g, src, dst, st);
+    case 16: return launch_gtile_e<16>(g, src, dst, st);
+    default: return LM_E_INVALID;
+  }
+}
+
 int launch_piece(const lm_plan& P, const Piece& pc, const char* src,
                  int64_t src_cap_bytes, char* dst, void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -1536,6 +1791,8 @@ int launch_piece(const lm_plan& P, const Piece& pc, const char* src,
     return launch_staged(pc.st, P.eb, src, src_cap_bytes, dst, st);
   if (pc.path == PATH_ZIP && ((ps | pd) % 16) == 0)
     return launch_zip(pc.vec, P.eb, src, dst, st);
+  if (pc.path == PATH_GTILE && ((ps | pd) % uintptr_t(P.eb)) == 0)
+    return launch_gtile(pc.gt, P.eb, src, dst, st);
   return launch_generic(pc.gen, src, dst, st);
 }
 

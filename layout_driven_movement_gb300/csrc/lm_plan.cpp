@@ -116,6 +116,92 @@ GenericArgs make_generic(const std::vector<Leaf>& sl,
   return g;
 }
 
+int env_int(const char* name, int dflt);
+
+// Tiled form of a copy without a common refinement (GTileArgs), when one
+// side's first leaf has unit stride and at least kGtU coordinates and the
+// other side's unit-stride leaf, of at least kGtU coordinates, sits behind
+// leaves spanning at least kGtU indices.  LM_GTILE=0 keeps one element per
+// thread.
+bool plan_gtile(const std::vector<Leaf>& sl, const std::vector<Leaf>& dl,
+                int64_t n, const Swz& ss, const Swz& ds, int eb,
+                GTileArgs& g) {
+  static const bool on = env_int("LM_GTILE", 1) != 0;
+  if (!on || n < 1 || n >= (int64_t(1) << 32)) return false;
+  auto unit_leaf = [](const std::vector<Leaf>& L) {
+    for (size_t k = 0; k < L.size(); ++k)
+      if (L[k].d == 1) return int(k);
+    return -1;
+  };
+  const int ks = unit_leaf(sl), kd = unit_leaf(dl);
+  bool outer_src;
+  if (kd == 0 && ks > 0)
+    outer_src = true;
+  else if (ks == 0 && kd > 0)
+    outer_src = false;
+  else
+    return false;
+  const std::vector<Leaf>& outer = outer_src ? sl : dl;
+  const std::vector<Leaf>& inner = outer_src ? dl : sl;
+  const int k = outer_src ? ks : kd;
+  int64_t W = 1;
+  for (int j = 0; j < k; ++j) W *= outer[size_t(j)].e;
+  if (W < kGtU || inner[0].e < kGtU || outer[size_t(k)].e < kGtU) return false;
+  if (k > kGtLeaves || int(outer.size()) - k > kGtLeaves ||
+      int(inner.size()) > kGtLeaves)
+    return false;
+  g = GTileArgs{};
+  g.n = uint64_t(n);
+  g.W = uint32_t(W);
+  g.nv = uint32_t(n / W);
+  g.n_ut = uint32_t((W + kGtU - 1) / kGtU);
+  g.n_vt = uint32_t((int64_t(g.nv) + kGtV - 1) / kGtV);
+  g.ut_div = make_fastdiv(g.n_ut);
+  g.outer_src = outer_src ? 1 : 0;
+  for (int j = 0; j < int(outer.size()); ++j) {
+    const Leaf& l = outer[size_t(j)];
+    if (j < k) {
+      g.lo_ext[g.n_lo] = uint32_t(l.e);
+      g.lo_div[g.n_lo] = make_fastdiv(uint32_t(l.e));
+      g.lo_str[g.n_lo++] = mul_chk(l.d, eb);
+    } else {
+      g.hi_ext[g.n_hi] = uint32_t(l.e);
+      g.hi_div[g.n_hi] = make_fastdiv(uint32_t(l.e));
+      g.hi_str[g.n_hi++] = mul_chk(l.d, eb);
+    }
+  }
+  for (const Leaf& l : inner) {
+    g.in_ext[g.n_in] = uint32_t(l.e);
+    g.in_div[g.n_in] = make_fastdiv(uint32_t(l.e));
+    g.in_str[g.n_in++] = mul_chk(l.d, eb);
+  }
+  // the steps as digits (colex)
+  auto digits = [](int64_t x, const uint32_t* ext, int n, uint32_t* out) {
+    for (int j = 0; j < n; ++j) {
+      out[j] = uint32_t(x % ext[j]);
+      x /= ext[j];
+    }
+  };
+  digits(4, g.lo_ext, g.n_lo, g.lo_step);
+  digits(8 * W, g.in_ext, g.n_in, g.in_step);
+  // 32-bit offsets when every offset of both sides, swizzled or not, stays
+  // below 2^31 bytes
+  auto reach = [&](const std::vector<Leaf>& L, const Swz& z) {
+    int64_t r = 0;
+    for (const Leaf& l : L) r = add_chk(r, mul_chk(l.e - 1, l.d));
+    r = mul_chk(add_chk(r, 1), eb);
+    if (z.on()) r = add_chk(r, int64_t(eb) << (z.b + z.m + z.s));
+    return r;
+  };
+  g.narrow = reach(sl, ss) < (int64_t(1) << 31) &&
+                     reach(dl, ds) < (int64_t(1) << 31)
+                 ? 1
+                 : 0;
+  g.s_swz = to_bytes(ss, eb);
+  g.d_swz = to_bytes(ds, eb);
+  return true;
+}
+
 GenericArgs generic_for_modes(const std::vector<JMode>& ms, int64_t s_base,
                               int64_t d_base, const lm_plan& P) {
   std::vector<Leaf> sl, dl;
@@ -1268,6 +1354,7 @@ static std::string describe(const lm_plan& P) {
     const char* path = pc.path == PATH_VEC      ? "VEC"
                        : pc.path == PATH_STAGED ? "STAGED"
                        : pc.path == PATH_ZIP    ? "ZIP"
+                       : pc.path == PATH_GTILE  ? "GTILE"
                                                 : "GENERIC";
     os << "{\"path\":\"" << path << "\",\"modes\":[";
     for (size_t k = 0; k < pc.modes.size(); ++k) {
@@ -1286,6 +1373,11 @@ static std::string describe(const lm_plan& P) {
     if (pc.path == PATH_ZIP)
       os << ",\"vec_bytes\":16,\"rows\":" << pc.vec.zip_rows
          << ",\"n_vec\":" << pc.vec.n_vec;
+    if (pc.path == PATH_GTILE)
+      os << ",\"outer\":\"" << (pc.gt.outer_src ? "src" : "dst")
+         << "\",\"u_extent\":" << pc.gt.W << ",\"v_extent\":" << pc.gt.nv
+         << ",\"tile\":[" << kGtU << ',' << kGtV << "],\"n_tiles\":"
+         << uint64_t(pc.gt.n_ut) * pc.gt.n_vt;
     if (pc.path == PATH_STAGED) {
       const StagedArgs& A = pc.st;
       os << ",\"tile_elems\":" << pc.tile_elems << ",\"n_tiles\":" << A.n_tiles
@@ -1553,6 +1645,9 @@ static int plan_copy_impl(const lm_layout* src, const lm_layout* dst,
                                 elem_bytes);
           pc.gen.i0 = uint64_t(lo);
           if (uint64_t(hi) >= (uint64_t(1) << 31)) pc.gen.wide = 1;
+          if (world == 1 && plan_gtile(sl, dl, P->size, P->s_swz, P->d_swz,
+                                       elem_bytes, pc.gt))
+            pc.path = PATH_GTILE;
           P->pieces.push_back(std::move(pc));
         }
       }

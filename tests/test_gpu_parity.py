@@ -166,6 +166,27 @@ SMALL = [
      ("layout", (700, 600), (1, 700)), 4),
     ("coalesced_refinement_small_u8", ("layout", (6, 5), (5, 1)),
      ("layout", (5, 6), (1, 5)), 1),
+    # no common refinement, tiled through shared memory (GTILE): the source
+    # outer (its unit-stride leaf behind 300 indices), the destination
+    # inner; then the other way round; ragged tiles on both axes
+    ("gtile_outer_src_f32", ("layout", (300, 350), (350, 1)),
+     ("layout", (350, 300), (1, 351)), 4),
+    ("gtile_outer_dst_f16", ("layout", (350, 300), (1, 351)),
+     ("layout", (300, 350), (350, 1)), 2),
+    ("gtile_u8", ("layout", (100, 90), (90, 1)),
+     ("layout", (90, 100), (1, 91)), 1),
+    ("gtile_ragged_f64", ("layout", (1000, 77), (77, 1)),
+     ("layout", (77, 1000), (1, 79)), 8),
+    ("gtile_b128", ("layout", (40, 50), (50, 1)),
+     ("layout", (50, 40), (1, 51)), 16),
+    ("gtile_swizzled_src_f32",
+     ("swizzle", 3, 0, 4, ("layout", (128, 100), (100, 1))),
+     ("layout", (100, 128), (1, 101)), 4),
+    ("gtile_three_leaves_f32", ("layout", (40, 40, 33), (40, 1, 1600)),
+     ("layout", (33, 1600), (1, 35)), 4),
+    # a destination of three leaves: the 4-leaf form with 64-bit offsets
+    ("gtile_wide_leaves_f32", ("layout", (40, 40, 33), (40, 1, 1600)),
+     ("layout", (33, 40, 40), (1, 35, 1401)), 4),
     ("transpose_tall_f32", ("layout", (2048, 96), (1, 2048)),
      ("layout", (2048, 96), (96, 1)), 4),
     ("vec_untiled_prime", ("layout", (8, 2053), (1, 8)),
@@ -187,7 +208,7 @@ def test_small_parity_paths_cover_every_kernel():
         for pc in p.describe()["pieces"]:
             seen.add(pc["path"] if pc["path"] != "STAGED"
                      else "STAGED/" + pc["store"] + str(pc["rows"]))
-    assert {"GENERIC", "VEC", "ZIP", "STAGED/gather0"} <= seen
+    assert {"GENERIC", "GTILE", "VEC", "ZIP", "STAGED/gather0"} <= seen
     assert {"STAGED/transpose2", "STAGED/transpose4",
             "STAGED/transpose8"} <= seen, seen
 
@@ -559,8 +580,8 @@ def test_copy_host_buffers_by_shards_on_streams():
 
 @pytest.mark.parametrize("dst_t,path", [
     # no common refinement: 6000 and 7000 do not nest and the padded
-    # destination does not coalesce (GENERIC)
-    ("(7000,6000):(1,7001)", "GENERIC"),
+    # destination does not coalesce; tiled through shared memory (GTILE)
+    ("(7000,6000):(1,7001)", "GTILE"),
     # the destination is the single run 42000000:1: a transpose (STAGED)
     ("(7000,6000):(1,7000)", "STAGED"),
 ])

@@ -644,7 +644,9 @@ def test_refinement_of_coalesced_sides():
     assert d["joint"] and [p["path"] for p in d["pieces"]] == ["STAGED"]
     assert d["pieces"][0]["modes"] == [[6000, 7000, 1], [7000, 1, 6000]]
     d = lm.Plan(S, lm.Layout.parse("(7000,6000):(1,7001)"), 4).describe()
-    assert not d["joint"] and d["pieces"][0]["path"] == "GENERIC"
+    assert not d["joint"] and d["pieces"][0]["path"] == "GTILE"
+    assert (d["pieces"][0]["outer"], d["pieces"][0]["u_extent"],
+            d["pieces"][0]["v_extent"]) == ("src", 6000, 7000)
     # every accepted joint plan still maps each logical index like the two
     # layouts do (sampled against the oracle)
     rng = np.random.default_rng(77)
@@ -665,3 +667,31 @@ def test_refinement_of_coalesced_sides():
             do += (rem % e) * dt
             rem //= e
         assert (so == OS.at(i)).all() and (do == OD.at(i)).all()
+
+
+def test_gtile_split_is_exact():
+    """The tiled path for pairs without a common refinement reads the outer
+    side as lo(u) + hi(v) with i = u + W*v: for every logical index of a
+    few pairs, that split (its leaves before the unit-stride leaf over u,
+    the rest over v) equals the oracle's offset, and the inner side's first
+    leaf has unit stride."""
+    for s_txt, d_txt, outer in [("(300,350):(350,1)", "(350,300):(1,351)", "src"),
+                                ("(350,300):(1,351)", "(300,350):(350,1)", "dst"),
+                                ("(40,40,33):(40,1,1600)", "(33,1600):(1,35)", "src")]:
+        d = lm.Plan(lm.Layout.parse(s_txt), lm.Layout.parse(d_txt), 4).describe()
+        pc = d["pieces"][0]
+        assert pc["path"] == "GTILE" and pc["outer"] == outer, (s_txt, pc)
+        W = pc["u_extent"]
+        O = lo.parse(s_txt if outer == "src" else d_txt)
+        leaves = lo.flatten(O.shape, O.stride)
+        k = next(j for j, (e, st) in enumerate(leaves) if st == 1)
+        assert int(np.prod([e for e, _ in leaves[:k]])) == W
+        i = np.arange(O.size)
+        u, v = i % W, i // W
+        lo_off = lo.Layout(tuple(e for e, _ in leaves[:k]),
+                           tuple(st for _, st in leaves[:k])).at(u)
+        hi_off = lo.Layout(tuple(e for e, _ in leaves[k:]),
+                           tuple(st for _, st in leaves[k:])).at(v)
+        assert (lo_off + hi_off == O.at(i)).all()
+        I = lo.parse(d_txt if outer == "src" else s_txt)
+        assert lo.flatten(I.shape, I.stride)[0][1] == 1
