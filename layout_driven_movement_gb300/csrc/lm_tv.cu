@@ -295,6 +295,17 @@ cudaError_t allow_tv_smem(const void* k, int dev, int smem) {
   return cudaSuccess;
 }
 
+// Blocks per resident slot (LM_TV_WAVES, default 1: one persistent wave
+// that strides over the tiles).
+int64_t tv_waves() {
+  static const int64_t v = [] {
+    const char* e = std::getenv("LM_TV_WAVES");
+    const long long w = e ? std::atoll(e) : 1;
+    return int64_t(w < 1 ? 1 : w);
+  }();
+  return v;
+}
+
 // One block per resident slot at most, grid-stride over the tiles.
 int launch_mbar(TvMbarKernel k, const lm_tv_args& a, const char* src,
                 char* dst, void* stream, int smem, unsigned int* status) {
@@ -311,7 +322,7 @@ int launch_mbar(TvMbarKernel k, const lm_tv_args& a, const char* src,
                                                     size_t(smem));
   if (e != cudaSuccess) return fail_cuda(e);
   if (per_sm < 1) return LM_E_INVALID;  // the block cannot be resident
-  const int64_t resident = int64_t(sms) * per_sm;
+  const int64_t resident = int64_t(sms) * per_sm * tv_waves();
   const unsigned grid =
       unsigned(a.n_tiles < resident ? a.n_tiles : resident);
   k<<<grid, unsigned(a.block_threads), size_t(smem),
@@ -376,7 +387,7 @@ int launch_tv(const lm_tv_plan& plan, const char* src, char* dst,
                                                     size_t(smem));
   if (e != cudaSuccess) return fail_cuda(e);
   if (per_sm < 1) return LM_E_INVALID;  // the block cannot be resident
-  const int64_t resident = int64_t(sms) * per_sm;
+  const int64_t resident = int64_t(sms) * per_sm * tv_waves();
   const unsigned grid =
       unsigned(a.n_tiles < resident ? a.n_tiles : resident);
   k<<<grid, unsigned(a.block_threads), size_t(smem),

@@ -607,3 +607,78 @@ def test_generic_without_common_refinement_full_size_sampled(dst_t, path):
     want = inp.view(np.int32)[so]
     assert (got.cpu().numpy() == want).all()
     assert (raw[D.cosize * 4:].cpu().numpy() == GUARD_FILL).all()
+
+
+# --------------------------------------------------------------------------
+# randomized: pairs without a common refinement, layout_eval tilings
+# --------------------------------------------------------------------------
+
+def _random_non_refinable(rng):
+    """Matrices (a, b) and (c, d) of equal size whose extents do not nest
+    (a and c do not divide each other), each side row- or column-major,
+    padded so that no side coalesces into one run."""
+    while True:
+        a, c = int(rng.integers(33, 160)), int(rng.integers(33, 160))
+        if a % c and c % a:
+            break
+    n = int(np.lcm(a, c)) * int(rng.integers(1, 3))
+    while n < 2000:
+        n *= 2
+    b, d = n // a, n // c
+
+    def side(r, k):
+        pad = int(rng.integers(1, 4))
+        if rng.integers(2):
+            return ("layout", (r, k), (k + pad, 1))   # rows, padded
+        return ("layout", (r, k), (1, r + pad))       # columns, padded
+
+    src, dst = side(a, b), side(c, d)
+    if rng.integers(4) == 0:
+        src = ("swizzle", 2, 0, 5, src)
+    return src, dst, int(rng.choice([1, 2, 4, 8, 16]))
+
+
+def test_random_non_refinable_pairs():
+    """Random pairs without a common refinement, on whichever path the
+    planner picks (GTILE when a side runs along the logical index, else
+    GENERIC), compared in full with the oracle."""
+    rng = np.random.default_rng(4242)
+    paths = set()
+    for k in range(24):
+        src, dst, eb = _random_non_refinable(rng)
+        S, D = lm.build_layout(src), lm.build_layout(dst)
+        try:
+            plan = lm.Plan(S, D, eb)
+        except lm.LayoutMoveError as e:       # a swizzle that collides
+            assert e.status == -4
+            continue
+        d = plan.describe()
+        assert not d["joint"], (src, dst)
+        paths.update(p["path"] for p in d["pieces"])
+        run_case(src, dst, eb, seed=300 + k)
+    assert "GTILE" in paths
+
+
+def test_random_layout_eval_tables():
+    """Random layouts of 2-4 leaves (some swizzled) into int32 and int64
+    tables, whichever kernel the shape gets (tiled or per element),
+    compared in full with the oracle."""
+    rng = np.random.default_rng(515)
+    for k in range(16):
+        nl = int(rng.integers(2, 5))
+        ext = [int(v) for v in rng.integers(2, 40, nl)]
+        perm = rng.permutation(nl)
+        stride, span = [0] * nl, 1
+        for j in perm:
+            stride[j] = span
+            span *= ext[j] + int(rng.integers(0, 3))
+        spec = ("layout", tuple(ext), tuple(stride))
+        if rng.integers(3) == 0:
+            spec = ("swizzle", 2, 1, 6, spec)
+        L, O = lm.build_layout(spec), lo.build(spec)
+        dt = torch.int32 if k % 2 else torch.int64
+        table = torch.full((O.size + 5,), -3, dtype=dt, device="cuda")
+        lm.layout_eval_device(L, table)
+        got = table.cpu().numpy()
+        assert (got[:O.size] == lo.image(O)).all(), spec
+        assert (got[O.size:] == -3).all()
