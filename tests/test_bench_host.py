@@ -52,13 +52,13 @@ def test_oracle_windows_threads_copy_the_same_bytes():
     outs = []
     for threads in (1, 4):
         bufs = {}
-        for name in ("C1", "C5b"):
+        for name in ("C5b",):
             w = WORKLOADS[name]
             from oracle import layout_oracle as lo
             S, D = lo.build(w.src), lo.build(w.dst)
             bufs[name] = (seeded_bytes(w.values, w.dtype, lo.cosize(S), w.seed),
                           np.zeros(lo.cosize(D) * w.elem_bytes, np.uint8))
-        ow = bench.OracleWindows(("C1", "C5b"), bufs)
+        ow = bench.OracleWindows(("C5b",), bufs)
         ow.run(2.0 ** -4, shift=3, threads=threads)
         outs.append({k: v[1].copy() for k, v in bufs.items()})
     for name in outs[0]:
