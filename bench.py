@@ -671,7 +671,7 @@ def measure_exchange(suite, args, torch, peak, world=4) -> dict:
     box = sizes[0]["send"][0] * eb
     one_copy = all(d["one_copy_per_side"] for d in dsc)
 
-    def one():
+    def one(exchange=True):
         for p, x in enumerate(xs):
             o, n = dsc[p]["src_origin"] * eb, dsc[p]["src_local"] * eb
             lm.exchange_pack_all(x, buf_in[o:o + n],
@@ -679,42 +679,53 @@ def measure_exchange(suite, args, torch, peak, world=4) -> dict:
         for q, x in enumerate(xs):
             o, n = dsc[q]["dst_origin"] * eb, dsc[q]["dst_local"] * eb
             r = recv[q * world * box:(q + 1) * world * box]
-            for p in range(world):      # the exchange, as device copies
-                r[p * box:(p + 1) * box].copy_(
-                    send[soff[p][q]:soff[p][q] + box])
+            if exchange:
+                for p in range(world):      # the exchange, as device copies
+                    r[p * box:(p + 1) * box].copy_(
+                        send[soff[p][q]:soff[p][q] + box])
             lm.exchange_unpack_all(x, r, buf_out[o:o + n])
 
-    for _ in range(3):
-        one()
-    torch.cuda.synchronize()
-    # small launches per pass: replay them as one CUDA graph so the
-    # host's launch rate does not set the time
-    run, how = one, "eager launches"
-    try:
-        side = torch.cuda.Stream()
-        side.wait_stream(torch.cuda.current_stream())
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=side):
-            one()
+    def timed_pass(fn):
+        """ms per pass of fn, replayed as one CUDA graph (the small
+        launches of a pass would otherwise be timed at the host's launch
+        rate)."""
+        for _ in range(3):
+            fn()
         torch.cuda.synchronize()
-        run, how = graph.replay, "one CUDA graph per pass"
-    except Exception as exc:  # capture unsupported: time eager launches
-        how = f"eager launches (graph capture failed: {type(exc).__name__})"
+        run, how = fn, "eager launches"
+        try:
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=side):
+                fn()
+            torch.cuda.synchronize()
+            run, how = graph.replay, "one CUDA graph per pass"
+        except Exception as exc:  # capture unsupported: time eager launches
+            how = f"eager launches (graph capture failed: {type(exc).__name__})"
+            torch.cuda.synchronize()
+        passes = min(args.steps, 200)
+        for _ in range(3):
+            run()
+        e0, e1 = (torch.cuda.Event(enable_timing=True),
+                  torch.cuda.Event(enable_timing=True))
         torch.cuda.synchronize()
-    passes = min(args.steps, 200)
-    for _ in range(3):
-        run()
-    e0, e1 = (torch.cuda.Event(enable_timing=True),
-              torch.cuda.Event(enable_timing=True))
-    torch.cuda.synchronize()
-    e0.record()
-    for _ in range(passes):
-        run()
-    e1.record()
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / passes
+        e0.record()
+        for _ in range(passes):
+            run()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / passes, how
+
+    ms, how = timed_pass(one)
+    # the library's part alone: every rank's pack and unpack
+    ms_lib, _ = timed_pass(lambda: one(exchange=False))
+    if lm.device_status() != 0:
+        raise RuntimeError("a copy kernel gave up a bounded wait "
+                           "(LM_E_TIMEOUT): the exchange run is invalid")
     # pack, stand-in exchange and unpack each read and write every element
     gbs = 3 * 2 * total / (ms * 1e-3) / 1e9
+    gbs_lib = 2 * 2 * total / (ms_lib * 1e-3) / 1e9
     return {"workload": f"4096x4096 fp32 transpose, rows sharded over {world} "
                         "ranks on both sides, all ranks' packs and unpacks on "
                         "this GPU; the all-to-all stands in as device copies "
@@ -722,7 +733,10 @@ def measure_exchange(suite, args, torch, peak, world=4) -> dict:
             "layout_copies_per_pass": 2 * world, "one_copy_per_side": one_copy,
             "launch": how,
             "us_per_pass": round(ms * 1e3, 2), "gbs": round(gbs, 1),
-            "frac_of_peak": round(gbs / peak, 4)}
+            "frac_of_peak": round(gbs / peak, 4),
+            "pack_unpack_us_per_pass": round(ms_lib * 1e3, 2),
+            "pack_unpack_gbs": round(gbs_lib, 1),
+            "pack_unpack_frac_of_peak": round(gbs_lib / peak, 4)}
 
 
 # --------------------------------------------------------------------------
