@@ -866,17 +866,27 @@ def pinned_near_gpu(topo: dict, local: int, items) -> tuple[list, str]:
             how = []
             node = topo["gpu_numa_node"]
             if node >= 0:
+                # placement is best effort: a refused binding is noted and
+                # the buffers are allocated all the same
                 want = set(_cpulist(topo["gpu_node_cpus"]))
                 cpus = want & set(os.sched_getaffinity(0))
-                if cpus:
-                    os.sched_setaffinity(0, cpus)
-                    how.append(f"allocated by a thread bound to CPUs "
-                               f"{_ranges(cpus)} of node {node}")
-                else:
-                    how.append(f"no CPU of node {node} in this process's "
-                               "affinity")
-                if _set_mempolicy(node):
-                    how.append(f"pages preferred on node {node}")
+                try:
+                    if cpus:
+                        os.sched_setaffinity(0, cpus)
+                        how.append(f"allocated by a thread bound to CPUs "
+                                   f"{_ranges(cpus)} of node {node}")
+                    else:
+                        how.append(f"no CPU of node {node} in this "
+                                   "process's affinity")
+                except OSError as exc:
+                    how.append(f"CPU binding refused ({exc.strerror})")
+                try:
+                    if _set_mempolicy(node):
+                        how.append(f"pages preferred on node {node}")
+                    else:
+                        how.append("memory policy not set")
+                except OSError:
+                    how.append("memory policy not set")
             else:
                 how.append("GPU NUMA node unknown: default placement")
             torch.cuda.set_device(local)

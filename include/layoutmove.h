@@ -382,8 +382,10 @@ int lm_layout_copy_host(const lm_plan* plan, const void* src_host,
  * after src_capacity_elems * elem_bytes; a copy whose two parts do not fit
  * is refused with LM_E_CAPACITY before anything is enqueued.  The first
  * call on a device, with that device current, looks up the area's device
- * address (cudaGetSymbolAddress); make that first call before any stream
- * capture.  Every call on a device shares the one area, which keeps the
+ * address (cudaGetSymbolAddress) and keeps it for later calls on that
+ * device; make that first call before any stream capture.  The address
+ * belongs to the device's context: after cudaDeviceReset this process must
+ * not call the function again.  Every call on a device shares the one area, which keeps the
  * last call's bytes: calls whose work overlaps on the GPU (other streams,
  * other host threads) race and must be ordered by the caller.  No part of
  * the area needs to start cleared: every destination byte that comes back
