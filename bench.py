@@ -581,7 +581,9 @@ def measure_d2d(suite, torch) -> float:
 
 def measure_tv(suite, args, torch, peak) -> dict:
     """Time lm_tv_copy on the suite's full-size buffers (TV_CONFIGS), the
-    copies of one pass back to back with events around each."""
+    copies of one pass back to back with events around each (each then
+    also writes back its predecessor's dirty lines), and each alone after a
+    read flush of L2 (`isolated_us`)."""
     lm = suite.lm
     items = {it["name"]: it for it in suite.items}
     runs = []
@@ -613,11 +615,19 @@ def measure_tv(suite, args, torch, peak) -> dict:
             lm.tv_copy(plan, it["src"], it["dst"])
             ev[r][k][1].record()
     torch.cuda.synchronize()
+    # each copy alone as well: L2 flushed by a read before each of 20 runs
+    flush = torch.ones(512 << 20, dtype=torch.uint8,
+                       device=suite.items[0]["src"].device)
+    iso = {key: _timed(torch, lambda it=it, plan=plan:
+                       lm.tv_copy(plan, it["src"], it["dst"]), flush=flush)
+           for key, it, plan in runs}
+    del flush
     out = {}
     for k, (key, it, plan) in enumerate(runs):
         ms = statistics.median(ev[r][k][0].elapsed_time(ev[r][k][1])
                                for r in range(passes))
         gbs = it["bytes"] / (ms * 1e-3) / 1e9
+        igbs = it["bytes"] / (iso[key] * 1e-3) / 1e9
         d = plan.describe()
         out[key] = {
             "smem": TV_CONFIGS[key][0], "thr_load": d["load"]["thr"],
@@ -628,7 +638,9 @@ def measure_tv(suite, args, torch, peak) -> dict:
                 [d["load"]["smem_wavefronts"], d["load"]["smem_wavefronts_ideal"]],
                 [d["store"]["smem_wavefronts"], d["store"]["smem_wavefronts_ideal"]]],
             "median_us": round(ms * 1e3, 2), "gbs": round(gbs, 1),
-            "frac_of_peak": round(gbs / peak, 4)}
+            "frac_of_peak": round(gbs / peak, 4),
+            "isolated_us": round(iso[key] * 1e3, 2),
+            "isolated_frac_of_peak": round(igbs / peak, 4)}
     return out
 
 
