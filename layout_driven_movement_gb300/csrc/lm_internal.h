@@ -284,7 +284,7 @@ struct StagedArgs {
 // i = u + W*v (u < W) the outer side's offset is lo(u) + hi(v) -- its
 // leaves before that leaf over u, the rest over v -- and contiguous along
 // v, while the inner side's offset (its full decomposition of i) is
-// contiguous along u.  Tiles of kGtU x kGtV (u, v) are staged through
+// contiguous along u.  Tiles of tile_u (32 or 64) x kGtV (u, v) are staged through
 // shared memory: read along the source's contiguous direction, written
 // along the destination's.  32-bit logical indices.
 constexpr int kGtU = 32, kGtV = 64;
@@ -293,6 +293,7 @@ struct GTileArgs {
   uint64_t n = 0;
   uint32_t W = 1;                       // u extent
   uint32_t nv = 0;                      // v extent, n / W
+  uint32_t tile_u = 32;                 // tile extent along u (32 | 64)
   uint32_t n_ut = 0, n_vt = 0;          // tiles along u and v
   FastDiv ut_div;                       // division by n_ut
   int32_t outer_src = 1;                // 1: the source is the outer side

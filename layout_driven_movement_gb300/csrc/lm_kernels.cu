@@ -366,24 +366,25 @@ __device__ __forceinline__ void elem_to_shared(void* s, const char* g) {
 // OUTER_SRC: the source is the outer side -- it is read along v (lanes
 // over v, its offset lo(u) + hi(v)) and the destination, the inner side,
 // written along u (lanes over u, its offset from the full index).  The
-// other way round otherwise.  Two shared tiles of kGtU x (kGtV + 1)
+// other way round otherwise.  Two shared tiles of TU x (kGtV + 1)
 // elements (the pad keeps the lanes that walk along u in distinct banks):
 // a block's next tile loads (cp.async) while it stores the current one.
-template <int EB, bool OUTER_SRC, int NL, typename OFF>
+template <int EB, bool OUTER_SRC, int NL, typename OFF, int TU>
 __global__ void __launch_bounds__(256)
     lm_gtile_kernel(const __grid_constant__ GTileArgs a,
                     const char* __restrict__ src, char* __restrict__ dst) {
   using T = typename VecT<EB>::T;
+  constexpr int RU = 256 / kGtV;  // rows of u per pass, lanes over v
+  constexpr int CV = 256 / TU;    // columns of v per pass, lanes over u
   extern __shared__ __align__(16) unsigned char gt_smem[];
-  typedef T Tile[kGtU][kGtV + 1];
+  typedef T Tile[TU][kGtV + 1];
   Tile* tiles = reinterpret_cast<Tile*>(gt_smem);
   pdl_trigger();
   pdl_wait();
   const uint32_t t = threadIdx.x;
   const uint32_t n_tiles = a.n_ut * a.n_vt;
-  // lanes over v: 4 rows of u per pass; lanes over u: 8 columns of v
   const uint32_t vl_v = t % kGtV, ul_v = t / kGtV;
-  const uint32_t ul_u = t % kGtU, vl_u = t / kGtU;
+  const uint32_t ul_u = t % TU, vl_u = t / TU;
   // swizzles only where a side has one (a uniform test, not per element)
   const bool sswz = a.s_swz.b > 0, dswz = a.d_swz.b > 0;
   auto sw_s = [&](OFF o) {
@@ -394,7 +395,7 @@ __global__ void __launch_bounds__(256)
   };
   auto origin = [&](uint32_t ti, uint32_t* u0, uint32_t* v0) {
     const uint32_t vt = fdiv(ti, a.ut_div);
-    *u0 = (ti - vt * a.n_ut) * kGtU;
+    *u0 = (ti - vt * a.n_ut) * TU;
     *v0 = vt * kGtV;
   };
   auto load = [&](uint32_t ti, Tile& tl) {
@@ -408,8 +409,8 @@ __global__ void __launch_bounds__(256)
       Digits<NL, OFF> lo;
       lo.set(u0 + ul_v, a.n_lo, a.lo_ext, a.lo_div, a.lo_str);
 #pragma unroll
-      for (int p = 0; p < kGtU / 4; ++p) {
-        const uint32_t ul = ul_v + 4u * uint32_t(p);
+      for (int p = 0; p < TU / RU; ++p) {
+        const uint32_t ul = ul_v + uint32_t(RU * p);
         if (u0 + ul >= a.W) break;
         if (p) lo.step(a.n_lo, a.lo_ext, a.lo_step, a.lo_str);
         elem_to_shared<EB>(&tl[ul][vl_v],
@@ -421,8 +422,8 @@ __global__ void __launch_bounds__(256)
       Digits<NL, OFF> in;
       in.set(u + a.W * (v0 + vl_u), a.n_in, a.in_ext, a.in_div, a.in_str);
 #pragma unroll
-      for (int p = 0; p < kGtV / 8; ++p) {
-        const uint32_t vl = vl_u + 8u * uint32_t(p);
+      for (int p = 0; p < kGtV / CV; ++p) {
+        const uint32_t vl = vl_u + uint32_t(CV * p);
         if (v0 + vl >= a.nv) break;
         if (p) in.step(a.n_in, a.in_ext, a.in_step, a.in_str);
         elem_to_shared<EB>(&tl[ul_u][vl],
@@ -439,8 +440,8 @@ __global__ void __launch_bounds__(256)
       Digits<NL, OFF> in;
       in.set(u + a.W * (v0 + vl_u), a.n_in, a.in_ext, a.in_div, a.in_str);
 #pragma unroll
-      for (int p = 0; p < kGtV / 8; ++p) {
-        const uint32_t vl = vl_u + 8u * uint32_t(p);
+      for (int p = 0; p < kGtV / CV; ++p) {
+        const uint32_t vl = vl_u + uint32_t(CV * p);
         if (v0 + vl >= a.nv) break;
         if (p) in.step(a.n_in, a.in_ext, a.in_step, a.in_str);
         *reinterpret_cast<T*>(dst + sw_d(OFF(a.d_base) + in.off)) =
@@ -454,8 +455,8 @@ __global__ void __launch_bounds__(256)
       Digits<NL, OFF> lo;
       lo.set(u0 + ul_v, a.n_lo, a.lo_ext, a.lo_div, a.lo_str);
 #pragma unroll
-      for (int p = 0; p < kGtU / 4; ++p) {
-        const uint32_t ul = ul_v + 4u * uint32_t(p);
+      for (int p = 0; p < TU / RU; ++p) {
+        const uint32_t ul = ul_v + uint32_t(RU * p);
         if (u0 + ul >= a.W) break;
         if (p) lo.step(a.n_lo, a.lo_ext, a.lo_step, a.lo_str);
         *reinterpret_cast<T*>(dst + sw_d(base + lo.off)) =
@@ -1723,11 +1724,11 @@ int launch_staged(const StagedArgs& a, int eb, const char* src, int64_t cap,
   }
 }
 
-template <int EB, bool OUTER_SRC, int NL, typename OFF>
+template <int EB, bool OUTER_SRC, int NL, typename OFF, int TU>
 int launch_gtile_t(const GTileArgs& g, const char* src, char* dst,
                    cudaStream_t st) {
-  auto kern = lm_gtile_kernel<EB, OUTER_SRC, NL, OFF>;
-  const int smem = 2 * kGtU * (kGtV + 1) * EB;
+  auto kern = lm_gtile_kernel<EB, OUTER_SRC, NL, OFF, TU>;
+  const int smem = 2 * TU * (kGtV + 1) * EB;
   if (!allow_smem(kern, smem)) return LM_E_CUDA;
   const DeviceInfo di = device_info();
   int per_sm = 0;
@@ -1747,11 +1748,18 @@ int launch_gtile_t(const GTileArgs& g, const char* src, char* dst,
 
 // kernels unrolled for 2 leaves per part with 32-bit offsets (the common
 // case), else for 4 leaves with 64-bit offsets
+template <int EB, int NL, typename OFF, int TU>
+int launch_gtile_u(const GTileArgs& g, const char* src, char* dst,
+                   cudaStream_t st) {
+  return g.outer_src ? launch_gtile_t<EB, true, NL, OFF, TU>(g, src, dst, st)
+                     : launch_gtile_t<EB, false, NL, OFF, TU>(g, src, dst, st);
+}
+
 template <int EB, int NL, typename OFF>
 int launch_gtile_n(const GTileArgs& g, const char* src, char* dst,
                    cudaStream_t st) {
-  return g.outer_src ? launch_gtile_t<EB, true, NL, OFF>(g, src, dst, st)
-                     : launch_gtile_t<EB, false, NL, OFF>(g, src, dst, st);
+  return g.tile_u == 64 ? launch_gtile_u<EB, NL, OFF, 64>(g, src, dst, st)
+                        : launch_gtile_u<EB, NL, OFF, 32>(g, src, dst, st);
 }
 
 template <int EB>

@@ -154,7 +154,10 @@ bool plan_gtile(const std::vector<Leaf>& sl, const std::vector<Leaf>& dl,
   g.n = uint64_t(n);
   g.W = uint32_t(W);
   g.nv = uint32_t(n / W);
-  g.n_ut = uint32_t((W + kGtU - 1) / kGtU);
+  // tiles of 64 along u when u runs that far (LM_GTILE_U=32 keeps 32)
+  static const int tu_env = env_int("LM_GTILE_U", 64);
+  g.tile_u = tu_env == 32 || W < 64 ? 32u : 64u;
+  g.n_ut = uint32_t((W + g.tile_u - 1) / g.tile_u);
   g.n_vt = uint32_t((int64_t(g.nv) + kGtV - 1) / kGtV);
   g.ut_div = make_fastdiv(g.n_ut);
   g.outer_src = outer_src ? 1 : 0;
@@ -182,8 +185,10 @@ bool plan_gtile(const std::vector<Leaf>& sl, const std::vector<Leaf>& dl,
       x /= ext[j];
     }
   };
-  digits(4, g.lo_ext, g.n_lo, g.lo_step);
-  digits(8 * W, g.in_ext, g.n_in, g.in_step);
+  // lanes over v: 256 / kGtV rows of u per pass; lanes over u:
+  // 256 / tile_u columns of v per pass
+  digits(256 / kGtV, g.lo_ext, g.n_lo, g.lo_step);
+  digits(int64_t(256 / g.tile_u) * W, g.in_ext, g.n_in, g.in_step);
   // 32-bit offsets when every offset of both sides, swizzled or not, stays
   // below 2^31 bytes
   auto reach = [&](const std::vector<Leaf>& L, const Swz& z) {
@@ -1376,7 +1381,7 @@ static std::string describe(const lm_plan& P) {
     if (pc.path == PATH_GTILE)
       os << ",\"outer\":\"" << (pc.gt.outer_src ? "src" : "dst")
          << "\",\"u_extent\":" << pc.gt.W << ",\"v_extent\":" << pc.gt.nv
-         << ",\"tile\":[" << kGtU << ',' << kGtV << "],\"n_tiles\":"
+         << ",\"tile\":[" << pc.gt.tile_u << ',' << kGtV << "],\"n_tiles\":"
          << uint64_t(pc.gt.n_ut) * pc.gt.n_vt;
     if (pc.path == PATH_STAGED) {
       const StagedArgs& A = pc.st;
