@@ -286,11 +286,16 @@ void lm_layout_destroy(lm_layout* layout);
  * coalesces and reorders them, checks that dst is injective, finds the
  * common contiguous run (the common vector of "CUTE布局代数" §2.3) and
  * chooses per piece of the domain a kernel: VEC (16-byte vectors along a run
- * both sides share), STAGED (tiles staged through swizzled shared memory,
- * loads contiguous along src, stores contiguous along dst) or GENERIC (one
- * element per thread).  Pairs without a common refinement of their leaves
- * are planned GENERIC over each side's own leaves.  The plan is host data
- * only; it holds no device memory and may be used on any device and stream.
+ * both sides share), ZIP (a short interleave in registers), STAGED (tiles
+ * staged through swizzled shared memory, loads contiguous along src, stores
+ * contiguous along dst) or GENERIC (one element per thread).  The common
+ * refinement is tried on each side's leaves as given and coalesced.  Pairs
+ * without one are planned over each side's own leaves: GTILE (tiles through
+ * shared memory, read along the source's unit-stride direction and written
+ * along the destination's) when one side has unit stride along the logical
+ * index and the other a unit-stride leaf behind at least 32 indices, else
+ * GENERIC.  The plan is host data only; it holds no device memory and may
+ * be used on any device and stream.
  * Errors: LM_E_INVALID, LM_E_INCOMPATIBLE (sizes differ),
  * LM_E_NOT_INJECTIVE (dst offsets could collide; proven exactly for every
  * layout up to 2^28 elements, otherwise by a sufficient test),
