@@ -315,6 +315,17 @@ struct GTileArgs {
   int64_t s_base = 0, d_base = 0;       // bytes
   Swz s_swz, d_swz;                     // bytes
   int32_t narrow = 0;                   // every byte offset below 2^31
+  // tensor-map form (tma == 1): an outer source that is a plain matrix --
+  // v its unit-stride leaf (nv coordinates), u one leaf of t_ustride bytes
+  // -- loaded one 128-byte-swizzled box of t_vpr v by tile_u u per 128-byte
+  // column region (t_regions per tile); the store phase reads 16-byte
+  // chunks and steps the inner digits by in_step1 (the next v) or in_jump
+  // (the first v of the thread's next chunk)
+  int32_t tma = 0;
+  uint32_t t_regions = 0, t_vpr = 0;
+  int64_t t_ustride = 0;
+  uint32_t in_step1[kMaxLeaves];
+  uint32_t in_jump[kMaxLeaves];
 };
 
 struct EvalArgs {

@@ -1297,6 +1297,119 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// ---------------------------------------------------------------------------
+// GTILE with tensor-map loads (GTileArgs::tma): the outer source is a plain
+// matrix, each 64 x 64 (u, v) tile arrives as 128-byte-swizzled boxes (one
+// per 128-byte column region: element chunk c of row u at chunk c ^ (u % 8))
+// issued by one thread, two tiles in flight on mbarriers.  Each thread then
+// reads 16-byte chunks of one row u -- 8 consecutive rows, one chunk
+// column, hit 8 distinct bank groups -- and writes their elements along u
+// into the inner destination, stepping its digits.  Every wait is bounded;
+// the block votes on the outcome, so it leaves together, and a timeout
+// drains the copies in flight as the bulk kernels do.
+// ---------------------------------------------------------------------------
+
+template <int EB, typename OFF>
+__global__ void __launch_bounds__(256)
+    lm_gtma_kernel(const __grid_constant__ GTileArgs a,
+                   const __grid_constant__ CUtensorMap tmap,
+                   char* __restrict__ dst) {
+  using T = typename VecT<EB>::T;
+  constexpr int TU = 64;
+  constexpr int VPC = 16 / EB;             // v per 16-byte chunk
+  constexpr int CP = 256 / TU;             // chunk columns a pass spans
+  constexpr int PER = kGtV / VPC / CP;     // chunks per thread per tile
+  constexpr uint32_t REGION = TU * 128;    // bytes of one column region
+  constexpr uint32_t STAGE = uint32_t(kGtV) * EB * TU;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const uint32_t base = uint32_t(__cvta_generic_to_shared(smem));
+  const uint32_t bar = (base + 127u) & ~127u;  // two mbarriers
+  const uint32_t st0 = (bar + 128u + 1023u) & ~1023u;
+  const unsigned char* stages = smem + (st0 - base);
+  const uint32_t t = threadIdx.x;
+  if (t == 0) {
+    mbar_init(bar, 1);
+    mbar_init(bar + 8, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  __syncthreads();
+  pdl_trigger();
+  pdl_wait();
+  const uint32_t n_tiles = a.n_ut * a.n_vt;
+  uint32_t ti = blockIdx.x;
+  if (ti >= n_tiles) return;
+  const uint32_t G = gridDim.x;
+  const uint32_t ul = t % TU, cl = t / TU;
+  const bool dswz = a.d_swz.b > 0;
+  auto origin = [&](uint32_t tile, uint32_t* u0, uint32_t* v0) {
+    const uint32_t vt = fdiv(tile, a.ut_div);
+    *u0 = (tile - vt * a.n_ut) * TU;
+    *v0 = vt * kGtV;
+  };
+  auto issue = [&](uint32_t tile, uint32_t s) {  // thread 0
+    uint32_t u0, v0;
+    origin(tile, &u0, &v0);
+    mbar_arrive_expect_tx(bar + 8u * s, STAGE);
+    for (uint32_t r = 0; r < a.t_regions; ++r)
+      tma_g2s(st0 + s * STAGE + r * REGION, &tmap, 2,
+              int32_t(v0 + r * a.t_vpr), int32_t(u0), 0, 0, 0, bar + 8u * s);
+  };
+  if (t == 0) issue(ti, 0);
+  bool ok = true;
+  uint32_t i = 0, next = 0;
+  for (;; ++i) {
+    const uint32_t s = i & 1u;
+    next = ti + G;
+    // stage s ^ 1 held the tile before, released by the last vote
+    if (t == 0 && next < n_tiles) issue(next, s ^ 1u);
+    ok = mbar_wait(bar + 8u * s, (i >> 1) & 1u);
+    if (ok) {
+      uint32_t u0, v0;
+      origin(ti, &u0, &v0);
+      const uint32_t u = u0 + ul;
+      if (u < a.W) {
+        const unsigned char* row = stages + s * STAGE + ul * 128u;
+        Digits<2, OFF> in;
+        in.set(u + a.W * (v0 + cl * VPC), a.n_in, a.in_ext, a.in_div,
+               a.in_str);
+#pragma unroll
+        for (int k = 0; k < PER; ++k) {
+          const uint32_t ch = cl + uint32_t(CP * k);
+          const uint32_t vf = v0 + ch * VPC;
+          if (vf >= a.nv) break;
+          if (k) in.step(a.n_in, a.in_ext, a.in_jump, a.in_str);
+          const uint4 w = *reinterpret_cast<const uint4*>(
+              row + (ch >> 3) * REGION + (((ch & 7u) ^ (ul & 7u)) << 4));
+          T vals[VPC];
+          memcpy(vals, &w, 16);
+#pragma unroll
+          for (int e = 0; e < VPC; ++e) {
+            if (vf + uint32_t(e) >= a.nv) break;
+            if (e) in.step(a.n_in, a.in_ext, a.in_step1, a.in_str);
+            const OFF o = OFF(a.d_base) + in.off;
+            *reinterpret_cast<T*>(
+                dst + (dswz ? OFF(swz_apply(a.d_swz, int64_t(o))) : o)) =
+                vals[e];
+          }
+        }
+      }
+    }
+    ok = __syncthreads_and(ok);
+    if (!ok || next >= n_tiles) break;
+    ti = next;
+  }
+  if (!ok && t == 0) {
+    atomicOr(&g_lm_device_status, 1u);
+    // drain this block's boxes still in flight: tile i's, and the next
+    // one's if it was issued
+    bool drained = mbar_wait(bar + 8u * (i & 1u), (i >> 1) & 1u, kDrainCycles);
+    if (drained && next < n_tiles)
+      drained = mbar_wait(bar + 8u * ((i + 1) & 1u), ((i + 1) >> 1) & 1u,
+                          kDrainCycles);
+    if (!drained) atomicOr(&g_lm_device_status, 2u);
+  }
+}
+
 // Self-test of the bounded wait: one warp waits on an mbarrier that, with
 // arrive == 0, nothing ever arrives at.  The wait gives up after kWaitCycles
 // and records the timeout exactly as the copy kernels do.
@@ -1762,9 +1875,61 @@ int launch_gtile_n(const GTileArgs& g, const char* src, char* dst,
                         : launch_gtile_u<EB, NL, OFF, 32>(g, src, dst, st);
 }
 
+// The tensor map of a GTILE outer source: dims (v, u), 128-byte swizzled
+// boxes of t_vpr x 64.
+bool encode_gtile_map(const GTileArgs& g, int eb, const char* src,
+                      CUtensorMap* m) {
+  const EncodeTiledFn fn = encode_tiled();
+  if (!fn) return false;
+  const CUtensorMapDataType dt = eb == 2   ? CU_TENSOR_MAP_DATA_TYPE_UINT16
+                                 : eb == 4 ? CU_TENSOR_MAP_DATA_TYPE_UINT32
+                                           : CU_TENSOR_MAP_DATA_TYPE_UINT64;
+  const cuuint64_t dims[2] = {g.nv, g.W};
+  const cuuint64_t strides[1] = {cuuint64_t(g.t_ustride)};
+  const cuuint32_t box[2] = {g.t_vpr, 64};
+  const cuuint32_t es[2] = {1, 1};
+  return fn(m, dt, 2, const_cast<char*>(src) + g.s_base, dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int EB, typename OFF>
+int launch_gtma_t(const GTileArgs& g, const char* src, char* dst,
+                  cudaStream_t st) {
+  auto kern = lm_gtma_kernel<EB, OFF>;
+  const int smem = 128 + 1024 + 2 * kGtV * EB * 64;
+  if (!allow_smem(kern, smem)) return LM_E_CUDA;
+  CUtensorMap m;
+  if (!encode_gtile_map(g, EB, src, &m)) {
+    set_cuda_error(0);
+    return LM_E_CUDA;
+  }
+  const DeviceInfo di = device_info();
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256,
+                                                    size_t(smem)) !=
+          cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  const uint64_t tiles = uint64_t(g.n_ut) * g.n_vt;
+  const unsigned grid = unsigned(std::max<uint64_t>(
+      1, std::min<uint64_t>((tiles + 1) / 2,
+                            uint64_t(di.sms) * uint64_t(per_sm) * 64)));
+  launch_k(kern, grid, 256, size_t(smem), st, g, m, dst);
+  return check_launch();
+}
+
 template <int EB>
 int launch_gtile_e(const GTileArgs& g, const char* src, char* dst,
                    cudaStream_t st) {
+  if constexpr (EB == 2 || EB == 4 || EB == 8) {
+    // tensor-map loads need a 16-byte aligned source
+    if (g.tma && reinterpret_cast<uintptr_t>(src + g.s_base) % 16 == 0 &&
+        encode_tiled())
+      return g.narrow ? launch_gtma_t<EB, int32_t>(g, src, dst, st)
+                      : launch_gtma_t<EB, int64_t>(g, src, dst, st);
+  }
   if (g.narrow && g.n_lo <= 2 && g.n_in <= 2)
     return launch_gtile_n<EB, 2, int32_t>(g, src, dst, st);
   return launch_gtile_n<EB, kGtLeaves, int64_t>(g, src, dst, st);

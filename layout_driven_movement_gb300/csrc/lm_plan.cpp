@@ -189,6 +189,24 @@ bool plan_gtile(const std::vector<Leaf>& sl, const std::vector<Leaf>& dl,
   // 256 / tile_u columns of v per pass
   digits(256 / kGtV, g.lo_ext, g.n_lo, g.lo_step);
   digits(int64_t(256 / g.tile_u) * W, g.in_ext, g.n_in, g.in_step);
+  // tensor-map loads (LM_GTILE_TMA=0 keeps cp.async): the source outer, a
+  // plain matrix (one leaf on each side of its unit-stride leaf), rows
+  // 16-byte aligned, 2- to 8-byte elements, no source swizzle, 64-row tiles
+  static const bool tma_on = env_int("LM_GTILE_TMA", 1) != 0;
+  if (tma_on && outer_src && !ss.on() && g.n_lo == 1 && g.n_hi == 1 &&
+      g.tile_u == 64 && (eb == 2 || eb == 4 || eb == 8) &&
+      g.lo_str[0] % 16 == 0 && g.lo_str[0] > 0 &&
+      g.lo_str[0] < (int64_t(1) << 40) && g.n_in <= 2 && g.nv >= 64 &&
+      W >= 64) {
+    const uint32_t vpc = uint32_t(16 / eb);       // v per 16-byte chunk
+    const uint32_t cp = 256u / g.tile_u;          // chunks a pass spans
+    g.tma = 1;
+    g.t_vpr = uint32_t(128 / eb);
+    g.t_regions = uint32_t(kGtV) / g.t_vpr;
+    g.t_ustride = g.lo_str[0];
+    digits(W, g.in_ext, g.n_in, g.in_step1);
+    digits(int64_t(cp * vpc - vpc + 1) * W, g.in_ext, g.n_in, g.in_jump);
+  }
   // 32-bit offsets when every offset of both sides, swizzled or not, stays
   // below 2^31 bytes
   auto reach = [&](const std::vector<Leaf>& L, const Swz& z) {
@@ -1381,6 +1399,7 @@ static std::string describe(const lm_plan& P) {
     if (pc.path == PATH_GTILE)
       os << ",\"outer\":\"" << (pc.gt.outer_src ? "src" : "dst")
          << "\",\"u_extent\":" << pc.gt.W << ",\"v_extent\":" << pc.gt.nv
+         << ",\"tma\":" << (pc.gt.tma ? "true" : "false")
          << ",\"tile\":[" << pc.gt.tile_u << ',' << kGtV << "],\"n_tiles\":"
          << uint64_t(pc.gt.n_ut) * pc.gt.n_vt;
     if (pc.path == PATH_STAGED) {

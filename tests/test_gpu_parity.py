@@ -184,6 +184,17 @@ SMALL = [
      ("layout", (100, 128), (1, 101)), 4),
     ("gtile_three_leaves_f32", ("layout", (40, 40, 33), (40, 1, 1600)),
      ("layout", (33, 1600), (1, 35)), 4),
+    # sources whose rows start on 16-byte boundaries: tensor-map loads of
+    # 128-byte swizzled boxes (fp16, fp32, fp64; ragged on both axes; a
+    # swizzled destination)
+    ("gtma_f32", ("layout", (300, 352), (352, 1)),
+     ("layout", (352, 300), (1, 353)), 4),
+    ("gtma_f16", ("layout", (200, 136), (136, 1)),
+     ("layout", (136, 200), (1, 137)), 2),
+    ("gtma_f64", ("layout", (130, 100), (100, 1)),
+     ("layout", (100, 130), (1, 101)), 8),
+    ("gtma_dst_swizzled_f32", ("layout", (128, 96), (96, 1)),
+     ("swizzle", 2, 0, 4, ("layout", (96, 128), (1, 97))), 4),
     # a destination of three leaves: the 4-leaf form with 64-bit offsets
     ("gtile_wide_leaves_f32", ("layout", (40, 40, 33), (40, 1, 1600)),
      ("layout", (33, 40, 40), (1, 35, 1401)), 4),
@@ -206,9 +217,14 @@ def test_small_parity_paths_cover_every_kernel():
     for _, src, dst, eb in SMALL:
         p = lm.Plan(lm.build_layout(src), lm.build_layout(dst), eb)
         for pc in p.describe()["pieces"]:
-            seen.add(pc["path"] if pc["path"] != "STAGED"
-                     else "STAGED/" + pc["store"] + str(pc["rows"]))
-    assert {"GENERIC", "GTILE", "VEC", "ZIP", "STAGED/gather0"} <= seen
+            if pc["path"] == "STAGED":
+                seen.add("STAGED/" + pc["store"] + str(pc["rows"]))
+            elif pc["path"] == "GTILE" and pc["tma"]:
+                seen.add("GTILE/tma")
+            else:
+                seen.add(pc["path"])
+    assert {"GENERIC", "GTILE", "GTILE/tma", "VEC", "ZIP",
+            "STAGED/gather0"} <= seen
     assert {"STAGED/transpose2", "STAGED/transpose4",
             "STAGED/transpose8"} <= seen, seen
 
