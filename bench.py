@@ -71,6 +71,7 @@ TV_CONFIGS = {
     "C2t": ("Sw<5,0,6> o (64,64):(1,64)", None, None, (64, 64)),
 }
 FALLBACK_HBM_GBS = 6800.0
+E2E_ROUNDS = 3
 
 
 def peaks() -> tuple[float, str]:
@@ -934,8 +935,11 @@ def measure_e2e(suite, args, torch, shards=4, topo=None) -> dict:
 
     In the same run, the same uploads and downloads without the copies give
     the link's ceilings for these byte counts: uploads alone, downloads
-    alone, and both at once (the end-to-end figure's own bound).  Pinned
-    buffers are allocated near the GPU (pinned_near_gpu)."""
+    alone, and both at once (the end-to-end figure's own bound).  The host
+    link is shared with the machine's other GPUs, so the four measurements
+    alternate over E2E_ROUNDS rounds and each figure is its median round:
+    a burst of outside traffic then weighs on the copies and their ceilings
+    alike.  Pinned buffers are allocated near the GPU (pinned_near_gpu)."""
     steps = max(20, min(args.steps, 40))
     lm = suite.lm
     local = suite.items[0]["src"].device.index or 0
@@ -1013,16 +1017,29 @@ def measure_e2e(suite, args, torch, shards=4, topo=None) -> dict:
         torch.cuda.synchronize()
         return start.elapsed_time(end) / steps
 
-    ms = timed(copies)
-    if lm.device_status() != 0:
-        raise RuntimeError("a copy kernel gave up a bounded wait "
-                           "(LM_E_TIMEOUT): the end-to-end run is invalid")
-    up_ms = timed(transfers(True, False))
-    down_ms = timed(transfers(False, True))
-    both_ms = timed(transfers(True, True))
+    rounds = {"copies": [], "up": [], "down": [], "both": []}
+    for _ in range(E2E_ROUNDS):
+        rounds["copies"].append(timed(copies))
+        if lm.device_status() != 0:
+            raise RuntimeError("a copy kernel gave up a bounded wait "
+                               "(LM_E_TIMEOUT): the end-to-end run is "
+                               "invalid")
+        rounds["up"].append(timed(transfers(True, False)))
+        rounds["down"].append(timed(transfers(False, True)))
+        rounds["both"].append(timed(transfers(True, True)))
+
+    def median(xs):
+        return sorted(xs)[len(xs) // 2]
+
+    ms, up_ms, down_ms, both_ms = (median(rounds[k]) for k in
+                                   ("copies", "up", "down", "both"))
     gb = 1e9
     return {"ms": ms * steps, "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": steps,
+            "d2h_bytes_per_step": d2h, "steps": steps, "rounds": E2E_ROUNDS,
+            "value_per_round": [round(suite.bytes_per_step / (m * 1e-3) / gb,
+                                      1) for m in rounds["copies"]],
+            "duplex_per_round": [round((h2d + d2h) / (m * 1e-3) / gb, 1)
+                                 for m in rounds["both"]],
             "path": f"layout_copy_host, {len(jobs)} plans on their own "
                     f"streams ({', '.join(sharded) or 'none'} as {shards} "
                     "shards each)",
@@ -1033,9 +1050,11 @@ def measure_e2e(suite, args, torch, shards=4, topo=None) -> dict:
             "transfers_only_value": round(
                 suite.bytes_per_step / (both_ms * 1e-3) / gb, 1),
             "ceilings": "the same uploads and downloads on the same streams "
-                        "without the copies, this run: uploads alone, "
-                        "downloads alone, both at once; transfers_only_value "
-                        "is the metric for the last (the bound of value)",
+                        "without the copies, this run, alternating with the "
+                        "copies' rounds: uploads alone, downloads alone, "
+                        "both at once; transfers_only_value is the metric "
+                        "for the last (the bound of value); each figure is "
+                        "the median of its rounds",
             "pinned": how, "topology": topo}
 
 
