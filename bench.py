@@ -25,6 +25,7 @@ max-over-ranks time.  ``--impl reference`` times the CPU oracle instead.
 from __future__ import annotations
 
 import argparse
+import contextlib
 import hashlib
 import json
 import os
@@ -290,6 +291,7 @@ def run_native(args) -> dict | None:
 
     peak, peak_kind = peaks()
     iso = isolated_times(suite, torch) if not args.quick else {}
+    mcp = memcpy_times(suite, torch, k2) if not args.quick else {}
     per_cfg = {}
     for it in suite.items:
         ms = statistics.median(per[it["name"]])
@@ -315,6 +317,14 @@ def run_native(args) -> dict | None:
             per_cfg[it["name"]].update({
                 "isolated_us": round(ims * 1e3, 2),
                 "isolated_frac_of_peak": round(igbs / peak, 4)})
+        if it["name"] in mcp:
+            nb, m_suite, m_alone = mcp[it["name"]]
+            per_cfg[it["name"]]["memcpy"] = {
+                "bytes": nb, "median_us": round(m_suite * 1e3, 2),
+                "frac_of_peak": round(nb / (m_suite * 1e-3) / 1e9 / peak, 4),
+                "isolated_us": round(m_alone * 1e3, 2),
+                "isolated_frac_of_peak": round(
+                    nb / (m_alone * 1e-3) / 1e9 / peak, 4)}
     dom_name = DOMINANT if DOMINANT in per else suite.items[0]["name"]
     dom_item = next(it for it in suite.items if it["name"] == dom_name)
     dom_kernel = kernel_name(dom_item["plan"], dom_item["w"].elem_bytes)
@@ -372,7 +382,10 @@ def run_native(args) -> dict | None:
                   "after >1.6 GB of other traffic (L2 126 MiB)",
             "wall_s_timed": round(wall, 4),
             "breakdown": "per_config: a second pass of " + str(k2) +
-                         " steps with CUDA events around every copy",
+                         " steps with CUDA events around every copy; "
+                         "isolated_*: each copy alone after a read flush of "
+                         "L2; memcpy: a cudaMemcpyAsync of the copy's bytes "
+                         "in its slot of the suite and alone",
             "per_config": per_cfg,
             "d2d_copy_ceiling_gbs": ceiling,
             "other_kernels": other,
@@ -478,6 +491,44 @@ def isolated_times(suite, torch, runs=20) -> dict:
             if r >= 3:
                 times.append(e0.elapsed_time(e1))
         out[it["name"]] = statistics.median(times)
+    del flush
+    return out
+
+
+def memcpy_times(suite, torch, steps, runs=20) -> dict:
+    """The same-run reference for the per-copy figures: a device-to-device
+    memcpy (torch's copy_, cudaMemcpyAsync) from each copy's source buffer
+    into its destination buffer of as many bytes as the copy moves -- half
+    read, half written, at most either buffer.  Timed in the copy's slot of
+    the suite (the suite with every copy replaced by its memcpy, events
+    around each, median over `steps`, so each memcpy also writes back its
+    predecessors' dirty lines) and alone after a read flush of L2 (as
+    isolated_times).  Returns {name: (bytes, suite ms, isolated ms)}."""
+    pairs = []
+    for it in suite.items:
+        src, dst = it["src"].view(torch.uint8), it["dst"].view(torch.uint8)
+        n = min(it["bytes"] // 2, src.numel(), dst.numel())
+        pairs.append((it["name"], src[:n], dst[:n]))
+    for _ in range(3):
+        for _, s, d in pairs:
+            d.copy_(s)
+    ev = [[(torch.cuda.Event(enable_timing=True),
+            torch.cuda.Event(enable_timing=True)) for _ in pairs]
+          for _ in range(steps)]
+    torch.cuda.synchronize()
+    for row in ev:
+        for (e0, e1), (_, s, d) in zip(row, pairs):
+            e0.record()
+            d.copy_(s)
+            e1.record()
+    torch.cuda.synchronize()
+    flush = torch.ones(512 << 20, dtype=torch.uint8, device=pairs[0][1].device)
+    out = {}
+    for k, (name, s, d) in enumerate(pairs):
+        in_suite = statistics.median(row[k][0].elapsed_time(row[k][1])
+                                     for row in ev)
+        alone = _timed(torch, lambda: d.copy_(s), runs, flush)
+        out[name] = (2 * s.numel(), in_suite, alone)
     del flush
     return out
 
@@ -648,10 +699,13 @@ def measure_tv(suite, args, torch, peak) -> dict:
 def measure_exchange(suite, args, torch, peak, world=4) -> dict:
     """The sharded relayout's device work on one GPU: the 4096x4096 fp32
     transpose with rows sharded over `world` ranks on both sides.  Every
-    rank's pack (one copy for all peers) and unpack run back to back on this
-    device, with device-to-device copies of the boxes standing in for the
-    all-to-all (a collective on several GPUs); reported as the bytes all of
-    them read and write over the time of all of them."""
+    rank's pack (one copy for all peers) and unpack run on this device, each
+    rank on its own stream as the ranks of a real run are separate GPUs
+    (every pack joined before any box moves), with device-to-device copies
+    of the boxes standing in for the all-to-all (a collective on several
+    GPUs); reported as the bytes all of them read and write over the time
+    of all of them.  The packs and unpacks are also timed one after another
+    on one stream (`pack_unpack_serial_us_per_pass`)."""
     it = next((i for i in suite.items if i["name"] == "C2"), None)
     if it is None:
         return {}
@@ -684,19 +738,46 @@ def measure_exchange(suite, args, torch, peak, world=4) -> dict:
     box = sizes[0]["send"][0] * eb
     one_copy = all(d["one_copy_per_side"] for d in dsc)
 
-    def one(exchange=True):
+    ranks = [torch.cuda.Stream(device=buf_in.device) for _ in range(world)]
+
+    def fork(concurrent):
+        if concurrent:
+            ev = torch.cuda.Event()
+            ev.record()
+            for st in ranks:
+                st.wait_event(ev)
+
+    def join(concurrent):
+        if concurrent:
+            cur = torch.cuda.current_stream()
+            for st in ranks:
+                ev = torch.cuda.Event()
+                ev.record(st)
+                cur.wait_event(ev)
+
+    def on(k, concurrent):
+        return (torch.cuda.stream(ranks[k]) if concurrent
+                else contextlib.nullcontext())
+
+    def one(exchange=True, concurrent=True):
+        fork(concurrent)
         for p, x in enumerate(xs):
             o, n = dsc[p]["src_origin"] * eb, dsc[p]["src_local"] * eb
-            lm.exchange_pack_all(x, buf_in[o:o + n],
-                                 send[soff[p][0]:soff[p][0] + world * box])
+            with on(p, concurrent):
+                lm.exchange_pack_all(x, buf_in[o:o + n],
+                                     send[soff[p][0]:soff[p][0] + world * box])
+        join(concurrent)   # every box packed before any moves
+        fork(concurrent)
         for q, x in enumerate(xs):
             o, n = dsc[q]["dst_origin"] * eb, dsc[q]["dst_local"] * eb
             r = recv[q * world * box:(q + 1) * world * box]
-            if exchange:
-                for p in range(world):      # the exchange, as device copies
-                    r[p * box:(p + 1) * box].copy_(
-                        send[soff[p][q]:soff[p][q] + box])
-            lm.exchange_unpack_all(x, r, buf_out[o:o + n])
+            with on(q, concurrent):
+                if exchange:
+                    for p in range(world):  # the exchange, as device copies
+                        r[p * box:(p + 1) * box].copy_(
+                            send[soff[p][q]:soff[p][q] + box])
+                lm.exchange_unpack_all(x, r, buf_out[o:o + n])
+        join(concurrent)
 
     def timed_pass(fn):
         """ms per pass of fn, replayed as one CUDA graph (the small
@@ -733,6 +814,7 @@ def measure_exchange(suite, args, torch, peak, world=4) -> dict:
     ms, how = timed_pass(one)
     # the library's part alone: every rank's pack and unpack
     ms_lib, _ = timed_pass(lambda: one(exchange=False))
+    ms_serial, _ = timed_pass(lambda: one(exchange=False, concurrent=False))
     if lm.device_status() != 0:
         raise RuntimeError("a copy kernel gave up a bounded wait "
                            "(LM_E_TIMEOUT): the exchange run is invalid")
@@ -749,7 +831,11 @@ def measure_exchange(suite, args, torch, peak, world=4) -> dict:
             "frac_of_peak": round(gbs / peak, 4),
             "pack_unpack_us_per_pass": round(ms_lib * 1e3, 2),
             "pack_unpack_gbs": round(gbs_lib, 1),
-            "pack_unpack_frac_of_peak": round(gbs_lib / peak, 4)}
+            "pack_unpack_frac_of_peak": round(gbs_lib / peak, 4),
+            "ranks": "each rank on its own stream",
+            "pack_unpack_serial_us_per_pass": round(ms_serial * 1e3, 2),
+            "pack_unpack_serial_frac_of_peak": round(
+                2 * 2 * total / (ms_serial * 1e-3) / 1e9 / peak, 4)}
 
 
 # --------------------------------------------------------------------------
