@@ -312,6 +312,12 @@ struct GTileArgs {
   // inner leaves
   uint32_t lo_step[kMaxLeaves];
   uint32_t in_step[kMaxLeaves];
+  // each step's offset change (bytes): without carries the sum of its
+  // digits times the strides (*_dstep), plus, per carry out of leaf k,
+  // stride[k + 1] - ext[k] * stride[k] (*_cadj)
+  int64_t lo_dstep = 0, in_dstep = 0;
+  int64_t lo_cadj[kMaxLeaves];
+  int64_t in_cadj[kMaxLeaves];
   int64_t s_base = 0, d_base = 0;       // bytes
   Swz s_swz, d_swz;                     // bytes
   int32_t narrow = 0;                   // every byte offset below 2^31
@@ -326,6 +332,7 @@ struct GTileArgs {
   int64_t t_ustride = 0;
   uint32_t in_step1[kMaxLeaves];
   uint32_t in_jump[kMaxLeaves];
+  int64_t in_dstep1 = 0, in_djump = 0;
 };
 
 struct EvalArgs {

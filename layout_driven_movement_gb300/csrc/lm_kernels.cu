@@ -324,21 +324,29 @@ struct Digits {
       }
     }
   }
-  // the last leaf may run past its extent: the step never leaves the
-  // caller's range, so no carry out of it is ever needed
+  // Add the step whose digits are d.  The offset changes by dsum (the
+  // digits times the strides) plus cadj[k] per carry out of leaf k
+  // (stride[k + 1] - ext[k] * stride[k]), both computed on the host.  The
+  // last leaf may run past its extent: the step never leaves the caller's
+  // range, so no carry out of it is ever needed, and its digit is not kept.
   __device__ __forceinline__ void step(int n, const uint32_t* ext,
-                                       const uint32_t* d, const int64_t* str) {
+                                       const uint32_t* d, int64_t dsum,
+                                       const int64_t* cadj) {
     uint32_t carry = 0;
+    OFF delta = OFF(dsum);
 #pragma unroll
-    for (int k = 0; k < NL; ++k) {
-      if (k < n) {
+    for (int k = 0; k + 1 < NL; ++k) {
+      if (k + 1 < n) {
         uint32_t x = c[k] + d[k] + carry;
-        carry = (k + 1 < n && x >= ext[k]) ? 1u : 0u;
-        x -= carry ? ext[k] : 0u;
-        off += (OFF(x) - OFF(c[k])) * OFF(str[k]);
+        carry = x >= ext[k] ? 1u : 0u;
+        if (carry) {
+          x -= ext[k];
+          delta += OFF(cadj[k]);
+        }
         c[k] = x;
       }
     }
+    off += delta;
   }
 };
 
@@ -412,7 +420,7 @@ __global__ void __launch_bounds__(256)
       for (int p = 0; p < TU / RU; ++p) {
         const uint32_t ul = ul_v + uint32_t(RU * p);
         if (u0 + ul >= a.W) break;
-        if (p) lo.step(a.n_lo, a.lo_ext, a.lo_step, a.lo_str);
+        if (p) lo.step(a.n_lo, a.lo_ext, a.lo_step, a.lo_dstep, a.lo_cadj);
         elem_to_shared<EB>(&tl[ul][vl_v],
                            src + sw_s(base + lo.off));
       }
@@ -425,7 +433,7 @@ __global__ void __launch_bounds__(256)
       for (int p = 0; p < kGtV / CV; ++p) {
         const uint32_t vl = vl_u + uint32_t(CV * p);
         if (v0 + vl >= a.nv) break;
-        if (p) in.step(a.n_in, a.in_ext, a.in_step, a.in_str);
+        if (p) in.step(a.n_in, a.in_ext, a.in_step, a.in_dstep, a.in_cadj);
         elem_to_shared<EB>(&tl[ul_u][vl],
                            src + sw_s(OFF(a.s_base) + in.off));
       }
@@ -443,7 +451,7 @@ __global__ void __launch_bounds__(256)
       for (int p = 0; p < kGtV / CV; ++p) {
         const uint32_t vl = vl_u + uint32_t(CV * p);
         if (v0 + vl >= a.nv) break;
-        if (p) in.step(a.n_in, a.in_ext, a.in_step, a.in_str);
+        if (p) in.step(a.n_in, a.in_ext, a.in_step, a.in_dstep, a.in_cadj);
         *reinterpret_cast<T*>(dst + sw_d(OFF(a.d_base) + in.off)) =
             tl[ul_u][vl];
       }
@@ -458,7 +466,7 @@ __global__ void __launch_bounds__(256)
       for (int p = 0; p < TU / RU; ++p) {
         const uint32_t ul = ul_v + uint32_t(RU * p);
         if (u0 + ul >= a.W) break;
-        if (p) lo.step(a.n_lo, a.lo_ext, a.lo_step, a.lo_str);
+        if (p) lo.step(a.n_lo, a.lo_ext, a.lo_step, a.lo_dstep, a.lo_cadj);
         *reinterpret_cast<T*>(dst + sw_d(base + lo.off)) =
             tl[ul][vl_v];
       }
@@ -1372,21 +1380,26 @@ __global__ void __launch_bounds__(256)
         Digits<2, OFF> in;
         in.set(u + a.W * (v0 + cl * VPC), a.n_in, a.in_ext, a.in_div,
                a.in_str);
+        in.off += OFF(a.d_base);
 #pragma unroll
         for (int k = 0; k < PER; ++k) {
           const uint32_t ch = cl + uint32_t(CP * k);
           const uint32_t vf = v0 + ch * VPC;
           if (vf >= a.nv) break;
-          if (k) in.step(a.n_in, a.in_ext, a.in_jump, a.in_str);
+          if (k)
+            in.step(a.n_in, a.in_ext, a.in_jump, a.in_djump, a.in_cadj);
           const uint4 w = *reinterpret_cast<const uint4*>(
               row + (ch >> 3) * REGION + (((ch & 7u) ^ (ul & 7u)) << 4));
           T vals[VPC];
           memcpy(vals, &w, 16);
+          const bool whole = vf + uint32_t(VPC) <= a.nv;
 #pragma unroll
           for (int e = 0; e < VPC; ++e) {
-            if (vf + uint32_t(e) >= a.nv) break;
-            if (e) in.step(a.n_in, a.in_ext, a.in_step1, a.in_str);
-            const OFF o = OFF(a.d_base) + in.off;
+            if (!whole && vf + uint32_t(e) >= a.nv) break;
+            if (e)
+              in.step(a.n_in, a.in_ext, a.in_step1, a.in_dstep1,
+                      a.in_cadj);
+            const OFF o = in.off;
             *reinterpret_cast<T*>(
                 dst + (dswz ? OFF(swz_apply(a.d_swz, int64_t(o))) : o)) =
                 vals[e];

@@ -185,10 +185,27 @@ bool plan_gtile(const std::vector<Leaf>& sl, const std::vector<Leaf>& dl,
       x /= ext[j];
     }
   };
+  // a step's offset change without carries, and each leaf's carry change
+  auto dstep = [](const uint32_t* d, const int64_t* str, int n) {
+    int64_t r = 0;
+    for (int j = 0; j < n; ++j) r = add_chk(r, mul_chk(int64_t(d[j]), str[j]));
+    return r;
+  };
+  auto cadj = [](const uint32_t* ext, const int64_t* str, int n,
+                 int64_t* out) {
+    for (int j = 0; j < kMaxLeaves; ++j)
+      out[j] = j + 1 < n ? add_chk(str[j + 1], -mul_chk(int64_t(ext[j]),
+                                                        str[j]))
+                         : 0;
+  };
+  cadj(g.lo_ext, g.lo_str, g.n_lo, g.lo_cadj);
+  cadj(g.in_ext, g.in_str, g.n_in, g.in_cadj);
   // lanes over v: 256 / kGtV rows of u per pass; lanes over u:
   // 256 / tile_u columns of v per pass
   digits(256 / kGtV, g.lo_ext, g.n_lo, g.lo_step);
   digits(int64_t(256 / g.tile_u) * W, g.in_ext, g.n_in, g.in_step);
+  g.lo_dstep = dstep(g.lo_step, g.lo_str, g.n_lo);
+  g.in_dstep = dstep(g.in_step, g.in_str, g.n_in);
   // tensor-map loads (LM_GTILE_TMA=0 keeps cp.async): the source outer, a
   // plain matrix (one leaf on each side of its unit-stride leaf), rows
   // 16-byte aligned, 2- to 8-byte elements, no source swizzle, 64-row tiles
@@ -206,6 +223,8 @@ bool plan_gtile(const std::vector<Leaf>& sl, const std::vector<Leaf>& dl,
     g.t_ustride = g.lo_str[0];
     digits(W, g.in_ext, g.n_in, g.in_step1);
     digits(int64_t(cp * vpc - vpc + 1) * W, g.in_ext, g.n_in, g.in_jump);
+    g.in_dstep1 = dstep(g.in_step1, g.in_str, g.n_in);
+    g.in_djump = dstep(g.in_jump, g.in_str, g.n_in);
   }
   // 32-bit offsets when every offset of both sides, swizzled or not, stays
   // below 2^31 bytes
@@ -216,8 +235,16 @@ bool plan_gtile(const std::vector<Leaf>& sl, const std::vector<Leaf>& dl,
     if (z.on()) r = add_chk(r, int64_t(eb) << (z.b + z.m + z.s));
     return r;
   };
+  // ... and so does every step's offset change (32-bit arithmetic)
+  auto small = [](int64_t x) {
+    return x > -(int64_t(1) << 31) && x < (int64_t(1) << 31);
+  };
+  bool steps32 = small(g.lo_dstep) && small(g.in_dstep) &&
+                 small(g.in_dstep1) && small(g.in_djump);
+  for (int j = 0; j < kMaxLeaves; ++j)
+    steps32 = steps32 && small(g.lo_cadj[j]) && small(g.in_cadj[j]);
   g.narrow = reach(sl, ss) < (int64_t(1) << 31) &&
-                     reach(dl, ds) < (int64_t(1) << 31)
+                     reach(dl, ds) < (int64_t(1) << 31) && steps32
                  ? 1
                  : 0;
   g.s_swz = to_bytes(ss, eb);

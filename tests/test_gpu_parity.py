@@ -453,6 +453,43 @@ def test_pipeline_variants_parity(env):
     assert r.returncode == 0 and "ok" in r.stdout, r.stdout + r.stderr
 
 
+GTILE_CASES = ["gtile_outer_src_f32", "gtile_outer_dst_f16", "gtile_u8",
+               "gtile_ragged_f64", "gtile_b128", "gtile_swizzled_src_f32",
+               "gtile_three_leaves_f32", "gtma_f32", "gtma_f16", "gtma_f64",
+               "gtma_dst_swizzled_f32", "gtile_wide_leaves_f32",
+               "non_refinable_generic"]
+
+
+@pytest.mark.parametrize("env", [{"LM_GTILE_TMA": "0"},
+                                 {"LM_GTILE_TMA": "0", "LM_GTILE_U": "32"},
+                                 {"LM_GTILE": "0"}])
+def test_gtile_variants_parity(env):
+    """The pairs without a common refinement in every form: tiles loaded by
+    per-thread cp.async instead of tensor map (LM_GTILE_TMA=0), 32-row tiles
+    (LM_GTILE_U=32), and one element per thread (LM_GTILE=0), each compared
+    in full with the oracle, in a fresh process since the knobs are read
+    once."""
+    import os
+    import subprocess
+    import sys
+    here = os.path.dirname(os.path.abspath(__file__))
+    code = (
+        "import sys; sys.path[:0] = [%r, %r]\n"
+        "import test_gpu_parity as t\n"
+        "t.lm.lib()\n"
+        "cases = {c[0]: c for c in t.SMALL}\n"
+        "for n in %r:\n"
+        "    _, s, d, eb = cases[n]\n"
+        "    p = t.run_case(s, d, eb)\n"
+        "    paths = [pc['path'] for pc in p.describe()['pieces']]\n"
+        "    if %r: assert 'GTILE' not in paths, (n, paths)\n"
+        "print('ok')\n" % (here, os.path.dirname(here), GTILE_CASES,
+                           env.get("LM_GTILE") == "0"))
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True,
+                       text=True, env={**os.environ, **env}, timeout=600)
+    assert r.returncode == 0 and "ok" in r.stdout, r.stdout + r.stderr
+
+
 def test_tensor_map_transposes_full_size():
     """The opt-in tensor-map loads (LM_TMA=1) on the full-size fp32
     transpose and NHWC->NCHW, compared in full with the oracle, in a fresh
