@@ -1423,12 +1423,46 @@ static std::string describe(const lm_plan& P) {
     if (pc.path == PATH_ZIP)
       os << ",\"vec_bytes\":16,\"rows\":" << pc.vec.zip_rows
          << ",\"n_vec\":" << pc.vec.n_vec;
-    if (pc.path == PATH_GTILE)
-      os << ",\"outer\":\"" << (pc.gt.outer_src ? "src" : "dst")
-         << "\",\"u_extent\":" << pc.gt.W << ",\"v_extent\":" << pc.gt.nv
-         << ",\"tma\":" << (pc.gt.tma ? "true" : "false")
-         << ",\"tile\":[" << pc.gt.tile_u << ',' << kGtV << "],\"n_tiles\":"
-         << uint64_t(pc.gt.n_ut) * pc.gt.n_vt;
+    if (pc.path == PATH_GTILE) {
+      const GTileArgs& g = pc.gt;
+      os << ",\"outer\":\"" << (g.outer_src ? "src" : "dst")
+         << "\",\"u_extent\":" << g.W << ",\"v_extent\":" << g.nv
+         << ",\"tma\":" << (g.tma ? "true" : "false")
+         << ",\"tile\":[" << g.tile_u << ',' << kGtV << "],\"n_tiles\":"
+         << uint64_t(g.n_ut) * g.n_vt
+         << ",\"offsets32\":" << (g.narrow ? "true" : "false");
+      // each part's leaves [extent, byte stride] and the steps its threads
+      // take: the step's digits, its offset change without carries and the
+      // extra change of a carry out of each leaf
+      auto leaves = [&](const char* name, int n, const uint32_t* ext,
+                        const int64_t* str) {
+        os << ",\"" << name << "_leaves\":[";
+        for (int k = 0; k < n; ++k)
+          os << (k ? "," : "") << '[' << ext[k] << ',' << str[k] << ']';
+        os << ']';
+      };
+      bool first = true;
+      auto step = [&](const char* name, int n, const uint32_t* d,
+                      int64_t dsum, const int64_t* cadj) {
+        os << (first ? "" : ",") << '"' << name << "\":{\"digits\":[";
+        first = false;
+        for (int k = 0; k < n; ++k) os << (k ? "," : "") << d[k];
+        os << "],\"dstep\":" << dsum << ",\"cadj\":[";
+        for (int k = 0; k < n; ++k) os << (k ? "," : "") << cadj[k];
+        os << "]}";
+      };
+      leaves("lo", g.n_lo, g.lo_ext, g.lo_str);
+      leaves("hi", g.n_hi, g.hi_ext, g.hi_str);
+      leaves("in", g.n_in, g.in_ext, g.in_str);
+      os << ",\"steps\":{";
+      step("lo", g.n_lo, g.lo_step, g.lo_dstep, g.lo_cadj);
+      step("in", g.n_in, g.in_step, g.in_dstep, g.in_cadj);
+      if (g.tma) {
+        step("in_next_v", g.n_in, g.in_step1, g.in_dstep1, g.in_cadj);
+        step("in_next_chunk", g.n_in, g.in_jump, g.in_djump, g.in_cadj);
+      }
+      os << '}';
+    }
     if (pc.path == PATH_STAGED) {
       const StagedArgs& A = pc.st;
       os << ",\"tile_elems\":" << pc.tile_elems << ",\"n_tiles\":" << A.n_tiles

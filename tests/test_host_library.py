@@ -669,6 +669,79 @@ def test_refinement_of_coalesced_sides():
         assert (so == OS.at(i)).all() and (do == OD.at(i)).all()
 
 
+def _gtile_walk(leaves, step, x0, count):
+    """The tiled kernels' walk over one part of a GTILE piece: the digits
+    of x0 in the part's mixed radix and their byte offset, then `count`
+    steps each adding the step's digits with carries and changing the
+    offset by its precomputed amounts (the last leaf runs on, no carry out
+    of it).  Returns the offsets visited, x0's included."""
+    ext = [e for e, _ in leaves]
+    st = [b for _, b in leaves]
+    n = len(ext)
+    c, q = [], x0
+    for e in ext:
+        c.append(q % e)
+        q //= e
+    off = sum(ck * sk for ck, sk in zip(c, st))
+    out = [off]
+    for _ in range(count):
+        carry, delta = 0, step["dstep"]
+        for k in range(n - 1):
+            x = c[k] + step["digits"][k] + carry
+            carry = 1 if x >= ext[k] else 0
+            if carry:
+                x -= ext[k]
+                delta += step["cadj"][k]
+            c[k] = x
+        off += delta
+        out.append(off)
+    return out
+
+
+def test_gtile_steps_reproduce_offsets():
+    """The steps the tiled kernels take between a thread's elements, as the
+    planner hands them over (each step's digits, its offset change without
+    carries and the change of each carry): walking them from random starts
+    visits exactly the byte offsets the oracle gives the logical indices
+    they land on, for the inner side over the whole index and the outer
+    side's lo leaves over u."""
+    rng = np.random.default_rng(5)
+    for s_txt, d_txt, eb in [("(6000,7000):(7000,1)", "(7000,6000):(1,7001)", 4),
+                             ("(300,350):(350,1)", "(350,300):(1,351)", 4),
+                             ("(350,300):(1,351)", "(300,350):(350,1)", 2),
+                             ("(40,40,33):(40,1,1600)", "(33,1600):(1,35)", 8),
+                             ("(3,14,37):(518,37,1)", "(37,42):(1,39)", 4),
+                             ("(37,42):(1,39)", "(3,14,37):(518,37,1)", 2)]:
+        pc = lm.Plan(lm.Layout.parse(s_txt), lm.Layout.parse(d_txt),
+                     eb).describe()["pieces"][0]
+        assert pc["path"] == "GTILE", (s_txt, pc)
+        outer_src = pc["outer"] == "src"
+        O = lo.parse(s_txt if outer_src else d_txt)
+        I = lo.parse(d_txt if outer_src else s_txt)
+        W, n = pc["u_extent"], I.size
+        oleaves = lo.flatten(O.shape, O.stride)
+        k = next(j for j, (e, st) in enumerate(oleaves) if st == 1)
+        LO = lo.Layout(tuple(e for e, _ in oleaves[:k]),
+                       tuple(st for _, st in oleaves[:k]))
+        parts = [("in", pc["in_leaves"], n, I),
+                 ("lo", pc["lo_leaves"], W, LO)]
+        names = {"in": ["in", "in_next_v", "in_next_chunk"], "lo": ["lo"]}
+        for part, leaves, size, L in parts:
+            radix = np.cumprod([1] + [e for e, _ in leaves[:-1]])
+            for name in names[part]:
+                if name not in pc["steps"]:
+                    continue
+                step = pc["steps"][name]
+                amount = int(sum(d * r for d, r in zip(step["digits"], radix)))
+                assert 0 < amount < size, (s_txt, name, amount)
+                count = min(12, (size - 1) // amount)
+                for x0 in rng.integers(0, size - count * amount, 20):
+                    got = _gtile_walk(leaves, step, int(x0), count)
+                    xs = int(x0) + amount * np.arange(count + 1)
+                    want = (L.at(xs) * eb).tolist()
+                    assert got == want, (s_txt, name, int(x0))
+
+
 def test_gtile_split_is_exact():
     """The tiled path for pairs without a common refinement reads the outer
     side as lo(u) + hi(v) with i = u + W*v: for every logical index of a
