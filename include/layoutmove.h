@@ -320,7 +320,11 @@ int lm_plan_copy_shard(const lm_layout* src, const lm_layout* dst,
  * element ranges of src and dst the copy can reach ("src_range",
  * "dst_range": [0, cosize) for a whole copy, the shard's own for a shard)
  * and whether no other shard writes inside the destination range
- * ("dst_own"). */
+ * ("dst_own").  A GTILE piece also gives its parts' leaves as [extent,
+ * byte stride] ("lo_leaves", "hi_leaves", "in_leaves") and the steps its
+ * threads take between elements ("steps": per step its digits in the
+ * part's mixed radix, "dstep" the byte offset change without carries and
+ * "cadj" the extra change of a carry out of each leaf). */
 int lm_plan_describe(const lm_plan* plan, char* buf, size_t cap);
 
 /* Elements of src and dst that the plan reads and writes (sizes of their
